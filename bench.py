@@ -1,0 +1,448 @@
+"""Benchmark: two-phase Block AttnRes throughput on GB300.
+
+Default workload (the headline metric): one block of the two-phase Block
+scheme over 9 cached block summaries [B=8, T=4096, D=4096] bf16 with S = 24
+sublayer queries -- phase 1 batched, then 23 phase-2 merges, each sublayer
+followed by the running-partial update with the synthetic sublayer
+f(h) = 0.5 tanh(u h).  One step = one such block pass over all B*T tokens.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
+                    [--workload NAME] [--rows R]
+
+Prints one JSON line (rank 0).  Multi-GPU (torchrun): every rank runs the
+same per-GPU workload on its own token rows (no data-path collective);
+value = all ranks' tokens / max-over-ranks time ("weak" scaling).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from transformer_depth_wise_gb300 import accounting  # noqa: E402
+from transformer_depth_wise_gb300 import workloads as wk  # noqa: E402
+
+METRIC = "Block AttnRes tokens/s and achieved HBM GB/s (% of GB300 peak), two-phase path"
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ---------------------------------------------------------------------------
+# process group / timing helpers
+# ---------------------------------------------------------------------------
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return rank, local, world
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.gpu_index = gpu_index
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(self.gpu_index), "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for name, val in zip(names, f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            j = json.load(fh)
+        return float(j["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from a committed ncu summary, if the kernel source is unchanged."""
+    path = os.path.join(ROOT, "profiles", f"traffic_{kernel}_{workload}.txt")
+    src = {"phase1": "phase1.cu", "merge": "merge.cu", "update": "merge.cu",
+           "aggregate": "aggregate.cu"}.get(kernel)
+    if not src or not os.path.exists(path):
+        return None
+    info = {}
+    for line in open(path):
+        if ":" in line:
+            k, v = line.split(":", 1)
+            info[k.strip()] = v.strip()
+    with open(os.path.join(ROOT, "transformer_depth_wise_gb300", "csrc", src), "rb") as fh:
+        sha = hashlib.sha256(fh.read()).hexdigest()
+    if info.get("source_sha256") != sha:
+        return None
+    try:
+        return float(info["traffic_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (baseline and reference arm)
+# ---------------------------------------------------------------------------
+def oracle_block_rows_per_s(wl, rows_target_s: float = 12.0, max_rows: int = 4096):
+    """Time the oracle's two-phase block chain on a bounded sample of token rows."""
+    import numpy as np
+    import oracle
+    inp = wk.two_phase_inputs(wl, rows=256, device="cpu")
+    blocks = [b.reshape(-1, wl.D).double().numpy() for b in inp["blocks"]]
+    W, G, U = (inp["queries"].double().numpy(), inp["gains"].double().numpy(),
+               inp["u"].double().numpy())
+    t0 = time.perf_counter()
+    oracle.block_two_phase_chain([b[:8] for b in blocks], W, G, U, inp["eps"], oracle.BF16)
+    per_row = (time.perf_counter() - t0) / 8
+    rows = int(min(max_rows, max(16, rows_target_s / max(per_row, 1e-6))))
+    rows = min(rows, 256)
+    reps = max(1, int(rows_target_s / max(per_row * rows, 1e-6)))
+    reps = min(reps, 64)
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        oracle.block_two_phase_chain([b[:rows] for b in blocks], W, G, U, inp["eps"], oracle.BF16)
+    dt = time.perf_counter() - t0
+    sample = f"{reps} x {rows} token rows of the {wl.name} block chain (phase 1 + {wl.S - 1} merges + {wl.S} updates), fp64 oracle, 1 thread"
+    return reps * rows / dt, dt, sample
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+def run_two_phase(args, wl, dev, rank, world):
+    from transformer_depth_wise_gb300 import api
+    if args.rows:
+        wl = wk.Workload(wl.name, 1, args.rows, wl.D, wl.n, wl.dtype, wl.scale_lo, wl.scale_hi,
+                         S=wl.S, seed=wl.seed)
+    n_blocks = wl.n if wl.name == "two_phase_bf16" else wl.n - 1
+    inp = wk.two_phase_inputs(wl, device=dev, n=n_blocks)
+    blk = api.TwoPhaseBlock(inp["blocks"], inp["queries"], inp["gains"], inp["u"], inp["eps"])
+    stream = torch.cuda.current_stream(dev)
+    rows, D, S, elt = wl.B * wl.T, wl.D, wl.S, 2
+
+    for _ in range(args.warmup):
+        blk.run()
+    torch.cuda.synchronize(dev)
+
+    ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    K = args.steps
+    events = [{"phase1": (ev(), ev()), "merge": [(ev(), ev()) for _ in range(S - 1)],
+               "update": [(ev(), ev()) for _ in range(S)]} for _ in range(K)]
+    t_start, t_end = ev(), ev()
+    clocks = ClockSampler(dev.index if dev.index is not None else 0)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    clocks.start()
+    time.sleep(0.3)
+    t_start.record(stream)
+    for k in range(K):
+        blk.run(events=events[k])
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    clk = clocks.stop()
+    barrier(world)
+    elapsed_ms = max_over_ranks(t_start.elapsed_time(t_end), world, dev)
+
+    p1 = [e["phase1"][0].elapsed_time(e["phase1"][1]) for e in events]
+    mg = [a.elapsed_time(b) for e in events for a, b in e["merge"]]
+    up = [a.elapsed_time(b) for e in events for a, b in e["update"]]
+    b = accounting.two_phase_block_bytes(n_blocks, S, rows, D, elt)
+    kern = {
+        "phase1": {"launches": K, "avg_ms": statistics.mean(p1), "bytes": b["phase1"]},
+        "merge": {"launches": K * (S - 1), "avg_ms": statistics.mean(mg),
+                  "bytes": accounting.merge_bytes(rows, D, elt)},
+        "update": {"launches": K * S, "avg_ms": statistics.mean(up),
+                   "bytes": b["updates"] / S},
+    }
+    peak, peak_src = measured_peak()
+    for name, k in kern.items():
+        k["total_ms"] = k["avg_ms"] * k["launches"]
+        k["gbs"] = k["bytes"] / (k["avg_ms"] * 1e-3) / 1e9
+        k["frac"] = k["gbs"] / peak
+    dom = max(kern, key=lambda n: kern[n]["total_ms"])
+    d = kern[dom]
+    traffic = kernel_traffic(dom, wl.name)
+    roofline = {"bound": "hbm", "kernel": dom, "achieved": round(d["gbs"], 1), "peak": peak,
+                "unit": "GB/s", "frac": round(d["frac"], 4), "traffic": traffic,
+                "algorithmic_bytes_per_launch": d["bytes"], "peak_source": peak_src + " hbm_gbs"}
+
+    tokens = rows * K * world
+    value = tokens / (elapsed_ms * 1e-3)
+
+    # End to end through the public API: pinned host inputs -> device, block
+    # pass, final partial (the new block summary) -> pinned host, every step.
+    e2e = run_two_phase_e2e(args, wl, dev, inp, n_blocks, world)
+
+    res = {
+        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": round(elapsed_ms / K, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": wl.name, "B": wl.B, "T": wl.T, "D": D, "n_blocks": n_blocks, "S": S,
+                   "step": f"phase 1 + {S - 1} phase-2 merges + {S} partial updates",
+                   "l2": "inputs larger than L2 (every kernel streams >= 268 MB); no flush",
+                   "parallelism": f"dp{world} (token rows; no collective)"},
+        "achieved_hbm_gbs_step": round(b["total"] / (elapsed_ms / K * 1e-3) / 1e9, 1),
+        "roofline": roofline,
+        "kernels": {n: {kk: (round(v, 5) if isinstance(v, float) else v) for kk, v in k.items()}
+                    for n, k in kern.items()},
+        "e2e": e2e,
+        "gpu_launches": K * blk.launches_per_run,
+        "clocks": clk,
+    }
+    return res
+
+
+def run_two_phase_e2e(args, wl, dev, inp, n_blocks, world):
+    from transformer_depth_wise_gb300 import api
+    host = {
+        "blocks": [b.cpu().pin_memory() for b in inp["blocks"]],
+        "queries": inp["queries"].cpu().pin_memory(),
+        "gains": inp["gains"].cpu().pin_memory(),
+        "u": inp["u"].cpu().pin_memory(),
+    }
+    dev_bufs = {
+        "blocks": [torch.empty_like(b) for b in inp["blocks"]],
+        "queries": torch.empty_like(inp["queries"]),
+        "gains": torch.empty_like(inp["gains"]),
+        "u": torch.empty_like(inp["u"]),
+    }
+    blk = api.TwoPhaseBlock(dev_bufs["blocks"], dev_bufs["queries"], dev_bufs["gains"],
+                            dev_bufs["u"], inp["eps"])
+    out_host = torch.empty(blk.partial.shape, dtype=blk.partial.dtype).pin_memory()
+    h2d = sum(b.numel() * b.element_size() for b in host["blocks"]) + sum(
+        host[k].numel() * host[k].element_size() for k in ("queries", "gains", "u"))
+    d2h = out_host.numel() * out_host.element_size()
+
+    def step():
+        for dst, src in zip(dev_bufs["blocks"], host["blocks"]):
+            dst.copy_(src, non_blocking=True)
+        for k in ("queries", "gains", "u"):
+            dev_bufs[k].copy_(host[k], non_blocking=True)
+        p = blk.run()
+        out_host.copy_(p, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        step()
+    torch.cuda.synchronize(dev)
+    stream = torch.cuda.current_stream(dev)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    K = max(1, args.steps // 2)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    a.record(stream)
+    for _ in range(K):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    ms = max_over_ranks(a.elapsed_time(b), world, dev)
+    tokens = wl.B * wl.T * K * world
+    return {"value": round(tokens / (ms * 1e-3), 1), "unit": "tokens/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": K,
+            "ms_per_step": round(ms / K, 4)}
+
+
+def run_single(args, wl, dev, world):
+    """Single depth aggregation workloads (for profiling; not the headline line)."""
+    from transformer_depth_wise_gb300 import api
+    inp = wk.single_aggregation_inputs(wl, device=dev, rows=args.rows or None)
+    out = torch.empty_like(inp["sources"][0])
+    for _ in range(args.warmup):
+        api.depth_aggregate(inp["sources"], inp["query"], inp["gain"], inp["eps"], out=out)
+    torch.cuda.synchronize(dev)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    times = []
+    for _ in range(args.steps):
+        flush.zero_()  # L2 flush between timed launches
+        a.record()
+        api.depth_aggregate(inp["sources"], inp["query"], inp["gain"], inp["eps"], out=out)
+        b.record()
+        torch.cuda.synchronize(dev)
+        times.append(a.elapsed_time(b))
+    rows = inp["sources"][0].numel() // wl.D
+    byts = accounting.aggregate_bytes(len(inp["sources"]), rows, wl.D, inp["sources"][0].element_size())
+    ms = statistics.median(times)
+    peak, src = measured_peak()
+    gbs = byts / (ms * 1e-3) / 1e9
+    return {"metric": "depth aggregation tokens/s", "value": round(rows / (ms * 1e-3), 1),
+            "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16" if wl.dtype == torch.bfloat16 else "f32",
+            "data": "synthetic", "config": {"workload": wl.name, "rows": rows, "D": wl.D,
+                                            "n": len(inp["sources"]), "l2": "flushed between launches"},
+            "roofline": {"bound": "hbm", "kernel": "aggregate", "achieved": round(gbs, 1),
+                         "peak": peak, "unit": "GB/s", "frac": round(gbs / peak, 4),
+                         "traffic": None, "peak_source": src}}
+
+
+def run_full_stack(args, wl, dev, world):
+    from transformer_depth_wise_gb300 import api
+    inp = wk.full_stack_inputs(wl, device=dev, rows=args.rows or None)
+    srcs = [inp["v0"]] + [torch.empty_like(inp["v0"]) for _ in range(wl.L)]
+    y = torch.empty_like(inp["v0"])
+    for _ in range(args.warmup):
+        api.full_stack_forward(inp["v0"], inp["queries"], inp["gains"], inp["u"], inp["eps"], srcs, y)
+    torch.cuda.synchronize(dev)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(args.steps):
+        api.full_stack_forward(inp["v0"], inp["queries"], inp["gains"], inp["u"], inp["eps"], srcs, y)
+    b.record()
+    torch.cuda.synchronize(dev)
+    ms = a.elapsed_time(b) / args.steps
+    rows = inp["v0"].numel() // wl.D
+    byts = accounting.full_stack_bytes(wl.L, rows, wl.D, 2)
+    peak, src = measured_peak()
+    gbs = byts / (ms * 1e-3) / 1e9
+    return {"metric": "Full AttnRes stack forward tokens/s", "value": round(rows / (ms * 1e-3), 1),
+            "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": wl.name, "rows": rows, "D": wl.D, "L": wl.L},
+            "roofline": {"bound": "hbm", "kernel": "aggregate (fused f)", "achieved": round(gbs, 1),
+                         "peak": peak, "unit": "GB/s", "frac": round(gbs / peak, 4),
+                         "traffic": None, "peak_source": src}}
+
+
+def cpu_baseline_block(wl):
+    v, dt, sample = oracle_block_rows_per_s(wl)
+    return {"value": round(v, 3), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": sample, "seconds": round(dt, 2)}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--workload", default="two_phase_bf16", choices=sorted(wk.WORKLOADS))
+    ap.add_argument("--rows", type=int, default=0, help="shrink to B=1, T=rows (profiling)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    wl = wk.WORKLOADS[args.workload]
+
+    rank, local, world = dist_setup()
+
+    if args.impl == "reference":
+        # The reference arm is the fp64 CPU oracle, on rank 0 only.
+        if rank == 0:
+            rates = []
+            for _ in range(args.warmup):
+                pass
+            t_total = 0.0
+            for _ in range(max(1, args.steps)):
+                v, dt, sample = oracle_block_rows_per_s(wl, rows_target_s=max(1.0, 60.0 / max(1, args.steps)))
+                rates.append(v)
+                t_total += dt
+            value = statistics.mean(rates)
+            line = {"impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "tokens/s",
+                    "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+                    "ms_per_step": round(t_total / max(1, args.steps) * 1e3, 2),
+                    "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                    "data": "synthetic",
+                    "config": {"workload": wl.name, "B": wl.B, "T": wl.T, "D": wl.D, "S": wl.S},
+                    "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "cores": 1,
+                                     "kind": "oracle", "sample": sample},
+                    "e2e": {"value": round(value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                            "d2h_bytes_per_step": 0}}
+            print(json.dumps(line), flush=True)
+        return
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU (the CUDA path has no CPU fallback)")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    from transformer_depth_wise_gb300 import _lib
+    _lib.lib()
+
+    if wl.name in ("two_phase_bf16", "long_prefill_bf16", "decode_bf16"):
+        res = run_two_phase(args, wl, dev, rank, world)
+    elif wl.name == "full_stack_bf16":
+        res = run_full_stack(args, wl, dev, world)
+    else:
+        res = run_single(args, wl, dev, world)
+
+    if rank == 0:
+        if not args.no_cpu_baseline and "two_phase" in wl.name and world == 1:
+            res["cpu_baseline"] = cpu_baseline_block(wl)
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

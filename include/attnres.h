@@ -1,0 +1,182 @@
+/*
+ * attnres.h -- C ABI of libattnres.so, the GB300 (sm_103a) hot path of
+ * Attention Residuals: the depth-wise softmax aggregation of earlier layer
+ * (or block) outputs, in its Full, Block and two-phase Block forms.
+ *
+ * The method (pages: "Attention Residual 深度残差", K3 course notes sec-09;
+ * "Attention Residuals：当网络深度也拥有寻址能力"):
+ *   A1  s_i   = w~^T RMS(v_i),  w~ = w (.) gamma (gain folded into the query),
+ *             RMS(v) = v / sqrt(mean_d v^2 + eps)  (no gain)
+ *   A2  alpha = softmax_i(s_i)  per token (b, t), over the source axis
+ *   A3  h     = sum_i alpha_i v_i  over the RAW (un-normalised) sources
+ *   OS1 (m, numer, denom) online-softmax state;  OS2 merge of two states.
+ *
+ * Conventions shared by every compute entry point:
+ *   - Token rows: a source, output or partial is a row-major [B, T, D]
+ *     tensor in device memory, rows contiguous with stride D.  Depth
+ *     attention never mixes tokens, so the kernels treat it as B*T
+ *     independent rows.
+ *   - dtype: ATTNRES_F32 or ATTNRES_BF16 for every [B,T,D] tensor of one
+ *     call.  Queries, gains, u and all statistics are fp32.  Arithmetic is
+ *     fp32; outputs are rounded once (to nearest even) to the I/O dtype.
+ *   - Alignment: every device pointer is 16-byte aligned and D is a
+ *     multiple of 8 (bf16) or 4 (fp32), so rows move as 16-byte vectors.
+ *   - gain == NULL means a gain of one.
+ *   - Statistics: m is the max depth score of a token, lse = m + ln(sum_i
+ *     exp(s_i - m)) (natural log).  Outputs named "optional" may be NULL.
+ *   - Ownership: the caller allocates and owns every buffer.  The library
+ *     allocates no device memory, keeps no state between calls and never
+ *     synchronises: work is queued on `stream` (a cudaStream_t; NULL is
+ *     the legacy default stream) and the call returns.
+ *   - Errors: arguments are checked before anything is launched; a bad
+ *     argument returns a negative attnres_status_t and launches nothing.
+ *     A launch failure returns ATTNRES_ERR_CUDA.  Nothing aborts or prints.
+ *   - Empty inputs (B*T == 0) are valid and launch nothing.
+ */
+#ifndef ATTNRES_H
+#define ATTNRES_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { ATTNRES_F32 = 0, ATTNRES_BF16 = 1 } attnres_dtype_t;
+
+typedef enum {
+    ATTNRES_OK = 0,
+    ATTNRES_ERR_NULL = -1,             /* a required pointer is NULL                 */
+    ATTNRES_ERR_SHAPE = -2,            /* n, S, L, B, T or D out of range           */
+    ATTNRES_ERR_DTYPE = -3,            /* dtype is not F32 / BF16                    */
+    ATTNRES_ERR_ALIGNMENT = -4,        /* pointer not 16-B aligned, or D % vec != 0  */
+    ATTNRES_ERR_TOO_MANY_SOURCES = -5, /* n > ATTNRES_MAX_SOURCES                    */
+    ATTNRES_ERR_CUDA = -6,             /* a kernel launch failed                     */
+    ATTNRES_ERR_CAPACITY = -7,         /* a host output buffer is too small          */
+    ATTNRES_ERR_VALUE = -8             /* eps negative / not finite, block size 0    */
+} attnres_status_t;
+
+/* Most sources one aggregation may read (Full stack: L + 1 <= this). */
+#define ATTNRES_MAX_SOURCES 256
+/* Most queries one phase-1 call may batch (S). */
+#define ATTNRES_MAX_QUERIES 64
+
+/*
+ * Depth aggregation, eq. A1-A3 ("DepthResidual.forward"; the pages'
+ * "block_attn_res" for the Block form, where the sources are the completed
+ * block summaries followed by the running partial).
+ *   sources  host array of n device pointers, each [B,T,D] of `dtype`
+ *   n        1 .. ATTNRES_MAX_SOURCES
+ *   query    device fp32 [D] (w); gain device fp32 [D] or NULL
+ *   eps      >= 0, added to the mean square inside the square root
+ *   out      device [B,T,D] of `dtype`: h = sum_i alpha_i v_i
+ *   out_max, out_lse  device fp32 [B,T], optional
+ * Sources are read once each, as an online softmax over the source axis.
+ */
+int attnres_depth_aggregate(const void *const *sources, int n, int64_t B, int64_t T, int64_t D,
+                            int dtype, const float *query, const float *gain, float eps, void *out,
+                            float *out_max, float *out_lse, void *stream);
+
+/*
+ * Phase 1 of the two-phase Block scheme ("两阶段算法（inter / intra）",
+ * inter step; "attn_with_stats"): the S pseudo-queries of one block score
+ * the same n completed block summaries in one pass.
+ *   blocks   host array of n_blocks device pointers, each [B,T,D]
+ *   queries  device fp32 [S,D]; gains device fp32 [S,D] or NULL
+ *   S        1 .. ATTNRES_MAX_QUERIES
+ *   out      device [S,B,T,D] of `dtype`: out[s] = normalised output o_s
+ *   out_lse  device fp32 [S,B,T], required (phase 2 consumes it)
+ *   out_max  device fp32 [S,B,T], optional
+ * Each summary is read from HBM once for all S queries.
+ */
+int attnres_block_phase1(const void *const *blocks, int n_blocks, int64_t B, int64_t T, int64_t D,
+                         int dtype, const float *queries, const float *gains, int S, float eps,
+                         void *out, float *out_max, float *out_lse, void *stream);
+
+/*
+ * Phase 2 of the two-phase Block scheme (intra step): merge the running
+ * intra-block partial p, as a single source with state (s_p, p, 1)
+ * ("single_source_stats"), into the phase-1 state of this sublayer's
+ * query by eq. OS2, then normalise:
+ *   M = max(lse, s_p),  h = (e^{lse-M} o + e^{s_p-M} p) / (e^{lse-M} + e^{s_p-M}).
+ *   inter_out  device [B,T,D]: phase-1 output o of this sublayer's query
+ *   inter_lse  device fp32 [B,T]: its lse
+ *   partial    device [B,T,D], or NULL for the first sublayer of a block,
+ *              in which case h = o (and out_lse = inter_lse)
+ *   query, gain  as in attnres_depth_aggregate (the same query phase 1 used)
+ *   h_out      device [B,T,D]; may not alias inter_out or partial
+ *   out_lse    device fp32 [B,T], optional: the merged lse
+ */
+int attnres_block_phase2_merge(const void *inter_out, const float *inter_lse, const void *partial,
+                               int64_t B, int64_t T, int64_t D, int dtype, const float *query,
+                               const float *gain, float eps, void *h_out, float *out_lse,
+                               void *stream);
+
+/*
+ * Running intra-block partial update ("forward_naive": partial = out, or
+ * partial + out) with the benchmark recipes' synthetic sublayer
+ * f(h) = 0.5 * tanh(u (.) h) standing in for the model's attention / FFN:
+ *   partial_out = (partial_in ? partial_in : 0) + 0.5 * tanh(u (.) h)
+ * computed in fp32 and rounded once.
+ *   h          device [B,T,D] (the sublayer input)
+ *   partial_in device [B,T,D] or NULL (first sublayer of a block)
+ *   u          device fp32 [D]
+ *   partial_out device [B,T,D]; may alias partial_in (in-place update)
+ */
+int attnres_partial_update(const void *h, const void *partial_in, const float *u, int64_t B,
+                           int64_t T, int64_t D, int dtype, void *partial_out, void *stream);
+
+/*
+ * Full AttnRes stack forward ("FullAttnResStack", eq. A1-A4) with the
+ * synthetic sublayer f_l(h) = 0.5 * tanh(u_l (.) h):
+ *   for l = 1..L:  h_l = aggregate(v_0..v_{l-1}; query_l, gain_l)
+ *                  v_l = f_l(h_l)            (written to sources[l])
+ *   y = aggregate(v_0..v_L; query_L, gain_L)  (the final aggregate)
+ * h_l never leaves the kernel: f_l is applied in its epilogue to the fp32
+ * h_l, and only v_l is rounded and stored.
+ *   sources  host array of L+1 device pointers [B,T,D]: sources[0] = v_0 is
+ *            read, sources[1..L] are written
+ *   L        1 .. ATTNRES_MAX_SOURCES - 1
+ *   queries  device fp32 [L+1, D] (row l-1 for sublayer l, row L final)
+ *   gains    device fp32 [L+1, D] or NULL;  u  device fp32 [L, D]
+ *   y_out    device [B,T,D]
+ */
+int attnres_full_stack_forward(void *const *sources, int L, int64_t B, int64_t T, int64_t D,
+                               int dtype, const float *queries, const float *gains, const float *u,
+                               float eps, void *y_out, void *stream);
+
+/*
+ * Host-only bookkeeping ("BlockAttnResStack.forward_naive"): the sources each
+ * atomic sublayer attends over, for num_atomic sublayers in blocks of
+ * block_size.  Block 0 is the embedding; a block boundary falls after
+ * sublayer idx (1-based) when idx % block_size == 0 or idx == num_atomic,
+ * and the partial sum then becomes a new block.  The first sublayer of a
+ * block sees only the completed blocks; later ones also see the partial.
+ *   n_sources_per_layer  host int [num_atomic + 1]; the last entry is the
+ *                        final aggregate over all blocks
+ *   source_ids           host int [capacity], flat: block id >= 0, or -1
+ *                        for the running partial
+ * Returns the number of ids written (>= 0), ATTNRES_ERR_CAPACITY if
+ * `capacity` is too small, ATTNRES_ERR_SHAPE / _VALUE / _NULL on bad input.
+ */
+int attnres_block_schedule(int num_atomic, int block_size, int *n_sources_per_layer,
+                           int *source_ids, int capacity);
+
+/*
+ * Config helper ("atomic_block_size"): the block size in DecoderBlocks of
+ * the config, converted to atomic sublayers (x2: attention + FFN).
+ * attnres_block_size < 0 means "unset": about eight blocks,
+ * max(1, ceil(num_hidden_layers / 8)) DecoderBlocks each.  A block size of
+ * 0 is invalid (ATTNRES_ERR_VALUE); num_hidden_layers < 1 is
+ * ATTNRES_ERR_SHAPE.
+ */
+int attnres_atomic_block_size(int num_hidden_layers, int attnres_block_size);
+
+/* Static, human-readable name of a status code. */
+const char *attnres_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTNRES_H */

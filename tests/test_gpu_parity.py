@@ -1,0 +1,286 @@
+"""GPU parity: every entry point of libattnres.so against the fp64 oracle.
+
+Inputs come from transformer_depth_wise_gb300.workloads (seeded); the oracle
+sees the exact same values widened to float64.  Tolerances (max |error|):
+fp32 I/O 1e-5 * max|v|, bf16 I/O 8e-3 * max|v|, max|v| over the call's
+input sources; statistics (m, lse) 2e-5 * max(1, |lse|).  Small cases span
+several CTAs and a ragged tail of rows; full-size cases run the launch the
+benchmark times and compare sampled token rows, which the oracle computes
+one by one (depth attention never mixes tokens).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from transformer_depth_wise_gb300 import api
+from transformer_depth_wise_gb300 import workloads as wk
+
+pytestmark = pytest.mark.gpu
+
+TOL = {torch.float32: 1e-5, torch.bfloat16: 8e-3}
+ODT = {torch.float32: oracle.F32, torch.bfloat16: oracle.BF16}
+
+
+def f64(t):
+    return t.detach().double().cpu().numpy()
+
+
+def vmax(tensors):
+    return max(float(t.abs().max()) for t in tensors)
+
+
+def check(got, want, tol_abs, what=""):
+    err = float(np.max(np.abs(f64(got) - want))) if want.size else 0.0
+    assert err <= tol_abs, f"{what}: max |err| {err:.3e} > {tol_abs:.3e}"
+    return err
+
+
+def check_stats(got, want, what=""):
+    g = f64(got)
+    err = np.abs(g - want) / np.maximum(1.0, np.abs(want))
+    assert float(err.max()) <= 2e-5, f"{what}: stats rel err {float(err.max()):.3e}"
+
+
+def rand_sources(n, shape, dtype, dev, seed, lo=0.5, hi=8.0):
+    g = wk.generator(seed, dev)
+    srcs, _ = wk.scaled_normal_sources(g, n, shape, lo, hi, dtype, dev)
+    w, gam = wk.queries_and_gains(g, 1, shape[-1], dev)
+    return srcs, w[0].contiguous(), gam[0].contiguous()
+
+
+# --------------------------------------------------------------------------
+# depth aggregation
+# --------------------------------------------------------------------------
+def test_aggregate_full_single_f32_config(gpu):
+    wl = wk.WORKLOADS["full_single_f32"]
+    for zero in (False, True):
+        inp = wk.single_aggregation_inputs(wl, device=gpu, zero_query=zero)
+        out, m, lse = api.depth_aggregate(inp["sources"], inp["query"], inp["gain"], inp["eps"],
+                                          stats=True)
+        V = np.stack([f64(s) for s in inp["sources"]])
+        h, om, olse = oracle.depth_aggregate(V, f64(inp["query"]), f64(inp["gain"]), inp["eps"])
+        tol = TOL[torch.float32] * vmax(inp["sources"])
+        check(out, oracle.round_to(h, oracle.F32), tol, "cfg1")
+        check_stats(m, om, "m")
+        check_stats(lse, olse, "lse")
+        if zero:   # zero query: the mean of the sources
+            check(out, V.mean(0), tol, "zero query mean")
+
+
+CASES = [  # (dtype, D, n, rows) -- covers warp teams of 4..32 lanes and CTA teams, ragged rows
+    (torch.bfloat16, 8, 3, 37), (torch.bfloat16, 24, 2, 65), (torch.bfloat16, 64, 5, 33),
+    (torch.bfloat16, 256, 4, 129), (torch.bfloat16, 520, 7, 19), (torch.bfloat16, 1032, 9, 23),
+    (torch.bfloat16, 2048, 10, 300), (torch.bfloat16, 4096, 9, 41), (torch.bfloat16, 7168, 10, 17),
+    (torch.bfloat16, 8192, 3, 5), (torch.float32, 4, 2, 9), (torch.float32, 12, 5, 50),
+    (torch.float32, 256, 5, 64), (torch.float32, 264, 6, 31), (torch.float32, 4096, 4, 13),
+]
+
+
+@pytest.mark.parametrize("dtype,D,n,rows", CASES)
+def test_aggregate_shapes(gpu, dtype, D, n, rows):
+    srcs, q, g = rand_sources(n, (1, rows, D), dtype, gpu, seed=D * 31 + n * 7 + rows)
+    out, m, lse = api.depth_aggregate(srcs, q, g, 1e-8, stats=True)
+    V = np.stack([f64(s) for s in srcs])
+    h, om, olse = oracle.depth_aggregate(V, f64(q), f64(g), 1e-8)
+    check(out, oracle.round_to(h, ODT[dtype]), TOL[dtype] * vmax(srcs), f"D={D} n={n}")
+    check_stats(lse, olse, "lse")
+    check_stats(m, om, "m")
+
+
+def test_aggregate_one_source_is_identity_bitwise(gpu):
+    for dtype, D in ((torch.bfloat16, 2048), (torch.float32, 256), (torch.bfloat16, 40)):
+        srcs, q, g = rand_sources(1, (2, 33, D), dtype, gpu, seed=5)
+        out = api.depth_aggregate(srcs, q, g, 1e-8)
+        assert torch.equal(out, srcs[0])
+
+
+def test_aggregate_no_mixing_across_tokens_bitwise(gpu):
+    srcs, q, g = rand_sources(10, (4, 64, 2048), torch.bfloat16, gpu, seed=11)
+    out0 = api.depth_aggregate(srcs, q, g, 1e-8).clone()
+    srcs2 = [s.clone() for s in srcs]
+    for s in srcs2:
+        s[2, 17] = -s[2, 17] * 3
+    out1 = api.depth_aggregate(srcs2, q, g, 1e-8)
+    mask = torch.ones(4, 64, dtype=torch.bool, device=gpu)
+    mask[2, 17] = False
+    assert torch.equal(out0[mask], out1[mask])
+    assert not torch.equal(out0[2, 17], out1[2, 17])
+
+
+def test_aggregate_empty_rows_is_a_noop(gpu):
+    srcs = [torch.empty((0, 5, 256), dtype=torch.bfloat16, device=gpu) for _ in range(3)]
+    q = torch.zeros(256, device=gpu)
+    out = api.depth_aggregate(srcs, q, None, 1e-8)
+    assert out.shape == (0, 5, 256)
+
+
+def test_aggregate_many_sources(gpu):
+    srcs, q, g = rand_sources(187, (1, 9, 256), torch.bfloat16, gpu, seed=187)
+    out = api.depth_aggregate(srcs, q, g, 1e-8)
+    h, _, _ = oracle.depth_aggregate(np.stack([f64(s) for s in srcs]), f64(q), f64(g), 1e-8)
+    check(out, h, TOL[torch.bfloat16] * vmax(srcs), "n=187")
+
+
+def pick(t, rows, D):
+    """Rows (numpy indices) of a [.., D] CUDA tensor viewed as [rows, D]."""
+    return t.reshape(-1, D)[torch.as_tensor(rows, device=t.device)]
+
+
+def sample_rows(B, T, k, seed):
+    rng = np.random.default_rng(seed)
+    rows = {0, B * T - 1}
+    for b in range(B):
+        rows |= {b * T, b * T + T - 1}
+    rows |= set(rng.integers(0, B * T, size=k).tolist())
+    return np.array(sorted(rows))
+
+
+def test_aggregate_block_single_full_size_sampled(gpu):
+    wl = wk.WORKLOADS["block_single_bf16"]
+    inp = wk.single_aggregation_inputs(wl, device=gpu)
+    out, m, lse = api.depth_aggregate(inp["sources"], inp["query"], inp["gain"], inp["eps"], stats=True)
+    rows = sample_rows(wl.B, wl.T, 48, 2)
+    V = np.stack([f64(pick(s, rows, wl.D)) for s in inp["sources"]])
+    h, om, olse = oracle.depth_aggregate(V, f64(inp["query"]), f64(inp["gain"]), inp["eps"])
+    check(pick(out, rows, wl.D), h, TOL[torch.bfloat16] * vmax(inp["sources"]), "cfg2")
+    check_stats(lse.reshape(-1)[torch.as_tensor(rows, device=gpu)], olse, "lse")
+
+
+# --------------------------------------------------------------------------
+# two-phase Block: phase 1, phase 2 merge, partial update, one block chain
+# --------------------------------------------------------------------------
+@pytest.mark.parametrize("dtype,D,n,S,rows", [
+    (torch.bfloat16, 4096, 9, 24, 37), (torch.bfloat16, 512, 3, 5, 130),
+    (torch.bfloat16, 7168, 9, 4, 9), (torch.float32, 256, 5, 7, 66), (torch.bfloat16, 64, 1, 3, 20),
+    (torch.bfloat16, 2048, 16, 2, 11),
+])
+def test_phase1_small(gpu, dtype, D, n, S, rows):
+    g = wk.generator(D + n + S, gpu)
+    blocks, _ = wk.scaled_normal_sources(g, n, (1, rows, D), 0.5, 8.0, dtype, gpu)
+    W, G = wk.queries_and_gains(g, S, D, gpu)
+    o, m, lse = api.block_phase1(blocks, W, G, 1e-8, want_max=True)
+    O, M, LSE = oracle.block_phase1([f64(b) for b in blocks], f64(W), f64(G), 1e-8)
+    tol = TOL[dtype] * vmax(blocks)
+    check(o.reshape(S, -1, D), oracle.round_to(O, ODT[dtype]), tol, "phase1 o")
+    check_stats(lse.reshape(S, -1), LSE, "phase1 lse")
+    check_stats(m.reshape(S, -1), M, "phase1 m")
+
+
+def test_phase1_two_phase_config_full_size_sampled(gpu):
+    wl = wk.WORKLOADS["two_phase_bf16"]
+    inp = wk.two_phase_inputs(wl, device=gpu)
+    o, _, lse = api.block_phase1(inp["blocks"], inp["queries"], inp["gains"], inp["eps"])
+    rows = sample_rows(wl.B, wl.T, 24, 3)
+    O, _, LSE = oracle.block_phase1([f64(pick(b, rows, wl.D)) for b in inp["blocks"]],
+                                    f64(inp["queries"]), f64(inp["gains"]), inp["eps"])
+    ix = torch.as_tensor(rows, device=gpu)
+    check(o.reshape(wl.S, -1, wl.D)[:, ix], O, TOL[torch.bfloat16] * vmax(inp["blocks"]), "cfg3 p1")
+    check_stats(lse.reshape(wl.S, -1)[:, ix], LSE, "cfg3 lse")
+
+
+def test_phase2_merge_small(gpu):
+    for dtype, D, rows in ((torch.bfloat16, 4096, 45), (torch.float32, 256, 70), (torch.bfloat16, 16, 33)):
+        g = wk.generator(D + rows, gpu)
+        (o, p), _ = wk.scaled_normal_sources(g, 2, (1, rows, D), 0.5, 8.0, dtype, gpu)
+        W, G = wk.queries_and_gains(g, 1, D, gpu)
+        lse = torch.empty(rows, device=gpu).normal_(0.0, 2.0, generator=g)
+        lse_out = torch.empty_like(lse)
+        h = api.block_phase2_merge(o, lse, p, W[0], G[0], 1e-8, out_lse=lse_out)
+        want, wl = oracle.block_phase2_merge(f64(o).reshape(rows, D), f64(lse), f64(p).reshape(rows, D),
+                                             f64(W[0]), f64(G[0]), 1e-8)
+        check(h.reshape(rows, D), oracle.round_to(want, ODT[dtype]), TOL[dtype] * vmax([o, p]), "merge")
+        check_stats(lse_out, wl, "merged lse")
+        h0 = api.block_phase2_merge(o, lse, None, W[0], G[0], 1e-8, out_lse=lse_out)
+        assert torch.equal(h0, o) and torch.equal(lse_out, lse)
+
+
+def test_partial_update(gpu):
+    for dtype, D, rows in ((torch.bfloat16, 4096, 21), (torch.float32, 12, 7)):
+        g = wk.generator(D, gpu)
+        (h, p), _ = wk.scaled_normal_sources(g, 2, (1, rows, D), 0.5, 3.0, dtype, gpu)
+        u = wk.sublayer_u(g, 1, D, gpu)[0].contiguous()
+        f = oracle.synthetic_sublayer(f64(u), f64(h).reshape(rows, D))
+        first = api.partial_update(h, None, u)
+        check(first.reshape(rows, D), oracle.round_to(f, ODT[dtype]), TOL[dtype] * 0.5, "update first")
+        want = oracle.round_to(f64(p).reshape(rows, D) + f, ODT[dtype])
+        pin = p.clone()
+        api.partial_update(h, pin, u, out=pin)                  # in place
+        check(pin.reshape(rows, D), want, TOL[dtype] * vmax([p]), "update in place")
+
+
+def test_two_phase_block_chain_small(gpu):
+    D, n, S, rows = 1024, 9, 6, 50
+    g = wk.generator(77, gpu)
+    blocks, _ = wk.scaled_normal_sources(g, n, (1, rows, D), 0.5, 8.0, torch.bfloat16, gpu)
+    W, G = wk.queries_and_gains(g, S, D, gpu)
+    U = wk.sublayer_u(g, S, D, gpu)
+    p, H = api.block_two_phase(blocks, W, G, U, 1e-8)
+    OH, OP = oracle.block_two_phase_chain([f64(b) for b in blocks], f64(W), f64(G), f64(U), 1e-8,
+                                          oracle.BF16)
+    tol = TOL[torch.bfloat16] * vmax(blocks)
+    check(H.reshape(S, rows, D), OH, tol, "chain h")
+    check(p.reshape(rows, D), OP, tol, "chain p")
+
+
+def test_two_phase_block_chain_full_size_sampled(gpu):
+    wl = wk.WORKLOADS["two_phase_bf16"]
+    inp = wk.two_phase_inputs(wl, device=gpu)
+    blk = api.TwoPhaseBlock(inp["blocks"], inp["queries"], inp["gains"], inp["u"], inp["eps"])
+    p = blk.run()
+    torch.cuda.synchronize()
+    rows = sample_rows(wl.B, wl.T, 16, 4)
+    _, OP = oracle.block_two_phase_chain([f64(pick(b, rows, wl.D)) for b in inp["blocks"]],
+                                         f64(inp["queries"]), f64(inp["gains"]), f64(inp["u"]),
+                                         inp["eps"], oracle.BF16)
+    check(pick(p, rows, wl.D), OP, TOL[torch.bfloat16] * vmax(inp["blocks"]), "cfg3 chain")
+
+
+@pytest.mark.parametrize("name", ["long_prefill_bf16", "decode_bf16"])
+def test_d7168_configs_sampled(gpu, name):
+    wl = wk.WORKLOADS[name]
+    inp = wk.single_aggregation_inputs(wl, device=gpu)
+    out = api.depth_aggregate(inp["sources"], inp["query"], inp["gain"], inp["eps"])
+    rows = sample_rows(wl.B, wl.T, 12, 5)
+    V = np.stack([f64(pick(s, rows, wl.D)) for s in inp["sources"]])
+    h, _, _ = oracle.depth_aggregate(V, f64(inp["query"]), f64(inp["gain"]), inp["eps"])
+    check(pick(out, rows, wl.D), h, TOL[torch.bfloat16] * vmax(inp["sources"]), name)
+    del out, inp
+    tp = wk.two_phase_inputs(wl, device=gpu)           # 9 summaries + S = 24 chain
+    blk = api.TwoPhaseBlock(tp["blocks"], tp["queries"], tp["gains"], tp["u"], tp["eps"])
+    p = blk.run()
+    torch.cuda.synchronize()
+    _, OP = oracle.block_two_phase_chain([f64(pick(b, rows, wl.D)) for b in tp["blocks"]],
+                                         f64(tp["queries"]), f64(tp["gains"]), f64(tp["u"]),
+                                         tp["eps"], oracle.BF16)
+    check(pick(p, rows, wl.D), OP, TOL[torch.bfloat16] * vmax(tp["blocks"]), name + " chain")
+
+
+# --------------------------------------------------------------------------
+# Full stack
+# --------------------------------------------------------------------------
+def test_full_stack_small(gpu):
+    for dtype, D, L, rows in ((torch.bfloat16, 256, 12, 40), (torch.float32, 128, 7, 19)):
+        wl = wk.WORKLOADS["full_stack_bf16"]
+        inp = wk.full_stack_inputs(wl, rows=rows, device=gpu, L=L, D=D)
+        v0 = inp["v0"].to(dtype)
+        y, srcs = api.full_stack_forward(v0, inp["queries"], inp["gains"], inp["u"], inp["eps"])
+        V, oy = oracle.full_stack_forward(f64(v0).reshape(rows, D), f64(inp["queries"]),
+                                          f64(inp["gains"]), f64(inp["u"]), inp["eps"], ODT[dtype])
+        tol = TOL[dtype] * float(v0.abs().max())
+        for l in range(1, L + 1):
+            check(srcs[l].reshape(rows, D), V[l], tol, f"v_{l}")
+        check(y.reshape(rows, D), oracle.round_to(oy, ODT[dtype]), tol, "y")
+
+
+def test_full_stack_config_full_size_sampled(gpu):
+    wl = wk.WORKLOADS["full_stack_bf16"]
+    inp = wk.full_stack_inputs(wl, device=gpu)
+    y, srcs = api.full_stack_forward(inp["v0"], inp["queries"], inp["gains"], inp["u"], inp["eps"])
+    rows = sample_rows(wl.B, wl.T, 6, 6)
+    V, oy = oracle.full_stack_forward(f64(pick(inp["v0"], rows, wl.D)), f64(inp["queries"]),
+                                      f64(inp["gains"]), f64(inp["u"]), inp["eps"], oracle.BF16)
+    tol = TOL[torch.bfloat16] * float(inp["v0"].abs().max())
+    for l in (1, 2, 50, 186):
+        check(pick(srcs[l], rows, wl.D), V[l], tol, f"v_{l}")
+    check(pick(y, rows, wl.D), oy, tol, "y")

@@ -1,0 +1,193 @@
+"""CPU-only checks of libattnres.so: it loads, exports every declared symbol,
+rejects bad arguments before launching anything, and its host bookkeeping
+matches the oracle bit for bit.  No compute entry point runs here."""
+import ctypes
+import json
+import math
+import os
+import re
+
+import pytest
+
+import oracle
+from transformer_depth_wise_gb300 import _lib, accounting, api
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+FAKE = 0x7F0000000000      # 16-byte aligned stand-in for a device pointer (never dereferenced)
+OK, NULL, SHAPE, DTYPE, ALIGN, MANY, CUDA, CAP, VALUE = 0, -1, -2, -3, -4, -5, -6, -7, -8
+
+
+def declared_symbols():
+    text = open(os.path.join(ROOT, "include", "attnres.h")).read()
+    return sorted(set(re.findall(r"^(?:int|const char \*)\s*(attnres_\w+)\(", text, re.M)))
+
+
+def test_library_exports_every_declared_symbol():
+    L = _lib.lib()
+    names = declared_symbols()
+    assert len(names) >= 8
+    for n in names:
+        assert hasattr(L, n), n
+    assert set(names) == set(_lib.SIGNATURES)
+
+
+def test_status_strings():
+    L = _lib.lib()
+    for code in _lib.STATUS:
+        s = L.attnres_status_string(code).decode()
+        assert s and s != "unknown status"
+    assert L.attnres_status_string(12345).decode() == "unknown status"
+
+
+def agg(sources, n=None, B=2, T=3, D=64, dtype=1, q=FAKE, g=None, eps=1e-8, out=FAKE):
+    L = _lib.lib()
+    arr = None if sources is None else _lib.ptr_array(sources)
+    return L.attnres_depth_aggregate(arr, len(sources) if n is None else n, B, T, D, dtype, q, g, eps,
+                                     out, None, None, None)
+
+
+def test_depth_aggregate_argument_checks():
+    assert agg([FAKE] * 3, dtype=7) == DTYPE
+    assert agg([FAKE] * 3, D=0) == SHAPE
+    assert agg([FAKE] * 3, B=-1) == SHAPE
+    assert agg([FAKE] * 3, D=36, dtype=1) == ALIGN           # bf16 needs D % 8 == 0
+    assert agg([FAKE] * 3, D=34, dtype=0) == ALIGN           # fp32 needs D % 4 == 0
+    assert agg(None, n=3) == NULL
+    assert agg([FAKE] * 3, q=None) == NULL
+    assert agg([FAKE] * 3, out=None) == NULL
+    assert agg([FAKE, 0, FAKE]) == NULL
+    assert agg([FAKE] * 3, n=0) == SHAPE
+    assert agg([FAKE] * 257) == MANY
+    assert agg([FAKE] * 3, eps=-1.0) == VALUE
+    assert agg([FAKE] * 3, eps=math.nan) == VALUE
+    assert agg([FAKE] * 3, eps=math.inf) == VALUE
+    assert agg([FAKE, FAKE + 8, FAKE]) == ALIGN
+    assert agg([FAKE] * 3, q=FAKE + 4) == ALIGN
+    assert agg([FAKE] * 3, g=FAKE + 4) == ALIGN
+    assert agg([FAKE] * 3, D=16384, dtype=1) == SHAPE        # beyond the kernel family
+    assert agg([FAKE] * 3, B=0) == OK                         # empty: nothing launched
+    assert agg([FAKE] * 3, T=0) == OK
+
+
+def test_phase1_argument_checks():
+    L = _lib.lib()
+    arr = _lib.ptr_array([FAKE] * 9)
+
+    def p1(n=9, S=24, lse=FAKE, out=FAKE, B=1, D=4096, dtype=1, q=FAKE):
+        return L.attnres_block_phase1(arr, n, B, 4, D, dtype, q, None, S, 1e-8, out, None, lse, None)
+
+    assert p1(lse=None) == NULL
+    assert p1(out=None) == NULL
+    assert p1(q=None) == NULL
+    assert p1(S=0) == SHAPE
+    assert p1(S=65) == SHAPE
+    assert p1(n=0) == SHAPE
+    assert p1(D=4100) == ALIGN
+    assert p1(B=0) == OK
+
+
+def test_merge_and_update_argument_checks():
+    L = _lib.lib()
+    m = L.attnres_block_phase2_merge
+    assert m(None, FAKE, FAKE, 1, 2, 64, 1, FAKE, None, 1e-8, FAKE, None, None) == NULL
+    assert m(FAKE, None, FAKE, 1, 2, 64, 1, FAKE, None, 1e-8, FAKE, None, None) == NULL
+    assert m(FAKE, FAKE, FAKE + 2, 1, 2, 64, 1, FAKE, None, 1e-8, FAKE, None, None) == ALIGN
+    assert m(FAKE, FAKE, FAKE, 1, 2, 64, 1, FAKE, None, -1.0, FAKE, None, None) == VALUE
+    assert m(FAKE, FAKE, None, 0, 2, 64, 1, FAKE, None, 1e-8, FAKE, None, None) == OK
+    u = L.attnres_partial_update
+    assert u(FAKE, None, None, 1, 2, 64, 1, FAKE, None) == NULL
+    assert u(FAKE, None, FAKE, 1, 2, 60, 1, FAKE, None) == ALIGN
+    assert u(FAKE, None, FAKE, 1, 0, 64, 1, FAKE, None) == OK
+
+
+def test_full_stack_argument_checks():
+    L = _lib.lib()
+    f = L.attnres_full_stack_forward
+    arr = _lib.ptr_array([FAKE] * 5)
+    assert f(arr, 0, 1, 2, 64, 1, FAKE, None, FAKE, 1e-8, FAKE, None) == SHAPE
+    assert f(arr, 4, 1, 2, 64, 1, FAKE, None, None, 1e-8, FAKE, None) == NULL
+    big = _lib.ptr_array([FAKE] * 257)
+    assert f(big, 256, 1, 2, 64, 1, FAKE, None, FAKE, 1e-8, FAKE, None) == MANY
+    assert f(arr, 4, 0, 2, 64, 1, FAKE, None, FAKE, 1e-8, FAKE, None) == OK
+
+
+@pytest.mark.parametrize("N", [1, 2, 5, 8, 23, 48, 93, 186])
+def test_schedule_matches_oracle_bit_exact(N):
+    for S in sorted({1, 2, 3, 4, 6, 7, 24, N, N + 5}):
+        assert api.block_schedule(N, S) == oracle.block_schedule(N, S), (N, S)
+
+
+def test_schedule_errors():
+    L = _lib.lib()
+    counts = (ctypes.c_int * 9)()
+    ids = (ctypes.c_int * 4)()
+    assert L.attnres_block_schedule(8, 2, counts, ids, 4) == CAP
+    assert L.attnres_block_schedule(0, 2, counts, ids, 4) == SHAPE
+    assert L.attnres_block_schedule(8, 0, counts, ids, 4) == VALUE
+    assert L.attnres_block_schedule(8, 2, None, ids, 4) == NULL
+
+
+def test_atomic_block_size_matches_oracle():
+    for layers in range(1, 200):
+        assert api.atomic_block_size(layers) == oracle.atomic_block_size(layers)
+        for bs in (1, 2, 3, 12, 40):
+            assert api.atomic_block_size(layers, bs) == oracle.atomic_block_size(layers, bs)
+    assert _lib.lib().attnres_atomic_block_size(24, 0) == VALUE
+    assert _lib.lib().attnres_atomic_block_size(0, -1) == SHAPE
+
+
+# --------------------------------------------------------------------------
+# Figures printed on the pages (tests/golden/pages_figures.json)
+# --------------------------------------------------------------------------
+GOLD = json.load(open(os.path.join(ROOT, "tests", "golden", "pages_figures.json")))
+
+
+def test_golden_atomic_block_size():
+    for c in GOLD["atomic_block_size"]["cases"]:
+        got = api.atomic_block_size(c["num_hidden_layers"], c["attnres_block_size"])
+        assert got == c["atomic"]
+        if "blocks_of_48" in c:
+            assert 2 * c["num_hidden_layers"] // got == c["blocks_of_48"]
+
+
+def test_golden_extra_parameter_table():
+    for r in GOLD["extra_parameters"]["rows"]:
+        N = 2 * r["L"]                                    # atomic sublayers
+        assert N == r["N"]
+        assert 2 * (N + 1) * r["D"] == r["params"]        # one query + one gain per aggregation
+
+
+def test_golden_k3_source_count():
+    g = GOLD["k3_sources"]
+    sched = api.block_schedule(g["num_atomic"], g["block_size"])
+    assert len(sched[-1]) == g["final_sources"]
+
+
+def test_golden_residual_io_model():
+    g = GOLD["residual_io_model"]
+    assert accounting.residual_io_per_layer("standard", g["L"], g["N"], g["S"]) == g["standard_d"]
+    assert accounting.residual_io_per_layer("block", g["L"], g["N"], g["S"]) == g["block_d"]
+    assert accounting.residual_io_per_layer("full_two_phase", g["L"], g["N"], g["S"]) == g["full_two_phase_d"]
+
+
+def test_golden_prefill_cache():
+    g = GOLD["prefill_cache"]
+    total = accounting.prefill_block_cache_bytes(g["tokens"], g["blocks"], g["D"], g["elt_bytes"])
+    assert round(total / 1e9) == g["total_gb_approx"]
+    per_rank = accounting.prefill_block_cache_bytes(g["tokens"], g["blocks"], g["D"], g["elt_bytes"],
+                                                    g["ranks"])
+    assert round(per_rank / 1e9, 1) == g["per_rank_gb_approx"]
+    chunk = accounting.prefill_block_cache_bytes(g["chunk_tokens"], g["blocks"], g["D"], g["elt_bytes"],
+                                                 g["ranks"])
+    assert chunk / 1e9 < g["chunk_gb_below"]
+
+
+def test_kernel_byte_accounting_by_hand():
+    # Block single aggregation [4,4096,2048] bf16, n = 10: 11 rows of 4 KiB per token.
+    assert accounting.aggregate_bytes(10, 4 * 4096, 2048, 2) == 11 * 16384 * 4096
+    # Two-phase block, 9 summaries [8,4096,4096] bf16, S = 24.
+    b = accounting.two_phase_block_bytes(9, 24, 32768, 4096, 2)
+    assert b["phase1"] == 32768 * (33 * 8192 + 24 * 4)
+    assert b["merges"] == 23 * 32768 * (3 * 8192 + 4)
+    # Full stack, 186 sublayers: 17391 + 187 reads and 187 writes per token row.
+    assert accounting.full_stack_bytes(186, 2048, 2048, 2) == 2048 * (17391 + 187 + 187) * 4096

@@ -1,0 +1,218 @@
+// abi.cu -- the extern "C" entry points of libattnres.so (declared in
+// include/attnres.h): argument checks, then dispatch to the kernels.
+// Nothing here allocates device memory, synchronises, prints or aborts.
+#include <cmath>
+#include <cstdint>
+
+#include "common.cuh"
+#include "launch.h"
+
+namespace attnres {
+
+int sm_count() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+  int &c = cache[dev & 63];
+  if (c == 0) {
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v < 1) v = 1;
+    c = v;
+  }
+  return c;
+}
+
+namespace {
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int vec_elems(int dtype) { return dtype == ATTNRES_BF16 ? 8 : 4; }
+
+// Common checks for a [B,T,D] problem; rows receives B*T.
+int check_rows(int64_t B, int64_t T, int64_t D, int dtype, int64_t &rows) {
+  if (dtype != ATTNRES_F32 && dtype != ATTNRES_BF16) return ATTNRES_ERR_DTYPE;
+  if (B < 0 || T < 0 || D < 1 || D > (int64_t)1 << 20) return ATTNRES_ERR_SHAPE;
+  if (T != 0 && B > INT64_MAX / T) return ATTNRES_ERR_SHAPE;
+  if (D % vec_elems(dtype) != 0) return ATTNRES_ERR_ALIGNMENT;
+  rows = B * T;
+  return ATTNRES_OK;
+}
+
+int check_eps(float eps) {
+  return (std::isfinite(eps) && eps >= 0.f) ? ATTNRES_OK : ATTNRES_ERR_VALUE;
+}
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? ATTNRES_OK : ATTNRES_ERR_CUDA; }
+
+}  // namespace
+}  // namespace attnres
+
+using namespace attnres;
+
+extern "C" {
+
+const char *attnres_status_string(int status) {
+  switch (status) {
+    case ATTNRES_OK: return "ok";
+    case ATTNRES_ERR_NULL: return "a required pointer is NULL";
+    case ATTNRES_ERR_SHAPE: return "a size (n, S, L, B, T or D) is out of range";
+    case ATTNRES_ERR_DTYPE: return "dtype must be ATTNRES_F32 or ATTNRES_BF16";
+    case ATTNRES_ERR_ALIGNMENT: return "pointers must be 16-byte aligned and D a multiple of the vector width";
+    case ATTNRES_ERR_TOO_MANY_SOURCES: return "too many sources for one call";
+    case ATTNRES_ERR_CUDA: return "a CUDA launch failed";
+    case ATTNRES_ERR_CAPACITY: return "a host output buffer is too small";
+    case ATTNRES_ERR_VALUE: return "a value is invalid (eps negative or not finite, block size 0)";
+    default: return "unknown status";
+  }
+}
+
+int attnres_depth_aggregate(const void *const *sources, int n, int64_t B, int64_t T, int64_t D,
+                            int dtype, const float *query, const float *gain, float eps, void *out,
+                            float *out_max, float *out_lse, void *stream) {
+  int64_t rows = 0;
+  int st = check_rows(B, T, D, dtype, rows);
+  if (st) return st;
+  if (!sources || !query || !out) return ATTNRES_ERR_NULL;
+  if (n < 1) return ATTNRES_ERR_SHAPE;
+  if (n > ATTNRES_MAX_SOURCES) return ATTNRES_ERR_TOO_MANY_SOURCES;
+  if ((st = check_eps(eps))) return st;
+  for (int i = 0; i < n; ++i) {
+    if (!sources[i]) return ATTNRES_ERR_NULL;
+    if (!aligned16(sources[i])) return ATTNRES_ERR_ALIGNMENT;
+  }
+  if (!aligned16(query) || (gain && !aligned16(gain)) || !aligned16(out)) return ATTNRES_ERR_ALIGNMENT;
+  if (!aggregate_supported((int)D, dtype)) return ATTNRES_ERR_SHAPE;
+  if (rows == 0) return ATTNRES_OK;
+  AggregateArgs a{sources, n, rows, (int)D, dtype, query, gain, nullptr, eps, out, out_max, out_lse,
+                  static_cast<cudaStream_t>(stream)};
+  return cuda_status(launch_aggregate(a));
+}
+
+int attnres_block_phase1(const void *const *blocks, int n_blocks, int64_t B, int64_t T, int64_t D,
+                         int dtype, const float *queries, const float *gains, int S, float eps,
+                         void *out, float *out_max, float *out_lse, void *stream) {
+  int64_t rows = 0;
+  int st = check_rows(B, T, D, dtype, rows);
+  if (st) return st;
+  if (!blocks || !queries || !out || !out_lse) return ATTNRES_ERR_NULL;
+  if (n_blocks < 1 || S < 1 || S > ATTNRES_MAX_QUERIES) return ATTNRES_ERR_SHAPE;
+  if (n_blocks > ATTNRES_MAX_SOURCES) return ATTNRES_ERR_TOO_MANY_SOURCES;
+  if ((st = check_eps(eps))) return st;
+  for (int i = 0; i < n_blocks; ++i) {
+    if (!blocks[i]) return ATTNRES_ERR_NULL;
+    if (!aligned16(blocks[i])) return ATTNRES_ERR_ALIGNMENT;
+  }
+  if (!aligned16(queries) || (gains && !aligned16(gains)) || !aligned16(out)) return ATTNRES_ERR_ALIGNMENT;
+  if ((st = phase1_check(n_blocks, (int)D, dtype, S))) return st;
+  if (rows == 0) return ATTNRES_OK;
+  Phase1Args a{blocks, n_blocks, rows, (int)D, dtype, queries, gains, S, eps, out, out_max, out_lse,
+               static_cast<cudaStream_t>(stream)};
+  return cuda_status(launch_phase1(a));
+}
+
+int attnres_block_phase2_merge(const void *inter_out, const float *inter_lse, const void *partial,
+                               int64_t B, int64_t T, int64_t D, int dtype, const float *query,
+                               const float *gain, float eps, void *h_out, float *out_lse,
+                               void *stream) {
+  int64_t rows = 0;
+  int st = check_rows(B, T, D, dtype, rows);
+  if (st) return st;
+  if (!inter_out || !inter_lse || !query || !h_out) return ATTNRES_ERR_NULL;
+  if ((st = check_eps(eps))) return st;
+  if (!aligned16(inter_out) || (partial && !aligned16(partial)) || !aligned16(query) ||
+      (gain && !aligned16(gain)) || !aligned16(h_out))
+    return ATTNRES_ERR_ALIGNMENT;
+  if (!merge_supported((int)D, dtype)) return ATTNRES_ERR_SHAPE;
+  if (rows == 0) return ATTNRES_OK;
+  MergeArgs a{inter_out, inter_lse, partial, rows, (int)D, dtype, query, gain, eps, h_out, out_lse,
+              static_cast<cudaStream_t>(stream)};
+  return cuda_status(launch_merge(a));
+}
+
+int attnres_partial_update(const void *h, const void *partial_in, const float *u, int64_t B,
+                           int64_t T, int64_t D, int dtype, void *partial_out, void *stream) {
+  int64_t rows = 0;
+  int st = check_rows(B, T, D, dtype, rows);
+  if (st) return st;
+  if (!h || !u || !partial_out) return ATTNRES_ERR_NULL;
+  if (!aligned16(h) || (partial_in && !aligned16(partial_in)) || !aligned16(u) ||
+      !aligned16(partial_out))
+    return ATTNRES_ERR_ALIGNMENT;
+  if (rows == 0) return ATTNRES_OK;
+  PartialUpdateArgs a{h, partial_in, u, rows, (int)D, dtype, partial_out,
+                      static_cast<cudaStream_t>(stream)};
+  return cuda_status(launch_partial_update(a));
+}
+
+int attnres_full_stack_forward(void *const *sources, int L, int64_t B, int64_t T, int64_t D,
+                               int dtype, const float *queries, const float *gains, const float *u,
+                               float eps, void *y_out, void *stream) {
+  int64_t rows = 0;
+  int st = check_rows(B, T, D, dtype, rows);
+  if (st) return st;
+  if (!sources || !queries || !u || !y_out) return ATTNRES_ERR_NULL;
+  if (L < 1) return ATTNRES_ERR_SHAPE;
+  if (L + 1 > ATTNRES_MAX_SOURCES) return ATTNRES_ERR_TOO_MANY_SOURCES;
+  if ((st = check_eps(eps))) return st;
+  for (int l = 0; l <= L; ++l) {
+    if (!sources[l]) return ATTNRES_ERR_NULL;
+    if (!aligned16(sources[l])) return ATTNRES_ERR_ALIGNMENT;
+  }
+  if (!aligned16(queries) || (gains && !aligned16(gains)) || !aligned16(u) || !aligned16(y_out))
+    return ATTNRES_ERR_ALIGNMENT;
+  // Rows of queries / gains / u must stay 16-byte aligned: D % 4 == 0 holds
+  // for both dtypes after check_rows.
+  if (!aggregate_supported((int)D, dtype)) return ATTNRES_ERR_SHAPE;
+  if (rows == 0) return ATTNRES_OK;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const void *const *srcs = const_cast<const void *const *>(sources);
+  for (int l = 1; l <= L; ++l) {
+    AggregateArgs a{srcs, l, rows, (int)D, dtype, queries + (size_t)(l - 1) * D,
+                    gains ? gains + (size_t)(l - 1) * D : nullptr, u + (size_t)(l - 1) * D, eps,
+                    sources[l], nullptr, nullptr, s};
+    if ((st = cuda_status(launch_aggregate(a)))) return st;
+  }
+  AggregateArgs fin{srcs, L + 1, rows, (int)D, dtype, queries + (size_t)L * D,
+                    gains ? gains + (size_t)L * D : nullptr, nullptr, eps, y_out, nullptr, nullptr, s};
+  return cuda_status(launch_aggregate(fin));
+}
+
+int attnres_block_schedule(int num_atomic, int block_size, int *n_sources_per_layer,
+                           int *source_ids, int capacity) {
+  if (num_atomic < 1) return ATTNRES_ERR_SHAPE;
+  if (block_size < 1) return ATTNRES_ERR_VALUE;
+  if (!n_sources_per_layer || !source_ids) return ATTNRES_ERR_NULL;
+  if (capacity < 0) return ATTNRES_ERR_CAPACITY;
+  // Completed blocks so far (block 0 = embedding) and whether a running
+  // partial exists.  Sublayer idx closes its block when idx % block_size == 0
+  // or it is the last sublayer.
+  int completed = 1;
+  bool partial = false;
+  int written = 0;
+  for (int idx = 1; idx <= num_atomic; ++idx) {
+    const int count = completed + (partial ? 1 : 0);
+    if (written + count > capacity) return ATTNRES_ERR_CAPACITY;
+    for (int b = 0; b < completed; ++b) source_ids[written++] = b;
+    if (partial) source_ids[written++] = -1;
+    n_sources_per_layer[idx - 1] = count;
+    partial = true;
+    if (idx % block_size == 0 || idx == num_atomic) {
+      ++completed;
+      partial = false;
+    }
+  }
+  if (written + completed > capacity) return ATTNRES_ERR_CAPACITY;
+  for (int b = 0; b < completed; ++b) source_ids[written++] = b;
+  n_sources_per_layer[num_atomic] = completed;
+  return written;
+}
+
+int attnres_atomic_block_size(int num_hidden_layers, int attnres_block_size) {
+  if (num_hidden_layers < 1) return ATTNRES_ERR_SHAPE;
+  if (attnres_block_size == 0) return ATTNRES_ERR_VALUE;
+  int decoder_blocks = attnres_block_size > 0 ? attnres_block_size : (num_hidden_layers + 7) / 8;
+  if (decoder_blocks < 1) decoder_blocks = 1;
+  return 2 * decoder_blocks;
+}
+
+}  // extern "C"

@@ -1,0 +1,109 @@
+// common.cuh -- device helpers shared by the AttnRes kernels (sm_103a).
+//
+// Rows move as 16-byte vectors (8 bf16 or 4 fp32 elements).  Arithmetic is
+// fp32 throughout; a bf16 element widens to fp32 exactly by placing its 16
+// bits in the high half of an fp32 word.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "attnres.h"
+
+namespace attnres {
+
+constexpr int kMaxSources = ATTNRES_MAX_SOURCES;
+constexpr int kMaxQueries = ATTNRES_MAX_QUERIES;
+
+// Element traits: EPV = elements per 16-byte vector.
+template <typename T> struct Elt;
+template <> struct Elt<float> {
+  static constexpr int EPV = 4;
+  static __device__ __forceinline__ void unpack(const uint4 &v, float *x) {
+    x[0] = __uint_as_float(v.x); x[1] = __uint_as_float(v.y);
+    x[2] = __uint_as_float(v.z); x[3] = __uint_as_float(v.w);
+  }
+  static __device__ __forceinline__ uint4 pack(const float *x) {
+    return make_uint4(__float_as_uint(x[0]), __float_as_uint(x[1]), __float_as_uint(x[2]),
+                      __float_as_uint(x[3]));
+  }
+};
+template <> struct Elt<__nv_bfloat16> {
+  static constexpr int EPV = 8;
+  static __device__ __forceinline__ void unpack_word(uint32_t w, float &lo, float &hi) {
+    lo = __uint_as_float(w << 16);
+    hi = __uint_as_float(w & 0xffff0000u);
+  }
+  static __device__ __forceinline__ void unpack(const uint4 &v, float *x) {
+    unpack_word(v.x, x[0], x[1]); unpack_word(v.y, x[2], x[3]);
+    unpack_word(v.z, x[4], x[5]); unpack_word(v.w, x[6], x[7]);
+  }
+  static __device__ __forceinline__ uint32_t pack_word(float lo, float hi) {
+    __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);  // round to nearest even
+    return *reinterpret_cast<uint32_t *>(&b);
+  }
+  static __device__ __forceinline__ uint4 pack(const float *x) {
+    return make_uint4(pack_word(x[0], x[1]), pack_word(x[2], x[3]), pack_word(x[4], x[5]),
+                      pack_word(x[6], x[7]));
+  }
+};
+
+// Streaming 16-byte load: read-only path, no L1 allocation (each source
+// byte is consumed once by the CTA that loads it).
+__device__ __forceinline__ uint4 ld_stream(const void *p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+// Plain 16-byte load through L1 (small, reused operands: queries, gains, u).
+__device__ __forceinline__ float4 ld_f4(const float *p) {
+  return __ldg(reinterpret_cast<const float4 *>(p));
+}
+
+__device__ __forceinline__ void st_vec(void *p, const uint4 &v) {
+  *reinterpret_cast<uint4 *>(p) = v;
+}
+
+// Streaming store (evict-first): outputs are not re-read by this kernel.
+__device__ __forceinline__ void st_stream(void *p, const uint4 &v) {
+  asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};"
+               :: "l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
+}
+
+// Sum over the TEAM lanes of an aligned power-of-two lane group of a warp.
+template <int TEAM>
+__device__ __forceinline__ float team_sum_shfl(float v) {
+#pragma unroll
+  for (int o = TEAM / 2; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// Sum of K values over a whole CTA.  Each warp reduces with shuffles, lane 0
+// publishes to red[parity][warp][K], one barrier, then every thread sums the
+// warps' values.  Alternating `parity` between consecutive calls makes a
+// second barrier unnecessary (a slot is rewritten only after every thread
+// has passed the barrier of the call in between).
+template <int K>
+__device__ __forceinline__ void cta_sum(float (&v)[K], float *red /*[2][32][K]*/, int parity) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+#pragma unroll
+  for (int k = 0; k < K; ++k) v[k] = team_sum_shfl<32>(v[k]);
+  float *slot = red + parity * 32 * K;
+  if (lane == 0) {
+#pragma unroll
+    for (int k = 0; k < K; ++k) slot[warp * K + k] = v[k];
+  }
+  __syncthreads();
+#pragma unroll
+  for (int k = 0; k < K; ++k) v[k] = 0.f;
+  for (int w = 0; w < nwarps; ++w) {
+#pragma unroll
+    for (int k = 0; k < K; ++k) v[k] += slot[w * K + k];
+  }
+}
+
+}  // namespace attnres

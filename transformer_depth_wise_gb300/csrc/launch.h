@@ -1,0 +1,80 @@
+// launch.h -- internal launchers behind the C ABI.  Arguments reaching these
+// functions have already been validated by the entry points in abi.cu.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace attnres {
+
+// Streaming-multiprocessor count of the current device (cached per device).
+int sm_count();
+
+struct AggregateArgs {
+  const void *const *sources;  // host array of n device pointers
+  int n;
+  int64_t rows;                // B * T
+  int D;
+  int dtype;
+  const float *query;          // [D]
+  const float *gain;           // [D] or nullptr
+  const float *u;              // [D]: apply f(h) = 0.5 tanh(u h) before storing, or nullptr
+  float eps;
+  void *out;                   // [rows, D]
+  float *out_max;              // [rows] or nullptr
+  float *out_lse;              // [rows] or nullptr
+  cudaStream_t stream;
+};
+// Returns false when D is beyond what the kernel family covers.
+bool aggregate_supported(int D, int dtype);
+cudaError_t launch_aggregate(const AggregateArgs &a);
+
+struct MergeArgs {
+  const void *inter_out;       // [rows, D]
+  const float *inter_lse;      // [rows]
+  const void *partial;         // [rows, D] or nullptr
+  int64_t rows;
+  int D;
+  int dtype;
+  const float *query;
+  const float *gain;
+  float eps;
+  void *h_out;
+  float *out_lse;
+  cudaStream_t stream;
+};
+bool merge_supported(int D, int dtype);
+cudaError_t launch_merge(const MergeArgs &a);
+
+struct PartialUpdateArgs {
+  const void *h;
+  const void *partial_in;      // or nullptr
+  const float *u;
+  int64_t rows;
+  int D;
+  int dtype;
+  void *partial_out;
+  cudaStream_t stream;
+};
+cudaError_t launch_partial_update(const PartialUpdateArgs &a);
+
+struct Phase1Args {
+  const void *const *blocks;   // host array of n device pointers
+  int n;
+  int64_t rows;
+  int D;
+  int dtype;
+  const float *queries;        // [S, D]
+  const float *gains;          // [S, D] or nullptr
+  int S;
+  float eps;
+  void *out;                   // [S, rows, D]
+  float *out_max;              // [S, rows] or nullptr
+  float *out_lse;              // [S, rows]
+  cudaStream_t stream;
+};
+// Returns ATTNRES_OK or a (negative) status for shapes the kernels cannot take.
+int phase1_check(int n, int D, int dtype, int S);
+cudaError_t launch_phase1(const Phase1Args &a);
+
+}  // namespace attnres

@@ -1,0 +1,273 @@
+// merge.cu -- phase 2 of the two-phase Block scheme and the running partial
+// update ("Attention Residual 深度残差", "两阶段算法（inter / intra）",
+// eq. OS2 and single_source_stats; "forward_naive" partial = partial + out).
+//
+// Phase-2 merge, per token row: the partial p is a single source with state
+// (s_p, p, 1); the phase-1 state of the same query is (lse, o, 1).  OS2 with
+// M = max(lse, s_p) gives
+//   h = (e^{lse-M} o + e^{s_p-M} p) / (e^{lse-M} + e^{s_p-M}).
+// Three rows move per token (read o, read p, write h): a pure HBM stream.
+#include "common.cuh"
+#include "launch.h"
+
+namespace attnres {
+
+struct MergeParams {
+  const void *o;
+  const float *lse;
+  const void *p;
+  int nvec;
+  int D;
+  float inv_D;
+  float eps;
+  int64_t rows;
+  const float *q;
+  const float *g;
+  void *h;
+  float *lse_out;
+};
+
+template <typename T, int VPT, int TEAM>
+__global__ void __launch_bounds__(TEAM ? 256 : 512)
+merge_kernel(const __grid_constant__ MergeParams p) {
+  using E = Elt<T>;
+  constexpr int EPV = E::EPV;
+  constexpr int NE = VPT * EPV;
+  __shared__ float red[TEAM ? 1 : 2 * 32 * 2];
+
+  const int tpr = TEAM ? TEAM : blockDim.x;
+  const int lt = TEAM ? (threadIdx.x % TEAM) : threadIdx.x;
+  const int teams_per_cta = TEAM ? blockDim.x / TEAM : 1;
+  const int team = TEAM ? threadIdx.x / TEAM : 0;
+  const bool has_p = p.p != nullptr;
+
+  float qe[NE];
+  bool valid[VPT];
+#pragma unroll
+  for (int k = 0; k < VPT; ++k) {
+    const int j = lt + k * tpr;
+    valid[k] = j < p.nvec;
+#pragma unroll
+    for (int e4 = 0; e4 < EPV; e4 += 4) {
+      float4 w4 = make_float4(0.f, 0.f, 0.f, 0.f), g4 = make_float4(1.f, 1.f, 1.f, 1.f);
+      if (valid[k] && has_p) {
+        w4 = ld_f4(p.q + j * EPV + e4);
+        if (p.g) g4 = ld_f4(p.g + j * EPV + e4);
+      }
+      qe[k * EPV + e4 + 0] = w4.x * g4.x;
+      qe[k * EPV + e4 + 1] = w4.y * g4.y;
+      qe[k * EPV + e4 + 2] = w4.z * g4.z;
+      qe[k * EPV + e4 + 3] = w4.w * g4.w;
+    }
+  }
+
+  const size_t row_bytes = (size_t)p.D * sizeof(T);
+  const int64_t groups = (p.rows + teams_per_cta - 1) / teams_per_cta;
+  int parity = 0;
+  for (int64_t rg = blockIdx.x; rg < groups; rg += gridDim.x) {
+    const int64_t row = rg * teams_per_cta + team;
+    const bool row_ok = row < p.rows;
+    const size_t row_off = (size_t)row * row_bytes;
+    uint4 ov[VPT], pv[VPT];
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+      ov[k] = make_uint4(0u, 0u, 0u, 0u);
+      pv[k] = make_uint4(0u, 0u, 0u, 0u);
+      const size_t off = row_off + (size_t)(lt + k * tpr) * 16;
+      if (row_ok && valid[k]) {
+        ov[k] = ld_stream(static_cast<const char *>(p.o) + off);
+        if (has_p) pv[k] = ld_stream(static_cast<const char *>(p.p) + off);
+      }
+    }
+    if (!has_p) {  // first sublayer of a block: h = o
+      if (row_ok) {
+#pragma unroll
+        for (int k = 0; k < VPT; ++k)
+          if (valid[k]) st_vec(static_cast<char *>(p.h) + row_off + (size_t)(lt + k * tpr) * 16, ov[k]);
+        if (lt == 0 && p.lse_out) p.lse_out[row] = p.lse[row];
+      }
+      continue;
+    }
+    float part[2] = {0.f, 0.f};
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+      float x[EPV];
+      E::unpack(pv[k], x);
+#pragma unroll
+      for (int e = 0; e < EPV; ++e) {
+        part[0] = fmaf(qe[k * EPV + e], x[e], part[0]);
+        part[1] = fmaf(x[e], x[e], part[1]);
+      }
+    }
+    if (TEAM) {
+      part[0] = team_sum_shfl<TEAM ? TEAM : 1>(part[0]);
+      part[1] = team_sum_shfl<TEAM ? TEAM : 1>(part[1]);
+    } else {
+      cta_sum<2>(part, red, parity);
+      parity ^= 1;
+    }
+    if (!row_ok) continue;
+    const float sp = part[0] * rsqrtf(fmaf(part[1], p.inv_D, p.eps));
+    const float l = p.lse[row];
+    const float M = fmaxf(l, sp);
+    const float a = expf(l - M), c = expf(sp - M);
+    const float inv = 1.f / (a + c);
+    const float wa = a * inv, wc = c * inv;
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+      if (!valid[k]) continue;
+      float xo[EPV], xp[EPV], h[EPV];
+      E::unpack(ov[k], xo);
+      E::unpack(pv[k], xp);
+#pragma unroll
+      for (int e = 0; e < EPV; ++e) h[e] = fmaf(wa, xo[e], wc * xp[e]);
+      st_vec(static_cast<char *>(p.h) + row_off + (size_t)(lt + k * tpr) * 16, E::pack(h));
+    }
+    if (lt == 0 && p.lse_out) p.lse_out[row] = M + logf(a + c);
+  }
+}
+
+// partial_out = (partial_in or 0) + 0.5 tanh(u (.) h), elementwise.
+template <typename T>
+__global__ void __launch_bounds__(256)
+partial_update_kernel(const void *__restrict__ h, const void *pin, const float *__restrict__ u,
+                      void *pout, int64_t total_vec, int nvec) {
+  // pin may alias pout (in-place update): every vector is read, then written,
+  // by the same thread, and pin is read through the coherent path.
+  using E = Elt<T>;
+  constexpr int EPV = E::EPV;
+  constexpr int U = 4;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  for (int64_t base = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; base < total_vec;
+       base += stride * U) {
+    uint4 hv[U], pv[U];
+#pragma unroll
+    for (int t = 0; t < U; ++t) {
+      const int64_t v = base + t * stride;
+      hv[t] = make_uint4(0u, 0u, 0u, 0u);
+      pv[t] = make_uint4(0u, 0u, 0u, 0u);
+      if (v < total_vec) {
+        hv[t] = ld_stream(static_cast<const uint4 *>(h) + v);
+        if (pin) pv[t] = static_cast<const uint4 *>(pin)[v];
+      }
+    }
+#pragma unroll
+    for (int t = 0; t < U; ++t) {
+      const int64_t v = base + t * stride;
+      if (v >= total_vec) continue;
+      const int j = (int)(v % nvec);
+      float xh[EPV], xp[EPV], y[EPV];
+      E::unpack(hv[t], xh);
+      E::unpack(pv[t], xp);
+#pragma unroll
+      for (int e4 = 0; e4 < EPV; e4 += 4) {
+        const float4 u4 = ld_f4(u + j * EPV + e4);
+        y[e4 + 0] = xp[e4 + 0] + 0.5f * tanhf(u4.x * xh[e4 + 0]);
+        y[e4 + 1] = xp[e4 + 1] + 0.5f * tanhf(u4.y * xh[e4 + 1]);
+        y[e4 + 2] = xp[e4 + 2] + 0.5f * tanhf(u4.z * xh[e4 + 2]);
+        y[e4 + 3] = xp[e4 + 3] + 0.5f * tanhf(u4.w * xh[e4 + 3]);
+      }
+      st_vec(static_cast<uint4 *>(pout) + v, E::pack(y));
+    }
+  }
+}
+
+namespace {
+
+int epv_of(int dtype) { return dtype == ATTNRES_BF16 ? 8 : 4; }
+
+struct Cfg {
+  int vpt, team, threads;
+};
+
+bool choose(int D, int dtype, Cfg &c) {
+  const int nvec = D / epv_of(dtype);
+  if (nvec <= 64) {
+    int need = (nvec + 1) / 2, team = 4;
+    while (team < need) team *= 2;
+    c = {2, team, 256};
+    return true;
+  }
+  if (nvec <= 2048) {
+    c = {4, 0, ((nvec + 3) / 4 + 31) / 32 * 32};
+    return true;
+  }
+  return false;
+}
+
+template <typename T, int VPT, int TEAM>
+cudaError_t run(const MergeParams &p, const Cfg &c, cudaStream_t st) {
+  auto kern = merge_kernel<T, VPT, TEAM>;
+  static int occ[16] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  int &o = occ[dev & 15];
+  if (o == 0) {
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, kern, c.threads, 0);
+    if (e != cudaSuccess) return e;
+    if (o < 1) o = 1;
+  }
+  const int per_cta = TEAM ? c.threads / TEAM : 1;
+  const int64_t groups = (p.rows + per_cta - 1) / per_cta;
+  const int64_t cap = (int64_t)o * sm_count();
+  const int grid = (int)(groups < cap ? groups : cap);
+  kern<<<grid, c.threads, 0, st>>>(p);
+  return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t dispatch(const MergeParams &p, const Cfg &c, cudaStream_t st) {
+  switch (c.team) {
+    case 0: return run<T, 4, 0>(p, c, st);
+    case 4: return run<T, 2, 4>(p, c, st);
+    case 8: return run<T, 2, 8>(p, c, st);
+    case 16: return run<T, 2, 16>(p, c, st);
+    default: return run<T, 2, 32>(p, c, st);
+  }
+}
+
+}  // namespace
+
+bool merge_supported(int D, int dtype) {
+  Cfg c;
+  return choose(D, dtype, c);
+}
+
+cudaError_t launch_merge(const MergeArgs &a) {
+  Cfg c;
+  if (!choose(a.D, a.dtype, c)) return cudaErrorInvalidValue;
+  MergeParams p;
+  p.o = a.inter_out;
+  p.lse = a.inter_lse;
+  p.p = a.partial;
+  p.nvec = a.D / epv_of(a.dtype);
+  p.D = a.D;
+  p.inv_D = 1.f / (float)a.D;
+  p.eps = a.eps;
+  p.rows = a.rows;
+  p.q = a.query;
+  p.g = a.gain;
+  p.h = a.h_out;
+  p.lse_out = a.out_lse;
+  return a.dtype == ATTNRES_BF16 ? dispatch<__nv_bfloat16>(p, c, a.stream)
+                                 : dispatch<float>(p, c, a.stream);
+}
+
+cudaError_t launch_partial_update(const PartialUpdateArgs &a) {
+  const int nvec = a.D / epv_of(a.dtype);
+  const int64_t total = a.rows * nvec;
+  const int threads = 256;
+  int64_t blocks = (total + threads * 4 - 1) / (threads * 4);
+  const int64_t cap = (int64_t)sm_count() * 8;
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  if (a.dtype == ATTNRES_BF16)
+    partial_update_kernel<__nv_bfloat16><<<(int)blocks, threads, 0, a.stream>>>(
+        a.h, a.partial_in, a.u, a.partial_out, total, nvec);
+  else
+    partial_update_kernel<float><<<(int)blocks, threads, 0, a.stream>>>(
+        a.h, a.partial_in, a.u, a.partial_out, total, nvec);
+  return cudaGetLastError();
+}
+
+}  // namespace attnres

@@ -31,7 +31,8 @@
  *   - Errors: arguments are checked before anything is launched; a bad
  *     argument returns a negative attnres_status_t and launches nothing.
  *     A launch failure returns ATTNRES_ERR_CUDA.  Nothing aborts or prints.
- *   - Empty inputs (B*T == 0) are valid and launch nothing.
+ *   - Empty inputs (B*T == 0) are valid and launch nothing; their data
+ *     pointers are not checked (an empty tensor's pointer may be NULL).
  */
 #ifndef ATTNRES_H
 #define ATTNRES_H
@@ -53,7 +54,8 @@ typedef enum {
     ATTNRES_ERR_TOO_MANY_SOURCES = -5, /* n > ATTNRES_MAX_SOURCES                    */
     ATTNRES_ERR_CUDA = -6,             /* a kernel launch failed                     */
     ATTNRES_ERR_CAPACITY = -7,         /* a host output buffer is too small          */
-    ATTNRES_ERR_VALUE = -8             /* eps negative / not finite, block size 0    */
+    ATTNRES_ERR_VALUE = -8,            /* eps negative / not finite, block size 0    */
+    ATTNRES_ERR_TIMEOUT = -9           /* a kernel wait gave up (see below)          */
 } attnres_status_t;
 
 /* Most sources one aggregation may read (Full stack: L + 1 <= this). */
@@ -171,6 +173,17 @@ int attnres_block_schedule(int num_atomic, int block_size, int *n_sources_per_la
  * ATTNRES_ERR_SHAPE.
  */
 int attnres_atomic_block_size(int num_hidden_layers, int attnres_block_size);
+
+/*
+ * Kernels that wait on in-kernel events (bulk-copy completion, peer CTAs of a
+ * cluster) bound every wait to about 2 s; a wait that runs out records a
+ * device-side flag and the kernel carries on to its end instead of hanging
+ * (its results are then invalid).  This call synchronises the current
+ * device, reads and clears those flags, and returns ATTNRES_ERR_TIMEOUT if
+ * any was set since the previous call (ATTNRES_ERR_CUDA if the device
+ * reports an error), else ATTNRES_OK.
+ */
+int attnres_take_device_error(void);
 
 /* Static, human-readable name of a status code. */
 const char *attnres_status_string(int status);

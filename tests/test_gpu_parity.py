@@ -151,9 +151,14 @@ def test_aggregate_block_single_full_size_sampled(gpu):
 # two-phase Block: phase 1, phase 2 merge, partial update, one block chain
 # --------------------------------------------------------------------------
 @pytest.mark.parametrize("dtype,D,n,S,rows", [
-    (torch.bfloat16, 4096, 9, 24, 37), (torch.bfloat16, 512, 3, 5, 130),
+    # tensor-core kernel (bf16, D = 512 x {1, 2, 4, 8}, n <= 9, S <= 24): clusters of
+    # 1..8 CTAs, one / several / ragged 8-token tiles
+    (torch.bfloat16, 512, 1, 1, 1), (torch.bfloat16, 512, 9, 24, 37), (torch.bfloat16, 512, 3, 5, 130),
+    (torch.bfloat16, 1024, 5, 7, 130), (torch.bfloat16, 2048, 9, 24, 64), (torch.bfloat16, 4096, 9, 24, 37),
+    (torch.bfloat16, 4096, 9, 24, 8), (torch.bfloat16, 4096, 2, 3, 1000), (torch.bfloat16, 4096, 8, 24, 4103),
+    # general kernel: other D, n > 9, fp32
     (torch.bfloat16, 7168, 9, 4, 9), (torch.float32, 256, 5, 7, 66), (torch.bfloat16, 64, 1, 3, 20),
-    (torch.bfloat16, 2048, 16, 2, 11),
+    (torch.bfloat16, 2048, 16, 2, 11), (torch.bfloat16, 4096, 10, 24, 21),
 ])
 def test_phase1_small(gpu, dtype, D, n, S, rows):
     g = wk.generator(D + n + S, gpu)
@@ -284,3 +289,9 @@ def test_full_stack_config_full_size_sampled(gpu):
     for l in (1, 2, 50, 186):
         check(pick(srcs[l], rows, wl.D), V[l], tol, f"v_{l}")
     check(pick(y, rows, wl.D), oy, tol, "y")
+
+
+def test_no_kernel_wait_ran_out(gpu):
+    """Every bounded in-kernel wait of the runs above completed in time."""
+    from transformer_depth_wise_gb300 import _lib
+    assert _lib.lib().attnres_take_device_error() == 0

@@ -27,6 +27,7 @@ STATUS = {
     -6: "ATTNRES_ERR_CUDA",
     -7: "ATTNRES_ERR_CAPACITY",
     -8: "ATTNRES_ERR_VALUE",
+    -9: "ATTNRES_ERR_TIMEOUT",
 }
 
 # Every symbol include/attnres.h declares, with its ctypes signature.
@@ -45,6 +46,7 @@ SIGNATURES = {
                                           _vp]),
     "attnres_block_schedule": (_int, [_int, _int, _ip, _ip, _int]),
     "attnres_atomic_block_size": (_int, [_int, _int]),
+    "attnres_take_device_error": (_int, []),
     "attnres_status_string": (ctypes.c_char_p, [_int]),
 }
 

@@ -62,6 +62,7 @@ const char *attnres_status_string(int status) {
     case ATTNRES_ERR_CUDA: return "a CUDA launch failed";
     case ATTNRES_ERR_CAPACITY: return "a host output buffer is too small";
     case ATTNRES_ERR_VALUE: return "a value is invalid (eps negative or not finite, block size 0)";
+    case ATTNRES_ERR_TIMEOUT: return "a kernel wait ran out of time and gave up (results invalid)";
     default: return "unknown status";
   }
 }
@@ -72,17 +73,17 @@ int attnres_depth_aggregate(const void *const *sources, int n, int64_t B, int64_
   int64_t rows = 0;
   int st = check_rows(B, T, D, dtype, rows);
   if (st) return st;
-  if (!sources || !query || !out) return ATTNRES_ERR_NULL;
   if (n < 1) return ATTNRES_ERR_SHAPE;
   if (n > ATTNRES_MAX_SOURCES) return ATTNRES_ERR_TOO_MANY_SOURCES;
   if ((st = check_eps(eps))) return st;
+  if (!aggregate_supported((int)D, dtype)) return ATTNRES_ERR_SHAPE;
+  if (rows == 0) return ATTNRES_OK;  // empty tensors may carry NULL data pointers
+  if (!sources || !query || !out) return ATTNRES_ERR_NULL;
   for (int i = 0; i < n; ++i) {
     if (!sources[i]) return ATTNRES_ERR_NULL;
     if (!aligned16(sources[i])) return ATTNRES_ERR_ALIGNMENT;
   }
   if (!aligned16(query) || (gain && !aligned16(gain)) || !aligned16(out)) return ATTNRES_ERR_ALIGNMENT;
-  if (!aggregate_supported((int)D, dtype)) return ATTNRES_ERR_SHAPE;
-  if (rows == 0) return ATTNRES_OK;
   AggregateArgs a{sources, n, rows, (int)D, dtype, query, gain, nullptr, eps, out, out_max, out_lse,
                   static_cast<cudaStream_t>(stream)};
   return cuda_status(launch_aggregate(a));
@@ -94,17 +95,17 @@ int attnres_block_phase1(const void *const *blocks, int n_blocks, int64_t B, int
   int64_t rows = 0;
   int st = check_rows(B, T, D, dtype, rows);
   if (st) return st;
-  if (!blocks || !queries || !out || !out_lse) return ATTNRES_ERR_NULL;
   if (n_blocks < 1 || S < 1 || S > ATTNRES_MAX_QUERIES) return ATTNRES_ERR_SHAPE;
   if (n_blocks > ATTNRES_MAX_SOURCES) return ATTNRES_ERR_TOO_MANY_SOURCES;
   if ((st = check_eps(eps))) return st;
+  if ((st = phase1_check(n_blocks, (int)D, dtype, S))) return st;
+  if (rows == 0) return ATTNRES_OK;
+  if (!blocks || !queries || !out || !out_lse) return ATTNRES_ERR_NULL;
   for (int i = 0; i < n_blocks; ++i) {
     if (!blocks[i]) return ATTNRES_ERR_NULL;
     if (!aligned16(blocks[i])) return ATTNRES_ERR_ALIGNMENT;
   }
   if (!aligned16(queries) || (gains && !aligned16(gains)) || !aligned16(out)) return ATTNRES_ERR_ALIGNMENT;
-  if ((st = phase1_check(n_blocks, (int)D, dtype, S))) return st;
-  if (rows == 0) return ATTNRES_OK;
   Phase1Args a{blocks, n_blocks, rows, (int)D, dtype, queries, gains, S, eps, out, out_max, out_lse,
                static_cast<cudaStream_t>(stream)};
   return cuda_status(launch_phase1(a));
@@ -117,13 +118,13 @@ int attnres_block_phase2_merge(const void *inter_out, const float *inter_lse, co
   int64_t rows = 0;
   int st = check_rows(B, T, D, dtype, rows);
   if (st) return st;
-  if (!inter_out || !inter_lse || !query || !h_out) return ATTNRES_ERR_NULL;
   if ((st = check_eps(eps))) return st;
+  if (!merge_supported((int)D, dtype)) return ATTNRES_ERR_SHAPE;
+  if (rows == 0) return ATTNRES_OK;
+  if (!inter_out || !inter_lse || !query || !h_out) return ATTNRES_ERR_NULL;
   if (!aligned16(inter_out) || (partial && !aligned16(partial)) || !aligned16(query) ||
       (gain && !aligned16(gain)) || !aligned16(h_out))
     return ATTNRES_ERR_ALIGNMENT;
-  if (!merge_supported((int)D, dtype)) return ATTNRES_ERR_SHAPE;
-  if (rows == 0) return ATTNRES_OK;
   MergeArgs a{inter_out, inter_lse, partial, rows, (int)D, dtype, query, gain, eps, h_out, out_lse,
               static_cast<cudaStream_t>(stream)};
   return cuda_status(launch_merge(a));
@@ -134,11 +135,11 @@ int attnres_partial_update(const void *h, const void *partial_in, const float *u
   int64_t rows = 0;
   int st = check_rows(B, T, D, dtype, rows);
   if (st) return st;
+  if (rows == 0) return ATTNRES_OK;
   if (!h || !u || !partial_out) return ATTNRES_ERR_NULL;
   if (!aligned16(h) || (partial_in && !aligned16(partial_in)) || !aligned16(u) ||
       !aligned16(partial_out))
     return ATTNRES_ERR_ALIGNMENT;
-  if (rows == 0) return ATTNRES_OK;
   PartialUpdateArgs a{h, partial_in, u, rows, (int)D, dtype, partial_out,
                       static_cast<cudaStream_t>(stream)};
   return cuda_status(launch_partial_update(a));
@@ -150,20 +151,20 @@ int attnres_full_stack_forward(void *const *sources, int L, int64_t B, int64_t T
   int64_t rows = 0;
   int st = check_rows(B, T, D, dtype, rows);
   if (st) return st;
-  if (!sources || !queries || !u || !y_out) return ATTNRES_ERR_NULL;
   if (L < 1) return ATTNRES_ERR_SHAPE;
   if (L + 1 > ATTNRES_MAX_SOURCES) return ATTNRES_ERR_TOO_MANY_SOURCES;
   if ((st = check_eps(eps))) return st;
+  if (!aggregate_supported((int)D, dtype)) return ATTNRES_ERR_SHAPE;
+  if (rows == 0) return ATTNRES_OK;
+  if (!sources || !queries || !u || !y_out) return ATTNRES_ERR_NULL;
   for (int l = 0; l <= L; ++l) {
     if (!sources[l]) return ATTNRES_ERR_NULL;
     if (!aligned16(sources[l])) return ATTNRES_ERR_ALIGNMENT;
   }
   if (!aligned16(queries) || (gains && !aligned16(gains)) || !aligned16(u) || !aligned16(y_out))
     return ATTNRES_ERR_ALIGNMENT;
-  // Rows of queries / gains / u must stay 16-byte aligned: D % 4 == 0 holds
-  // for both dtypes after check_rows.
-  if (!aggregate_supported((int)D, dtype)) return ATTNRES_ERR_SHAPE;
-  if (rows == 0) return ATTNRES_OK;
+  // Rows of queries / gains / u stay 16-byte aligned: D % 4 == 0 holds for
+  // both dtypes after check_rows.
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const void *const *srcs = const_cast<const void *const *>(sources);
   for (int l = 1; l <= L; ++l) {
@@ -175,6 +176,14 @@ int attnres_full_stack_forward(void *const *sources, int L, int64_t B, int64_t T
   AggregateArgs fin{srcs, L + 1, rows, (int)D, dtype, queries + (size_t)L * D,
                     gains ? gains + (size_t)L * D : nullptr, nullptr, eps, y_out, nullptr, nullptr, s};
   return cuda_status(launch_aggregate(fin));
+}
+
+int attnres_take_device_error(void) {
+  if (cudaDeviceSynchronize() != cudaSuccess) return ATTNRES_ERR_CUDA;
+  const unsigned int f = take_error_aggregate() | take_error_merge() | take_error_phase1() |
+                           take_error_phase1_tc();
+  if (f & 2u) return ATTNRES_ERR_CUDA;
+  return f ? ATTNRES_ERR_TIMEOUT : ATTNRES_OK;
 }
 
 int attnres_block_schedule(int num_atomic, int block_size, int *n_sources_per_layer,

@@ -16,6 +16,8 @@
 #include "common.cuh"
 #include "launch.h"
 
+ATTNRES_DEFINE_ERROR_FLAG(take_error_aggregate)
+
 namespace attnres {
 
 struct AggParams {

@@ -107,3 +107,82 @@ __device__ __forceinline__ void cta_sum(float (&v)[K], float *red /*[2][32][K]*/
 }
 
 }  // namespace attnres
+
+// ---------------------------------------------------------------------------
+// mbarrier / bulk-copy helpers (sm_90+ PTX, used on sm_103a)
+// ---------------------------------------------------------------------------
+namespace attnres {
+
+// Upper bound on any single wait inside a kernel.  A wait that runs out sets
+// the translation unit's error flag and gives up instead of spinning forever.
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
+
+__device__ __forceinline__ unsigned long long globaltimer_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" :: "r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" :: "r"(bar), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" :: "r"(bar) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+  return ok != 0;
+}
+
+// Wait for the phase of `parity` to complete; false if the time limit ran out.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+  if (mbar_try(bar, parity)) return true;
+  const unsigned long long t0 = globaltimer_ns();
+  while (!mbar_try(bar, parity))
+    if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+  return true;
+}
+
+// 1-D bulk copy global -> shared (this CTA), completion counted on `bar`.
+// Both addresses 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes,
+                                         uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      :: "r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
+}
+
+}  // namespace attnres
+
+// Per translation unit: a device flag that records a wait that ran out, and
+// a host function (declared in launch.h) that reads and clears it.
+#define ATTNRES_DEFINE_ERROR_FLAG(host_fn)                                            \
+  namespace attnres {                                                               \
+  static __device__ unsigned int g_error_flag = 0;                                  \
+  __device__ __forceinline__ void raise_timeout() { atomicOr(&g_error_flag, 1u); }  \
+  unsigned int host_fn() {                                                          \
+    unsigned int v = 0, zero = 0;                                                   \
+    if (cudaMemcpyFromSymbol(&v, g_error_flag, sizeof(v)) != cudaSuccess) return 2; \
+    if (v) cudaMemcpyToSymbol(g_error_flag, &zero, sizeof(zero));                   \
+    return v;                                                                       \
+  }                                                                                 \
+  }

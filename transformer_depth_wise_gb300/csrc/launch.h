@@ -76,5 +76,15 @@ struct Phase1Args {
 // Returns ATTNRES_OK or a (negative) status for shapes the kernels cannot take.
 int phase1_check(int n, int D, int dtype, int S);
 cudaError_t launch_phase1(const Phase1Args &a);
+// Tensor-core phase 1 (bf16, D = 512 * {1,2,4,8}, n <= 9, S <= 24).
+bool phase1_tc_supported(int n, int D, int dtype, int S);
+cudaError_t launch_phase1_tc(const Phase1Args &a);
+
+// Read and clear the per-file flag that records a kernel wait that ran out
+// (non-zero: at least one wait gave up).
+unsigned int take_error_aggregate();
+unsigned int take_error_merge();
+unsigned int take_error_phase1();
+unsigned int take_error_phase1_tc();
 
 }  // namespace attnres

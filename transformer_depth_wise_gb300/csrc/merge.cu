@@ -10,6 +10,8 @@
 #include "common.cuh"
 #include "launch.h"
 
+ATTNRES_DEFINE_ERROR_FLAG(take_error_merge)
+
 namespace attnres {
 
 struct MergeParams {

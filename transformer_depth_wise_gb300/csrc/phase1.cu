@@ -4,6 +4,8 @@
 // summaries, and each query's normalised output o_s plus its statistics
 // (m_s, lse_s) are written.
 //
+// This file holds the general kernel (any D up to 8192 bf16, n <= 16, S <= 64);
+// the tensor-core kernel in phase1_tc.cu takes the shapes it supports.
 // One CTA owns one token row at a time.  The row's n summaries are read
 // from HBM once, into a thread-private shared-memory stage, together with
 // their sums of squares; then every query reuses the staged row: the CTA
@@ -12,6 +14,8 @@
 // n summaries and writes o_s = sum_i alpha_i v_i.
 #include "common.cuh"
 #include "launch.h"
+
+ATTNRES_DEFINE_ERROR_FLAG(take_error_phase1)
 
 namespace attnres {
 
@@ -193,14 +197,16 @@ cudaError_t run(const P1Params &p, const Cfg &c, cudaStream_t st) {
 }  // namespace
 
 int phase1_check(int n, int D, int dtype, int S) {
-  if (n > kP1MaxN) return ATTNRES_ERR_TOO_MANY_SOURCES;
   if (S < 1 || S > kMaxQueries) return ATTNRES_ERR_SHAPE;
+  if (phase1_tc_supported(n, D, dtype, S)) return ATTNRES_OK;
+  if (n > kP1MaxN) return ATTNRES_ERR_TOO_MANY_SOURCES;
   Cfg c;
   if (!choose(n, D, dtype, c)) return ATTNRES_ERR_SHAPE;
   return ATTNRES_OK;
 }
 
 cudaError_t launch_phase1(const Phase1Args &a) {
+  if (phase1_tc_supported(a.n, a.D, a.dtype, a.S)) return launch_phase1_tc(a);
   Cfg c;
   if (!choose(a.n, a.D, a.dtype, c)) return cudaErrorInvalidValue;
   P1Params p;

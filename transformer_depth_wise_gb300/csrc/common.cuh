@@ -28,6 +28,7 @@ template <> struct Elt<float> {
     return make_uint4(__float_as_uint(x[0]), __float_as_uint(x[1]), __float_as_uint(x[2]),
                       __float_as_uint(x[3]));
   }
+  static __device__ __forceinline__ void unpack_again(const uint4 &v, float *x) { unpack(v, x); }
 };
 template <> struct Elt<__nv_bfloat16> {
   static constexpr int EPV = 8;
@@ -38,6 +39,18 @@ template <> struct Elt<__nv_bfloat16> {
   static __device__ __forceinline__ void unpack(const uint4 &v, float *x) {
     unpack_word(v.x, x[0], x[1]); unpack_word(v.y, x[2], x[3]);
     unpack_word(v.z, x[4], x[5]); unpack_word(v.w, x[6], x[7]);
+  }
+  // Same, but re-derived at the point of use (the compiler may not keep an
+  // earlier unpacked copy alive across a reduction: saves registers).
+  static __device__ __forceinline__ void unpack_again(const uint4 &v, float *x) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      uint32_t lo, hi;
+      asm volatile("shl.b32 %0, %2, 16;\n\tand.b32 %1, %2, 0xffff0000;" : "=r"(lo), "=r"(hi) : "r"(w[i]));
+      x[2 * i] = __uint_as_float(lo);
+      x[2 * i + 1] = __uint_as_float(hi);
+    }
   }
   static __device__ __forceinline__ uint32_t pack_word(float lo, float hi) {
     __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);  // round to nearest even

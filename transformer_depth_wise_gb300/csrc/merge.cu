@@ -65,39 +65,46 @@ merge_kernel(const __grid_constant__ MergeParams p) {
 
   const size_t row_bytes = (size_t)p.D * sizeof(T);
   const int64_t groups = (p.rows + teams_per_cta - 1) / teams_per_cta;
-  int parity = 0;
-  for (int64_t rg = blockIdx.x; rg < groups; rg += gridDim.x) {
-    const int64_t row = rg * teams_per_cta + team;
+  const int64_t my_groups = groups > (int64_t)blockIdx.x
+                                ? (groups - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
+  // Row stream of this CTA; the (o, p) loads of the next row are issued
+  // before the current row is reduced (two alternating register buffers).
+  auto load_row = [&](int64_t k, uint4 (&ov)[VPT], uint4 (&pv)[VPT]) {
+    const int64_t row = ((int64_t)blockIdx.x + k * gridDim.x) * teams_per_cta + team;
     const bool row_ok = row < p.rows;
-    const size_t row_off = (size_t)row * row_bytes;
-    uint4 ov[VPT], pv[VPT];
 #pragma unroll
-    for (int k = 0; k < VPT; ++k) {
-      ov[k] = make_uint4(0u, 0u, 0u, 0u);
-      pv[k] = make_uint4(0u, 0u, 0u, 0u);
-      const size_t off = row_off + (size_t)(lt + k * tpr) * 16;
-      if (row_ok && valid[k]) {
-        ov[k] = ld_stream(static_cast<const char *>(p.o) + off);
-        if (has_p) pv[k] = ld_stream(static_cast<const char *>(p.p) + off);
+    for (int kk = 0; kk < VPT; ++kk) {
+      ov[kk] = make_uint4(0u, 0u, 0u, 0u);
+      pv[kk] = make_uint4(0u, 0u, 0u, 0u);
+      const size_t off = (size_t)row * row_bytes + (size_t)(lt + kk * tpr) * 16;
+      if (row_ok && valid[kk]) {
+        ov[kk] = ld_stream(static_cast<const char *>(p.o) + off);
+        if (has_p) pv[kk] = ld_stream(static_cast<const char *>(p.p) + off);
       }
     }
+  };
+  int parity = 0;
+  auto process = [&](int64_t k, const uint4 (&ov)[VPT], const uint4 (&pv)[VPT]) {
+    const int64_t row = ((int64_t)blockIdx.x + k * gridDim.x) * teams_per_cta + team;
+    const bool row_ok = row < p.rows;
+    const size_t row_off = (size_t)row * row_bytes;
     if (!has_p) {  // first sublayer of a block: h = o
       if (row_ok) {
 #pragma unroll
-        for (int k = 0; k < VPT; ++k)
-          if (valid[k]) st_vec(static_cast<char *>(p.h) + row_off + (size_t)(lt + k * tpr) * 16, ov[k]);
+        for (int kk = 0; kk < VPT; ++kk)
+          if (valid[kk]) st_vec(static_cast<char *>(p.h) + row_off + (size_t)(lt + kk * tpr) * 16, ov[kk]);
         if (lt == 0 && p.lse_out) p.lse_out[row] = p.lse[row];
       }
-      continue;
+      return;
     }
     float part[2] = {0.f, 0.f};
 #pragma unroll
-    for (int k = 0; k < VPT; ++k) {
+    for (int kk = 0; kk < VPT; ++kk) {
       float x[EPV];
-      E::unpack(pv[k], x);
+      E::unpack(pv[kk], x);
 #pragma unroll
       for (int e = 0; e < EPV; ++e) {
-        part[0] = fmaf(qe[k * EPV + e], x[e], part[0]);
+        part[0] = fmaf(qe[kk * EPV + e], x[e], part[0]);
         part[1] = fmaf(x[e], x[e], part[1]);
       }
     }
@@ -108,7 +115,7 @@ merge_kernel(const __grid_constant__ MergeParams p) {
       cta_sum<2>(part, red, parity);
       parity ^= 1;
     }
-    if (!row_ok) continue;
+    if (!row_ok) return;
     const float sp = part[0] * rsqrtf(fmaf(part[1], p.inv_D, p.eps));
     const float l = p.lse[row];
     const float M = fmaxf(l, sp);
@@ -116,16 +123,27 @@ merge_kernel(const __grid_constant__ MergeParams p) {
     const float inv = 1.f / (a + c);
     const float wa = a * inv, wc = c * inv;
 #pragma unroll
-    for (int k = 0; k < VPT; ++k) {
-      if (!valid[k]) continue;
+    for (int kk = 0; kk < VPT; ++kk) {
+      if (!valid[kk]) continue;
       float xo[EPV], xp[EPV], h[EPV];
-      E::unpack(ov[k], xo);
-      E::unpack(pv[k], xp);
+      E::unpack(ov[kk], xo);
+      E::unpack_again(pv[kk], xp);
 #pragma unroll
       for (int e = 0; e < EPV; ++e) h[e] = fmaf(wa, xo[e], wc * xp[e]);
-      st_vec(static_cast<char *>(p.h) + row_off + (size_t)(lt + k * tpr) * 16, E::pack(h));
+      st_vec(static_cast<char *>(p.h) + row_off + (size_t)(lt + kk * tpr) * 16, E::pack(h));
     }
     if (lt == 0 && p.lse_out) p.lse_out[row] = M + logf(a + c);
+  };
+
+  uint4 oA[VPT], pA[VPT], oB[VPT], pB[VPT];
+  if (my_groups > 0) load_row(0, oA, pA);
+  for (int64_t k = 0; k < my_groups; k += 2) {
+    if (k + 1 < my_groups) load_row(k + 1, oB, pB);
+    process(k, oA, pA);
+    if (k + 1 < my_groups) {
+      if (k + 2 < my_groups) load_row(k + 2, oA, pA);
+      process(k + 1, oB, pB);
+    }
   }
 }
 
@@ -190,6 +208,10 @@ bool choose(int D, int dtype, Cfg &c) {
     c = {2, team, 256};
     return true;
   }
+  if (nvec <= 1024) {
+    c = {2, 0, ((nvec + 1) / 2 + 31) / 32 * 32};
+    return true;
+  }
   if (nvec <= 2048) {
     c = {4, 0, ((nvec + 3) / 4 + 31) / 32 * 32};
     return true;
@@ -220,7 +242,7 @@ cudaError_t run(const MergeParams &p, const Cfg &c, cudaStream_t st) {
 template <typename T>
 cudaError_t dispatch(const MergeParams &p, const Cfg &c, cudaStream_t st) {
   switch (c.team) {
-    case 0: return run<T, 4, 0>(p, c, st);
+    case 0: return c.vpt == 2 ? run<T, 2, 0>(p, c, st) : run<T, 4, 0>(p, c, st);
     case 4: return run<T, 2, 4>(p, c, st);
     case 8: return run<T, 2, 8>(p, c, st);
     case 16: return run<T, 2, 16>(p, c, st);

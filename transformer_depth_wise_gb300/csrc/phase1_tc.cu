@@ -21,9 +21,10 @@
 //     add hi + lo, and compute each row's partial sum of squares from the
 //     staged tile.
 //   * The partial scores and sums of squares of all CL CTAs are combined
-//     through distributed shared memory: CTA c reduces the tokens t with
-//     t % CL == c, takes the softmax over the n summaries, writes m and lse,
-//     and stores alpha into every CTA of the cluster.
+//     through distributed shared memory: every CTA pushes (remote stores)
+//     its partials of token t into the inbox of CTA t % CL, which reduces
+//     them locally, takes the softmax over the n summaries, writes m and
+//     lse, and stores alpha into every CTA of the cluster.
 //   * Eight output warps (one token each) form o_q for the CTA's slice from
 //     the staged tile and alpha, and store it.
 // Every summary byte is read from HBM once; the queries never leave the SM.
@@ -48,7 +49,7 @@ constexpr int kDc = 512;            // feature slice per CTA
 constexpr int kKB = kDc / 64;       // 64-feature K-atoms per slice
 constexpr int kMaxN = 9;            // summaries (72 of the 128 MMA rows)
 constexpr int kMaxS = 24;           // queries (2S <= 48 B-operand rows)
-constexpr int kPs = 25;             // floats per row of the partial-score table
+constexpr int kPs = kMaxS + 1;      // floats per inbox row: S partial scores + sum of squares
 constexpr int kAl = 12;             // floats per (token, query) alpha row
 constexpr int kWarps = 13;
 constexpr int kThreads = kWarps * 32;
@@ -66,7 +67,7 @@ struct Params {
   int64_t rows;
   int n, S, D, CL;
   float eps, inv_D;
-  uint32_t off_v1, off_q, off_ps, off_ss, off_al, off_bar, vbytes;
+  uint32_t off_v1, off_q, off_ps, off_al, off_bar, vbytes;
 };
 
 // --- small PTX wrappers ------------------------------------------------------
@@ -225,8 +226,7 @@ __global__ void __launch_bounds__(kThreads, 1) phase1_tc_kernel(const __grid_con
   auto OUTDONE = [&](int b) { return b0 + 8u * (11 + b); };
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 13);
 
-  float *ps = reinterpret_cast<float *>(sm + p.off_ps);    // [128][kPs] partial scores
-  float *ss = reinterpret_cast<float *>(sm + p.off_ss);    // [128] partial sums of squares
+  float *ps = reinterpret_cast<float *>(sm + p.off_ps);    // inbox [CL][8/CL][n][kPs]
   float *al = reinterpret_cast<float *>(sm + p.off_al);    // [2][8][S][kAl] alpha
 
   if (threadIdx.x == 0) {
@@ -370,21 +370,29 @@ __global__ void __launch_bounds__(kThreads, 1) phase1_tc_kernel(const __grid_con
       // CTA's output warps are done with the alpha slot about to be refilled
       if (j >= 1) wait_cluster(AREADY((int)((j - 1) & 1)), (uint32_t)(((j - 1) >> 1) & 1));
       if (j >= 2) wait_local(OUTDONE(b), (uint32_t)(((j - 2) >> 1) & 1));
+      // Push this row's partial scores and sum of squares into the inbox of
+      // the CTA that reduces token `tok` (tok % CL): slot [this CTA][tok / CL][src].
       if (live) {
+        const int owner = tok % CL, u = tok / CL;
+        const uint32_t dst = map_rank(base + p.off_ps +
+                                      (uint32_t)((((int)cta * (kTile / CL) + u) * n + src) * kPs) * 4u,
+                                      (uint32_t)owner);
 #pragma unroll
         for (int q = 0; q < kMaxS; ++q)
-          if (q < S) ps[r * kPs + q] = acc[q] + acc[kMaxS + q];
-        ss[r] = sq;
+          if (q < S) st_dsmem(dst + 4u * q, acc[q] + acc[kMaxS + q]);
+        st_dsmem(dst + 4u * kMaxS, sq);
       }
       fence_cluster();
       epi_bar();
       if (e == 0)
         for (int k = 0; k < CL; ++k) arrive_remote(map_rank(PREADY, (uint32_t)k));
       wait_cluster(PREADY, (uint32_t)(j & 1));
-      // reduce the tokens t == cta (mod CL): scores, softmax, alpha, m, lse
+      // reduce the tokens t == cta (mod CL) from the local inbox: scores,
+      // softmax, alpha, m, lse
       const int per = kTile / CL;
       for (int pr = e; pr < per * S; pr += 96) {
-        const int t = (int)cta + CL * (pr / S), q = pr % S;
+        const int u = pr / S, q = pr % S;
+        const int t = (int)cta + CL * u;
         float sc[kMaxN];
         float m = -INFINITY;
 #pragma unroll
@@ -393,8 +401,9 @@ __global__ void __launch_bounds__(kThreads, 1) phase1_tc_kernel(const __grid_con
           if (i < n) {
             float dot = 0.f, sq2 = 0.f;
             for (int k = 0; k < CL; ++k) {
-              dot += ld_dsmem(map_rank(base + p.off_ps + (uint32_t)((i * 8 + t) * kPs + q) * 4u, (uint32_t)k));
-              sq2 += ld_dsmem(map_rank(base + p.off_ss + (uint32_t)(i * 8 + t) * 4u, (uint32_t)k));
+              const float *slot = ps + ((k * per + u) * n + i) * kPs;
+              dot += slot[q];
+              sq2 += slot[kMaxS];
             }
             sc[i] = dot * rsqrtf(fmaf(sq2, p.inv_D, p.eps));
             m = fmaxf(m, sc[i]);
@@ -514,7 +523,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 struct Layout {
-  uint32_t off_v1, off_q, off_ps, off_ss, off_al, off_bar, vbytes, total;
+  uint32_t off_v1, off_q, off_ps, off_al, off_bar, vbytes, total;
 };
 
 Layout layout(int n, int S) {
@@ -524,8 +533,7 @@ Layout layout(int n, int S) {
   L.off_v1 = L.vbytes;
   L.off_q = 2 * L.vbytes;
   L.off_ps = L.off_q + (uint32_t)(kKB * NQ * 128);
-  L.off_ss = L.off_ps + 128 * kPs * 4;
-  L.off_al = L.off_ss + 128 * 4;
+  L.off_al = L.off_ps + (uint32_t)(kTile * kMaxN * kPs * 4);   // inbox: 8 tokens x n rows
   L.off_bar = L.off_al + (uint32_t)(2 * kTile * S * kAl * 4);
   L.off_bar = (L.off_bar + 15) & ~15u;
   // The MMA's A operand spans 128 rows (16 KB per K-atom); rows beyond the
@@ -582,7 +590,6 @@ cudaError_t launch_phase1_tc(const Phase1Args &a) {
   p.off_v1 = L.off_v1;
   p.off_q = L.off_q;
   p.off_ps = L.off_ps;
-  p.off_ss = L.off_ss;
   p.off_al = L.off_al;
   p.off_bar = L.off_bar;
   p.vbytes = L.vbytes;

@@ -130,7 +130,7 @@ def measured_peak():
 def kernel_traffic(kernel: str, workload: str):
     """DRAM bytes per launch from a committed ncu summary, if the kernel source is unchanged."""
     path = os.path.join(ROOT, "profiles", f"traffic_{kernel}_{workload}.txt")
-    src = {"phase1": "phase1.cu", "merge": "merge.cu", "update": "merge.cu",
+    src = {"phase1": "phase1_tc.cu", "merge": "merge.cu", "merge_update": "merge.cu", "update": "merge.cu",
            "aggregate": "aggregate.cu"}.get(kernel)
     if not src or not os.path.exists(path):
         return None
@@ -178,25 +178,12 @@ def oracle_block_rows_per_s(wl, rows_target_s: float = 12.0, max_rows: int = 409
 # ---------------------------------------------------------------------------
 # GPU arm
 # ---------------------------------------------------------------------------
-def run_two_phase(args, wl, dev, rank, world):
-    from transformer_depth_wise_gb300 import api
-    if args.rows:
-        wl = wk.Workload(wl.name, 1, args.rows, wl.D, wl.n, wl.dtype, wl.scale_lo, wl.scale_hi,
-                         S=wl.S, seed=wl.seed)
-    n_blocks = wl.n if wl.name == "two_phase_bf16" else wl.n - 1
-    inp = wk.two_phase_inputs(wl, device=dev, n=n_blocks)
-    blk = api.TwoPhaseBlock(inp["blocks"], inp["queries"], inp["gains"], inp["u"], inp["eps"])
-    stream = torch.cuda.current_stream(dev)
-    rows, D, S, elt = wl.B * wl.T, wl.D, wl.S, 2
-
-    for _ in range(args.warmup):
-        blk.run()
-    torch.cuda.synchronize(dev)
-
+def time_block(blk, K, dev, world, stream, fused):
+    """Run K block passes with per-kernel events; returns (elapsed max over ranks, events, clocks)."""
+    S = blk.S
     ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
-    K = args.steps
     events = [{"phase1": (ev(), ev()), "merge": [(ev(), ev()) for _ in range(S - 1)],
-               "update": [(ev(), ev()) for _ in range(S)]} for _ in range(K)]
+               "update": [(ev(), ev()) for _ in range(1 if fused else S)]} for _ in range(K)]
     t_start, t_end = ev(), ev()
     clocks = ClockSampler(dev.index if dev.index is not None else 0)
     barrier(world)
@@ -210,18 +197,35 @@ def run_two_phase(args, wl, dev, rank, world):
     torch.cuda.synchronize(dev)
     clk = clocks.stop()
     barrier(world)
-    elapsed_ms = max_over_ranks(t_start.elapsed_time(t_end), world, dev)
+    return max_over_ranks(t_start.elapsed_time(t_end), world, dev), events, clk
+
+
+def run_two_phase(args, wl, dev, rank, world):
+    from transformer_depth_wise_gb300 import api
+    if args.rows:
+        wl = wk.Workload(wl.name, 1, args.rows, wl.D, wl.n, wl.dtype, wl.scale_lo, wl.scale_hi,
+                         S=wl.S, seed=wl.seed)
+    n_blocks = wl.n if wl.name == "two_phase_bf16" else wl.n - 1
+    inp = wk.two_phase_inputs(wl, device=dev, n=n_blocks)
+    stream = torch.cuda.current_stream(dev)
+    rows, D, S, elt = wl.B * wl.T, wl.D, wl.S, 2
+    K = args.steps
+
+    blk = api.TwoPhaseBlock(inp["blocks"], inp["queries"], inp["gains"], inp["u"], inp["eps"], fused=True)
+    for _ in range(args.warmup):
+        blk.run()
+    torch.cuda.synchronize(dev)
+    elapsed_ms, events, clk = time_block(blk, K, dev, world, stream, fused=True)
 
     p1 = [e["phase1"][0].elapsed_time(e["phase1"][1]) for e in events]
     mg = [a.elapsed_time(b) for e in events for a, b in e["merge"]]
     up = [a.elapsed_time(b) for e in events for a, b in e["update"]]
-    b = accounting.two_phase_block_bytes(n_blocks, S, rows, D, elt)
+    b = accounting.two_phase_block_bytes(n_blocks, S, rows, D, elt, fused=True)
     kern = {
         "phase1": {"launches": K, "avg_ms": statistics.mean(p1), "bytes": b["phase1"]},
-        "merge": {"launches": K * (S - 1), "avg_ms": statistics.mean(mg),
-                  "bytes": accounting.merge_bytes(rows, D, elt)},
-        "update": {"launches": K * S, "avg_ms": statistics.mean(up),
-                   "bytes": b["updates"] / S},
+        "merge_update": {"launches": K * (S - 1), "avg_ms": statistics.mean(mg),
+                         "bytes": b["merges"] / (S - 1)},
+        "update": {"launches": K, "avg_ms": statistics.mean(up), "bytes": b["updates"]},
     }
     peak, peak_src = measured_peak()
     for name, k in kern.items():
@@ -233,10 +237,27 @@ def run_two_phase(args, wl, dev, rank, world):
     traffic = kernel_traffic(dom, wl.name)
     roofline = {"bound": "hbm", "kernel": dom, "achieved": round(d["gbs"], 1), "peak": peak,
                 "unit": "GB/s", "frac": round(d["frac"], 4), "traffic": traffic,
-                "algorithmic_bytes_per_launch": d["bytes"], "peak_source": peak_src + " hbm_gbs"}
+                "algorithmic_bytes_per_launch": d["bytes"],
+                "peak_source": peak_src + " hbm_gbs (copy bandwidth)"}
 
     tokens = rows * K * world
     value = tokens / (elapsed_ms * 1e-3)
+
+    # The same block pass without the fused update+merge, for comparison.
+    blk_u = api.TwoPhaseBlock(inp["blocks"], inp["queries"], inp["gains"], inp["u"], inp["eps"],
+                              fused=False)
+    for _ in range(args.warmup):
+        blk_u.run()
+    torch.cuda.synchronize(dev)
+    el_u, ev_u, _ = time_block(blk_u, K, dev, world, stream, fused=False)
+    bu = accounting.two_phase_block_bytes(n_blocks, S, rows, D, elt, fused=False)
+    mg_u = [a.elapsed_time(c) for e in ev_u for a, c in e["merge"]]
+    up_u = [a.elapsed_time(c) for e in ev_u for a, c in e["update"]]
+    unfused = {"value": round(rows * K * world / (el_u * 1e-3), 1), "ms_per_step": round(el_u / K, 4),
+               "merge_gbs": round(bu["merges"] / (S - 1) / (statistics.mean(mg_u) * 1e-3) / 1e9, 1),
+               "update_gbs": round(bu["updates"] / S / (statistics.mean(up_u) * 1e-3) / 1e9, 1),
+               "launches_per_step": blk_u.launches_per_run}
+    del blk_u
 
     # End to end through the public API: pinned host inputs -> device, block
     # pass, final partial (the new block summary) -> pinned host, every step.
@@ -248,13 +269,15 @@ def run_two_phase(args, wl, dev, rank, world):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
         "config": {"workload": wl.name, "B": wl.B, "T": wl.T, "D": D, "n_blocks": n_blocks, "S": S,
-                   "step": f"phase 1 + {S - 1} phase-2 merges + {S} partial updates",
+                   "step": f"phase 1 + {S - 1} fused partial-update+merge + 1 partial update "
+                           f"(= phase 1 + {S - 1} merges + {S} updates)",
                    "l2": "inputs larger than L2 (every kernel streams >= 268 MB); no flush",
                    "parallelism": f"dp{world} (token rows; no collective)"},
         "achieved_hbm_gbs_step": round(b["total"] / (elapsed_ms / K * 1e-3) / 1e9, 1),
         "roofline": roofline,
         "kernels": {n: {kk: (round(v, 5) if isinstance(v, float) else v) for kk, v in k.items()}
                     for n, k in kern.items()},
+        "unfused": unfused,
         "e2e": e2e,
         "gpu_launches": K * blk.launches_per_run,
         "clocks": clk,

@@ -129,6 +129,29 @@ int attnres_partial_update(const void *h, const void *partial_in, const float *u
                            int64_t T, int64_t D, int dtype, void *partial_out, void *stream);
 
 /*
+ * Fused intra-block step: the partial-sum update of sublayer k-1 and the
+ * phase-2 merge of sublayer k in one pass (the decode-path fusion of
+ * "intra-block merge + partial-sum update" described for K3 in
+ * "Attention Residuals：当网络深度也拥有寻址能力", section "Kimi Linear 与 K3
+ * 中的接入"):
+ *   out_{k-1} = sub_out                        (u == NULL: the sublayer output)
+ *             = 0.5 * tanh(u (.) sub_out)      (u != NULL: sub_out is h_{k-1},
+ *                                               synthetic sublayer)
+ *   p_{k-1}   = (partial_in ? partial_in : 0) + out_{k-1}, rounded once,
+ *               written to partial_out
+ *   h_k       = attnres_block_phase2_merge(inter_out, inter_lse, p_{k-1}, ...)
+ * Per token it reads 3 rows and writes 2; the separate update and merge move 6.
+ *   inter_out, inter_lse, query, gain, eps, out_lse: as attnres_block_phase2_merge
+ *   partial_in  device [B,T,D] or NULL;  sub_out  device [B,T,D];  u  fp32 [D] or NULL
+ *   partial_out device [B,T,D]: may alias partial_in
+ *   h_out       device [B,T,D]: may alias sub_out (not inter_out)
+ */
+int attnres_block_merge_update(const void *inter_out, const float *inter_lse, const void *partial_in,
+                               const void *sub_out, const float *u, int64_t B, int64_t T, int64_t D,
+                               int dtype, const float *query, const float *gain, float eps,
+                               void *partial_out, void *h_out, float *out_lse, void *stream);
+
+/*
  * Full AttnRes stack forward ("FullAttnResStack", eq. A1-A4) with the
  * synthetic sublayer f_l(h) = 0.5 * tanh(u_l (.) h):
  *   for l = 1..L:  h_l = aggregate(v_0..v_{l-1}; query_l, gain_l)

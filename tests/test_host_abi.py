@@ -189,5 +189,11 @@ def test_kernel_byte_accounting_by_hand():
     b = accounting.two_phase_block_bytes(9, 24, 32768, 4096, 2)
     assert b["phase1"] == 32768 * (33 * 8192 + 24 * 4)
     assert b["merges"] == 23 * 32768 * (3 * 8192 + 4)
+    fb = accounting.two_phase_block_bytes(9, 24, 32768, 4096, 2, fused=True)
+    assert fb["merges"] == 32768 * ((4 * 8192 + 4) + 22 * (5 * 8192 + 4))
+    assert fb["updates"] == 32768 * 3 * 8192
+    # fused: 117 row transfers per token after phase 1, against 140 unfused
+    assert (fb["merges"] + fb["updates"]) // 32768 // 8192 == 117
+    assert (b["merges"] + b["updates"]) // 32768 // 8192 == 140
     # Full stack, 186 sublayers: 17391 + 187 reads and 187 writes per token row.
     assert accounting.full_stack_bytes(186, 2048, 2048, 2) == 2048 * (17391 + 187 + 187) * 4096

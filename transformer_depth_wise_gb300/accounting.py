@@ -30,11 +30,25 @@ def partial_update_bytes(rows: int, D: int, elt: int, first: bool) -> int:
     return rows * ((2 if first else 3) * D * elt)
 
 
-def two_phase_block_bytes(n: int, S: int, rows: int, D: int, elt: int) -> dict:
-    """Per-kernel algorithmic bytes of one block pass (phase 1, S-1 merges, S updates)."""
+def merge_update_bytes(rows: int, D: int, elt: int, first: bool) -> int:
+    """Fused update + merge: read o, the sublayer row and p_in (not on the first
+    step), and lse; write p and h."""
+    return rows * (((4 if first else 5) * D * elt) + 4)
+
+
+def two_phase_block_bytes(n: int, S: int, rows: int, D: int, elt: int, fused: bool = False) -> dict:
+    """Per-kernel algorithmic bytes of one block pass.
+
+    Unfused: phase 1, S-1 merges, S updates.  Fused: phase 1, S-1 fused
+    update+merge steps, 1 final update.
+    """
     p1 = phase1_bytes(n, S, rows, D, elt)
-    mg = (S - 1) * merge_bytes(rows, D, elt)
-    up = partial_update_bytes(rows, D, elt, True) + (S - 1) * partial_update_bytes(rows, D, elt, False)
+    if fused:
+        mg = merge_update_bytes(rows, D, elt, True) + (S - 2) * merge_update_bytes(rows, D, elt, False)
+        up = partial_update_bytes(rows, D, elt, S == 1)
+    else:
+        mg = (S - 1) * merge_bytes(rows, D, elt)
+        up = partial_update_bytes(rows, D, elt, True) + (S - 1) * partial_update_bytes(rows, D, elt, False)
     return {"phase1": p1, "merges": mg, "updates": up, "attnres": p1 + mg, "total": p1 + mg + up}
 
 

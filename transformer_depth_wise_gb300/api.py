@@ -155,16 +155,44 @@ def full_stack_forward(v0, queries, gains, u, eps: float = 1e-8, sources=None, y
     return y, sources
 
 
+def block_merge_update(inter_out, inter_lse, partial_in, sub_out, u, query, gain=None,
+                       eps: float = 1e-8, partial_out=None, h_out=None, out_lse=None):
+    """Fused partial update (p = p_in + f(sub_out) or p_in + sub_out) and phase-2 merge.
+
+    Returns (partial_out, h_out).
+    """
+    _cuda(inter_out, "inter_out")
+    _cuda(sub_out, "sub_out")
+    B, T, D = _btd(inter_out)
+    if partial_out is None:
+        partial_out = torch.empty_like(inter_out)
+    if h_out is None:
+        h_out = torch.empty_like(inter_out)
+    rc = _lib.lib().attnres_block_merge_update(inter_out.data_ptr(), inter_lse.data_ptr(),
+                                               _ptr(partial_in), sub_out.data_ptr(), _ptr(u), B, T, D,
+                                               _code(inter_out), _ptr(query), _ptr(gain), float(eps),
+                                               partial_out.data_ptr(), h_out.data_ptr(), _ptr(out_lse),
+                                               _stream(h_out))
+    _lib.check("attnres_block_merge_update", rc)
+    return partial_out, h_out
+
+
 class TwoPhaseBlock:
     """One block of the two-phase Block scheme over preallocated buffers.
 
-    run(): phase 1 over the cached summaries for the block's S queries, then
-    for k = 1..S the phase-2 merge (k >= 2; h_1 is the phase-1 output itself)
-    and the partial update p_k = p_{k-1} + f_k(h_k) with the synthetic
-    sublayer.  The final partial (the block's summary b_n) is returned.
+    run() computes phase 1 over the cached summaries for the block's S
+    queries, then walks the S sublayers: h_1 is the phase-1 output itself,
+    h_k (k >= 2) merges the running partial into the phase-1 state, and
+    after each sublayer the partial grows by f_k(h_k) (synthetic sublayer).
+    The final partial (the block's summary b_n) is returned.
+
+    fused=False: 23 merges + 24 partial updates (attnres_block_phase2_merge,
+    attnres_partial_update).  fused=True: 23 fused update+merge steps
+    (attnres_block_merge_update) + 1 final update.  Both give the same values.
     """
 
-    def __init__(self, blocks, queries, gains, u, eps: float = 1e-8, keep_h: bool = False):
+    def __init__(self, blocks, queries, gains, u, eps: float = 1e-8, keep_h: bool = False,
+                 fused: bool = True):
         self.blocks = list(blocks)
         self.queries, self.gains, self.u, self.eps = queries, gains, u, float(eps)
         S = queries.shape[0]
@@ -175,14 +203,18 @@ class TwoPhaseBlock:
         self.h = (torch.empty((S, *ref.shape), dtype=ref.dtype, device=ref.device) if keep_h
                   else torch.empty_like(ref))
         self.keep_h = keep_h
+        self.fused = fused
         self._arr = _lib.ptr_array([b.data_ptr() for b in self.blocks])
         self.B, self.T, self.D = _btd(ref)
         self.code = _code(ref)
         self.S = S
-        self.launches_per_run = 1 + (S - 1) + S
+        self.launches_per_run = (1 + (S - 1) + 1) if fused else (1 + (S - 1) + S)
 
-    def h_buffer(self, k: int):
-        return self.h[k] if self.keep_h else self.h
+    def _hptr(self, k: int) -> int:
+        """Device address of h_k (0-based k); h_0 is the phase-1 output o_0."""
+        if k == 0 and not self.keep_h:
+            return self.o.data_ptr()
+        return (self.h[k] if self.keep_h else self.h).data_ptr()
 
     def run(self, stream=None, events=None):
         L = _lib.lib()
@@ -192,42 +224,52 @@ class TwoPhaseBlock:
         qp, gp, up = self.queries.data_ptr(), _ptr(self.gains), self.u.data_ptr()
         row_bytes = self.o[0].numel() * self.o.element_size()
         rows = B * T
+        rec = (lambda name, k, i: events[name][k][i].record()) if events else (lambda *a: None)
         if events:
             events["phase1"][0].record()
-        rc = L.attnres_block_phase1(self._arr, len(self.blocks), B, T, D, code, qp, gp, self.S, eps,
-                                    self.o.data_ptr(), None, self.lse.data_ptr(), st)
-        _lib.check("attnres_block_phase1", rc)
+        _lib.check("attnres_block_phase1",
+                   L.attnres_block_phase1(self._arr, len(self.blocks), B, T, D, code, qp, gp, self.S, eps,
+                                          self.o.data_ptr(), None, self.lse.data_ptr(), st))
         if events:
             events["phase1"][1].record()
         op, lp, pp = self.o.data_ptr(), self.lse.data_ptr(), self.partial.data_ptr()
+        if self.keep_h:
+            self.h[0].copy_(self.o[0])
+        gk = (lambda k: None) if gp is None else (lambda k: gp + k * D4)
+        if self.fused:
+            for k in range(1, self.S):
+                rec("merge", k - 1, 0)
+                _lib.check("attnres_block_merge_update",
+                           L.attnres_block_merge_update(op + k * row_bytes, lp + k * rows * 4,
+                                                        None if k == 1 else pp, self._hptr(k - 1),
+                                                        up + (k - 1) * D4, B, T, D, code, qp + k * D4,
+                                                        gk(k), eps, pp, self._hptr(k), None, st))
+                rec("merge", k - 1, 1)
+            rec("update", 0, 0)
+            _lib.check("attnres_partial_update",
+                       L.attnres_partial_update(self._hptr(self.S - 1), pp if self.S > 1 else None,
+                                                up + (self.S - 1) * D4, B, T, D, code, pp, st))
+            rec("update", 0, 1)
+            return self.partial
         for k in range(self.S):
-            if k == 0:
-                hk = op                      # no partial yet: h_1 = o_1
-                if self.keep_h:
-                    self.h[0].copy_(self.o[0])
-            else:
-                hk = self.h_buffer(k).data_ptr()
-                if events:
-                    events["merge"][k - 1][0].record()
-                rc = L.attnres_block_phase2_merge(op + k * row_bytes, lp + k * rows * 4, pp, B, T, D,
-                                                  code, qp + k * D4, None if gp is None else gp + k * D4,
-                                                  eps, hk, None, st)
-                _lib.check("attnres_block_phase2_merge", rc)
-                if events:
-                    events["merge"][k - 1][1].record()
-            if events:
-                events["update"][k][0].record()
-            rc = L.attnres_partial_update(hk, None if k == 0 else pp, up + k * D4, B, T, D, code, pp,
-                                          st)
-            _lib.check("attnres_partial_update", rc)
-            if events:
-                events["update"][k][1].record()
+            if k > 0:
+                rec("merge", k - 1, 0)
+                _lib.check("attnres_block_phase2_merge",
+                           L.attnres_block_phase2_merge(op + k * row_bytes, lp + k * rows * 4, pp, B, T, D,
+                                                        code, qp + k * D4, gk(k), eps, self._hptr(k), None,
+                                                        st))
+                rec("merge", k - 1, 1)
+            rec("update", k, 0)
+            _lib.check("attnres_partial_update",
+                       L.attnres_partial_update(self._hptr(k), None if k == 0 else pp, up + k * D4, B, T, D,
+                                                code, pp, st))
+            rec("update", k, 1)
         return self.partial
 
 
-def block_two_phase(blocks, queries, gains, u, eps: float = 1e-8):
+def block_two_phase(blocks, queries, gains, u, eps: float = 1e-8, fused: bool = True):
     """Run one block of the two-phase scheme; returns (final partial, [h_1..h_S])."""
-    blk = TwoPhaseBlock(blocks, queries, gains, u, eps, keep_h=True)
+    blk = TwoPhaseBlock(blocks, queries, gains, u, eps, keep_h=True, fused=fused)
     p = blk.run()
     return p, blk.h
 

@@ -3,8 +3,7 @@
 //
 // A "team" of threads owns one token row; each thread owns VPT 16-byte
 // vectors of the row (vector j = lane + k * team_size, so the team's loads
-// are contiguous).  Sources are streamed in groups of G (the next group's
-// loads are issued before the current one is reduced): the team loads G
+// are contiguous).  Sources are streamed in groups of G: the team loads G
 // rows, reduces the G dot products w~.v and sums of squares v.v, turns them
 // into scores s = (w~.v) * rsqrt(v.v / D + eps) (the RMS factored out of the
 // dot), and folds the group into a running online-softmax state (m, denom,
@@ -84,101 +83,88 @@ aggregate_kernel(const __grid_constant__ AggParams p) {
   }
 
   const size_t row_bytes = (size_t)p.D * sizeof(T);
-  // The CTA walks a stream of units: unit u = (row group of this CTA, group of
-  // G sources).  Two register buffers alternate so the loads of unit u + 1
-  // are in flight while unit u is reduced.  Every thread of the CTA walks the
-  // same number of units (rows past the end are masked), so shuffles and
-  // barriers stay uniform.
   const int64_t groups = (p.rows + teams_per_cta - 1) / teams_per_cta;
-  const int ng = (p.n + G - 1) / G;
-  const int64_t my_groups = groups > (int64_t)blockIdx.x
-                                ? (groups - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
-  const int64_t units = my_groups * ng;
-
-  auto load_unit = [&](int64_t u, uint4 (&buf)[G][VPT]) {
-    const int64_t row = ((int64_t)blockIdx.x + (u / ng) * gridDim.x) * teams_per_cta + team;
-    const int i0 = (int)(u % ng) * G;
-    const bool row_ok = row < p.rows;
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-#pragma unroll
-      for (int k = 0; k < VPT; ++k) {
-        buf[g][k] = make_uint4(0u, 0u, 0u, 0u);
-        if (i0 + g < p.n && row_ok && valid[k])
-          buf[g][k] = ld_stream(static_cast<const char *>(p.src[i0 + g]) + (size_t)row * row_bytes +
-                                (size_t)(lt + k * tpr) * 16);
-      }
-    }
-  };
-
-  float acc[NE];
-  float m = -INFINITY, den = 0.f;
   int parity = 0;
-  auto process = [&](int64_t u, const uint4 (&buf)[G][VPT]) {
-    const int64_t row = ((int64_t)blockIdx.x + (u / ng) * gridDim.x) * teams_per_cta + team;
-    const int gi = (int)(u % ng), i0 = gi * G;
-    if (gi == 0) {
+  // Every team of the CTA runs the same number of iterations (rows past the
+  // end are masked), so warp shuffles and barriers stay uniform.
+  for (int64_t rg = blockIdx.x; rg < groups; rg += gridDim.x) {
+    const int64_t row = rg * teams_per_cta + team;
+    const bool row_ok = row < p.rows;
+    const size_t row_off = (size_t)row * row_bytes;
+    float acc[NE];
 #pragma unroll
-      for (int e = 0; e < NE; ++e) acc[e] = 0.f;
-      m = -INFINITY;
-      den = 0.f;
-    }
-    float part[2 * G];
+    for (int e = 0; e < NE; ++e) acc[e] = 0.f;
+    float m = -INFINITY, den = 0.f;
+
+    for (int i0 = 0; i0 < p.n; i0 += G) {
+      uint4 buf[G][VPT];
 #pragma unroll
-    for (int g = 0; g < G; ++g) {
-      float dot = 0.f, ss = 0.f;
+      for (int g = 0; g < G; ++g) {
 #pragma unroll
-      for (int k = 0; k < VPT; ++k) {
-        float x[EPV];
-        E::unpack(buf[g][k], x);
-#pragma unroll
-        for (int e = 0; e < EPV; ++e) {
-          dot = fmaf(qe[k * EPV + e], x[e], dot);
-          ss = fmaf(x[e], x[e], ss);
+        for (int k = 0; k < VPT; ++k) {
+          buf[g][k] = make_uint4(0u, 0u, 0u, 0u);
+          if (i0 + g < p.n && row_ok && valid[k])
+            buf[g][k] = ld_stream(static_cast<const char *>(p.src[i0 + g]) + row_off +
+                                  (size_t)(lt + k * tpr) * 16);
         }
       }
-      part[2 * g] = dot;
-      part[2 * g + 1] = ss;
-    }
-    if (TEAM) {
+      float part[2 * G];
 #pragma unroll
-      for (int t = 0; t < 2 * G; ++t) part[t] = team_sum_shfl<TEAM ? TEAM : 1>(part[t]);
-    } else {
-      cta_sum<2 * G>(part, red, parity);
-      parity ^= 1;
-    }
-    float s[G];
-    float gmax = -INFINITY;
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-      s[g] = -INFINITY;
-      if (i0 + g < p.n) {
-        s[g] = part[2 * g] * rsqrtf(fmaf(part[2 * g + 1], p.inv_D, p.eps));
-        gmax = fmaxf(gmax, s[g]);
-      }
-    }
-    const float m_new = fmaxf(m, gmax);
-    const float scale = expf(m - m_new);  // 0 on the first group (m = -inf)
-    den *= scale;
-#pragma unroll
-    for (int e = 0; e < NE; ++e) acc[e] *= scale;
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-      if (i0 + g < p.n) {
-        const float w = expf(s[g] - m_new);
-        den += w;
+      for (int g = 0; g < G; ++g) {
+        float dot = 0.f, ss = 0.f;
 #pragma unroll
         for (int k = 0; k < VPT; ++k) {
           float x[EPV];
-          E::unpack_again(buf[g][k], x);
+          E::unpack(buf[g][k], x);
 #pragma unroll
-          for (int e = 0; e < EPV; ++e) acc[k * EPV + e] = fmaf(w, x[e], acc[k * EPV + e]);
+          for (int e = 0; e < EPV; ++e) {
+            dot = fmaf(qe[k * EPV + e], x[e], dot);
+            ss = fmaf(x[e], x[e], ss);
+          }
+        }
+        part[2 * g] = dot;
+        part[2 * g + 1] = ss;
+      }
+      if (TEAM) {
+#pragma unroll
+        for (int t = 0; t < 2 * G; ++t) part[t] = team_sum_shfl<TEAM ? TEAM : 1>(part[t]);
+      } else {
+        cta_sum<2 * G>(part, red, parity);
+        parity ^= 1;
+      }
+      float s[G];
+      float gmax = -INFINITY;
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        s[g] = -INFINITY;
+        if (i0 + g < p.n) {
+          s[g] = part[2 * g] * rsqrtf(fmaf(part[2 * g + 1], p.inv_D, p.eps));
+          gmax = fmaxf(gmax, s[g]);
         }
       }
+      const float m_new = fmaxf(m, gmax);
+      const float scale = expf(m - m_new);  // 0 on the first group (m = -inf)
+      den *= scale;
+#pragma unroll
+      for (int e = 0; e < NE; ++e) acc[e] *= scale;
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        if (i0 + g < p.n) {
+          const float w = expf(s[g] - m_new);
+          den += w;
+#pragma unroll
+          for (int k = 0; k < VPT; ++k) {
+            float x[EPV];
+            E::unpack(buf[g][k], x);
+#pragma unroll
+            for (int e = 0; e < EPV; ++e) acc[k * EPV + e] = fmaf(w, x[e], acc[k * EPV + e]);
+          }
+        }
+      }
+      m = m_new;
     }
-    m = m_new;
-    if (gi == ng - 1 && row < p.rows) {
-      const size_t row_off = (size_t)row * row_bytes;
+
+    if (row_ok) {
       const float inv = 1.f / den;
 #pragma unroll
       for (int k = 0; k < VPT; ++k) {
@@ -195,17 +181,6 @@ aggregate_kernel(const __grid_constant__ AggParams p) {
         if (p.out_lse) p.out_lse[row] = m + logf(den);
         if (p.out_max) p.out_max[row] = m;
       }
-    }
-  };
-
-  uint4 bufA[G][VPT], bufB[G][VPT];
-  if (units > 0) load_unit(0, bufA);
-  for (int64_t u = 0; u < units; u += 2) {
-    if (u + 1 < units) load_unit(u + 1, bufB);
-    process(u, bufA);
-    if (u + 1 < units) {
-      if (u + 2 < units) load_unit(u + 2, bufA);
-      process(u + 1, bufB);
     }
   }
 }
@@ -229,10 +204,6 @@ bool choose(int D, int dtype, Cfg &c) {
     int need = (nvec + 1) / 2, team = 4;
     while (team < need) team *= 2;
     c = {2, team, 256};
-    return true;
-  }
-  if (nvec <= 512) {
-    c = {1, 0, (nvec + 31) / 32 * 32};
     return true;
   }
   if (nvec <= 1024) {
@@ -264,7 +235,7 @@ cudaError_t run(const AggParams &p, const Cfg &c, cudaStream_t st) {
 
 template <typename T, bool F>
 cudaError_t dispatch(const AggParams &p, const Cfg &c, cudaStream_t st) {
-  if (c.team == 0) return c.vpt == 1 ? run<T, 1, 0, F>(p, c, st) : run<T, 2, 0, F>(p, c, st);
+  if (c.team == 0) return run<T, 2, 0, F>(p, c, st);
   switch (c.team) {
     case 4: return run<T, 2, 4, F>(p, c, st);
     case 8: return run<T, 2, 8, F>(p, c, st);

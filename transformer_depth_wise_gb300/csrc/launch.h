@@ -46,6 +46,25 @@ struct MergeArgs {
 bool merge_supported(int D, int dtype);
 cudaError_t launch_merge(const MergeArgs &a);
 
+struct MergeUpdateArgs {
+  const void *inter_out;       // [rows, D]: phase-1 output o_k
+  const float *inter_lse;      // [rows]
+  const void *partial_in;      // [rows, D] p_{k-2} or nullptr
+  const void *sub_out;         // [rows, D] sublayer output (or input, with u)
+  const float *u;              // [D] synthetic sublayer, or nullptr
+  int64_t rows;
+  int D;
+  int dtype;
+  const float *query;
+  const float *gain;
+  float eps;
+  void *partial_out;           // [rows, D] p_{k-1}
+  void *h_out;                 // [rows, D] h_k
+  float *out_lse;
+  cudaStream_t stream;
+};
+cudaError_t launch_merge_update(const MergeUpdateArgs &a);
+
 struct PartialUpdateArgs {
   const void *h;
   const void *partial_in;      // or nullptr

@@ -65,43 +65,171 @@ merge_kernel(const __grid_constant__ MergeParams p) {
 
   const size_t row_bytes = (size_t)p.D * sizeof(T);
   const int64_t groups = (p.rows + teams_per_cta - 1) / teams_per_cta;
+  int parity = 0;
+  for (int64_t rg = blockIdx.x; rg < groups; rg += gridDim.x) {
+    const int64_t row = rg * teams_per_cta + team;
+    const bool row_ok = row < p.rows;
+    const size_t row_off = (size_t)row * row_bytes;
+    uint4 ov[VPT], pv[VPT];
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+      ov[k] = make_uint4(0u, 0u, 0u, 0u);
+      pv[k] = make_uint4(0u, 0u, 0u, 0u);
+      const size_t off = row_off + (size_t)(lt + k * tpr) * 16;
+      if (row_ok && valid[k]) {
+        ov[k] = ld_stream(static_cast<const char *>(p.o) + off);
+        if (has_p) pv[k] = ld_stream(static_cast<const char *>(p.p) + off);
+      }
+    }
+    if (!has_p) {  // first sublayer of a block: h = o
+      if (row_ok) {
+#pragma unroll
+        for (int k = 0; k < VPT; ++k)
+          if (valid[k]) st_vec(static_cast<char *>(p.h) + row_off + (size_t)(lt + k * tpr) * 16, ov[k]);
+        if (lt == 0 && p.lse_out) p.lse_out[row] = p.lse[row];
+      }
+      continue;
+    }
+    float part[2] = {0.f, 0.f};
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+      float x[EPV];
+      E::unpack(pv[k], x);
+#pragma unroll
+      for (int e = 0; e < EPV; ++e) {
+        part[0] = fmaf(qe[k * EPV + e], x[e], part[0]);
+        part[1] = fmaf(x[e], x[e], part[1]);
+      }
+    }
+    if (TEAM) {
+      part[0] = team_sum_shfl<TEAM ? TEAM : 1>(part[0]);
+      part[1] = team_sum_shfl<TEAM ? TEAM : 1>(part[1]);
+    } else {
+      cta_sum<2>(part, red, parity);
+      parity ^= 1;
+    }
+    if (!row_ok) continue;
+    const float sp = part[0] * rsqrtf(fmaf(part[1], p.inv_D, p.eps));
+    const float l = p.lse[row];
+    const float M = fmaxf(l, sp);
+    const float a = expf(l - M), c = expf(sp - M);
+    const float inv = 1.f / (a + c);
+    const float wa = a * inv, wc = c * inv;
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+      if (!valid[k]) continue;
+      float xo[EPV], xp[EPV], h[EPV];
+      E::unpack(ov[k], xo);
+      E::unpack(pv[k], xp);
+#pragma unroll
+      for (int e = 0; e < EPV; ++e) h[e] = fmaf(wa, xo[e], wc * xp[e]);
+      st_vec(static_cast<char *>(p.h) + row_off + (size_t)(lt + k * tpr) * 16, E::pack(h));
+    }
+    if (lt == 0 && p.lse_out) p.lse_out[row] = M + logf(a + c);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Fused partial update + phase-2 merge (the intra-block fusion of the K3
+// decode path: "intra-block merge + partial-sum update"), per token row:
+//   out     = sub_out                      (u == nullptr: the sublayer output)
+//           = 0.5 tanh(u (.) sub_out)      (u != nullptr: sub_out is the
+//                                           sublayer input, synthetic f)
+//   p_new   = (p_in or 0) + out            rounded once, stored
+//   h       = merge(o, lse; p_new)         eq. OS2 with the stored p_new
+// Three rows are read (o, p_in, sub_out) and two written (p_new, h), against
+// six for the separate update and merge.  p_out may alias p_in, and h_out
+// may alias sub_out (every element is read before it is written, by the
+// thread that writes it, and the rows are reduced in between).
+// ---------------------------------------------------------------------------
+struct MergeUpdateParams {
+  MergeParams m;       // o, lse, (p unused), q, g, h, lse_out, sizes
+  const void *p_in;    // or nullptr
+  const void *sub;     // sublayer output, or its input when u != nullptr
+  const float *u;      // or nullptr
+  void *p_out;
+};
+
+template <typename T, int VPT, int TEAM, bool SYNTH>
+__global__ void __launch_bounds__(TEAM ? 256 : 512)
+merge_update_kernel(const __grid_constant__ MergeUpdateParams P) {
+  using E = Elt<T>;
+  constexpr int EPV = E::EPV;
+  constexpr int NE = VPT * EPV;
+  __shared__ float red[TEAM ? 1 : 2 * 32 * 2];
+  const MergeParams &p = P.m;
+  const int tpr = TEAM ? TEAM : blockDim.x;
+  const int lt = TEAM ? (threadIdx.x % TEAM) : threadIdx.x;
+  const int teams_per_cta = TEAM ? blockDim.x / TEAM : 1;
+  const int team = TEAM ? threadIdx.x / TEAM : 0;
+  const bool has_pin = P.p_in != nullptr;
+
+  float qe[NE];
+  float ue[SYNTH ? NE : 1];
+  bool valid[VPT];
+#pragma unroll
+  for (int k = 0; k < VPT; ++k) {
+    const int j = lt + k * tpr;
+    valid[k] = j < p.nvec;
+#pragma unroll
+    for (int e4 = 0; e4 < EPV; e4 += 4) {
+      float4 w4 = make_float4(0.f, 0.f, 0.f, 0.f), g4 = make_float4(1.f, 1.f, 1.f, 1.f);
+      float4 u4 = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (valid[k]) {
+        w4 = ld_f4(p.q + j * EPV + e4);
+        if (p.g) g4 = ld_f4(p.g + j * EPV + e4);
+        if (SYNTH) u4 = ld_f4(P.u + j * EPV + e4);
+      }
+      qe[k * EPV + e4 + 0] = w4.x * g4.x;
+      qe[k * EPV + e4 + 1] = w4.y * g4.y;
+      qe[k * EPV + e4 + 2] = w4.z * g4.z;
+      qe[k * EPV + e4 + 3] = w4.w * g4.w;
+      if (SYNTH) {
+        ue[k * EPV + e4 + 0] = u4.x; ue[k * EPV + e4 + 1] = u4.y;
+        ue[k * EPV + e4 + 2] = u4.z; ue[k * EPV + e4 + 3] = u4.w;
+      }
+    }
+  }
+
+  const size_t row_bytes = (size_t)p.D * sizeof(T);
+  const int64_t groups = (p.rows + teams_per_cta - 1) / teams_per_cta;
   const int64_t my_groups = groups > (int64_t)blockIdx.x
                                 ? (groups - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
-  // Row stream of this CTA; the (o, p) loads of the next row are issued
-  // before the current row is reduced (two alternating register buffers).
-  auto load_row = [&](int64_t k, uint4 (&ov)[VPT], uint4 (&pv)[VPT]) {
+  auto load_row = [&](int64_t k, uint4 (&ov)[VPT], uint4 (&pv)[VPT], uint4 (&sv)[VPT]) {
     const int64_t row = ((int64_t)blockIdx.x + k * gridDim.x) * teams_per_cta + team;
     const bool row_ok = row < p.rows;
 #pragma unroll
     for (int kk = 0; kk < VPT; ++kk) {
-      ov[kk] = make_uint4(0u, 0u, 0u, 0u);
-      pv[kk] = make_uint4(0u, 0u, 0u, 0u);
+      ov[kk] = pv[kk] = sv[kk] = make_uint4(0u, 0u, 0u, 0u);
       const size_t off = (size_t)row * row_bytes + (size_t)(lt + kk * tpr) * 16;
       if (row_ok && valid[kk]) {
         ov[kk] = ld_stream(static_cast<const char *>(p.o) + off);
-        if (has_p) pv[kk] = ld_stream(static_cast<const char *>(p.p) + off);
+        // p_in and sub may be overwritten by this kernel: coherent loads
+        if (has_pin) pv[kk] = *reinterpret_cast<const uint4 *>(static_cast<const char *>(P.p_in) + off);
+        sv[kk] = *reinterpret_cast<const uint4 *>(static_cast<const char *>(P.sub) + off);
       }
     }
   };
   int parity = 0;
-  auto process = [&](int64_t k, const uint4 (&ov)[VPT], const uint4 (&pv)[VPT]) {
+  auto process = [&](int64_t k, const uint4 (&ov)[VPT], const uint4 (&pv)[VPT], const uint4 (&sv)[VPT]) {
     const int64_t row = ((int64_t)blockIdx.x + k * gridDim.x) * teams_per_cta + team;
     const bool row_ok = row < p.rows;
     const size_t row_off = (size_t)row * row_bytes;
-    if (!has_p) {  // first sublayer of a block: h = o
-      if (row_ok) {
-#pragma unroll
-        for (int kk = 0; kk < VPT; ++kk)
-          if (valid[kk]) st_vec(static_cast<char *>(p.h) + row_off + (size_t)(lt + kk * tpr) * 16, ov[kk]);
-        if (lt == 0 && p.lse_out) p.lse_out[row] = p.lse[row];
-      }
-      return;
-    }
+    uint4 pn[VPT];
     float part[2] = {0.f, 0.f};
 #pragma unroll
     for (int kk = 0; kk < VPT; ++kk) {
+      float xp[EPV], xs[EPV], y[EPV];
+      E::unpack(pv[kk], xp);
+      E::unpack(sv[kk], xs);
+#pragma unroll
+      for (int e = 0; e < EPV; ++e) {
+        const float out = SYNTH ? 0.5f * tanhf(ue[kk * EPV + e] * xs[e]) : xs[e];
+        y[e] = xp[e] + out;
+      }
+      pn[kk] = E::pack(y);              // the stored (rounded) partial
       float x[EPV];
-      E::unpack(pv[kk], x);
+      E::unpack_again(pn[kk], x);
 #pragma unroll
       for (int e = 0; e < EPV; ++e) {
         part[0] = fmaf(qe[kk * EPV + e], x[e], part[0]);
@@ -125,25 +253,22 @@ merge_kernel(const __grid_constant__ MergeParams p) {
 #pragma unroll
     for (int kk = 0; kk < VPT; ++kk) {
       if (!valid[kk]) continue;
+      const size_t off = row_off + (size_t)(lt + kk * tpr) * 16;
+      st_vec(static_cast<char *>(P.p_out) + off, pn[kk]);
       float xo[EPV], xp[EPV], h[EPV];
       E::unpack(ov[kk], xo);
-      E::unpack_again(pv[kk], xp);
+      E::unpack_again(pn[kk], xp);
 #pragma unroll
       for (int e = 0; e < EPV; ++e) h[e] = fmaf(wa, xo[e], wc * xp[e]);
-      st_vec(static_cast<char *>(p.h) + row_off + (size_t)(lt + kk * tpr) * 16, E::pack(h));
+      st_vec(static_cast<char *>(p.h) + off, E::pack(h));
     }
     if (lt == 0 && p.lse_out) p.lse_out[row] = M + logf(a + c);
   };
 
-  uint4 oA[VPT], pA[VPT], oB[VPT], pB[VPT];
-  if (my_groups > 0) load_row(0, oA, pA);
-  for (int64_t k = 0; k < my_groups; k += 2) {
-    if (k + 1 < my_groups) load_row(k + 1, oB, pB);
-    process(k, oA, pA);
-    if (k + 1 < my_groups) {
-      if (k + 2 < my_groups) load_row(k + 2, oA, pA);
-      process(k + 1, oB, pB);
-    }
+  for (int64_t k = 0; k < my_groups; ++k) {
+    uint4 ov[VPT], pv[VPT], sv[VPT];
+    load_row(k, ov, pv, sv);
+    process(k, ov, pv, sv);
   }
 }
 
@@ -208,10 +333,6 @@ bool choose(int D, int dtype, Cfg &c) {
     c = {2, team, 256};
     return true;
   }
-  if (nvec <= 1024) {
-    c = {2, 0, ((nvec + 1) / 2 + 31) / 32 * 32};
-    return true;
-  }
   if (nvec <= 2048) {
     c = {4, 0, ((nvec + 3) / 4 + 31) / 32 * 32};
     return true;
@@ -242,7 +363,7 @@ cudaError_t run(const MergeParams &p, const Cfg &c, cudaStream_t st) {
 template <typename T>
 cudaError_t dispatch(const MergeParams &p, const Cfg &c, cudaStream_t st) {
   switch (c.team) {
-    case 0: return c.vpt == 2 ? run<T, 2, 0>(p, c, st) : run<T, 4, 0>(p, c, st);
+    case 0: return run<T, 4, 0>(p, c, st);
     case 4: return run<T, 2, 4>(p, c, st);
     case 8: return run<T, 2, 8>(p, c, st);
     case 16: return run<T, 2, 16>(p, c, st);
@@ -250,6 +371,68 @@ cudaError_t dispatch(const MergeParams &p, const Cfg &c, cudaStream_t st) {
   }
 }
 
+
+template <typename T, int VPT, int TEAM, bool SYNTH>
+cudaError_t run_mu(const MergeUpdateParams &P, const Cfg &c, cudaStream_t st) {
+  auto kern = merge_update_kernel<T, VPT, TEAM, SYNTH>;
+  static int occ[16] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  int &o = occ[dev & 15];
+  if (o == 0) {
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, kern, c.threads, 0);
+    if (e != cudaSuccess) return e;
+    if (o < 1) o = 1;
+  }
+  const int per_cta = TEAM ? c.threads / TEAM : 1;
+  const int64_t groups = (P.m.rows + per_cta - 1) / per_cta;
+  const int64_t cap = (int64_t)o * sm_count();
+  const int grid = (int)(groups < cap ? groups : cap);
+  kern<<<grid, c.threads, 0, st>>>(P);
+  return cudaGetLastError();
+}
+
+template <typename T, bool SYNTH>
+cudaError_t dispatch_mu(const MergeUpdateParams &P, const Cfg &c, cudaStream_t st) {
+  switch (c.team) {
+    case 0: return c.vpt == 2 ? run_mu<T, 2, 0, SYNTH>(P, c, st) : run_mu<T, 4, 0, SYNTH>(P, c, st);
+    case 4: return run_mu<T, 2, 4, SYNTH>(P, c, st);
+    case 8: return run_mu<T, 2, 8, SYNTH>(P, c, st);
+    case 16: return run_mu<T, 2, 16, SYNTH>(P, c, st);
+    default: return run_mu<T, 2, 32, SYNTH>(P, c, st);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_merge_update(const MergeUpdateArgs &a) {
+  Cfg c;
+  if (!choose(a.D, a.dtype, c)) return cudaErrorInvalidValue;
+  MergeUpdateParams P;
+  P.m.o = a.inter_out;
+  P.m.lse = a.inter_lse;
+  P.m.p = nullptr;
+  P.m.nvec = a.D / epv_of(a.dtype);
+  P.m.D = a.D;
+  P.m.inv_D = 1.f / (float)a.D;
+  P.m.eps = a.eps;
+  P.m.rows = a.rows;
+  P.m.q = a.query;
+  P.m.g = a.gain;
+  P.m.h = a.h_out;
+  P.m.lse_out = a.out_lse;
+  P.p_in = a.partial_in;
+  P.sub = a.sub_out;
+  P.u = a.u;
+  P.p_out = a.partial_out;
+  const bool synth = a.u != nullptr;
+  if (a.dtype == ATTNRES_BF16)
+    return synth ? dispatch_mu<__nv_bfloat16, true>(P, c, a.stream)
+                 : dispatch_mu<__nv_bfloat16, false>(P, c, a.stream);
+  return synth ? dispatch_mu<float, true>(P, c, a.stream) : dispatch_mu<float, false>(P, c, a.stream);
+}
+
+namespace {
 }  // namespace
 
 bool merge_supported(int D, int dtype) {

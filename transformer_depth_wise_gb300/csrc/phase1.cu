@@ -198,7 +198,6 @@ cudaError_t run(const P1Params &p, const Cfg &c, cudaStream_t st) {
 
 int phase1_check(int n, int D, int dtype, int S) {
   if (S < 1 || S > kMaxQueries) return ATTNRES_ERR_SHAPE;
-  if (phase1_tc_supported(n, D, dtype, S)) return ATTNRES_OK;
   if (n > kP1MaxN) return ATTNRES_ERR_TOO_MANY_SOURCES;
   Cfg c;
   if (!choose(n, D, dtype, c)) return ATTNRES_ERR_SHAPE;
@@ -206,7 +205,10 @@ int phase1_check(int n, int D, int dtype, int S) {
 }
 
 cudaError_t launch_phase1(const Phase1Args &a) {
-  if (phase1_tc_supported(a.n, a.D, a.dtype, a.S)) return launch_phase1_tc(a);
+  // The tensor-core path parks the split queries in the last 48 D-rows of
+  // `out`, which must not overlap out[0] (where it parks alpha).
+  if (phase1_tc_supported(a.n, a.D, a.dtype, a.S) && (int64_t)(a.S - 1) * a.rows >= 48)
+    return launch_phase1_tc(a);
   Cfg c;
   if (!choose(a.n, a.D, a.dtype, c)) return cudaErrorInvalidValue;
   P1Params p;

@@ -1,38 +1,41 @@
-// phase1_tc.cu -- phase 1 of the two-phase Block scheme on the 5th-generation
-// tensor cores ("Attention Residual 深度残差", "两阶段算法（inter / intra）",
-// inter step / attn_with_stats; eq. A1-A3 for S queries at once).
+// phase1_tc.cu -- phase 1 of the two-phase Block scheme ("Attention Residual
+// 深度残差", "两阶段算法（inter / intra）", inter step / attn_with_stats;
+// eq. A1-A3 for S queries at once) for bf16 sources, in two kernels.
 //
 // Per token, phase 1 is two contractions over the n completed block
-// summaries v_i: the S x n scores s_{q,i} = w~_q . v_i / rms(v_i) (a dense
-// contraction over D with the queries shared by every token) and the S
-// outputs o_q = sum_i alpha_{q,i} v_i.  The scores run on tcgen05.mma; the
-// outputs (n = 9 terms per element) run as packed fp32x2 FMAs.
+// summaries v_i: the S x n scores s_{q,i} = w~_q . v_i / rms(v_i), a dense
+// contraction over D whose queries are shared by every token, and the S
+// outputs o_q = sum_i alpha_{q,i} v_i (n terms per element, different for
+// every token).
 //
-// Work split.  A thread-block cluster of CL = D / 512 CTAs owns a tile of 8
-// tokens; CTA c owns the feature slice [512 c, 512 c + 512).
-//   * Its slice of the folded queries w~ = w (.) gamma stays in shared memory
-//     for the whole kernel, as bf16 hi + lo parts (w~ ~= hi + lo to ~16 bits),
-//     K-major with the 128-byte swizzle: the MMA's B operand (N = 2S rows).
-//   * The tile's summary rows arrive by TMA (box 64 features x 8 tokens,
-//     128-byte swizzle) into a double-buffered stage laid out as the MMA's A
-//     operand: M = 128 rows = (source i, token t) pairs, 72 of them used.
-//   * tcgen05.mma accumulates the partial scores over the slice in TMEM
-//     (128 lanes x 2S fp32 columns); three epilogue warps read them back,
-//     add hi + lo, and compute each row's partial sum of squares from the
-//     staged tile.
-//   * The partial scores and sums of squares of all CL CTAs are combined
-//     through distributed shared memory: every CTA pushes (remote stores)
-//     its partials of token t into the inbox of CTA t % CL, which reduces
-//     them locally, takes the softmax over the n summaries, writes m and
-//     lse, and stores alpha into every CTA of the cluster.
-//   * Eight output warps (one token each) form o_q for the CTA's slice from
-//     the staged tile and alpha, and store it.
-// Every summary byte is read from HBM once; the queries never leave the SM.
+// Query split.  A small kernel folds w~ = w (.) gamma once per call and
+// splits it into bf16 hi + lo parts (w~ ~= hi + lo to ~16 bits), 48 rows of
+// D (hi at 0..S-1, lo at 24..24+S-1, unused rows zero), parked in the last
+// 48 * D elements of the output buffer -- rows that kernel B overwrites
+// after kernel A is done with them (so no scratch memory is needed).
 //
-// Synchronisation is by mbarriers only (TMA completion, MMA completion,
-// buffer release, cluster-wide "partials ready" / "alpha ready" with remote
-// arrivals).  Every wait is bounded; one that runs out records a flag and
-// the kernel runs to its end.
+// Kernel A (scores, tensor cores).  A CTA owns a tile of 128 token rows.
+// TMA streams every summary of the tile in 64-feature chunks (box 64 x 128,
+// 128-byte swizzle) through a ring of shared-memory stages, and the parked
+// query parts for the same 64 features (box 64 x 48) as the MMA's B operand
+// (N = 48); tcgen05.mma
+// accumulates, per summary i, the 128 x 48 partial scores in its own TMEM
+// columns [48 i, 48 i + 48).  Four warps (one thread per token row) read the
+// same stages to accumulate each row's sum of squares, then run the
+// epilogue: scores = (hi + lo) * rsqrt(ss / D + eps), the softmax over the n
+// summaries, m and lse to their outputs, and alpha (fp32, [n][S rounded up to
+// even]) into the
+// first S*n*4 bytes of the token's own o[0] row -- a region kernel B reads
+// before it overwrites that row with o_0, so no scratch memory is needed.
+//
+// Kernel B (outputs).  A CTA owns one token at a time, one thread per 16-byte
+// chunk of the row (D <= 4096); cp.async double-buffers the next token's n summary
+// chunks and alpha while the current token's S outputs are formed with fp32
+// FMAs and stored.
+//
+// Each summary byte is read twice (once per kernel); there is no cluster or
+// cross-CTA exchange.  Every in-kernel wait is bounded: one that runs out
+// records a flag and the kernel runs to its end.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -44,80 +47,45 @@ ATTNRES_DEFINE_ERROR_FLAG(take_error_phase1_tc)
 namespace attnres {
 namespace tc {
 
-constexpr int kTile = 8;            // tokens per tile (rows of one swizzle atom)
-constexpr int kDc = 512;            // feature slice per CTA
-constexpr int kKB = kDc / 64;       // 64-feature K-atoms per slice
-constexpr int kMaxN = 9;            // summaries (72 of the 128 MMA rows)
-constexpr int kMaxS = 24;           // queries (2S <= 48 B-operand rows)
-constexpr int kPs = kMaxS + 1;      // floats per inbox row: S partial scores + sum of squares
-constexpr int kAl = 12;             // floats per (token, query) alpha row
-constexpr int kWarps = 13;
-constexpr int kThreads = kWarps * 32;
-constexpr int kEpiWarp0 = 4;        // warps 4, 5, 6 read TMEM lanes 0-95
-constexpr int kNQ = 2 * kMaxS;      // B rows: hi parts at 0..S-1, lo parts at 24..24+S-1
-constexpr int kTmemCols = 128;      // two accumulators of kNQ (<= 64) columns
+constexpr int kRows = 128;            // token rows per tile of kernel A (MMA M)
+constexpr int kKc = 64;               // features per chunk (one 128-byte swizzle row)
+constexpr int kMaxN = 10;             // summaries: TMEM columns n * 48 <= 480
+constexpr int kMaxS = 24;             // queries
+constexpr int kNQ = 2 * kMaxS;        // B rows: hi parts at 0..S-1, lo parts at 24..24+S-1
+constexpr int kVStages = 8;           // summary chunk ring (16 KB each)
+constexpr int kQStages = 4;           // query chunk ring (6 KB each)
+constexpr uint32_t kVBytes = kRows * kKc * 2;
+constexpr uint32_t kQBytes = kNQ * kKc * 2;
+constexpr int kTmemCols = 512;
+constexpr int kWarpsA = 6;            // 0-3: sums of squares + epilogue, 4: TMA, 5: MMA
+constexpr int kThreadsA = kWarpsA * 32;
+constexpr uint32_t kOffQ = kVStages * kVBytes;
+constexpr uint32_t kOffBar = kOffQ + kQStages * kQBytes;
+constexpr uint32_t kSmemA = kOffBar + 64 * 8 + 1024;     // barriers + alignment slack
 
-struct Params {
-  CUtensorMap tmap[kMaxN];          // one per summary: [rows, D] bf16, box 64 x 8
-  const float *q;                   // [S, D]
-  const float *g;                   // [S, D] or nullptr
-  void *out;                        // [S, rows, D] bf16
-  float *out_max;                   // [S, rows] or nullptr
-  float *out_lse;                   // [S, rows]
+struct ParamsA {
+  CUtensorMap tmap[kMaxN];            // one per summary: [rows, D] bf16, box 64 x 128
+  CUtensorMap qmap;                   // parked query parts: [48, D] bf16, box 64 x 48
+  void *out;                          // [S, rows, D] bf16 (alpha parked in o[0])
+  float *out_max;                     // [S, rows] or nullptr
+  float *out_lse;                     // [S, rows]
   int64_t rows;
-  int n, S, D, CL;
+  int n, S, D;
   float eps, inv_D;
-  uint32_t off_v1, off_q, off_ps, off_al, off_bar, vbytes;
+};
+
+struct ParamsB {
+  const void *src[kMaxN];
+  void *out;
+  int64_t rows;
+  int n, S, D, nvec;
 };
 
 // --- small PTX wrappers ------------------------------------------------------
-__device__ __forceinline__ uint32_t cluster_rank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-__device__ __forceinline__ uint32_t cluster_id() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
-  return r;
-}
-__device__ __forceinline__ uint32_t cluster_count() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
-  return r;
-}
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-__device__ __forceinline__ uint32_t map_rank(uint32_t addr, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
-  return r;
-}
-__device__ __forceinline__ void arrive_remote(uint32_t addr_cluster) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" :: "r"(addr_cluster) : "memory");
-}
-__device__ __forceinline__ bool try_cluster(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
-      " selp.u32 %0, 1, 0, p;\n}"
-      : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
-  return ok != 0;
-}
 // After any wait in the process has run out, every later wait gives up at
 // once, so a broken run ends quickly instead of spending the limit per wait.
 __device__ __forceinline__ bool aborted() {
   return *reinterpret_cast<volatile unsigned int *>(&g_error_flag) != 0;
-}
-// Wait with cluster-scope acquire (the phase was completed by remote arrivals).
-__device__ __forceinline__ void wait_cluster(uint32_t bar, uint32_t parity) {
-  if (try_cluster(bar, parity)) return;
-  const unsigned long long t0 = globaltimer_ns();
-  while (!try_cluster(bar, parity)) {
-    if (aborted()) return;
-    if (globaltimer_ns() - t0 > kWaitLimitNs) { raise_timeout(); return; }
-  }
 }
 __device__ __forceinline__ void wait_local(uint32_t bar, uint32_t parity) {
   if (mbar_try(bar, parity)) return;
@@ -127,16 +95,6 @@ __device__ __forceinline__ void wait_local(uint32_t bar, uint32_t parity) {
     if (globaltimer_ns() - t0 > kWaitLimitNs) { raise_timeout(); return; }
   }
 }
-__device__ __forceinline__ float ld_dsmem(uint32_t addr) {
-  float v;
-  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
-  return v;
-}
-__device__ __forceinline__ void st_dsmem(uint32_t addr, float v) {
-  asm volatile("st.shared::cluster.f32 [%0], %1;" :: "r"(addr), "f"(v) : "memory");
-}
-__device__ __forceinline__ void fence_cluster() { asm volatile("fence.acq_rel.cluster;" ::: "memory"); }
-__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 96;" ::: "memory"); }
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y,
                                             uint32_t bar) {
@@ -186,321 +144,301 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float *v) {
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-// Packed fp32 pair helpers (fma.rn.f32x2).
-__device__ __forceinline__ uint64_t pk(float lo, float hi) {
-  uint64_t r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-  return r;
-}
-__device__ __forceinline__ void upk(uint64_t v, float &lo, float &hi) {
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-}
-__device__ __forceinline__ void fma2(uint64_t &acc, uint64_t a, uint64_t x) {
-  asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(a), "l"(x));
-}
-
 // Byte offset of 16-byte chunk `j` of row `r` inside a 1024-byte, 8-row atom
 // written by TMA (or by hand) with the 128-byte swizzle.
 __device__ __forceinline__ uint32_t swz(uint32_t r, uint32_t j) { return r * 128u + ((j ^ (r & 7u)) << 4); }
 
+
 // -----------------------------------------------------------------------------
-__global__ void __launch_bounds__(kThreads, 1) phase1_tc_kernel(const __grid_constant__ Params p) {
+// Query split: parts[row][d], row < 24: bf16(w~), row >= 24: bf16(w~ - hi)
+// -----------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) p1_qsplit_kernel(const float *__restrict__ q,
+                                                        const float *__restrict__ g, int S, int D,
+                                                        __nv_bfloat16 *__restrict__ parts) {
+  const int64_t total = (int64_t)kMaxS * D;
+  for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
+       idx += (int64_t)gridDim.x * blockDim.x) {
+    const int row = (int)(idx / D), d = (int)(idx % D);
+    float hi = 0.f, lo = 0.f;
+    if (row < S) {
+      const float qe = q[(size_t)row * D + d] * (g ? g[(size_t)row * D + d] : 1.f);
+      hi = __bfloat162float(__float2bfloat16_rn(qe));
+      lo = qe - hi;
+    }
+    parts[(size_t)row * D + d] = __float2bfloat16_rn(hi);
+    parts[(size_t)(kMaxS + row) * D + d] = __float2bfloat16_rn(lo);
+  }
+}
+
+// -----------------------------------------------------------------------------
+// Kernel A: scores on tcgen05, softmax, alpha / m / lse
+// -----------------------------------------------------------------------------
+__global__ void __launch_bounds__(kThreadsA, 1) p1_scores_kernel(const __grid_constant__ ParamsA p) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char *sm = reinterpret_cast<unsigned char *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   const uint32_t base = smem_u32(sm);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint32_t cta = cluster_rank();
-  const int n = p.n, S = p.S, CL = p.CL;
-  const uint32_t vbytes = p.vbytes;                    // one stage: n * kKB atoms of 1 KB
-
-  // barriers
-  uint64_t *bars = reinterpret_cast<uint64_t *>(sm + p.off_bar);
-  const uint32_t b0 = base + p.off_bar;
-  auto FULL = [&](int b) { return b0 + 8u * (0 + b); };
-  auto VFREE = [&](int b) { return b0 + 8u * (2 + b); };
-  auto MMADONE = [&](int b) { return b0 + 8u * (4 + b); };
-  auto TFREE = [&](int b) { return b0 + 8u * (6 + b); };
-  const uint32_t PREADY = b0 + 8u * 8;
-  auto AREADY = [&](int b) { return b0 + 8u * (9 + b); };
-  auto OUTDONE = [&](int b) { return b0 + 8u * (11 + b); };
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 13);
-
-  float *ps = reinterpret_cast<float *>(sm + p.off_ps);    // inbox [CL][8/CL][n][kPs]
-  float *al = reinterpret_cast<float *>(sm + p.off_al);    // [2][8][S][kAl] alpha
+  const int n = p.n, S = p.S;
+  const uint32_t b0 = base + kOffBar;
+  auto VFULL = [&](int s) { return b0 + 8u * s; };
+  auto VEMPTY = [&](int s) { return b0 + 8u * (kVStages + s); };
+  auto QFULL = [&](int s) { return b0 + 8u * (2 * kVStages + s); };
+  auto QEMPTY = [&](int s) { return b0 + 8u * (2 * kVStages + kQStages + s); };
+  const uint32_t TDONE = b0 + 8u * (2 * kVStages + 2 * kQStages);
+  const uint32_t TFREE = TDONE + 8u;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + kOffBar + 8 * (2 * kVStages + 2 * kQStages + 2));
 
   if (threadIdx.x == 0) {
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(FULL(b), 1);
-      mbar_init(VFREE(b), 8 + 3);
-      mbar_init(MMADONE(b), 1);
-      mbar_init(TFREE(b), 3);
-      mbar_init(AREADY(b), CL);
-      mbar_init(OUTDONE(b), 8);
+    for (int s = 0; s < kVStages; ++s) {
+      mbar_init(VFULL(s), 1);
+      mbar_init(VEMPTY(s), 1 + 4);    // the MMA's commit + the four row warps
     }
-    mbar_init(PREADY, CL);
+    for (int s = 0; s < kQStages; ++s) {
+      mbar_init(QFULL(s), 1);
+      mbar_init(QEMPTY(s), 1);
+    }
+    mbar_init(TDONE, 1);
+    mbar_init(TFREE, 4);
     fence_mbar_init();
   }
-  if (warp == 1) {
+  if (warp == 5) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
                  :: "r"(smem_u32(tmem_slot)), "r"(kTmemCols));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
-
-  // Folded query slice, bf16 hi / lo, as the B operand: row q holds the hi
-  // part of query q, row kMaxS + q its lo part, unused rows are zero; K-atom
-  // kb of all kNQ rows is contiguous (8-row groups 1 KB apart).
-  {
-    const int gq = kNQ / 8;
-    const int chunks = kNQ * (kDc / 8);
-    for (int c = threadIdx.x; c < chunks; c += kThreads) {
-      const int row = c / (kDc / 8), ch = c % (kDc / 8);
-      const int q = row < kMaxS ? row : row - kMaxS;
-      float v[8];
-      if (q < S) {
-        const int d = (int)cta * kDc + ch * 8;
-        const float4 w0 = ld_f4(p.q + (size_t)q * p.D + d), w1 = ld_f4(p.q + (size_t)q * p.D + d + 4);
-        float4 g0 = make_float4(1.f, 1.f, 1.f, 1.f), g1 = g0;
-        if (p.g) { g0 = ld_f4(p.g + (size_t)q * p.D + d); g1 = ld_f4(p.g + (size_t)q * p.D + d + 4); }
-        const float qe[8] = {w0.x * g0.x, w0.y * g0.y, w0.z * g0.z, w0.w * g0.w,
-                             w1.x * g1.x, w1.y * g1.y, w1.z * g1.z, w1.w * g1.w};
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const float hi = __bfloat162float(__float2bfloat16_rn(qe[e]));
-          v[e] = row < kMaxS ? hi : qe[e] - hi;
-        }
-      } else {
-#pragma unroll
-        for (int e = 0; e < 8; ++e) v[e] = 0.f;
-      }
-      const int kb = ch >> 3, j = ch & 7;
-      const uint32_t off = p.off_q + (uint32_t)(kb * gq + (row >> 3)) * 1024u + swz(row & 7, j);
-      *reinterpret_cast<uint4 *>(sm + off) = Elt<__nv_bfloat16>::pack(v);
-    }
-  }
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // generic writes -> tensor core
-  cluster_sync_all();
+  __syncthreads();
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   const uint32_t tmem_base = *tmem_slot;
 
-  const int64_t tiles = (p.rows + kTile - 1) / kTile;
-  const int64_t cid = cluster_id(), ncl = cluster_count();
-  const int64_t my_tiles = tiles > cid ? (tiles - cid + ncl - 1) / ncl : 0;
-  const uint32_t idesc = idesc_bf16(128, kNQ);
+  const int64_t tiles = (p.rows + kRows - 1) / kRows;
+  const int64_t my_tiles = tiles > (int64_t)blockIdx.x ? (tiles - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
+  const int KC = p.D / kKc;
 
-  if (warp == 0) {
-    // ---------------- TMA producer ----------------
+  if (warp == 4) {
+    // ---------------- TMA producer: (tile, chunk, summary) stages ----------------
     if (lane == 0) {
-      for (int64_t j = 0; j < my_tiles; ++j) {
-        const int b = (int)(j & 1);
-        const int64_t tile = cid + j * ncl;
-        if (j >= 2) wait_local(VFREE(b), (uint32_t)(((j - 2) >> 1) & 1));
-        mbar_expect_tx(FULL(b), vbytes);
-        const uint32_t vb = base + (b ? p.off_v1 : 0u);
-        for (int kb = 0; kb < kKB; ++kb)
-          for (int i = 0; i < n; ++i)
-            tma_load_2d(vb + (uint32_t)(kb * n + i) * 1024u, &p.tmap[i], (int)cta * kDc + kb * 64,
-                        (int)(tile * kTile), FULL(b));
+      int64_t g = 0, gq = 0;
+      for (int64_t tl = 0; tl < my_tiles; ++tl) {
+        const int64_t tile = blockIdx.x + tl * gridDim.x;
+        for (int kc = 0; kc < KC; ++kc, ++gq) {
+          const int sq = (int)(gq % kQStages);
+          if (gq >= kQStages) wait_local(QEMPTY(sq), (uint32_t)((gq / kQStages - 1) & 1));
+          mbar_expect_tx(QFULL(sq), kQBytes);
+          tma_load_2d(base + kOffQ + (uint32_t)sq * kQBytes, &p.qmap, kc * kKc, 0, QFULL(sq));
+          for (int i = 0; i < n; ++i, ++g) {
+            const int s = (int)(g % kVStages);
+            if (g >= kVStages) wait_local(VEMPTY(s), (uint32_t)((g / kVStages - 1) & 1));
+            mbar_expect_tx(VFULL(s), kVBytes);
+            tma_load_2d(base + (uint32_t)s * kVBytes, &p.tmap[i], kc * kKc, (int)(tile * kRows), VFULL(s));
+          }
+        }
       }
-      // drain: the last stages this CTA filled have landed before it may exit
-      for (int64_t j = my_tiles - 2 < 0 ? 0 : my_tiles - 2; j < my_tiles; ++j)
-        wait_local(FULL((int)(j & 1)), (uint32_t)((j >> 1) & 1));
+      // the last stages have landed before the CTA may exit
+      for (int64_t k = g - kVStages < 0 ? 0 : g - kVStages; k < g; ++k)
+        wait_local(VFULL((int)(k % kVStages)), (uint32_t)((k / kVStages) & 1));
     }
-  } else if (warp == 1) {
+  } else if (warp == 5) {
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
-      for (int64_t j = 0; j < my_tiles; ++j) {
-        const int b = (int)(j & 1);
-        wait_local(FULL(b), (uint32_t)((j >> 1) & 1));
-        if (j >= 2) wait_local(TFREE(b), (uint32_t)(((j - 2) >> 1) & 1));
+      const uint32_t idesc = idesc_bf16(kRows, kNQ);
+      int64_t g = 0, gq = 0;
+      for (int64_t tl = 0; tl < my_tiles; ++tl) {
+        if (tl >= 1) wait_local(TFREE, (uint32_t)((tl - 1) & 1));   // epilogue read the last tile
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-        const uint32_t vb = base + (b ? p.off_v1 : 0u);
-        const uint32_t qb = base + p.off_q;
-        const uint32_t gq = (uint32_t)(kNQ / 8);
-        for (int kb = 0; kb < kKB; ++kb) {
+        for (int kc = 0; kc < KC; ++kc, ++gq) {
+          const int sq = (int)(gq % kQStages);
+          wait_local(QFULL(sq), (uint32_t)((gq / kQStages) & 1));
+          for (int i = 0; i < n; ++i, ++g) {
+            const int s = (int)(g % kVStages);
+            wait_local(VFULL(s), (uint32_t)((g / kVStages) & 1));
+            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            const uint64_t a = sw128_desc(vb + (uint32_t)(kb * n) * 1024u + kk * 32u, 1024u);
-            const uint64_t bq = sw128_desc(qb + (uint32_t)kb * gq * 1024u + kk * 32u, 1024u);
-            mma_bf16(tmem_base + (uint32_t)b * 64u, a, bq, idesc, (kb | kk) != 0);
-          }
-        }
-        mma_commit(MMADONE(b));
-      }
-    }
-  } else if (warp >= kEpiWarp0 && warp < kEpiWarp0 + 3) {
-    // ---------------- epilogue: scores, sums of squares, cluster reduce ----------------
-    const int e = threadIdx.x - kEpiWarp0 * 32;          // 0..95 = TMEM lane = MMA row
-    const int r = e, src = r >> 3, tok = r & 7;
-    const bool live = r < 8 * n;
-    for (int64_t j = 0; j < my_tiles; ++j) {
-      const int b = (int)(j & 1);
-      const uint32_t ph = (uint32_t)((j >> 1) & 1);
-      const int64_t tile = cid + j * ncl;
-      wait_local(FULL(b), ph);
-      wait_local(MMADONE(b), ph);
-      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-      float acc[48];
-      const uint32_t taddr = tmem_base + ((uint32_t)((warp & 3) * 32) << 16) + (uint32_t)b * 64u;
-      tmem_ld16(taddr, acc);
-      tmem_ld16(taddr + 16, acc + 16);
-      tmem_ld16(taddr + 32, acc + 32);
-      asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-      asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-      __syncwarp();
-      if (lane == 0) mbar_arrive(TFREE(b));
-      // partial sum of squares of row (src, tok) over this CTA's slice
-      float sq = 0.f;
-      if (live) {
-        const unsigned char *vrow = sm + (b ? p.off_v1 : 0u) + src * 1024;
-        for (int kb = 0; kb < kKB; ++kb) {
-#pragma unroll
-          for (int jj = 0; jj < 8; ++jj) {
-            float x[8];
-            Elt<__nv_bfloat16>::unpack(
-                *reinterpret_cast<const uint4 *>(vrow + kb * n * 1024 + swz(tok, jj)), x);
-#pragma unroll
-            for (int q = 0; q < 8; ++q) sq = fmaf(x[q], x[q], sq);
-          }
-        }
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(VFREE(b));
-      // every CTA has finished reading this CTA's previous partials, and every
-      // CTA's output warps are done with the alpha slot about to be refilled
-      if (j >= 1) wait_cluster(AREADY((int)((j - 1) & 1)), (uint32_t)(((j - 1) >> 1) & 1));
-      if (j >= 2) wait_local(OUTDONE(b), (uint32_t)(((j - 2) >> 1) & 1));
-      // Push this row's partial scores and sum of squares into the inbox of
-      // the CTA that reduces token `tok` (tok % CL): slot [this CTA][tok / CL][src].
-      if (live) {
-        const int owner = tok % CL, u = tok / CL;
-        const uint32_t dst = map_rank(base + p.off_ps +
-                                      (uint32_t)((((int)cta * (kTile / CL) + u) * n + src) * kPs) * 4u,
-                                      (uint32_t)owner);
-#pragma unroll
-        for (int q = 0; q < kMaxS; ++q)
-          if (q < S) st_dsmem(dst + 4u * q, acc[q] + acc[kMaxS + q]);
-        st_dsmem(dst + 4u * kMaxS, sq);
-      }
-      fence_cluster();
-      epi_bar();
-      if (e == 0)
-        for (int k = 0; k < CL; ++k) arrive_remote(map_rank(PREADY, (uint32_t)k));
-      wait_cluster(PREADY, (uint32_t)(j & 1));
-      // reduce the tokens t == cta (mod CL) from the local inbox: scores,
-      // softmax, alpha, m, lse
-      const int per = kTile / CL;
-      for (int pr = e; pr < per * S; pr += 96) {
-        const int u = pr / S, q = pr % S;
-        const int t = (int)cta + CL * u;
-        float sc[kMaxN];
-        float m = -INFINITY;
-#pragma unroll
-        for (int i = 0; i < kMaxN; ++i) {
-          sc[i] = -INFINITY;
-          if (i < n) {
-            float dot = 0.f, sq2 = 0.f;
-            for (int k = 0; k < CL; ++k) {
-              const float *slot = ps + ((k * per + u) * n + i) * kPs;
-              dot += slot[q];
-              sq2 += slot[kMaxS];
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint64_t a = sw128_desc(base + (uint32_t)s * kVBytes + kk * 32u, 1024u);
+              const uint64_t b = sw128_desc(base + kOffQ + (uint32_t)sq * kQBytes + kk * 32u, 1024u);
+              mma_bf16(tmem_base + (uint32_t)(i * kNQ), a, b, idesc, (kc | kk) != 0);
             }
-            sc[i] = dot * rsqrtf(fmaf(sq2, p.inv_D, p.eps));
-            m = fmaxf(m, sc[i]);
+            mma_commit(VEMPTY(s));
           }
+          mma_commit(QEMPTY(sq));
         }
-        float den = 0.f;
-#pragma unroll
-        for (int i = 0; i < kMaxN; ++i) {
-          sc[i] = i < n ? expf(sc[i] - m) : 0.f;
-          den += sc[i];
-        }
-        const float inv = 1.f / den;
-        const uint32_t aoff = p.off_al + (uint32_t)(((b * kTile + t) * S + q) * kAl) * 4u;
-        for (int k = 0; k < CL; ++k) {
-          const uint32_t ra = map_rank(base + aoff, (uint32_t)k);
-#pragma unroll
-          for (int i = 0; i < kMaxN; ++i)
-            if (i < n) st_dsmem(ra + 4u * i, sc[i] * inv);
-        }
-        const int64_t row = tile * kTile + t;
-        if (row < p.rows) {
-          p.out_lse[(size_t)q * p.rows + row] = m + logf(den);
-          if (p.out_max) p.out_max[(size_t)q * p.rows + row] = m;
-        }
+        mma_commit(TDONE);
       }
-      fence_cluster();
-      epi_bar();
-      if (e == 0)
-        for (int k = 0; k < CL; ++k) arrive_remote(map_rank(AREADY(b), (uint32_t)k));
     }
   } else {
-    // ---------------- output warps: o_q = sum_i alpha_qi v_i for one token ----------------
-    const int ow = warp < kEpiWarp0 ? warp - 2 : warp - (kEpiWarp0 + 3) + 2;   // 0..7
-    const int t = ow;
-    for (int64_t j = 0; j < my_tiles; ++j) {
-      const int b = (int)(j & 1);
-      const uint32_t ph = (uint32_t)((j >> 1) & 1);
-      const int64_t tile = cid + j * ncl;
-      const int64_t row = tile * kTile + t;
-      wait_local(FULL(b), ph);
-      wait_cluster(AREADY(b), ph);
-      if (row < p.rows) {
-        const unsigned char *vb = sm + (b ? p.off_v1 : 0u);
-        const float *arow = al + (size_t)((b * kTile + t) * S) * kAl;
-#pragma unroll 1
-        for (int it = 0; it < 2; ++it) {
-          const int ch = lane + 32 * it;                 // 16-byte chunk of the slice
-          const int kb = ch >> 3, jj = ch & 7;
-          uint64_t x[kMaxN][4];
+    // ---------------- warps 0-3: row sums of squares, then the epilogue ----------------
+    const int r = threadIdx.x;                                   // token row in the tile = TMEM lane
+    const uint32_t taddr = tmem_base + ((uint32_t)(warp * 32) << 16);
+    int64_t g = 0;
+    for (int64_t tl = 0; tl < my_tiles; ++tl) {
+      const int64_t tile = blockIdx.x + tl * gridDim.x;
+      float ss[kMaxN];
 #pragma unroll
-          for (int i = 0; i < kMaxN; ++i) {
-            if (i < n) {
-              const uint4 v = *reinterpret_cast<const uint4 *>(vb + (kb * n + i) * 1024 + swz(t, jj));
-              float f[8];
-              Elt<__nv_bfloat16>::unpack(v, f);
+      for (int i = 0; i < kMaxN; ++i) ss[i] = 0.f;
+      for (int kc = 0; kc < KC; ++kc) {
 #pragma unroll
-              for (int m2 = 0; m2 < 4; ++m2) x[i][m2] = pk(f[2 * m2], f[2 * m2 + 1]);
+        for (int i = 0; i < kMaxN; ++i) {
+          if (i < n) {
+            const int s = (int)(g % kVStages);
+            wait_local(VFULL(s), (uint32_t)((g / kVStages) & 1));
+            const unsigned char *row = sm + (uint32_t)s * kVBytes;
+            float acc = 0.f;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              float x[8];
+              Elt<__nv_bfloat16>::unpack(*reinterpret_cast<const uint4 *>(row + swz((uint32_t)r, (uint32_t)j)), x);
+#pragma unroll
+              for (int e = 0; e < 8; ++e) acc = fmaf(x[e], x[e], acc);
             }
-          }
-          char *dst = static_cast<char *>(p.out) +
-                      ((size_t)row * p.D + (size_t)cta * kDc + (size_t)ch * 8) * 2;
-          const size_t qstride = (size_t)p.rows * p.D * 2;
-#pragma unroll 2
-          for (int q = 0; q < S; ++q) {
-            const float4 a0 = *reinterpret_cast<const float4 *>(arow + q * kAl);
-            const float4 a1 = *reinterpret_cast<const float4 *>(arow + q * kAl + 4);
-            const float a2 = arow[q * kAl + 8];
-            const float av[kMaxN] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w, a2};
-            uint64_t acc[4] = {0, 0, 0, 0};
-#pragma unroll
-            for (int i = 0; i < kMaxN; ++i) {
-              if (i < n) {
-                const uint64_t ai = pk(av[i], av[i]);
-#pragma unroll
-                for (int m2 = 0; m2 < 4; ++m2) fma2(acc[m2], ai, x[i][m2]);
-              }
-            }
-            float h[8];
-#pragma unroll
-            for (int m2 = 0; m2 < 4; ++m2) upk(acc[m2], h[2 * m2], h[2 * m2 + 1]);
-            st_stream(dst + (size_t)q * qstride, Elt<__nv_bfloat16>::pack(h));
+            ss[i] += acc;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(VEMPTY(s));
+            ++g;
           }
         }
       }
+      // epilogue: scores -> softmax over the n summaries -> alpha, m, lse
+      wait_local(TDONE, (uint32_t)(tl & 1));
+      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      float rinv[kMaxN];
+#pragma unroll
+      for (int i = 0; i < kMaxN; ++i) rinv[i] = rsqrtf(fmaf(ss[i], p.inv_D, p.eps));
+      float m[kMaxS], den[kMaxS];
+#pragma unroll
+      for (int q = 0; q < kMaxS; ++q) { m[q] = -INFINITY; den[q] = 0.f; }
+      float c[kNQ];
+#pragma unroll
+      for (int i = 0; i < kMaxN; ++i) {                          // pass 1: max
+        if (i >= n) continue;
+        tmem_ld16(taddr + i * kNQ, c);
+        tmem_ld16(taddr + i * kNQ + 16, c + 16);
+        tmem_ld16(taddr + i * kNQ + 32, c + 32);
+        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+        for (int q = 0; q < kMaxS; ++q) m[q] = fmaxf(m[q], (c[q] + c[kMaxS + q]) * rinv[i]);
+      }
+#pragma unroll
+      for (int i = 0; i < kMaxN; ++i) {                          // pass 2: denominators
+        if (i >= n) continue;
+        tmem_ld16(taddr + i * kNQ, c);
+        tmem_ld16(taddr + i * kNQ + 16, c + 16);
+        tmem_ld16(taddr + i * kNQ + 32, c + 32);
+        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+        for (int q = 0; q < kMaxS; ++q) den[q] += expf((c[q] + c[kMaxS + q]) * rinv[i] - m[q]);
+      }
+      const int64_t row = tile * kRows + r;
+      const bool row_ok = row < p.rows;
+      float *alpha = reinterpret_cast<float *>(static_cast<char *>(p.out) + (size_t)row * p.D * 2);
+#pragma unroll
+      for (int i = 0; i < kMaxN; ++i) {                          // pass 3: alpha [n][S]
+        if (i >= n) continue;
+        tmem_ld16(taddr + i * kNQ, c);
+        tmem_ld16(taddr + i * kNQ + 16, c + 16);
+        tmem_ld16(taddr + i * kNQ + 32, c + 32);
+        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+        float a[kMaxS];
+#pragma unroll
+        for (int q = 0; q < kMaxS; ++q) a[q] = expf((c[q] + c[kMaxS + q]) * rinv[i] - m[q]) / den[q];
+        if (row_ok) {
+          const int Sp = S + (S & 1);
+#pragma unroll
+          for (int q = 0; q < kMaxS; ++q)
+            if (q < S) alpha[i * Sp + q] = a[q];
+        }
+      }
+      asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(VFREE(b));
-        mbar_arrive(OUTDONE(b));
+      if (lane == 0) mbar_arrive(TFREE);
+      if (row_ok) {
+#pragma unroll
+        for (int q = 0; q < kMaxS; ++q) {
+          if (q < S) {
+            p.out_lse[(size_t)q * p.rows + row] = m[q] + logf(den[q]);
+            if (p.out_max) p.out_max[(size_t)q * p.rows + row] = m[q];
+          }
+        }
       }
     }
   }
-
-  __syncwarp();
-  cluster_sync_all();   // no CTA leaves while a peer may still touch its shared memory
-  if (warp == 1) {
+  __syncthreads();
+  if (warp == 5) {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" :: "r"(tmem_base), "r"(kTmemCols));
+  }
+}
+
+// -----------------------------------------------------------------------------
+// Kernel B: outputs o_q = sum_i alpha_{q,i} v_i
+// -----------------------------------------------------------------------------
+__device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" :: "r"(smem_u32(smem)), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" :: "n"(N) : "memory"); }
+
+__global__ void __launch_bounds__(512, 1) p1_outputs_kernel(const __grid_constant__ ParamsB p) {
+  extern __shared__ uint4 vbuf[];                     // [2][n][nvec] 16-byte chunks
+  __shared__ __align__(16) float alpha[2][kMaxN * kMaxS];   // [n][S rounded up to even]
+  const int tid = threadIdx.x;
+  const int n = p.n, S = p.S, nvec = p.nvec;
+  const size_t row_bytes = (size_t)p.D * 2;
+  const int64_t my = p.rows > (int64_t)blockIdx.x ? (p.rows - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
+  const int Sp = S + (S & 1);                          // alpha row stride (8-byte pairs)
+  const int alpha_vecs = (n * Sp + 3) / 4;
+
+  auto prefetch = [&](int64_t k, int buf) {
+    const int64_t t = blockIdx.x + k * gridDim.x;
+    if (tid < nvec) {
+      for (int i = 0; i < n; ++i)
+        cp_async16(&vbuf[(size_t)(buf * n + i) * nvec + tid],
+                   static_cast<const char *>(p.src[i]) + (size_t)t * row_bytes + (size_t)tid * 16);
+    }
+    if (tid < alpha_vecs)
+      cp_async16(&alpha[buf][tid * 4], static_cast<const char *>(p.out) + (size_t)t * row_bytes + (size_t)tid * 16);
+    cp_async_commit();
+  };
+
+  if (my > 0) prefetch(0, 0);
+  for (int64_t k = 0; k < my; ++k) {
+    const int buf = (int)(k & 1);
+    const int64_t t = blockIdx.x + k * gridDim.x;
+    if (k + 1 < my) {
+      prefetch(k + 1, buf ^ 1);
+      cp_async_wait<1>();
+    } else {
+      cp_async_wait<0>();
+    }
+    __syncthreads();    // stage `buf` complete for every thread; alpha of t read before o[0][t] is written
+    if (tid < nvec) {
+      float x[kMaxN][8];
+#pragma unroll
+      for (int i = 0; i < kMaxN; ++i)
+        if (i < n) Elt<__nv_bfloat16>::unpack(vbuf[(size_t)(buf * n + i) * nvec + tid], x[i]);
+      char *dst = static_cast<char *>(p.out) + (size_t)t * row_bytes + (size_t)tid * 16;
+      const size_t qstride = (size_t)p.rows * row_bytes;
+      const float *al = alpha[buf];
+      for (int q = 0; q < S; q += 2) {                 // queries in pairs; an odd tail is dropped
+        float h0[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        float h1[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int i = 0; i < kMaxN; ++i) {
+          if (i < n) {
+            const float2 a = *reinterpret_cast<const float2 *>(al + i * Sp + q);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              h0[e] = fmaf(a.x, x[i][e], h0[e]);
+              h1[e] = fmaf(a.y, x[i][e], h1[e]);
+            }
+          }
+        }
+        st_stream(dst + (size_t)q * qstride, Elt<__nv_bfloat16>::pack(h0));
+        if (q + 1 < S) st_stream(dst + (size_t)(q + 1) * qstride, Elt<__nv_bfloat16>::pack(h1));
+      }
+    }
+    __syncthreads();    // every thread is done with stage `buf` before it is refilled
   }
 }
 
@@ -522,38 +460,15 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-struct Layout {
-  uint32_t off_v1, off_q, off_ps, off_al, off_bar, vbytes, total;
-};
-
-Layout layout(int n, int S) {
-  Layout L;
-  const int NQ = kNQ;
-  L.vbytes = (uint32_t)(n * kKB * 1024);
-  L.off_v1 = L.vbytes;
-  L.off_q = 2 * L.vbytes;
-  L.off_ps = L.off_q + (uint32_t)(kKB * NQ * 128);
-  L.off_al = L.off_ps + (uint32_t)(kTile * kMaxN * kPs * 4);   // inbox: 8 tokens x n rows
-  L.off_bar = L.off_al + (uint32_t)(2 * kTile * S * kAl * 4);
-  L.off_bar = (L.off_bar + 15) & ~15u;
-  // The MMA's A operand spans 128 rows (16 KB per K-atom); rows beyond the
-  // n * 8 staged ones read whatever follows (their results are unused), so
-  // keep at least 16 KB past the start of the last K-atom of stage 1.
-  uint32_t need = L.off_bar + 14 * 8 + 16;
-  const uint32_t a_reach = L.off_v1 + (uint32_t)((kKB - 1) * n * 1024) + 16 * 1024;
-  if (need < a_reach) need = a_reach;
-  L.total = need + 1024;   // alignment slack
-  return L;
-}
+size_t smem_b(int n, int D) { return (size_t)2 * n * (D / 8) * 16; }
 
 }  // namespace tc
 
 bool phase1_tc_supported(int n, int D, int dtype, int S) {
   if (dtype != ATTNRES_BF16 || n < 1 || n > tc::kMaxN || S < 1 || S > tc::kMaxS) return false;
-  if (D % tc::kDc != 0) return false;
-  const int CL = D / tc::kDc;
-  if (CL != 1 && CL != 2 && CL != 4 && CL != 8) return false;
-  if (tc::layout(n, S).total > 227 * 1024) return false;
+  if (D % tc::kKc != 0 || D > 4096) return false;            // kernel B: one thread per 16 bytes
+  if ((size_t)(S + (S & 1)) * n * 4 > (size_t)D * 2) return false;   // alpha fits in o[0]'s row
+  if (tc::smem_b(n, D) > 200 * 1024) return false;
   return tc::encode_fn() != nullptr;
 }
 
@@ -561,63 +476,75 @@ cudaError_t launch_phase1_tc(const Phase1Args &a) {
   using namespace tc;
   auto encode = encode_fn();
   if (!encode) return cudaErrorNotSupported;
-  Params p;
-  memset(&p, 0, sizeof(p));
+  // Kernel A
+  ParamsA pa;
+  memset(&pa, 0, sizeof(pa));
   for (int i = 0; i < a.n; ++i) {
     cuuint64_t dims[2] = {(cuuint64_t)a.D, (cuuint64_t)a.rows};
     cuuint64_t strides[1] = {(cuuint64_t)a.D * 2};
-    cuuint32_t box[2] = {64, kTile};
+    cuuint32_t box[2] = {kKc, kRows};
     cuuint32_t estr[2] = {1, 1};
-    CUresult r = encode(&p.tmap[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(a.blocks[i]),
+    CUresult r = encode(&pa.tmap[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(a.blocks[i]),
                         dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
   }
-  const Layout L = layout(a.n, a.S);
-  p.q = a.queries;
-  p.g = a.gains;
-  p.out = a.out;
-  p.out_max = a.out_max;
-  p.out_lse = a.out_lse;
-  p.rows = a.rows;
-  p.n = a.n;
-  p.S = a.S;
-  p.D = a.D;
-  p.CL = a.D / kDc;
-  p.eps = a.eps;
-  p.inv_D = 1.f / (float)a.D;
-  p.off_v1 = L.off_v1;
-  p.off_q = L.off_q;
-  p.off_ps = L.off_ps;
-  p.off_al = L.off_al;
-  p.off_bar = L.off_bar;
-  p.vbytes = L.vbytes;
-
-  cudaError_t e = cudaFuncSetAttribute(phase1_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)L.total);
+  // park the query parts in the last 48 rows (of D) of the output buffer
+  __nv_bfloat16 *parts = static_cast<__nv_bfloat16 *>(a.out) + ((size_t)a.S * a.rows - kNQ) * a.D;
+  {
+    const int64_t total = (int64_t)kMaxS * a.D;
+    const int blocks = (int)((total + 255) / 256 < 4 * sm_count() ? (total + 255) / 256 : 4 * sm_count());
+    p1_qsplit_kernel<<<blocks, 256, 0, a.stream>>>(a.queries, a.gains, a.S, a.D, parts);
+    cudaError_t e0 = cudaGetLastError();
+    if (e0 != cudaSuccess) return e0;
+  }
+  {
+    cuuint64_t dims[2] = {(cuuint64_t)a.D, (cuuint64_t)kNQ};
+    cuuint64_t strides[1] = {(cuuint64_t)a.D * 2};
+    cuuint32_t box[2] = {kKc, kNQ};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = encode(&pa.qmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, parts, dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  }
+  pa.out = a.out;
+  pa.out_max = a.out_max;
+  pa.out_lse = a.out_lse;
+  pa.rows = a.rows;
+  pa.n = a.n;
+  pa.S = a.S;
+  pa.D = a.D;
+  pa.eps = a.eps;
+  pa.inv_D = 1.f / (float)a.D;
+  cudaError_t e = cudaFuncSetAttribute(p1_scores_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)kSmemA);
   if (e != cudaSuccess) return e;
-  cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = (unsigned)p.CL;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  cfg.blockDim = dim3(kThreads, 1, 1);
-  cfg.dynamicSmemBytes = L.total;
-  cfg.stream = a.stream;
-  cfg.gridDim = dim3((unsigned)p.CL, 1, 1);
-  int max_clusters = 0;
-  e = cudaOccupancyMaxActiveClusters(&max_clusters, phase1_tc_kernel, &cfg);
+  const int64_t tiles = (a.rows + kRows - 1) / kRows;
+  const int64_t ga = tiles < sm_count() ? tiles : sm_count();
+  p1_scores_kernel<<<(int)ga, kThreadsA, kSmemA, a.stream>>>(pa);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  // Kernel B
+  ParamsB pb;
+  for (int i = 0; i < a.n; ++i) pb.src[i] = a.blocks[i];
+  pb.out = a.out;
+  pb.rows = a.rows;
+  pb.n = a.n;
+  pb.S = a.S;
+  pb.D = a.D;
+  pb.nvec = a.D / 8;
+  const int threads = (pb.nvec + 31) / 32 * 32;
+  const size_t smem = smem_b(a.n, a.D);
+  e = cudaFuncSetAttribute(p1_outputs_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
   if (e != cudaSuccess) return e;
-  if (max_clusters < 1) return cudaErrorInvalidConfiguration;
-  const int64_t tiles = (a.rows + kTile - 1) / kTile;
-  const int64_t ncl = tiles < max_clusters ? tiles : max_clusters;
-  cfg.gridDim = dim3((unsigned)(ncl * p.CL), 1, 1);
-  e = cudaLaunchKernelEx(&cfg, phase1_tc_kernel, p);
+  int occ = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, p1_outputs_kernel, threads, smem);
   if (e != cudaSuccess) return e;
+  if (occ < 1) occ = 1;
+  const int64_t cap = (int64_t)occ * sm_count();
+  const int64_t gb = a.rows < cap ? a.rows : cap;
+  p1_outputs_kernel<<<(int)gb, threads, smem, a.stream>>>(pb);
   return cudaGetLastError();
 }
 

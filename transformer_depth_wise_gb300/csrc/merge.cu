@@ -164,32 +164,27 @@ merge_update_kernel(const __grid_constant__ MergeUpdateParams P) {
   const int team = TEAM ? threadIdx.x / TEAM : 0;
   const bool has_pin = P.p_in != nullptr;
 
-  float qe[NE];
-  float ue[SYNTH ? NE : 1];
+  // The folded query w~ = w (.) gamma and u live in shared memory (loaded
+  // once per CTA), not in registers: fewer registers, more rows in flight.
+  // Layout [quarter e4 / 4][vector j] of float4, so consecutive lanes read
+  // consecutive 16 bytes.
+  extern __shared__ float4 qu[];                      // [EPV/4][nvec] q~, then [EPV/4][nvec] u
+  constexpr int Q4 = EPV / 4;
+  for (int idx = threadIdx.x; idx < p.nvec * Q4; idx += blockDim.x) {
+    const int j = idx / Q4, e4 = (idx % Q4) * 4;
+    const float4 w4 = ld_f4(p.q + j * EPV + e4);
+    const float4 g4 = p.g ? ld_f4(p.g + j * EPV + e4) : make_float4(1.f, 1.f, 1.f, 1.f);
+    qu[(e4 / 4) * p.nvec + j] = make_float4(w4.x * g4.x, w4.y * g4.y, w4.z * g4.z, w4.w * g4.w);
+    if (SYNTH) qu[(Q4 + e4 / 4) * p.nvec + j] = ld_f4(P.u + j * EPV + e4);
+  }
+  __syncthreads();
   bool valid[VPT];
 #pragma unroll
-  for (int k = 0; k < VPT; ++k) {
-    const int j = lt + k * tpr;
-    valid[k] = j < p.nvec;
-#pragma unroll
-    for (int e4 = 0; e4 < EPV; e4 += 4) {
-      float4 w4 = make_float4(0.f, 0.f, 0.f, 0.f), g4 = make_float4(1.f, 1.f, 1.f, 1.f);
-      float4 u4 = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (valid[k]) {
-        w4 = ld_f4(p.q + j * EPV + e4);
-        if (p.g) g4 = ld_f4(p.g + j * EPV + e4);
-        if (SYNTH) u4 = ld_f4(P.u + j * EPV + e4);
-      }
-      qe[k * EPV + e4 + 0] = w4.x * g4.x;
-      qe[k * EPV + e4 + 1] = w4.y * g4.y;
-      qe[k * EPV + e4 + 2] = w4.z * g4.z;
-      qe[k * EPV + e4 + 3] = w4.w * g4.w;
-      if (SYNTH) {
-        ue[k * EPV + e4 + 0] = u4.x; ue[k * EPV + e4 + 1] = u4.y;
-        ue[k * EPV + e4 + 2] = u4.z; ue[k * EPV + e4 + 3] = u4.w;
-      }
-    }
-  }
+  for (int k = 0; k < VPT; ++k) valid[k] = lt + k * tpr < p.nvec;
+  auto qv = [&](int k, int e) -> float {           // element e of this thread's vector k of w~
+    const float4 v = qu[(e >> 2) * p.nvec + lt + k * tpr];
+    return (e & 3) == 0 ? v.x : (e & 3) == 1 ? v.y : (e & 3) == 2 ? v.z : v.w;
+  };
 
   const size_t row_bytes = (size_t)p.D * sizeof(T);
   const int64_t groups = (p.rows + teams_per_cta - 1) / teams_per_cta;
@@ -223,18 +218,33 @@ merge_update_kernel(const __grid_constant__ MergeUpdateParams P) {
       E::unpack(pv[kk], xp);
       E::unpack(sv[kk], xs);
 #pragma unroll
+      float uu[EPV];
+      if (SYNTH && valid[kk]) {
+#pragma unroll
+        for (int e4 = 0; e4 < EPV; e4 += 4) {
+          const float4 v = qu[(Q4 + e4 / 4) * p.nvec + lt + kk * tpr];
+          uu[e4] = v.x; uu[e4 + 1] = v.y; uu[e4 + 2] = v.z; uu[e4 + 3] = v.w;
+        }
+      }
+#pragma unroll
       for (int e = 0; e < EPV; ++e) {
-        const float out = SYNTH ? 0.5f * tanhf(ue[kk * EPV + e] * xs[e]) : xs[e];
+        const float out = SYNTH ? 0.5f * tanhf((valid[kk] ? uu[e] : 0.f) * xs[e]) : xs[e];
         y[e] = xp[e] + out;
       }
       pn[kk] = E::pack(y);              // the stored (rounded) partial
+      if (!valid[kk]) continue;
       float x[EPV];
       E::unpack_again(pn[kk], x);
 #pragma unroll
-      for (int e = 0; e < EPV; ++e) {
-        part[0] = fmaf(qe[kk * EPV + e], x[e], part[0]);
-        part[1] = fmaf(x[e], x[e], part[1]);
+      for (int e4 = 0; e4 < EPV; e4 += 4) {
+        const float4 q4 = qu[(e4 / 4) * p.nvec + lt + kk * tpr];
+        part[0] = fmaf(q4.x, x[e4], part[0]);
+        part[0] = fmaf(q4.y, x[e4 + 1], part[0]);
+        part[0] = fmaf(q4.z, x[e4 + 2], part[0]);
+        part[0] = fmaf(q4.w, x[e4 + 3], part[0]);
       }
+#pragma unroll
+      for (int e = 0; e < EPV; ++e) part[1] = fmaf(x[e], x[e], part[1]);
     }
     if (TEAM) {
       part[0] = team_sum_shfl<TEAM ? TEAM : 1>(part[0]);
@@ -363,7 +373,7 @@ cudaError_t run(const MergeParams &p, const Cfg &c, cudaStream_t st) {
 template <typename T>
 cudaError_t dispatch(const MergeParams &p, const Cfg &c, cudaStream_t st) {
   switch (c.team) {
-    case 0: return run<T, 4, 0>(p, c, st);
+    case 0: return c.vpt == 2 ? run<T, 2, 0>(p, c, st) : run<T, 4, 0>(p, c, st);
     case 4: return run<T, 2, 4>(p, c, st);
     case 8: return run<T, 2, 8>(p, c, st);
     case 16: return run<T, 2, 16>(p, c, st);
@@ -375,20 +385,27 @@ cudaError_t dispatch(const MergeParams &p, const Cfg &c, cudaStream_t st) {
 template <typename T, int VPT, int TEAM, bool SYNTH>
 cudaError_t run_mu(const MergeUpdateParams &P, const Cfg &c, cudaStream_t st) {
   auto kern = merge_update_kernel<T, VPT, TEAM, SYNTH>;
-  static int occ[16] = {0};
-  int dev = 0;
+  const size_t smem = (size_t)P.m.D * sizeof(float) * (SYNTH ? 2 : 1);
+  struct Entry { int dev; size_t smem; int occ; };
+  static Entry cache[16];
+  static int used = 0;
+  int dev = 0, o = 0;
   cudaGetDevice(&dev);
-  int &o = occ[dev & 15];
+  for (int i = 0; i < used; ++i)
+    if (cache[i].dev == dev && cache[i].smem == smem) o = cache[i].occ;
   if (o == 0) {
-    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, kern, c.threads, 0);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 128 * 1024);
+    if (e != cudaSuccess) return e;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, kern, c.threads, smem);
     if (e != cudaSuccess) return e;
     if (o < 1) o = 1;
+    if (used < 16) cache[used++] = {dev, smem, o};
   }
   const int per_cta = TEAM ? c.threads / TEAM : 1;
   const int64_t groups = (P.m.rows + per_cta - 1) / per_cta;
   const int64_t cap = (int64_t)o * sm_count();
   const int grid = (int)(groups < cap ? groups : cap);
-  kern<<<grid, c.threads, 0, st>>>(P);
+  kern<<<grid, c.threads, smem, st>>>(P);
   return cudaGetLastError();
 }
 

@@ -23,15 +23,16 @@
 // columns [48 i, 48 i + 48).  Four warps (one thread per token row) read the
 // same stages to accumulate each row's sum of squares, then run the
 // epilogue: scores = (hi + lo) * rsqrt(ss / D + eps), the softmax over the n
-// summaries, m and lse to their outputs, and alpha (fp32, [n][S rounded up to
-// even]) into the
+// summaries, m and lse to their outputs, and alpha (fp32, [n][Sp][2] with
+// Sp = S rounded up to even, each value twice) into the
 // first S*n*4 bytes of the token's own o[0] row -- a region kernel B reads
 // before it overwrites that row with o_0, so no scratch memory is needed.
 //
 // Kernel B (outputs).  A CTA owns one token at a time, one thread per 16-byte
-// chunk of the row (D <= 4096); cp.async double-buffers the next token's n summary
-// chunks and alpha while the current token's S outputs are formed with fp32
-// FMAs and stored.
+// chunk of the row (D <= 4096); cp.async double-buffers the next token's n
+// summary chunks and alpha (two tokens ahead) while the current token's S
+// outputs are formed,
+// two queries at a time, with packed fp32x2 FMAs and stored.
 //
 // Each summary byte is read twice (once per kernel); there is no cluster or
 // cross-CTA exchange.  Every in-kernel wait is bounded: one that runs out
@@ -52,11 +53,13 @@ constexpr int kKc = 64;               // features per chunk (one 128-byte swizzl
 constexpr int kMaxN = 10;             // summaries: TMEM columns n * 48 <= 480
 constexpr int kMaxS = 24;             // queries
 constexpr int kNQ = 2 * kMaxS;        // B rows: hi parts at 0..S-1, lo parts at 24..24+S-1
-constexpr int kVStages = 8;           // summary chunk ring (16 KB each)
+constexpr int kVStages = 12;          // summary chunk ring (16 KB each)
 constexpr int kQStages = 4;           // query chunk ring (6 KB each)
 constexpr uint32_t kVBytes = kRows * kKc * 2;
 constexpr uint32_t kQBytes = kNQ * kKc * 2;
 constexpr int kTmemCols = 512;
+constexpr int kBStages = 3;           // kernel B: tokens in flight (cp.async stages)
+constexpr long long kWaitLimitCycles = 4000000000ll;   // ~2 s at 2 GHz: bound on any wait
 constexpr int kWarpsA = 6;            // 0-3: sums of squares + epilogue, 4: TMA, 5: MMA
 constexpr int kThreadsA = kWarpsA * 32;
 constexpr uint32_t kOffQ = kVStages * kVBytes;
@@ -89,10 +92,16 @@ __device__ __forceinline__ bool aborted() {
 }
 __device__ __forceinline__ void wait_local(uint32_t bar, uint32_t parity) {
   if (mbar_try(bar, parity)) return;
-  const unsigned long long t0 = globaltimer_ns();
-  while (!mbar_try(bar, parity)) {
-    if (aborted()) return;
-    if (globaltimer_ns() - t0 > kWaitLimitNs) { raise_timeout(); return; }
+  // try_wait already parks the thread for a while; the clock and the global
+  // abort flag are looked at only every 1024 tries, so a short wait costs
+  // no global-memory round trip.
+  const long long t0 = clock64();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try(bar, parity)) return;
+    if ((it & 1023u) == 0) {
+      if (aborted()) return;
+      if (clock64() - t0 > kWaitLimitCycles) { raise_timeout(); return; }
+    }
   }
 }
 
@@ -142,6 +151,19 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float *v) {
       : "r"(taddr));
 #pragma unroll
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Packed fp32 pairs (fma.rn.f32x2): two lanes of work per instruction.
+__device__ __forceinline__ uint64_t pk(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void upk(uint64_t v, float &lo, float &hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ void fma2(uint64_t &acc, uint64_t a, uint64_t x) {
+  asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(a), "l"(x));
 }
 
 // Byte offset of 16-byte chunk `j` of row `r` inside a 1024-byte, 8-row atom
@@ -283,15 +305,18 @@ __global__ void __launch_bounds__(kThreadsA, 1) p1_scores_kernel(const __grid_co
             const int s = (int)(g % kVStages);
             wait_local(VFULL(s), (uint32_t)((g / kVStages) & 1));
             const unsigned char *row = sm + (uint32_t)s * kVBytes;
-            float acc = 0.f;
+            uint4 v[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) v[j] = *reinterpret_cast<const uint4 *>(row + swz((uint32_t)r, (uint32_t)j));
+            float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};   // eight independent chains
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
               float x[8];
-              Elt<__nv_bfloat16>::unpack(*reinterpret_cast<const uint4 *>(row + swz((uint32_t)r, (uint32_t)j)), x);
+              Elt<__nv_bfloat16>::unpack(v[j], x);
 #pragma unroll
-              for (int e = 0; e < 8; ++e) acc = fmaf(x[e], x[e], acc);
+              for (int e = 0; e < 8; ++e) acc[e] = fmaf(x[e], x[e], acc[e]);
             }
-            ss[i] += acc;
+            ss[i] += ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
             __syncwarp();
             if (lane == 0) mbar_arrive(VEMPTY(s));
             ++g;
@@ -344,8 +369,9 @@ __global__ void __launch_bounds__(kThreadsA, 1) p1_scores_kernel(const __grid_co
         if (row_ok) {
           const int Sp = S + (S & 1);
 #pragma unroll
-          for (int q = 0; q < kMaxS; ++q)
-            if (q < S) alpha[i * Sp + q] = a[q];
+          for (int q = 0; q < kMaxS; q += 2)
+            if (q < S)
+              *reinterpret_cast<float4 *>(alpha + 2 * (i * Sp + q)) = make_float4(a[q], a[q], a[q + 1], a[q + 1]);
         }
       }
       asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -380,14 +406,14 @@ template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" :: "n"(N) : "memory"); }
 
 __global__ void __launch_bounds__(512, 1) p1_outputs_kernel(const __grid_constant__ ParamsB p) {
-  extern __shared__ uint4 vbuf[];                     // [2][n][nvec] 16-byte chunks
-  __shared__ __align__(16) float alpha[2][kMaxN * kMaxS];   // [n][S rounded up to even]
+  extern __shared__ uint4 vbuf[];                     // [kBStages][n][nvec] 16-byte chunks
+  __shared__ __align__(16) float alpha[kBStages][2 * kMaxN * kMaxS];   // [n][Sp][2]
   const int tid = threadIdx.x;
   const int n = p.n, S = p.S, nvec = p.nvec;
   const size_t row_bytes = (size_t)p.D * 2;
   const int64_t my = p.rows > (int64_t)blockIdx.x ? (p.rows - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
-  const int Sp = S + (S & 1);                          // alpha row stride (8-byte pairs)
-  const int alpha_vecs = (n * Sp + 3) / 4;
+  const int Sp = S + (S & 1);                          // queries per alpha row (even)
+  const int alpha_vecs = (2 * n * Sp) / 4;
 
   auto prefetch = [&](int64_t k, int buf) {
     const int64_t t = blockIdx.x + k * gridDim.x;
@@ -401,38 +427,51 @@ __global__ void __launch_bounds__(512, 1) p1_outputs_kernel(const __grid_constan
     cp_async_commit();
   };
 
-  if (my > 0) prefetch(0, 0);
+  // Tokens k + 1 and k + 2 are in flight while token k is formed.
+  for (int64_t k = 0; k < kBStages - 1; ++k) {
+    if (k < my) prefetch(k, (int)k);
+    else cp_async_commit();                           // keep one group per token
+  }
   for (int64_t k = 0; k < my; ++k) {
-    const int buf = (int)(k & 1);
+    const int buf = (int)(k % kBStages);
     const int64_t t = blockIdx.x + k * gridDim.x;
-    if (k + 1 < my) {
-      prefetch(k + 1, buf ^ 1);
-      cp_async_wait<1>();
-    } else {
-      cp_async_wait<0>();
-    }
+    if (k + kBStages - 1 < my) prefetch(k + kBStages - 1, (int)((k + kBStages - 1) % kBStages));
+    else cp_async_commit();
+    cp_async_wait<kBStages - 1>();
     __syncthreads();    // stage `buf` complete for every thread; alpha of t read before o[0][t] is written
     if (tid < nvec) {
-      float x[kMaxN][8];
+      uint64_t xp[kMaxN][4];                        // the row chunk of every summary, as fp32 pairs
 #pragma unroll
-      for (int i = 0; i < kMaxN; ++i)
-        if (i < n) Elt<__nv_bfloat16>::unpack(vbuf[(size_t)(buf * n + i) * nvec + tid], x[i]);
+      for (int i = 0; i < kMaxN; ++i) {
+        if (i < n) {
+          float x[8];
+          Elt<__nv_bfloat16>::unpack(vbuf[(size_t)(buf * n + i) * nvec + tid], x);
+#pragma unroll
+          for (int m = 0; m < 4; ++m) xp[i][m] = pk(x[2 * m], x[2 * m + 1]);
+        }
+      }
       char *dst = static_cast<char *>(p.out) + (size_t)t * row_bytes + (size_t)tid * 16;
       const size_t qstride = (size_t)p.rows * row_bytes;
       const float *al = alpha[buf];
-      for (int q = 0; q < S; q += 2) {                 // queries in pairs; an odd tail is dropped
-        float h0[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        float h1[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      for (int q = 0; q < S; q += 2) {              // queries in pairs
+        uint64_t acc0[4] = {0, 0, 0, 0}, acc1[4] = {0, 0, 0, 0};
 #pragma unroll
         for (int i = 0; i < kMaxN; ++i) {
           if (i < n) {
-            const float2 a = *reinterpret_cast<const float2 *>(al + i * Sp + q);
+            const float4 a = *reinterpret_cast<const float4 *>(al + 2 * (i * Sp + q));
+            const uint64_t a0 = pk(a.x, a.y), a1 = pk(a.z, a.w);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              h0[e] = fmaf(a.x, x[i][e], h0[e]);
-              h1[e] = fmaf(a.y, x[i][e], h1[e]);
+            for (int m = 0; m < 4; ++m) {
+              fma2(acc0[m], a0, xp[i][m]);
+              fma2(acc1[m], a1, xp[i][m]);
             }
           }
+        }
+        float h0[8], h1[8];
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+          upk(acc0[m], h0[2 * m], h0[2 * m + 1]);
+          upk(acc1[m], h1[2 * m], h1[2 * m + 1]);
         }
         st_stream(dst + (size_t)q * qstride, Elt<__nv_bfloat16>::pack(h0));
         if (q + 1 < S) st_stream(dst + (size_t)(q + 1) * qstride, Elt<__nv_bfloat16>::pack(h1));
@@ -460,15 +499,16 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-size_t smem_b(int n, int D) { return (size_t)2 * n * (D / 8) * 16; }
+size_t smem_b(int n, int D) { return (size_t)kBStages * n * (D / 8) * 16; }
 
 }  // namespace tc
 
 bool phase1_tc_supported(int n, int D, int dtype, int S) {
   if (dtype != ATTNRES_BF16 || n < 1 || n > tc::kMaxN || S < 1 || S > tc::kMaxS) return false;
   if (D % tc::kKc != 0 || D > 4096) return false;            // kernel B: one thread per 16 bytes
-  if ((size_t)(S + (S & 1)) * n * 4 > (size_t)D * 2) return false;   // alpha fits in o[0]'s row
-  if (tc::smem_b(n, D) > 200 * 1024) return false;
+  if ((size_t)(S + (S & 1)) * n * 8 > (size_t)D * 2) return false;   // alpha fits in o[0]'s row
+  if (tc::smem_b(n, D) + sizeof(float) * tc::kBStages * 2 * tc::kMaxN * tc::kMaxS > 227 * 1024)
+    return false;
   return tc::encode_fn() != nullptr;
 }
 
@@ -521,8 +561,10 @@ cudaError_t launch_phase1_tc(const Phase1Args &a) {
   cudaError_t e = cudaFuncSetAttribute(p1_scores_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)kSmemA);
   if (e != cudaSuccess) return e;
+  // Every CTA gets the same number of tiles (no partly empty last wave).
   const int64_t tiles = (a.rows + kRows - 1) / kRows;
-  const int64_t ga = tiles < sm_count() ? tiles : sm_count();
+  const int64_t waves = (tiles + sm_count() - 1) / sm_count();
+  const int64_t ga = (tiles + waves - 1) / waves;
   p1_scores_kernel<<<(int)ga, kThreadsA, kSmemA, a.stream>>>(pa);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   // Kernel B
@@ -536,7 +578,7 @@ cudaError_t launch_phase1_tc(const Phase1Args &a) {
   pb.nvec = a.D / 8;
   const int threads = (pb.nvec + 31) / 32 * 32;
   const size_t smem = smem_b(a.n, a.D);
-  e = cudaFuncSetAttribute(p1_outputs_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+  e = cudaFuncSetAttribute(p1_outputs_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   int occ = 0;
   e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, p1_outputs_kernel, threads, smem);

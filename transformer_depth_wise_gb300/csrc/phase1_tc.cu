@@ -15,10 +15,11 @@
 // after kernel A is done with them (so no scratch memory is needed).
 //
 // Kernel A (scores, tensor cores).  A CTA owns a tile of 128 token rows.
-// TMA streams every summary of the tile in 64-feature chunks (box 64 x 128,
-// 128-byte swizzle) through a ring of shared-memory stages, and the parked
-// query parts for the same 64 features (box 64 x 48) as the MMA's B operand
-// (N = 48); tcgen05.mma
+// TMA streams each summary of the tile in 64-feature chunks (box 64 x 128,
+// 128-byte swizzle), one summary after the other, through a ring of
+// shared-memory stages; each stage also carries the parked query parts for
+// the same 64 features (box 64 x 48), the MMA's B operand (N = 48);
+// tcgen05.mma
 // accumulates, per summary i, the 128 x 48 partial scores in its own TMEM
 // columns [48 i, 48 i + 48).  Four warps (one thread per token row) read the
 // same stages to accumulate each row's sum of squares, then run the
@@ -53,17 +54,16 @@ constexpr int kKc = 64;               // features per chunk (one 128-byte swizzl
 constexpr int kMaxN = 10;             // summaries: TMEM columns n * 48 <= 480
 constexpr int kMaxS = 24;             // queries
 constexpr int kNQ = 2 * kMaxS;        // B rows: hi parts at 0..S-1, lo parts at 24..24+S-1
-constexpr int kVStages = 12;          // summary chunk ring (16 KB each)
-constexpr int kQStages = 4;           // query chunk ring (6 KB each)
+constexpr int kStages = 9;            // ring of (summary chunk 16 KB + query chunk 6 KB) stages
 constexpr uint32_t kVBytes = kRows * kKc * 2;
 constexpr uint32_t kQBytes = kNQ * kKc * 2;
+constexpr uint32_t kStageBytes = kVBytes + kQBytes;   // both parts 1024-byte aligned
 constexpr int kTmemCols = 512;
 constexpr int kBStages = 3;           // kernel B: tokens in flight (cp.async stages)
 constexpr long long kWaitLimitCycles = 4000000000ll;   // ~2 s at 2 GHz: bound on any wait
 constexpr int kWarpsA = 6;            // 0-3: sums of squares + epilogue, 4: TMA, 5: MMA
 constexpr int kThreadsA = kWarpsA * 32;
-constexpr uint32_t kOffQ = kVStages * kVBytes;
-constexpr uint32_t kOffBar = kOffQ + kQStages * kQBytes;
+constexpr uint32_t kOffBar = kStages * kStageBytes;
 constexpr uint32_t kSmemA = kOffBar + 64 * 8 + 1024;     // barriers + alignment slack
 
 struct ParamsA {
@@ -204,21 +204,15 @@ __global__ void __launch_bounds__(kThreadsA, 1) p1_scores_kernel(const __grid_co
   const int n = p.n, S = p.S;
   const uint32_t b0 = base + kOffBar;
   auto VFULL = [&](int s) { return b0 + 8u * s; };
-  auto VEMPTY = [&](int s) { return b0 + 8u * (kVStages + s); };
-  auto QFULL = [&](int s) { return b0 + 8u * (2 * kVStages + s); };
-  auto QEMPTY = [&](int s) { return b0 + 8u * (2 * kVStages + kQStages + s); };
-  const uint32_t TDONE = b0 + 8u * (2 * kVStages + 2 * kQStages);
+  auto VEMPTY = [&](int s) { return b0 + 8u * (kStages + s); };
+  const uint32_t TDONE = b0 + 8u * (2 * kStages);
   const uint32_t TFREE = TDONE + 8u;
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + kOffBar + 8 * (2 * kVStages + 2 * kQStages + 2));
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + kOffBar + 8 * (2 * kStages + 2));
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kVStages; ++s) {
+    for (int s = 0; s < kStages; ++s) {
       mbar_init(VFULL(s), 1);
       mbar_init(VEMPTY(s), 1 + 4);    // the MMA's commit + the four row warps
-    }
-    for (int s = 0; s < kQStages; ++s) {
-      mbar_init(QFULL(s), 1);
-      mbar_init(QEMPTY(s), 1);
     }
     mbar_init(TDONE, 1);
     mbar_init(TFREE, 4);
@@ -238,53 +232,50 @@ __global__ void __launch_bounds__(kThreadsA, 1) p1_scores_kernel(const __grid_co
   const int KC = p.D / kKc;
 
   if (warp == 4) {
-    // ---------------- TMA producer: (tile, chunk, summary) stages ----------------
+    // ---------------- TMA producer: (tile, summary, chunk) stages ----------------
+    // Each stage carries 64 features of one summary for the tile's 128 rows
+    // and the same 64 features of the query parts.  Walking the features of
+    // one summary in order keeps consecutive stages on neighbouring bytes.
     if (lane == 0) {
-      int64_t g = 0, gq = 0;
+      int64_t g = 0;
       for (int64_t tl = 0; tl < my_tiles; ++tl) {
         const int64_t tile = blockIdx.x + tl * gridDim.x;
-        for (int kc = 0; kc < KC; ++kc, ++gq) {
-          const int sq = (int)(gq % kQStages);
-          if (gq >= kQStages) wait_local(QEMPTY(sq), (uint32_t)((gq / kQStages - 1) & 1));
-          mbar_expect_tx(QFULL(sq), kQBytes);
-          tma_load_2d(base + kOffQ + (uint32_t)sq * kQBytes, &p.qmap, kc * kKc, 0, QFULL(sq));
-          for (int i = 0; i < n; ++i, ++g) {
-            const int s = (int)(g % kVStages);
-            if (g >= kVStages) wait_local(VEMPTY(s), (uint32_t)((g / kVStages - 1) & 1));
-            mbar_expect_tx(VFULL(s), kVBytes);
-            tma_load_2d(base + (uint32_t)s * kVBytes, &p.tmap[i], kc * kKc, (int)(tile * kRows), VFULL(s));
+        for (int i = 0; i < n; ++i)
+          for (int kc = 0; kc < KC; ++kc, ++g) {
+            const int s = (int)(g % kStages);
+            if (g >= kStages) wait_local(VEMPTY(s), (uint32_t)((g / kStages - 1) & 1));
+            mbar_expect_tx(VFULL(s), kStageBytes);
+            const uint32_t st = base + (uint32_t)s * kStageBytes;
+            tma_load_2d(st, &p.tmap[i], kc * kKc, (int)(tile * kRows), VFULL(s));
+            tma_load_2d(st + kVBytes, &p.qmap, kc * kKc, 0, VFULL(s));
           }
-        }
       }
       // the last stages have landed before the CTA may exit
-      for (int64_t k = g - kVStages < 0 ? 0 : g - kVStages; k < g; ++k)
-        wait_local(VFULL((int)(k % kVStages)), (uint32_t)((k / kVStages) & 1));
+      for (int64_t k = g - kStages < 0 ? 0 : g - kStages; k < g; ++k)
+        wait_local(VFULL((int)(k % kStages)), (uint32_t)((k / kStages) & 1));
     }
   } else if (warp == 5) {
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
       const uint32_t idesc = idesc_bf16(kRows, kNQ);
-      int64_t g = 0, gq = 0;
+      int64_t g = 0;
       for (int64_t tl = 0; tl < my_tiles; ++tl) {
         if (tl >= 1) wait_local(TFREE, (uint32_t)((tl - 1) & 1));   // epilogue read the last tile
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-        for (int kc = 0; kc < KC; ++kc, ++gq) {
-          const int sq = (int)(gq % kQStages);
-          wait_local(QFULL(sq), (uint32_t)((gq / kQStages) & 1));
-          for (int i = 0; i < n; ++i, ++g) {
-            const int s = (int)(g % kVStages);
-            wait_local(VFULL(s), (uint32_t)((g / kVStages) & 1));
+        for (int i = 0; i < n; ++i)
+          for (int kc = 0; kc < KC; ++kc, ++g) {
+            const int s = (int)(g % kStages);
+            wait_local(VFULL(s), (uint32_t)((g / kStages) & 1));
             asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+            const uint32_t st = base + (uint32_t)s * kStageBytes;
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
-              const uint64_t a = sw128_desc(base + (uint32_t)s * kVBytes + kk * 32u, 1024u);
-              const uint64_t b = sw128_desc(base + kOffQ + (uint32_t)sq * kQBytes + kk * 32u, 1024u);
+              const uint64_t a = sw128_desc(st + kk * 32u, 1024u);
+              const uint64_t b = sw128_desc(st + kVBytes + kk * 32u, 1024u);
               mma_bf16(tmem_base + (uint32_t)(i * kNQ), a, b, idesc, (kc | kk) != 0);
             }
             mma_commit(VEMPTY(s));
           }
-          mma_commit(QEMPTY(sq));
-        }
         mma_commit(TDONE);
       }
     }
@@ -298,29 +289,27 @@ __global__ void __launch_bounds__(kThreadsA, 1) p1_scores_kernel(const __grid_co
       float ss[kMaxN];
 #pragma unroll
       for (int i = 0; i < kMaxN; ++i) ss[i] = 0.f;
-      for (int kc = 0; kc < KC; ++kc) {
 #pragma unroll
-        for (int i = 0; i < kMaxN; ++i) {
-          if (i < n) {
-            const int s = (int)(g % kVStages);
-            wait_local(VFULL(s), (uint32_t)((g / kVStages) & 1));
-            const unsigned char *row = sm + (uint32_t)s * kVBytes;
-            uint4 v[8];
+      for (int i = 0; i < kMaxN; ++i) {
+        if (i >= n) continue;
+        for (int kc = 0; kc < KC; ++kc, ++g) {
+          const int s = (int)(g % kStages);
+          wait_local(VFULL(s), (uint32_t)((g / kStages) & 1));
+          const unsigned char *row = sm + (uint32_t)s * kStageBytes;
+          uint4 v[8];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) v[j] = *reinterpret_cast<const uint4 *>(row + swz((uint32_t)r, (uint32_t)j));
-            float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};   // eight independent chains
+          for (int j = 0; j < 8; ++j) v[j] = *reinterpret_cast<const uint4 *>(row + swz((uint32_t)r, (uint32_t)j));
+          float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};   // eight independent chains
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              float x[8];
-              Elt<__nv_bfloat16>::unpack(v[j], x);
+          for (int j = 0; j < 8; ++j) {
+            float x[8];
+            Elt<__nv_bfloat16>::unpack(v[j], x);
 #pragma unroll
-              for (int e = 0; e < 8; ++e) acc[e] = fmaf(x[e], x[e], acc[e]);
-            }
-            ss[i] += ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
-            __syncwarp();
-            if (lane == 0) mbar_arrive(VEMPTY(s));
-            ++g;
+            for (int e = 0; e < 8; ++e) acc[e] = fmaf(x[e], x[e], acc[e]);
           }
+          ss[i] += ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
+          __syncwarp();
+          if (lane == 0) mbar_arrive(VEMPTY(s));
         }
       }
       // epilogue: scores -> softmax over the n summaries -> alpha, m, lse

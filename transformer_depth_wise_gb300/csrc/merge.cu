@@ -155,7 +155,6 @@ __global__ void __launch_bounds__(TEAM ? 256 : 512)
 merge_update_kernel(const __grid_constant__ MergeUpdateParams P) {
   using E = Elt<T>;
   constexpr int EPV = E::EPV;
-  constexpr int NE = VPT * EPV;
   __shared__ float red[TEAM ? 1 : 2 * 32 * 2];
   const MergeParams &p = P.m;
   const int tpr = TEAM ? TEAM : blockDim.x;
@@ -217,7 +216,6 @@ merge_update_kernel(const __grid_constant__ MergeUpdateParams P) {
       float xp[EPV], xs[EPV], y[EPV];
       E::unpack(pv[kk], xp);
       E::unpack(sv[kk], xs);
-#pragma unroll
       float uu[EPV];
       if (SYNTH && valid[kk]) {
 #pragma unroll

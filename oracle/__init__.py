@@ -69,10 +69,11 @@ def _load():
             "oracle_block_phase1": (c_int, [c_int, i64, i64, PP, c_int, _D, _D, c_dbl, _D, _D, _D]),
             "oracle_block_phase2_merge": (c_int, [i64, i64, _D, _D, _D, _D, _D, c_dbl, _D, _D]),
             "oracle_synthetic_sublayer": (None, [i64, i64, _D, _D, _D]),
-            "oracle_block_two_phase_chain": (c_int, [c_int, i64, i64, PP, c_int, _D, _D, _D, c_dbl,
-                                                     c_int, _D, _D]),
-            "oracle_block_forward_naive": (c_int, [c_int, c_int, i64, i64, _D, _D, _D, _D, c_dbl,
-                                                   _D, _D]),
+            "oracle_rms_norm": (None, [i64, i64, _D, _D, c_dbl, _D]),
+            "oracle_block_two_phase_chain": (c_int, [c_int, i64, i64, PP, c_int, _D, _D, _D, _D, c_dbl,
+                                                     c_dbl, c_int, _D, _D]),
+            "oracle_block_forward_naive": (c_int, [c_int, c_int, i64, i64, _D, _D, _D, _D, _D, c_dbl,
+                                                   c_dbl, _D, _D]),
             "oracle_block_forward_two_phase": (c_int, [c_int, c_int, i64, i64, _D, _D, _D, _D,
                                                        c_dbl, _D, _D]),
             "oracle_full_stack_forward": (c_int, [c_int, i64, i64, _D, _D, _D, _D, c_dbl, c_int,
@@ -236,9 +237,23 @@ def synthetic_sublayer(u, h) -> np.ndarray:
     return out
 
 
-def block_two_phase_chain(blocks, W, G, U, eps: float, dtype: int):
+def rms_norm(x, weight=None, eps: float = 1e-6) -> np.ndarray:
+    """y = x / sqrt(mean(x^2) + eps) (.) weight, row by row (the sublayer pre-norm)."""
+    x = _arr(x)
+    shape = x.shape
+    x2 = x.reshape(-1, shape[-1])
+    R, D = x2.shape
+    weight = None if weight is None else _arr(weight)
+    y = np.empty((R, D))
+    _load().oracle_rms_norm(R, D, _p(x2), _p(weight), float(eps), _p(y))
+    return y.reshape(shape)
+
+
+def block_two_phase_chain(blocks, W, G, U, eps: float, dtype: int, NW=None, norm_eps: float = 1e-6):
     """One block of the two-phase recurrence with materialisation rounding.
 
+    NW ([S, D] or None): the sublayers' pre-norm weights; with them each
+    sublayer reads rms_norm(h_k) (formed from the unrounded h_k).
     Returns (H [S, R, D] rounded sublayer inputs, P [R, D] rounded final partial).
     """
     Bk = [_arr(b).reshape(-1, _arr(b).shape[-1]) for b in blocks]
@@ -249,13 +264,18 @@ def block_two_phase_chain(blocks, W, G, U, eps: float, dtype: int):
     U = _arr(U)
     H = np.empty((S, R, D))
     P = np.empty((R, D))
+    NW = None if NW is None else _arr(NW)
     _check(_load().oracle_block_two_phase_chain(len(Bk), R, D, _plist(Bk), S, _p(W), _p(G), _p(U),
-                                                float(eps), int(dtype), _p(H), _p(P)))
+                                                _p(NW), float(norm_eps), float(eps), int(dtype),
+                                                _p(H), _p(P)))
     return H, P
 
 
-def block_forward_naive(x, W, G, U, S: int, eps: float = 1e-8):
-    """forward_naive with the synthetic sublayer, exact fp64: returns (H [N,R,D], y [R,D])."""
+def block_forward_naive(x, W, G, U, S: int, eps: float = 1e-8, NW=None, norm_eps: float = 1e-6):
+    """forward_naive with the synthetic sublayer, exact fp64: returns (H [N,R,D], y [R,D]).
+
+    NW ([N, D] or None): pre-norm weights; sublayer l then reads rms_norm(h_l).
+    """
     x = _arr(x)
     R, D = x.reshape(-1, x.shape[-1]).shape
     U = _arr(U)
@@ -264,8 +284,9 @@ def block_forward_naive(x, W, G, U, S: int, eps: float = 1e-8):
     G = None if G is None else _arr(G)
     H = np.empty((N, R, D))
     y = np.empty((R, D))
-    _check(_load().oracle_block_forward_naive(N, S, R, D, _p(x), _p(W), _p(G), _p(U), float(eps),
-                                              _p(H), _p(y)))
+    NW = None if NW is None else _arr(NW)
+    _check(_load().oracle_block_forward_naive(N, S, R, D, _p(x), _p(W), _p(G), _p(U), _p(NW),
+                                              float(norm_eps), float(eps), _p(H), _p(y)))
     return H, y
 
 

@@ -274,6 +274,25 @@ void oracle_synthetic_sublayer(int64_t R, int64_t D, const double *u, const doub
 }
 
 /*
+ * The next sublayer's pre-norm applied to h ("Attention Residuals：当网络深度
+ * 也拥有寻址能力", sections "Depth attention 与 online merge reference" -- the
+ * optional fused output RMSNorm -- and "Kimi Linear 与 K3 中的接入", where the
+ * decode path fuses the merge, the partial update and the RMSNorm):
+ *   y = x / sqrt(mean_d x^2 + eps) (.) weight      (weight == NULL: one)
+ * row by row.  y may alias x.
+ */
+void oracle_rms_norm(int64_t R, int64_t D, const double *x, const double *weight, double eps,
+                     double *y)
+{
+    for (int64_t r = 0; r < R; ++r) {
+        double ss = 0.0;
+        for (int64_t d = 0; d < D; ++d) ss += x[r * D + d] * x[r * D + d];
+        double inv = 1.0 / sqrt(ss / (double)D + eps);
+        for (int64_t d = 0; d < D; ++d) y[r * D + d] = x[r * D + d] * inv * (weight ? weight[d] : 1.0);
+    }
+}
+
+/*
  * One block of the two-phase Block recurrence ("_run_block_two_phase")
  * with the synthetic sublayer:
  *   phase 1 over the n completed summaries for the block's S queries;
@@ -282,10 +301,15 @@ void oracle_synthetic_sublayer(int64_t R, int64_t D, const double *u, const doub
  * Rounding follows the tensors the API materialises: o_k (phase-1 output),
  * h_k (merge output, the sublayer's input) and p_k (the stored partial) are
  * rounded to the I/O dtype; lse stays fp32.
- * U: [S][D].  H_out: [S][R][D] rounded h_k; P_out: [R][D] rounded p_S.
+ * With NW ([S][D], the sublayers' pre-norm weights) the sublayer input is
+ * y_k = rms_norm(h_k, NW_k, norm_eps), formed from the unrounded h_k; then
+ * y_k is the materialised tensor (rounded) and h_k is not.
+ * U: [S][D].  H_out: [S][R][D] rounded sublayer inputs (h_k, or y_k with NW);
+ * P_out: [R][D] rounded p_S.
  */
 int oracle_block_two_phase_chain(int n, int64_t R, int64_t D, const double *const *blocks, int S,
-                                 const double *W, const double *G, const double *U, double eps,
+                                 const double *W, const double *G, const double *U,
+                                 const double *NW, double norm_eps, double eps,
                                  int dtype, double *H_out, double *P_out)
 {
     int64_t RD = R * D;
@@ -305,6 +329,7 @@ int oracle_block_two_phase_chain(int n, int64_t R, int64_t D, const double *cons
                                        s == 0 ? NULL : p, W + (int64_t)s * D,
                                        G ? G + (int64_t)s * D : NULL, eps, hk, NULL);
         if (rc) goto done;
+        if (NW) oracle_rms_norm(R, D, hk, NW + (int64_t)s * D, norm_eps, hk);
         for (int64_t k = 0; k < RD; ++k) hk[k] = oracle_round(hk[k], dtype);
         oracle_synthetic_sublayer(R, D, U + (int64_t)s * D, hk, f);
         for (int64_t k = 0; k < RD; ++k) p[k] = oracle_round((s == 0 ? 0.0 : p[k]) + f[k], dtype);
@@ -323,12 +348,15 @@ done:
 /*
  * N atomic sublayers, block size S (in sublayers).  x: [R][D] embedding.
  * W, G: [N+1][D] (row N is the final aggregate's query), U: [N][D].
- * H_out: [N][R][D] (the input h of every sublayer), y: [R][D] final.
+ * NW: [N][D] pre-norm weights or NULL; with NW, sublayer idx reads
+ * rms_norm(h, NW_idx, norm_eps) instead of h.
+ * H_out: [N][R][D] (the input of every sublayer), y: [R][D] final.
  * Nothing is rounded: this is the exact reference the two-phase form must
  * reproduce.
  */
 int oracle_block_forward_naive(int N, int S, int64_t R, int64_t D, const double *x,
-                               const double *W, const double *G, const double *U, double eps,
+                               const double *W, const double *G, const double *U,
+                               const double *NW, double norm_eps, double eps,
                                double *H_out, double *y)
 {
     int64_t RD = R * D;
@@ -349,6 +377,7 @@ int oracle_block_forward_naive(int N, int S, int64_t R, int64_t D, const double 
         rc = oracle_depth_aggregate_list(ns, R, D, srcs, W + (int64_t)(idx - 1) * D,
                                          G ? G + (int64_t)(idx - 1) * D : NULL, eps, h, NULL, NULL);
         if (rc) goto done;
+        if (NW) oracle_rms_norm(R, D, h, NW + (int64_t)(idx - 1) * D, norm_eps, h);
         oracle_synthetic_sublayer(R, D, U + (int64_t)(idx - 1) * D, h, out);
         for (int64_t k = 0; k < RD; ++k) partial[k] = have_partial ? partial[k] + out[k] : out[k];
         have_partial = 1;

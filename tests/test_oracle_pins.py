@@ -295,6 +295,58 @@ def test_chain_rounding_points():
 
 
 # --------------------------------------------------------------------------
+# The sublayer pre-norm fused into the merge ("Depth attention 与 online merge
+# reference": optional fused output RMSNorm; "Kimi Linear 与 K3 中的接入":
+# merge + partial update + RMSNorm fused on the decode path)
+# --------------------------------------------------------------------------
+def test_rms_norm_closed_forms():
+    # x = (2, 0): mean square 2; with eps = 2 the root is 2, so y = (1, 0) (.) w.
+    assert np.array_equal(oracle.rms_norm([[2.0, 0.0]], [3.0, 5.0], 2.0), [[3.0, 0.0]])
+    # eps inside the root, added to the MEAN (not the sum): x = (3, 4), eps = 0 -> root sqrt(12.5).
+    y = oracle.rms_norm([[3.0, 4.0]], None, 0.0)
+    assert np.allclose(y, [[3 / math.sqrt(12.5), 4 / math.sqrt(12.5)]], rtol=0, atol=1e-15)
+    # a constant row normalises to the weight (eps = 0), whatever its scale and sign
+    w = np.array([0.5, -1.0, 2.0, 3.0])
+    assert np.allclose(oracle.rms_norm([[7.0] * 4], w, 0.0), [w], rtol=0, atol=1e-15)
+    assert np.allclose(oracle.rms_norm([[-0.25] * 4], w, 0.0), [-w], rtol=0, atol=1e-15)
+
+
+def test_rms_norm_invariants():
+    rng = np.random.default_rng(16)
+    x = rng.normal(size=(5, 32)) * rng.uniform(0.1, 10, size=(5, 1))
+    y = oracle.rms_norm(x, None, 0.0)
+    assert np.allclose((y ** 2).mean(axis=1), 1.0, rtol=0, atol=1e-13)      # unit mean square
+    assert np.allclose(oracle.rms_norm(3.5 * x, None, 0.0), y, rtol=0, atol=1e-13)  # scale-free
+    assert np.allclose(y * np.sign(x), np.abs(y), rtol=0, atol=0)           # sign kept per element
+    w = rng.normal(1, 0.2, size=32)
+    yw = oracle.rms_norm(x, w, 1e-6)
+    # a second formulation: numpy's norm of the row, sqrt(||x||^2 / D + eps)
+    want = x / np.sqrt(np.linalg.norm(x, axis=1, keepdims=True) ** 2 / 32 + 1e-6) * w
+    assert np.allclose(yw, want, rtol=1e-14, atol=0)
+    assert np.array_equal(oracle.rms_norm(x[2:3], w, 1e-6), yw[2:3])        # rows independent
+
+
+def test_normed_chain_equals_normed_naive_stack():
+    # One block over the embedding alone: the two-phase chain (phase 1 + merges) with
+    # pre-norm weights equals forward_naive (direct aggregation) with the same weights.
+    rng = np.random.default_rng(17)
+    S, R, D = 4, 3, 8
+    x = rng.normal(size=(R, D)) * 2
+    W, G = rng.normal(0, 0.5, size=(S + 1, D)), rng.normal(1, 0.1, size=(S + 1, D))
+    U, NW = rng.normal(1, 0.25, size=(S, D)), rng.normal(1, 0.1, size=(S, D))
+    Hn, _ = oracle.block_forward_naive(x, W, G, U, S, NW=NW, norm_eps=1e-5)
+    Hc, Pc = oracle.block_two_phase_chain([x], W[:S], G[:S], U, 1e-8, oracle.F64, NW=NW, norm_eps=1e-5)
+    assert np.allclose(Hc, Hn, rtol=0, atol=1e-12)
+    # the sublayer inputs are normalised rows: mean square of y / NW is 1 up to eps
+    assert np.allclose(((Hc / NW[:, None, :]) ** 2).mean(axis=2), 1.0, atol=1e-4)
+    # and the norm changes the recurrence (not silently ignored)
+    H0, P0 = oracle.block_two_phase_chain([x], W[:S], G[:S], U, 1e-8, oracle.F64)
+    assert not np.allclose(P0, Pc, atol=1e-3)
+    # step by step by hand: partial = sum_k 0.5 tanh(u_k (.) y_k)
+    assert np.allclose(Pc, sum(0.5 * np.tanh(U[k] * Hc[k]) for k in range(S)), rtol=0, atol=1e-12)
+
+
+# --------------------------------------------------------------------------
 # Rounding to the I/O dtype
 # --------------------------------------------------------------------------
 def test_bf16_rounding_ties_and_ranges():

@@ -259,9 +259,26 @@ def run_two_phase(args, wl, dev, rank, world):
                "launches_per_step": blk_u.launches_per_run}
     del blk_u
 
+    # The fused pass with each sublayer's pre-norm formed inside the
+    # update+merge (norm weights drawn like the gains), for comparison.
+    nw = wk.queries_and_gains(wk.generator(wl.seed + 7, dev), S, D, dev)[1]
+    blk_n = api.TwoPhaseBlock(inp["blocks"], inp["queries"], inp["gains"], inp["u"], inp["eps"],
+                              fused=True, norm_weights=nw, norm_eps=1e-6)
+    for _ in range(args.warmup):
+        blk_n.run()
+    torch.cuda.synchronize(dev)
+    el_n, ev_n, _ = time_block(blk_n, K, dev, world, stream, fused=True)
+    mg_n = [a.elapsed_time(c) for e in ev_n for a, c in e["merge"]]
+    prenorm = {"value": round(rows * K * world / (el_n * 1e-3), 1), "ms_per_step": round(el_n / K, 4),
+               "merge_update_ms": round(statistics.mean(mg_n), 5),
+               "launches_per_step": blk_n.launches_per_run,
+               "step": "as the headline, each sublayer reading rms_norm(h) (.) w_n formed in the same pass"}
+    del blk_n, nw
+
     # End to end through the public API: pinned host inputs -> device, block
     # pass, final partial (the new block summary) -> pinned host, every step.
     e2e = run_two_phase_e2e(args, wl, dev, inp, n_blocks, world)
+    decode = run_decode(dev) if wl.name == "two_phase_bf16" and not args.rows else None
 
     res = {
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
@@ -278,10 +295,53 @@ def run_two_phase(args, wl, dev, rank, world):
         "kernels": {n: {kk: (round(v, 5) if isinstance(v, float) else v) for kk, v in k.items()}
                     for n, k in kern.items()},
         "unfused": unfused,
+        "prenorm": prenorm,
+        "decode": decode,
         "e2e": e2e,
         "gpu_launches": K * blk.launches_per_run,
         "clocks": clk,
     }
+    return res
+
+
+def run_decode(dev, reps: int = 60):
+    """The D = 7168 decode block pass ([256, 1, 7168], 9 summaries, S = 24): eager
+    launches, one CUDA graph, and the graph with the side-stream inter-block pass.
+    Each pass is timed alone with events, L2 flushed (and the stream idle) before it;
+    the median is reported."""
+    from transformer_depth_wise_gb300 import api
+    wl = wk.WORKLOADS["decode_bf16"]
+    tp = wk.two_phase_inputs(wl, device=dev)
+    args = (tp["blocks"], tp["queries"], tp["gains"], tp["u"], tp["eps"])
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+
+    def time_pass(fn):
+        ts = []
+        for _ in range(reps):
+            flush.fill_(1)
+            torch.cuda.synchronize(dev)
+            a, b = ev(), ev()
+            a.record()
+            fn()
+            b.record()
+            torch.cuda.synchronize(dev)
+            ts.append(a.elapsed_time(b) * 1e3)
+        return statistics.median(ts)
+
+    eager = api.TwoPhaseBlock(*args)
+    graph = api.TwoPhaseBlock(*args)
+    graph.capture()
+    ov = api.TwoPhaseBlock(*args, overlap=True)
+    ov.capture()
+    for _ in range(3):
+        eager.run(), graph.replay(), ov.replay()
+    res = {"workload": wl.name, "tokens": wl.B * wl.T, "eager_launches": eager.launches_per_run,
+           "eager_us": round(time_pass(eager.run), 2), "graph_us": round(time_pass(graph.replay), 2),
+           "graph_side_stream_us": round(time_pass(ov.replay), 2),
+           "timing": "one pass per sample, median of %d; L2 flushed before each" % reps}
+    res["tokens_per_s_graph"] = round(wl.B * wl.T / (min(res["graph_us"], res["graph_side_stream_us"]) * 1e-6), 1)
+    del eager, graph, ov, flush
     return res
 
 

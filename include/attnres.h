@@ -144,12 +144,35 @@ int attnres_partial_update(const void *h, const void *partial_in, const float *u
  *   inter_out, inter_lse, query, gain, eps, out_lse: as attnres_block_phase2_merge
  *   partial_in  device [B,T,D] or NULL;  sub_out  device [B,T,D];  u  fp32 [D] or NULL
  *   partial_out device [B,T,D]: may alias partial_in
- *   h_out       device [B,T,D]: may alias sub_out (not inter_out)
+ *   h_out       device [B,T,D] or NULL (then normed_out is required): may
+ *               alias sub_out (not inter_out)
+ * Optional pre-norm of the next sublayer, fused ("Depth attention 与 online
+ * merge reference": the optional fused output RMSNorm; the K3 decode path
+ * fuses it with the merge and the partial update):
+ *   normed_out = h_k / sqrt(mean_d h_k^2 + norm_eps) (.) norm_weight,
+ * formed from the unrounded fp32 h_k and rounded once.
+ *   norm_weight device fp32 [D] or NULL;  norm_eps finite, >= 0
+ *   normed_out  device [B,T,D] or NULL; NULL exactly when norm_weight is NULL;
+ *               may alias sub_out (not inter_out, not h_out)
  */
 int attnres_block_merge_update(const void *inter_out, const float *inter_lse, const void *partial_in,
                                const void *sub_out, const float *u, int64_t B, int64_t T, int64_t D,
                                int dtype, const float *query, const float *gain, float eps,
-                               void *partial_out, void *h_out, float *out_lse, void *stream);
+                               void *partial_out, void *h_out, float *out_lse,
+                               const float *norm_weight, float norm_eps, void *normed_out,
+                               void *stream);
+
+/*
+ * The sublayer pre-norm as a pass of its own (for the first sublayer of a
+ * block, whose input h_1 is the phase-1 output; same definition as the fused
+ * form above):
+ *   y = x / sqrt(mean_d x^2 + eps) (.) weight,   row by row, fp32, rounded once.
+ *   x       device [B,T,D];  weight device fp32 [D];  eps finite, >= 0
+ *   y       device [B,T,D]; may alias x
+ * Same D limits as attnres_block_phase2_merge.
+ */
+int attnres_rms_norm(const void *x, int64_t B, int64_t T, int64_t D, int dtype, const float *weight,
+                     float eps, void *y, void *stream);
 
 /*
  * Full AttnRes stack forward ("FullAttnResStack", eq. A1-A4) with the

@@ -231,7 +231,7 @@ def test_merge_update_fused_step(gpu):
             u = wk.sublayer_u(g, 1, D, gpu)[0].contiguous() if synth else None
             lse = torch.empty(rows, device=gpu).normal_(0.0, 2.0, generator=g)
             p_in = pin if with_pin else None
-            p_out, h = api.block_merge_update(o, lse, p_in, sub, u, W[0], G[0], 1e-8)
+            p_out, h, _ = api.block_merge_update(o, lse, p_in, sub, u, W[0], G[0], 1e-8)
             subn = f64(sub).reshape(rows, D)
             out = oracle.synthetic_sublayer(f64(u), subn) if synth else subn
             want_p = oracle.round_to((f64(pin).reshape(rows, D) if with_pin else 0.0) + out, ODT[dtype])
@@ -244,6 +244,71 @@ def test_merge_update_fused_step(gpu):
                 pi, hs = pin.clone(), sub.clone()              # h_out aliases sub_out
                 api.block_merge_update(o, lse, pi, hs, u, W[0], G[0], 1e-8, partial_out=pi, h_out=hs)
                 assert torch.equal(pi, p_out) and torch.equal(hs, h)
+
+
+# The next sublayer's pre-norm, standalone and fused into the update+merge.
+# Its output is a normalised row (values of order |w_n|), so the bound is
+# the dtype tolerance times the largest |y| rather than the sources' scale.
+def test_rms_norm(gpu):
+    for dtype, D, rows in ((torch.bfloat16, 4096, 45), (torch.float32, 256, 70), (torch.bfloat16, 16, 33),
+                           (torch.bfloat16, 16384, 5), (torch.float32, 8192, 3), (torch.bfloat16, 7168, 9)):
+        g = wk.generator(D + rows + 5, gpu)
+        (x,), _ = wk.scaled_normal_sources(g, 1, (1, rows, D), 0.5, 8.0, dtype, gpu)
+        _, Wn = wk.queries_and_gains(g, 1, D, gpu)
+        y = api.rms_norm(x, Wn[0], 1e-6)
+        want = oracle.rms_norm(f64(x).reshape(rows, D), f64(Wn[0]), 1e-6)
+        check(y.reshape(rows, D), oracle.round_to(want, ODT[dtype]), TOL[dtype] * np.abs(want).max(), "rms_norm")
+        xi = x.clone()
+        api.rms_norm(xi, Wn[0], 1e-6, out=xi)                  # in place
+        assert torch.equal(xi, y)
+
+
+def test_merge_update_with_prenorm(gpu):
+    for dtype, D, rows in ((torch.bfloat16, 4096, 45), (torch.float32, 256, 70), (torch.bfloat16, 16, 33),
+                           (torch.bfloat16, 16384, 6), (torch.bfloat16, 7168, 11)):
+        for synth, with_pin in ((True, True), (True, False), (False, True)):
+            g = wk.generator(D + rows + 3 * synth + with_pin + 11, gpu)
+            (o, pin, sub), _ = wk.scaled_normal_sources(g, 3, (1, rows, D), 0.5, 3.0, dtype, gpu)
+            W, G = wk.queries_and_gains(g, 1, D, gpu)
+            _, Wn = wk.queries_and_gains(g, 1, D, gpu)
+            u = wk.sublayer_u(g, 1, D, gpu)[0].contiguous() if synth else None
+            lse = torch.empty(rows, device=gpu).normal_(0.0, 2.0, generator=g)
+            p_in = pin if with_pin else None
+            p_out, h, y = api.block_merge_update(o, lse, p_in, sub, u, W[0], G[0], 1e-8,
+                                                 norm_weight=Wn[0], norm_eps=1e-5)
+            subn = f64(sub).reshape(rows, D)
+            out = oracle.synthetic_sublayer(f64(u), subn) if synth else subn
+            want_p = oracle.round_to((f64(pin).reshape(rows, D) if with_pin else 0.0) + out, ODT[dtype])
+            want_h, _ = oracle.block_phase2_merge(f64(o).reshape(rows, D), f64(lse), want_p, f64(W[0]),
+                                                  f64(G[0]), 1e-8)
+            want_y = oracle.rms_norm(want_h, f64(Wn[0]), 1e-5)      # from the unrounded h
+            tol = TOL[dtype] * vmax([o, pin, sub])
+            check(p_out.reshape(rows, D), want_p, tol, "prenorm p")
+            check(h.reshape(rows, D), oracle.round_to(want_h, ODT[dtype]), tol, "prenorm h")
+            check(y.reshape(rows, D), oracle.round_to(want_y, ODT[dtype]), TOL[dtype] * np.abs(want_y).max(),
+                  "prenorm y")
+            # h not stored; y written over the sublayer row it was computed from
+            pi, ys = (pin.clone() if with_pin else torch.empty_like(pin)), sub.clone()
+            api.block_merge_update(o, lse, pi if with_pin else None, ys, u, W[0], G[0], 1e-8, partial_out=pi,
+                                   norm_weight=Wn[0], norm_eps=1e-5, normed_out=ys, write_h=False)
+            assert torch.equal(pi, p_out) and torch.equal(ys, y)
+
+
+@pytest.mark.parametrize("fused", [True, False])
+def test_two_phase_block_chain_with_prenorm(gpu, fused):
+    D, n, S, rows = 2048, 9, 6, 40
+    g = wk.generator(78, gpu)
+    blocks, _ = wk.scaled_normal_sources(g, n, (1, rows, D), 0.5, 8.0, torch.bfloat16, gpu)
+    W, G = wk.queries_and_gains(g, S, D, gpu)
+    U = wk.sublayer_u(g, S, D, gpu)
+    _, NW = wk.queries_and_gains(g, S, D, gpu)
+    p, Y = api.block_two_phase(blocks, W, G, U, 1e-8, fused=fused, norm_weights=NW, norm_eps=1e-6)
+    OY, OP = oracle.block_two_phase_chain([f64(b) for b in blocks], f64(W), f64(G), f64(U), 1e-8,
+                                          oracle.BF16, NW=f64(NW), norm_eps=1e-6)
+    # fused: y_k from the unrounded h_k (as the oracle); unfused: from the stored h_k,
+    # one bf16 rounding apart, inside the same bound
+    check(Y.reshape(S, rows, D), OY, TOL[torch.bfloat16] * np.abs(OY).max(), "chain y")
+    check(p.reshape(rows, D), OP, TOL[torch.bfloat16] * vmax(blocks), "chain p")
 
 
 @pytest.mark.parametrize("fused", [True, False])
@@ -293,6 +358,42 @@ def test_d7168_configs_sampled(gpu, name):
                                          f64(tp["queries"]), f64(tp["gains"]), f64(tp["u"]),
                                          tp["eps"], oracle.BF16)
     check(pick(p, rows, wl.D), OP, TOL[torch.bfloat16] * vmax(tp["blocks"]), name + " chain")
+
+
+# --------------------------------------------------------------------------
+# Decode: side-stream inter-block pass, and the block pass as one CUDA graph
+# --------------------------------------------------------------------------
+def test_decode_overlap_and_graph(gpu):
+    wl = wk.WORKLOADS["decode_bf16"]                     # [256, 1, 7168], 9 summaries, S = 24
+    tp = wk.two_phase_inputs(wl, device=gpu)
+    args = (tp["blocks"], tp["queries"], tp["gains"], tp["u"], tp["eps"])
+    eager = api.TwoPhaseBlock(*args, keep_h=True)
+    p_eager = eager.run().clone()
+    ov = api.TwoPhaseBlock(*args, keep_h=True, overlap=True)
+    p_ov = ov.run().clone()
+    torch.cuda.synchronize()
+    rows = sample_rows(wl.B, wl.T, 16, 6)
+    OH, OP = oracle.block_two_phase_chain([f64(pick(b, rows, wl.D)) for b in tp["blocks"]],
+                                          f64(tp["queries"]), f64(tp["gains"]), f64(tp["u"]),
+                                          tp["eps"], oracle.BF16)
+    tol = TOL[torch.bfloat16] * vmax(tp["blocks"])
+    ix = torch.as_tensor(rows, device=gpu)
+    for p, H, name in ((p_eager, eager.h, "eager"), (p_ov, ov.h, "overlap")):
+        check(pick(p, rows, wl.D), OP, tol, name + " p")
+        check(H.reshape(wl.S, -1, wl.D)[:, ix], OH, tol, name + " h")
+    # graphs replay exactly the eager launches: bitwise equal
+    for blk, want in ((eager, p_eager), (ov, p_ov)):
+        blk.capture()
+        got = blk.replay().clone()
+        torch.cuda.synchronize()
+        assert torch.equal(got, want)
+    # a replay reads the live buffers: new summaries in place, new result
+    for b in tp["blocks"]:
+        b.mul_(-0.5)
+    p_new = eager.replay().clone()
+    ref = api.TwoPhaseBlock(*args).run()
+    torch.cuda.synchronize()
+    assert torch.equal(p_new, ref) and not torch.equal(p_new, p_eager)
 
 
 # --------------------------------------------------------------------------

@@ -94,6 +94,27 @@ def test_merge_and_update_argument_checks():
     assert m(FAKE, FAKE, FAKE + 2, 1, 2, 64, 1, FAKE, None, 1e-8, FAKE, None, None) == ALIGN
     assert m(FAKE, FAKE, FAKE, 1, 2, 64, 1, FAKE, None, -1.0, FAKE, None, None) == VALUE
     assert m(FAKE, FAKE, None, 0, 2, 64, 1, FAKE, None, 1e-8, FAKE, None, None) == OK
+    mu = L.attnres_block_merge_update
+
+    def fused(h=FAKE, nw=None, neps=1e-6, y=None, lse=FAKE, B=1, D=64):
+        return mu(FAKE, lse, FAKE, FAKE, None, B, 2, D, 1, FAKE, None, 1e-8, FAKE, h, None, nw, neps, y, None)
+
+    assert fused(lse=None) == NULL
+    assert fused(h=None) == NULL                              # nothing to write
+    assert fused(nw=FAKE) == NULL                             # weight without an output
+    assert fused(y=FAKE) == NULL                              # output without a weight
+    assert fused(nw=FAKE, y=FAKE, neps=-1.0) == VALUE
+    assert fused(nw=FAKE, y=FAKE, neps=math.nan) == VALUE
+    assert fused(nw=FAKE + 4, y=FAKE) == ALIGN
+    assert fused(D=60) == ALIGN
+    assert fused(D=32768) == SHAPE                            # beyond the kernel family
+    assert fused(B=0, h=None) == OK
+    n = L.attnres_rms_norm
+    assert n(FAKE, 1, 2, 64, 1, None, 1e-6, FAKE, None) == NULL
+    assert n(FAKE, 1, 2, 64, 1, FAKE, -1.0, FAKE, None) == VALUE
+    assert n(FAKE + 8, 1, 2, 64, 1, FAKE, 1e-6, FAKE, None) == ALIGN
+    assert n(FAKE, 1, 2, 64, 9, FAKE, 1e-6, FAKE, None) == DTYPE
+    assert n(FAKE, 1, 0, 64, 1, FAKE, 1e-6, FAKE, None) == OK
     u = L.attnres_partial_update
     assert u(FAKE, None, None, 1, 2, 64, 1, FAKE, None) == NULL
     assert u(FAKE, None, FAKE, 1, 2, 60, 1, FAKE, None) == ALIGN

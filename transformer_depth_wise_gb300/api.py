@@ -156,25 +156,44 @@ def full_stack_forward(v0, queries, gains, u, eps: float = 1e-8, sources=None, y
 
 
 def block_merge_update(inter_out, inter_lse, partial_in, sub_out, u, query, gain=None,
-                       eps: float = 1e-8, partial_out=None, h_out=None, out_lse=None):
+                       eps: float = 1e-8, partial_out=None, h_out=None, out_lse=None,
+                       norm_weight=None, norm_eps: float = 1e-6, normed_out=None, write_h: bool = True):
     """Fused partial update (p = p_in + f(sub_out) or p_in + sub_out) and phase-2 merge.
 
-    Returns (partial_out, h_out).
+    With norm_weight, also the next sublayer's pre-norm of the unrounded h:
+    normed_out = rms_norm(h) (.) norm_weight.  write_h=False skips storing h.
+    Returns (partial_out, h_out, normed_out); h_out / normed_out are None when
+    not written.
     """
     _cuda(inter_out, "inter_out")
     _cuda(sub_out, "sub_out")
     B, T, D = _btd(inter_out)
     if partial_out is None:
         partial_out = torch.empty_like(inter_out)
-    if h_out is None:
+    if h_out is None and write_h:
         h_out = torch.empty_like(inter_out)
+    if norm_weight is not None and normed_out is None:
+        normed_out = torch.empty_like(inter_out)
     rc = _lib.lib().attnres_block_merge_update(inter_out.data_ptr(), inter_lse.data_ptr(),
                                                _ptr(partial_in), sub_out.data_ptr(), _ptr(u), B, T, D,
                                                _code(inter_out), _ptr(query), _ptr(gain), float(eps),
-                                               partial_out.data_ptr(), h_out.data_ptr(), _ptr(out_lse),
-                                               _stream(h_out))
+                                               partial_out.data_ptr(), _ptr(h_out if write_h else None),
+                                               _ptr(out_lse), _ptr(norm_weight), float(norm_eps),
+                                               _ptr(normed_out), _stream(partial_out))
     _lib.check("attnres_block_merge_update", rc)
-    return partial_out, h_out
+    return partial_out, (h_out if write_h else None), normed_out
+
+
+def rms_norm(x, weight, eps: float = 1e-6, out=None):
+    """y = x / sqrt(mean(x^2) + eps) (.) weight per token row (out may be x)."""
+    _cuda(x, "x")
+    B, T, D = _btd(x)
+    if out is None:
+        out = torch.empty_like(x)
+    rc = _lib.lib().attnres_rms_norm(x.data_ptr(), B, T, D, _code(x), _ptr(weight), float(eps),
+                                     out.data_ptr(), _stream(out))
+    _lib.check("attnres_rms_norm", rc)
+    return out
 
 
 class TwoPhaseBlock:
@@ -189,12 +208,33 @@ class TwoPhaseBlock:
     fused=False: 23 merges + 24 partial updates (attnres_block_phase2_merge,
     attnres_partial_update).  fused=True: 23 fused update+merge steps
     (attnres_block_merge_update) + 1 final update.  Both give the same values.
+
+    norm_weights ([S, D] fp32 or None): each sublayer reads its pre-norm
+    y_k = rms_norm(h_k) (.) norm_weights[k] instead of h_k.  Fused, the norm
+    is formed inside the update+merge step from the unrounded h_k (the first
+    sublayer's by attnres_rms_norm); unfused, by attnres_rms_norm after each
+    merge.  The stored sublayer inputs are then the y_k.
+
+    overlap=True (decode): the batched inter-block pass for sublayers 2..S
+    runs on a side stream while the main stream forms sublayer 1's input by
+    a direct aggregation over the summaries (the only phase-1 result the
+    first sublayer needs); the main stream joins the side stream before the
+    first merge.  capture() records the whole pass as one CUDA graph and
+    replay() launches it.
     """
 
     def __init__(self, blocks, queries, gains, u, eps: float = 1e-8, keep_h: bool = False,
-                 fused: bool = True):
+                 fused: bool = True, norm_weights=None, norm_eps: float = 1e-6, overlap: bool = False):
         self.blocks = list(blocks)
         self.queries, self.gains, self.u, self.eps = queries, gains, u, float(eps)
+        self.nw, self.norm_eps = norm_weights, float(norm_eps)
+        self.overlap = overlap
+        self.graph = None
+        if overlap:
+            if not fused or norm_weights is not None:
+                raise ValueError("overlap=True runs the fused pass without a pre-norm")
+            self.side = torch.cuda.Stream(device=blocks[0].device)
+            self.ev_fork, self.ev_join = torch.cuda.Event(), torch.cuda.Event()
         S = queries.shape[0]
         ref = self.blocks[0]
         self.o = torch.empty((S, *ref.shape), dtype=ref.dtype, device=ref.device)
@@ -209,10 +249,15 @@ class TwoPhaseBlock:
         self.code = _code(ref)
         self.S = S
         self.launches_per_run = (1 + (S - 1) + 1) if fused else (1 + (S - 1) + S)
+        if norm_weights is not None:
+            self.launches_per_run += 1 if fused else S
+        if overlap:
+            self.launches_per_run += 1
 
     def _hptr(self, k: int) -> int:
-        """Device address of h_k (0-based k); h_0 is the phase-1 output o_0."""
-        if k == 0 and not self.keep_h:
+        """Device address of sublayer k's input (0-based k); without a pre-norm
+        h_0 is the phase-1 output o_0 itself."""
+        if k == 0 and not self.keep_h and self.nw is None and not self.overlap:
             return self.o.data_ptr()
         return (self.h[k] if self.keep_h else self.h).data_ptr()
 
@@ -224,26 +269,40 @@ class TwoPhaseBlock:
         qp, gp, up = self.queries.data_ptr(), _ptr(self.gains), self.u.data_ptr()
         row_bytes = self.o[0].numel() * self.o.element_size()
         rows = B * T
-        rec = (lambda name, k, i: events[name][k][i].record()) if events else (lambda *a: None)
-        if events:
-            events["phase1"][0].record()
-        _lib.check("attnres_block_phase1",
-                   L.attnres_block_phase1(self._arr, len(self.blocks), B, T, D, code, qp, gp, self.S, eps,
-                                          self.o.data_ptr(), None, self.lse.data_ptr(), st))
-        if events:
-            events["phase1"][1].record()
+        rec = ((lambda name, k, i: events[name][k][i].record() if name in events else None) if events
+               else (lambda *a: None))
+        if self.overlap:
+            self._overlapped_phase1(L, st)
+        else:
+            if events:
+                events["phase1"][0].record()
+            _lib.check("attnres_block_phase1",
+                       L.attnres_block_phase1(self._arr, len(self.blocks), B, T, D, code, qp, gp, self.S, eps,
+                                              self.o.data_ptr(), None, self.lse.data_ptr(), st))
+            if events:
+                events["phase1"][1].record()
         op, lp, pp = self.o.data_ptr(), self.lse.data_ptr(), self.partial.data_ptr()
-        if self.keep_h:
+        nwp, neps = _ptr(self.nw), self.norm_eps
+        if self.nw is not None:
+            # first sublayer: y_1 = rms_norm(o_1), its pre-norm as a pass of its own
+            rec("norm", 0, 0)
+            _lib.check("attnres_rms_norm", L.attnres_rms_norm(op, B, T, D, code, nwp, neps, self._hptr(0), st))
+            rec("norm", 0, 1)
+        elif self.keep_h and not self.overlap:
             self.h[0].copy_(self.o[0])
         gk = (lambda k: None) if gp is None else (lambda k: gp + k * D4)
         if self.fused:
             for k in range(1, self.S):
                 rec("merge", k - 1, 0)
+                h_dst = self._hptr(k)
                 _lib.check("attnres_block_merge_update",
                            L.attnres_block_merge_update(op + k * row_bytes, lp + k * rows * 4,
                                                         None if k == 1 else pp, self._hptr(k - 1),
                                                         up + (k - 1) * D4, B, T, D, code, qp + k * D4,
-                                                        gk(k), eps, pp, self._hptr(k), None, st))
+                                                        gk(k), eps, pp,
+                                                        None if nwp else h_dst, None,
+                                                        (nwp + k * D4) if nwp else None, neps,
+                                                        h_dst if nwp else None, st))
                 rec("merge", k - 1, 1)
             rec("update", 0, 0)
             _lib.check("attnres_partial_update",
@@ -258,6 +317,10 @@ class TwoPhaseBlock:
                            L.attnres_block_phase2_merge(op + k * row_bytes, lp + k * rows * 4, pp, B, T, D,
                                                         code, qp + k * D4, gk(k), eps, self._hptr(k), None,
                                                         st))
+                if nwp:
+                    _lib.check("attnres_rms_norm",
+                               L.attnres_rms_norm(self._hptr(k), B, T, D, code, nwp + k * D4, neps,
+                                                  self._hptr(k), st))
                 rec("merge", k - 1, 1)
             rec("update", k, 0)
             _lib.check("attnres_partial_update",
@@ -267,9 +330,53 @@ class TwoPhaseBlock:
         return self.partial
 
 
-def block_two_phase(blocks, queries, gains, u, eps: float = 1e-8, fused: bool = True):
-    """Run one block of the two-phase scheme; returns (final partial, [h_1..h_S])."""
-    blk = TwoPhaseBlock(blocks, queries, gains, u, eps, keep_h=True, fused=fused)
+    def _overlapped_phase1(self, L, st):
+        """Side stream: phase 1 for queries 2..S.  Main stream: sublayer 1's
+        input by a direct aggregation over the summaries; then join."""
+        main = torch.cuda.current_stream(self.o.device)
+        if st != main.cuda_stream:
+            raise ValueError("overlap=True runs on the current stream")
+        B, T, D, code, eps, S = self.B, self.T, self.D, self.code, self.eps, self.S
+        D4, row_bytes, rows = D * 4, self.o[0].numel() * self.o.element_size(), B * T
+        qp, gp = self.queries.data_ptr(), _ptr(self.gains)
+        self.ev_fork.record(main)
+        self.side.wait_event(self.ev_fork)
+        if S > 1:
+            _lib.check("attnres_block_phase1",
+                       L.attnres_block_phase1(self._arr, len(self.blocks), B, T, D, code, qp + D4,
+                                              None if gp is None else gp + D4, S - 1, eps,
+                                              self.o.data_ptr() + row_bytes, None,
+                                              self.lse.data_ptr() + rows * 4, self.side.cuda_stream))
+        self.ev_join.record(self.side)
+        _lib.check("attnres_depth_aggregate",
+                   L.attnres_depth_aggregate(self._arr, len(self.blocks), B, T, D, code, qp, gp, eps,
+                                             self._hptr(0), None, None, st))
+        main.wait_event(self.ev_join)
+
+    def capture(self):
+        """Record one whole block pass as a CUDA graph (after one eager pass,
+        which settles the library's per-kernel launch settings)."""
+        self.run()
+        torch.cuda.synchronize(self.o.device)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            self.run()
+        self.graph = g
+        return g
+
+    def replay(self):
+        """Launch the captured block pass on the current stream; returns the final partial."""
+        if self.graph is None:
+            raise RuntimeError("capture() first")
+        self.graph.replay()
+        return self.partial
+
+
+def block_two_phase(blocks, queries, gains, u, eps: float = 1e-8, fused: bool = True,
+                    norm_weights=None, norm_eps: float = 1e-6):
+    """Run one block of the two-phase scheme; returns (final partial, sublayer inputs [S, ...])."""
+    blk = TwoPhaseBlock(blocks, queries, gains, u, eps, keep_h=True, fused=fused,
+                        norm_weights=norm_weights, norm_eps=norm_eps)
     p = blk.run()
     return p, blk.h
 

@@ -133,21 +133,42 @@ int attnres_block_phase2_merge(const void *inter_out, const float *inter_lse, co
 int attnres_block_merge_update(const void *inter_out, const float *inter_lse, const void *partial_in,
                                const void *sub_out, const float *u, int64_t B, int64_t T, int64_t D,
                                int dtype, const float *query, const float *gain, float eps,
-                               void *partial_out, void *h_out, float *out_lse, void *stream) {
+                               void *partial_out, void *h_out, float *out_lse,
+                               const float *norm_weight, float norm_eps, void *normed_out,
+                               void *stream) {
+  int64_t rows = 0;
+  int st = check_rows(B, T, D, dtype, rows);
+  if (st) return st;
+  if ((st = check_eps(eps))) return st;
+  if (norm_weight && (st = check_eps(norm_eps))) return st;
+  if (!merge_supported((int)D, dtype)) return ATTNRES_ERR_SHAPE;
+  if (rows == 0) return ATTNRES_OK;
+  if (!inter_out || !inter_lse || !sub_out || !query || !partial_out) return ATTNRES_ERR_NULL;
+  if (!norm_weight != !normed_out) return ATTNRES_ERR_NULL;   // both or neither
+  if (!h_out && !normed_out) return ATTNRES_ERR_NULL;         // something must be written
+  if (!aligned16(inter_out) || (partial_in && !aligned16(partial_in)) || !aligned16(sub_out) ||
+      (u && !aligned16(u)) || !aligned16(query) || (gain && !aligned16(gain)) ||
+      !aligned16(partial_out) || (h_out && !aligned16(h_out)) ||
+      (norm_weight && (!aligned16(norm_weight) || !aligned16(normed_out))))
+    return ATTNRES_ERR_ALIGNMENT;
+  MergeUpdateArgs m{inter_out, inter_lse, partial_in, sub_out, u, rows, (int)D, dtype, query, gain, eps,
+                    partial_out, h_out, out_lse, norm_weight, norm_eps, normed_out,
+                    static_cast<cudaStream_t>(stream)};
+  return cuda_status(launch_merge_update(m));
+}
+
+int attnres_rms_norm(const void *x, int64_t B, int64_t T, int64_t D, int dtype, const float *weight,
+                     float eps, void *y, void *stream) {
   int64_t rows = 0;
   int st = check_rows(B, T, D, dtype, rows);
   if (st) return st;
   if ((st = check_eps(eps))) return st;
   if (!merge_supported((int)D, dtype)) return ATTNRES_ERR_SHAPE;
   if (rows == 0) return ATTNRES_OK;
-  if (!inter_out || !inter_lse || !sub_out || !query || !partial_out || !h_out) return ATTNRES_ERR_NULL;
-  if (!aligned16(inter_out) || (partial_in && !aligned16(partial_in)) || !aligned16(sub_out) ||
-      (u && !aligned16(u)) || !aligned16(query) || (gain && !aligned16(gain)) ||
-      !aligned16(partial_out) || !aligned16(h_out))
-    return ATTNRES_ERR_ALIGNMENT;
-  MergeUpdateArgs m{inter_out, inter_lse, partial_in, sub_out, u, rows, (int)D, dtype, query, gain, eps,
-                    partial_out, h_out, out_lse, static_cast<cudaStream_t>(stream)};
-  return cuda_status(launch_merge_update(m));
+  if (!x || !weight || !y) return ATTNRES_ERR_NULL;
+  if (!aligned16(x) || !aligned16(weight) || !aligned16(y)) return ATTNRES_ERR_ALIGNMENT;
+  RmsNormArgs a{x, rows, (int)D, dtype, weight, eps, y, static_cast<cudaStream_t>(stream)};
+  return cuda_status(launch_rms_norm(a));
 }
 
 int attnres_partial_update(const void *h, const void *partial_in, const float *u, int64_t B,

@@ -59,11 +59,26 @@ struct MergeUpdateArgs {
   const float *gain;
   float eps;
   void *partial_out;           // [rows, D] p_{k-1}
-  void *h_out;                 // [rows, D] h_k
+  void *h_out;                 // [rows, D] h_k, or nullptr
   float *out_lse;
+  const float *norm_weight;    // [D] pre-norm weight, or nullptr
+  float norm_eps;
+  void *normed_out;            // [rows, D] RMSNorm(h_k) (.) norm_weight, or nullptr
   cudaStream_t stream;
 };
 cudaError_t launch_merge_update(const MergeUpdateArgs &a);
+
+struct RmsNormArgs {
+  const void *x;               // [rows, D]
+  int64_t rows;
+  int D;
+  int dtype;
+  const float *weight;         // [D]
+  float eps;
+  void *y;                     // [rows, D], may alias x
+  cudaStream_t stream;
+};
+cudaError_t launch_rms_norm(const RmsNormArgs &a);
 
 struct PartialUpdateArgs {
   const void *h;

@@ -148,14 +148,18 @@ struct MergeUpdateParams {
   const void *sub;     // sublayer output, or its input when u != nullptr
   const float *u;      // or nullptr
   void *p_out;
+  const float *nw;     // pre-norm weight [D] (NORM)
+  float neps;          // pre-norm eps (NORM)
+  void *y;             // RMSNorm(h) (.) nw, [rows, D] (NORM)
 };
 
-template <typename T, int VPT, int TEAM, bool SYNTH>
+template <typename T, int VPT, int TEAM, bool SYNTH, bool NORM>
 __global__ void __launch_bounds__(TEAM ? 256 : 512)
 merge_update_kernel(const __grid_constant__ MergeUpdateParams P) {
   using E = Elt<T>;
   constexpr int EPV = E::EPV;
   __shared__ float red[TEAM ? 1 : 2 * 32 * 2];
+  __shared__ float red_n[(TEAM || !NORM) ? 1 : 2 * 32];
   const MergeParams &p = P.m;
   const int tpr = TEAM ? TEAM : blockDim.x;
   const int lt = TEAM ? (threadIdx.x % TEAM) : threadIdx.x;
@@ -163,18 +167,20 @@ merge_update_kernel(const __grid_constant__ MergeUpdateParams P) {
   const int team = TEAM ? threadIdx.x / TEAM : 0;
   const bool has_pin = P.p_in != nullptr;
 
-  // The folded query w~ = w (.) gamma and u live in shared memory (loaded
-  // once per CTA), not in registers: fewer registers, more rows in flight.
-  // Layout [quarter e4 / 4][vector j] of float4, so consecutive lanes read
-  // consecutive 16 bytes.
-  extern __shared__ float4 qu[];                      // [EPV/4][nvec] q~, then [EPV/4][nvec] u
+  // The folded query w~ = w (.) gamma, u and the pre-norm weight live in
+  // shared memory (loaded once per CTA), not in registers: fewer registers,
+  // more rows in flight.  Layout [quarter e4 / 4][vector j] of float4, so
+  // consecutive lanes read consecutive 16 bytes.
+  extern __shared__ float4 qu[];   // [EPV/4][nvec] q~, then u (SYNTH), then the norm weight (NORM)
   constexpr int Q4 = EPV / 4;
+  constexpr int NW_AT = SYNTH ? 2 * Q4 : Q4;
   for (int idx = threadIdx.x; idx < p.nvec * Q4; idx += blockDim.x) {
     const int j = idx / Q4, e4 = (idx % Q4) * 4;
     const float4 w4 = ld_f4(p.q + j * EPV + e4);
     const float4 g4 = p.g ? ld_f4(p.g + j * EPV + e4) : make_float4(1.f, 1.f, 1.f, 1.f);
     qu[(e4 / 4) * p.nvec + j] = make_float4(w4.x * g4.x, w4.y * g4.y, w4.z * g4.z, w4.w * g4.w);
     if (SYNTH) qu[(Q4 + e4 / 4) * p.nvec + j] = ld_f4(P.u + j * EPV + e4);
+    if (NORM) qu[(NW_AT + e4 / 4) * p.nvec + j] = ld_f4(P.nw + j * EPV + e4);
   }
   __syncthreads();
   bool valid[VPT];
@@ -204,7 +210,7 @@ merge_update_kernel(const __grid_constant__ MergeUpdateParams P) {
       }
     }
   };
-  int parity = 0;
+  int parity = 0, parity_n = 0;
   auto process = [&](int64_t k, const uint4 (&ov)[VPT], const uint4 (&pv)[VPT], const uint4 (&sv)[VPT]) {
     const int64_t row = ((int64_t)blockIdx.x + k * gridDim.x) * teams_per_cta + team;
     const bool row_ok = row < p.rows;
@@ -251,16 +257,21 @@ merge_update_kernel(const __grid_constant__ MergeUpdateParams P) {
       cta_sum<2>(part, red, parity);
       parity ^= 1;
     }
-    if (!row_ok) return;
-    const float sp = part[0] * rsqrtf(fmaf(part[1], p.inv_D, p.eps));
-    const float l = p.lse[row];
-    const float M = fmaxf(l, sp);
-    const float a = expf(l - M), c = expf(sp - M);
-    const float inv = 1.f / (a + c);
-    const float wa = a * inv, wc = c * inv;
+    float wa = 0.f, wc = 0.f, M = 0.f, a = 0.f, c = 0.f;
+    if (row_ok) {
+      const float sp = part[0] * rsqrtf(fmaf(part[1], p.inv_D, p.eps));
+      const float l = p.lse[row];
+      M = fmaxf(l, sp);
+      a = expf(l - M);
+      c = expf(sp - M);
+      const float inv = 1.f / (a + c);
+      wa = a * inv;
+      wc = c * inv;
+    }
+    float hs = 0.f;                     // NORM: sum of h^2 over the row
 #pragma unroll
     for (int kk = 0; kk < VPT; ++kk) {
-      if (!valid[kk]) continue;
+      if (!valid[kk] || !row_ok) continue;
       const size_t off = row_off + (size_t)(lt + kk * tpr) * 16;
       st_vec(static_cast<char *>(P.p_out) + off, pn[kk]);
       float xo[EPV], xp[EPV], h[EPV];
@@ -268,15 +279,114 @@ merge_update_kernel(const __grid_constant__ MergeUpdateParams P) {
       E::unpack_again(pn[kk], xp);
 #pragma unroll
       for (int e = 0; e < EPV; ++e) h[e] = fmaf(wa, xo[e], wc * xp[e]);
-      st_vec(static_cast<char *>(p.h) + off, E::pack(h));
+      if (p.h) st_vec(static_cast<char *>(p.h) + off, E::pack(h));
+      if (NORM) {
+#pragma unroll
+        for (int e = 0; e < EPV; ++e) hs = fmaf(h[e], h[e], hs);
+      }
     }
-    if (lt == 0 && p.lse_out) p.lse_out[row] = M + logf(a + c);
+    if (NORM) {
+      // The next sublayer's pre-norm on the unrounded h: y = h / sqrt(mean h^2 + eps) (.) w_n.
+      if (TEAM) {
+        hs = team_sum_shfl<TEAM ? TEAM : 1>(hs);
+      } else {
+        float v1[1] = {hs};
+        cta_sum<1>(v1, red_n, parity_n);
+        parity_n ^= 1;
+        hs = v1[0];
+      }
+      if (row_ok) {
+        const float rn = rsqrtf(fmaf(hs, p.inv_D, P.neps));
+#pragma unroll
+        for (int kk = 0; kk < VPT; ++kk) {
+          if (!valid[kk]) continue;
+          float xo[EPV], xp[EPV], y[EPV];
+          E::unpack(ov[kk], xo);
+          E::unpack_again(pn[kk], xp);
+#pragma unroll
+          for (int e4 = 0; e4 < EPV; e4 += 4) {
+            const float4 w4 = qu[(NW_AT + e4 / 4) * p.nvec + lt + kk * tpr];
+            y[e4 + 0] = fmaf(wa, xo[e4 + 0], wc * xp[e4 + 0]) * rn * w4.x;
+            y[e4 + 1] = fmaf(wa, xo[e4 + 1], wc * xp[e4 + 1]) * rn * w4.y;
+            y[e4 + 2] = fmaf(wa, xo[e4 + 2], wc * xp[e4 + 2]) * rn * w4.z;
+            y[e4 + 3] = fmaf(wa, xo[e4 + 3], wc * xp[e4 + 3]) * rn * w4.w;
+          }
+          st_vec(static_cast<char *>(P.y) + row_off + (size_t)(lt + kk * tpr) * 16, E::pack(y));
+        }
+      }
+    }
+    if (row_ok && lt == 0 && p.lse_out) p.lse_out[row] = M + logf(a + c);
   };
 
   for (int64_t k = 0; k < my_groups; ++k) {
     uint4 ov[VPT], pv[VPT], sv[VPT];
     load_row(k, ov, pv, sv);
     process(k, ov, pv, sv);
+  }
+}
+
+// The next sublayer's pre-norm as a pass of its own, for the first sublayer
+// of a block, whose input is the phase-1 output itself:
+//   y = x / sqrt(mean_d x^2 + eps) (.) w,   row by row.
+// y may alias x: each thread reads its elements, the row is reduced, and the
+// same thread writes the same elements.
+template <typename T, int VPT, int TEAM>
+__global__ void __launch_bounds__(TEAM ? 256 : 512)
+rms_norm_kernel(const void *x, const float *__restrict__ w, void *y, int64_t rows, int nvec,
+                float inv_D, float eps) {
+  using E = Elt<T>;
+  constexpr int EPV = E::EPV;
+  __shared__ float red[TEAM ? 1 : 2 * 32];
+  const int tpr = TEAM ? TEAM : blockDim.x;
+  const int lt = TEAM ? (threadIdx.x % TEAM) : threadIdx.x;
+  const int teams_per_cta = TEAM ? blockDim.x / TEAM : 1;
+  const int team = TEAM ? threadIdx.x / TEAM : 0;
+  const size_t row_bytes = (size_t)nvec * 16;
+  const int64_t groups = (rows + teams_per_cta - 1) / teams_per_cta;
+  int parity = 0;
+  for (int64_t rg = blockIdx.x; rg < groups; rg += gridDim.x) {
+    const int64_t row = rg * teams_per_cta + team;
+    const bool row_ok = row < rows;
+    const size_t row_off = (size_t)row * row_bytes;
+    uint4 xv[VPT];
+    float ss = 0.f;
+#pragma unroll
+    for (int kk = 0; kk < VPT; ++kk) {
+      xv[kk] = make_uint4(0u, 0u, 0u, 0u);
+      if (row_ok && lt + kk * tpr < nvec)
+        xv[kk] = *reinterpret_cast<const uint4 *>(static_cast<const char *>(x) + row_off +
+                                                  (size_t)(lt + kk * tpr) * 16);
+      float v[EPV];
+      E::unpack(xv[kk], v);
+#pragma unroll
+      for (int e = 0; e < EPV; ++e) ss = fmaf(v[e], v[e], ss);
+    }
+    if (TEAM) {
+      ss = team_sum_shfl<TEAM ? TEAM : 1>(ss);
+    } else {
+      float v1[1] = {ss};
+      cta_sum<1>(v1, red, parity);
+      parity ^= 1;
+      ss = v1[0];
+    }
+    if (!row_ok) continue;
+    const float rn = rsqrtf(fmaf(ss, inv_D, eps));
+#pragma unroll
+    for (int kk = 0; kk < VPT; ++kk) {
+      const int j = lt + kk * tpr;
+      if (j >= nvec) continue;
+      float v[EPV], o[EPV];
+      E::unpack(xv[kk], v);
+#pragma unroll
+      for (int e4 = 0; e4 < EPV; e4 += 4) {
+        const float4 w4 = ld_f4(w + j * EPV + e4);
+        o[e4 + 0] = v[e4 + 0] * rn * w4.x;
+        o[e4 + 1] = v[e4 + 1] * rn * w4.y;
+        o[e4 + 2] = v[e4 + 2] * rn * w4.z;
+        o[e4 + 3] = v[e4 + 3] * rn * w4.w;
+      }
+      st_vec(static_cast<char *>(y) + row_off + (size_t)j * 16, E::pack(o));
+    }
   }
 }
 
@@ -380,10 +490,14 @@ cudaError_t dispatch(const MergeParams &p, const Cfg &c, cudaStream_t st) {
 }
 
 
-template <typename T, int VPT, int TEAM, bool SYNTH>
+// Largest dynamic shared memory a fused update+merge launch asks for: the
+// query, u and the norm weight at the widest supported row (2048 vectors).
+constexpr int kMuMaxSmem = 3 * 2048 * 8 * (int)sizeof(float);
+
+template <typename T, int VPT, int TEAM, bool SYNTH, bool NORM>
 cudaError_t run_mu(const MergeUpdateParams &P, const Cfg &c, cudaStream_t st) {
-  auto kern = merge_update_kernel<T, VPT, TEAM, SYNTH>;
-  const size_t smem = (size_t)P.m.D * sizeof(float) * (SYNTH ? 2 : 1);
+  auto kern = merge_update_kernel<T, VPT, TEAM, SYNTH, NORM>;
+  const size_t smem = (size_t)P.m.D * sizeof(float) * (1 + (SYNTH ? 1 : 0) + (NORM ? 1 : 0));
   struct Entry { int dev; size_t smem; int occ; };
   static Entry cache[16];
   static int used = 0;
@@ -392,7 +506,7 @@ cudaError_t run_mu(const MergeUpdateParams &P, const Cfg &c, cudaStream_t st) {
   for (int i = 0; i < used; ++i)
     if (cache[i].dev == dev && cache[i].smem == smem) o = cache[i].occ;
   if (o == 0) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, 128 * 1024);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kMuMaxSmem);
     if (e != cudaSuccess) return e;
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, kern, c.threads, smem);
     if (e != cudaSuccess) return e;
@@ -407,14 +521,53 @@ cudaError_t run_mu(const MergeUpdateParams &P, const Cfg &c, cudaStream_t st) {
   return cudaGetLastError();
 }
 
-template <typename T, bool SYNTH>
+template <typename T, bool SYNTH, bool NORM>
 cudaError_t dispatch_mu(const MergeUpdateParams &P, const Cfg &c, cudaStream_t st) {
   switch (c.team) {
-    case 0: return c.vpt == 2 ? run_mu<T, 2, 0, SYNTH>(P, c, st) : run_mu<T, 4, 0, SYNTH>(P, c, st);
-    case 4: return run_mu<T, 2, 4, SYNTH>(P, c, st);
-    case 8: return run_mu<T, 2, 8, SYNTH>(P, c, st);
-    case 16: return run_mu<T, 2, 16, SYNTH>(P, c, st);
-    default: return run_mu<T, 2, 32, SYNTH>(P, c, st);
+    case 0: return c.vpt == 2 ? run_mu<T, 2, 0, SYNTH, NORM>(P, c, st) : run_mu<T, 4, 0, SYNTH, NORM>(P, c, st);
+    case 4: return run_mu<T, 2, 4, SYNTH, NORM>(P, c, st);
+    case 8: return run_mu<T, 2, 8, SYNTH, NORM>(P, c, st);
+    case 16: return run_mu<T, 2, 16, SYNTH, NORM>(P, c, st);
+    default: return run_mu<T, 2, 32, SYNTH, NORM>(P, c, st);
+  }
+}
+
+template <typename T>
+cudaError_t dispatch_mu_t(const MergeUpdateParams &P, const Cfg &c, cudaStream_t st) {
+  const bool synth = P.u != nullptr, norm = P.nw != nullptr;
+  if (synth) return norm ? dispatch_mu<T, true, true>(P, c, st) : dispatch_mu<T, true, false>(P, c, st);
+  return norm ? dispatch_mu<T, false, true>(P, c, st) : dispatch_mu<T, false, false>(P, c, st);
+}
+
+template <typename T, int VPT, int TEAM>
+cudaError_t run_norm(const RmsNormArgs &a, const Cfg &c) {
+  auto kern = rms_norm_kernel<T, VPT, TEAM>;
+  static int occ[16] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  int &o = occ[dev & 15];
+  if (o == 0) {
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, kern, c.threads, 0);
+    if (e != cudaSuccess) return e;
+    if (o < 1) o = 1;
+  }
+  const int per_cta = TEAM ? c.threads / TEAM : 1;
+  const int64_t groups = (a.rows + per_cta - 1) / per_cta;
+  const int64_t cap = (int64_t)o * sm_count();
+  const int grid = (int)(groups < cap ? groups : cap);
+  kern<<<grid, c.threads, 0, a.stream>>>(a.x, a.weight, a.y, a.rows, a.D / epv_of(a.dtype),
+                                         1.f / (float)a.D, a.eps);
+  return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t dispatch_norm(const RmsNormArgs &a, const Cfg &c) {
+  switch (c.team) {
+    case 0: return c.vpt == 2 ? run_norm<T, 2, 0>(a, c) : run_norm<T, 4, 0>(a, c);
+    case 4: return run_norm<T, 2, 4>(a, c);
+    case 8: return run_norm<T, 2, 8>(a, c);
+    case 16: return run_norm<T, 2, 16>(a, c);
+    default: return run_norm<T, 2, 32>(a, c);
   }
 }
 
@@ -440,11 +593,18 @@ cudaError_t launch_merge_update(const MergeUpdateArgs &a) {
   P.sub = a.sub_out;
   P.u = a.u;
   P.p_out = a.partial_out;
-  const bool synth = a.u != nullptr;
-  if (a.dtype == ATTNRES_BF16)
-    return synth ? dispatch_mu<__nv_bfloat16, true>(P, c, a.stream)
-                 : dispatch_mu<__nv_bfloat16, false>(P, c, a.stream);
-  return synth ? dispatch_mu<float, true>(P, c, a.stream) : dispatch_mu<float, false>(P, c, a.stream);
+  P.nw = a.norm_weight;
+  P.neps = a.norm_eps;
+  P.y = a.normed_out;
+  if (a.dtype == ATTNRES_BF16) return dispatch_mu_t<__nv_bfloat16>(P, c, a.stream);
+  return dispatch_mu_t<float>(P, c, a.stream);
+}
+
+cudaError_t launch_rms_norm(const RmsNormArgs &a) {
+  Cfg c;
+  if (!choose(a.D, a.dtype, c)) return cudaErrorInvalidValue;
+  if (a.dtype == ATTNRES_BF16) return dispatch_norm<__nv_bfloat16>(a, c);
+  return dispatch_norm<float>(a, c);
 }
 
 namespace {

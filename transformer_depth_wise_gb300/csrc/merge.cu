@@ -257,6 +257,32 @@ merge_update_kernel(const __grid_constant__ MergeUpdateParams P) {
       cta_sum<2>(part, red, parity);
       parity ^= 1;
     }
+    if (!NORM) {
+      // No pre-norm: h is always stored (the entry point requires h_out then).
+      if (!row_ok) return;
+      const float sp = part[0] * rsqrtf(fmaf(part[1], p.inv_D, p.eps));
+      const float l = p.lse[row];
+      const float M = fmaxf(l, sp);
+      const float a = expf(l - M), c = expf(sp - M);
+      const float inv = 1.f / (a + c);
+      const float wa = a * inv, wc = c * inv;
+#pragma unroll
+      for (int kk = 0; kk < VPT; ++kk) {
+        if (!valid[kk]) continue;
+        const size_t off = row_off + (size_t)(lt + kk * tpr) * 16;
+        st_vec(static_cast<char *>(P.p_out) + off, pn[kk]);
+        float xo[EPV], xp[EPV], h[EPV];
+        E::unpack(ov[kk], xo);
+        E::unpack_again(pn[kk], xp);
+#pragma unroll
+        for (int e = 0; e < EPV; ++e) h[e] = fmaf(wa, xo[e], wc * xp[e]);
+        st_vec(static_cast<char *>(p.h) + off, E::pack(h));
+      }
+      if (lt == 0 && p.lse_out) p.lse_out[row] = M + logf(a + c);
+      return;
+    }
+    // With the pre-norm every lane of a team takes part in its second
+    // reduction, so rows past the end run through with zero weights.
     float wa = 0.f, wc = 0.f, M = 0.f, a = 0.f, c = 0.f;
     if (row_ok) {
       const float sp = part[0] * rsqrtf(fmaf(part[1], p.inv_D, p.eps));
@@ -280,12 +306,10 @@ merge_update_kernel(const __grid_constant__ MergeUpdateParams P) {
 #pragma unroll
       for (int e = 0; e < EPV; ++e) h[e] = fmaf(wa, xo[e], wc * xp[e]);
       if (p.h) st_vec(static_cast<char *>(p.h) + off, E::pack(h));
-      if (NORM) {
 #pragma unroll
-        for (int e = 0; e < EPV; ++e) hs = fmaf(h[e], h[e], hs);
-      }
+      for (int e = 0; e < EPV; ++e) hs = fmaf(h[e], h[e], hs);
     }
-    if (NORM) {
+    {
       // The next sublayer's pre-norm on the unrounded h: y = h / sqrt(mean h^2 + eps) (.) w_n.
       if (TEAM) {
         hs = team_sum_shfl<TEAM ? TEAM : 1>(hs);
@@ -491,8 +515,9 @@ cudaError_t dispatch(const MergeParams &p, const Cfg &c, cudaStream_t st) {
 
 
 // Largest dynamic shared memory a fused update+merge launch asks for: the
-// query, u and the norm weight at the widest supported row (2048 vectors).
-constexpr int kMuMaxSmem = 3 * 2048 * 8 * (int)sizeof(float);
+// query and u (and the norm weight with the pre-norm) at the widest
+// supported row (2048 vectors).
+constexpr int mu_max_smem(bool norm) { return (norm ? 3 : 2) * 2048 * 8 * (int)sizeof(float); }
 
 template <typename T, int VPT, int TEAM, bool SYNTH, bool NORM>
 cudaError_t run_mu(const MergeUpdateParams &P, const Cfg &c, cudaStream_t st) {
@@ -506,7 +531,7 @@ cudaError_t run_mu(const MergeUpdateParams &P, const Cfg &c, cudaStream_t st) {
   for (int i = 0; i < used; ++i)
     if (cache[i].dev == dev && cache[i].smem == smem) o = cache[i].occ;
   if (o == 0) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kMuMaxSmem);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, mu_max_smem(NORM));
     if (e != cudaSuccess) return e;
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, kern, c.threads, smem);
     if (e != cudaSuccess) return e;

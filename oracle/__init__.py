@@ -63,6 +63,8 @@ def _load():
             "oracle_fold_query": (None, [i64, _D, _D, _D]),
             "oracle_depth_aggregate": (c_int, [c_int, i64, i64, _D, _D, _D, c_dbl, _D, _D, _D]),
             "oracle_depth_aggregate_list": (c_int, [c_int, i64, i64, PP, _D, _D, c_dbl, _D, _D, _D]),
+            "oracle_depth_aggregate_backward": (c_int, [c_int, i64, i64, PP, _D, _D, c_dbl, _D, PP,
+                                                        _D, _D]),
             "oracle_os1_stats": (None, [c_int, i64, PP, _D, c_dbl, _D, _D, _D]),
             "oracle_single_source_stats": (None, [i64, _D, _D, c_dbl, _D, _D, _D]),
             "oracle_os2_merge": (None, [i64, c_dbl, _D, c_dbl, c_dbl, _D, c_dbl, _D, _D, _D]),
@@ -156,6 +158,25 @@ def depth_aggregate(sources, w, gamma=None, eps: float = 1e-8):
 # --------------------------------------------------------------------------
 # OS1 / OS2 / single_source_stats
 # --------------------------------------------------------------------------
+def depth_aggregate_backward(sources, w, gamma, eps: float, dh):
+    """Gradients of the depth aggregation for the upstream gradient dh:
+    returns (dV [n, ..., D], dw [D], dgamma [D] or None).  Exact fp64."""
+    srcs = [_arr(s) for s in sources]
+    shape = srcs[0].shape
+    D = shape[-1]
+    src2 = [s.reshape(-1, D) for s in srcs]
+    R = src2[0].shape[0]
+    dh = _arr(dh).reshape(R, D)
+    w = _arr(w)
+    gamma = None if gamma is None else _arr(gamma)
+    dV = [np.empty((R, D)) for _ in src2]
+    dw = np.empty(D)
+    dg = None if gamma is None else np.empty(D)
+    _check(_load().oracle_depth_aggregate_backward(len(src2), R, D, _plist(src2), _p(w), _p(gamma),
+                                                   float(eps), _p(dh), _plist(dV), _p(dw), _p(dg)))
+    return np.stack([x.reshape(shape) for x in dV]), dw, dg
+
+
 def os1_stats(sources_row, q_eff, eps: float = 1e-8):
     """Eq. OS1 for one token: sources_row [n, D] -> (m, numer [D], denom)."""
     V = _arr(sources_row)

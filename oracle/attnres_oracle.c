@@ -160,6 +160,90 @@ int oracle_depth_aggregate_list(int n, int64_t R, int64_t D, const double *const
     return 0;
 }
 
+/*
+ * Backward of the depth aggregation (the operator's backward pass that the
+ * fused AttnRes operator computes by recomputation; "Attention Residuals：当
+ * 网络深度也拥有寻址能力", sections "Depth attention 与 online merge reference"
+ * and "公开实现边界").  The chain rule taken through the forward's steps in
+ * reverse order, for each token row:
+ *   A3  h = sum_i alpha_i v_i      ->  da_i = dh . v_i,   dv_i  = alpha_i dh
+ *   A2  alpha = softmax(s)         ->  ds_i = alpha_i (da_i - sum_j alpha_j da_j)
+ *   A1  s_i = q~ . k_i             ->  dq~ += ds_i k_i,   dk_i  = ds_i q~
+ *   RMS k_i = v_i r_i, r_i = (mean_d v_i^2 + eps)^(-1/2)
+ *                                  ->  dv_i += r_i dk_i - (r_i^3 / D)(v_i . dk_i) v_i
+ * and, over all rows, the fold q~ = w (.) gamma  ->  dw = dq~ (.) gamma,
+ * dgamma = dq~ (.) w.
+ * src: n arrays [R][D]; dh: [R][D].  dV: n arrays [R][D] (overwritten).
+ * dw: [D]; dgamma: [D] or NULL (only when gamma is given).
+ */
+int oracle_depth_aggregate_backward(int n, int64_t R, int64_t D, const double *const *src,
+                                    const double *w, const double *gamma, double eps,
+                                    const double *dh, double *const *dV, double *dw,
+                                    double *dgamma)
+{
+    if (n < 1 || R < 0 || D < 1) return -1;
+    double *q_eff = malloc(sizeof(double) * D);
+    double *dq = calloc((size_t)D, sizeof(double));
+    double *k = malloc(sizeof(double) * (size_t)n * D);
+    double *r = malloc(sizeof(double) * n);
+    double *s = malloc(sizeof(double) * n);
+    double *alpha = malloc(sizeof(double) * n);
+    double *da = malloc(sizeof(double) * n);
+    if (!q_eff || !dq || !k || !r || !s || !alpha || !da) {
+        free(q_eff); free(dq); free(k); free(r); free(s); free(alpha); free(da);
+        return -1;
+    }
+    oracle_fold_query(D, w, gamma, q_eff);
+    for (int64_t row = 0; row < R; ++row) {
+        const double *g = dh + row * D;
+        /* forward, recomputed: k_i, r_i, s_i, alpha_i */
+        for (int i = 0; i < n; ++i) {
+            const double *v = src[i] + row * D;
+            double ss = 0.0;
+            for (int64_t d = 0; d < D; ++d) ss += v[d] * v[d];
+            r[i] = 1.0 / sqrt(ss / (double)D + eps);
+            s[i] = 0.0;
+            for (int64_t d = 0; d < D; ++d) {
+                k[(int64_t)i * D + d] = v[d] * r[i];
+                s[i] += q_eff[d] * k[(int64_t)i * D + d];
+            }
+        }
+        double m = s[0];
+        for (int i = 1; i < n; ++i) if (s[i] > m) m = s[i];
+        double z = 0.0;
+        for (int i = 0; i < n; ++i) z += exp(s[i] - m);
+        for (int i = 0; i < n; ++i) alpha[i] = exp(s[i] - m) / z;
+        /* A3 */
+        double mean_da = 0.0;
+        for (int i = 0; i < n; ++i) {
+            const double *v = src[i] + row * D;
+            da[i] = 0.0;
+            for (int64_t d = 0; d < D; ++d) da[i] += g[d] * v[d];
+            mean_da += alpha[i] * da[i];
+        }
+        for (int i = 0; i < n; ++i) {
+            const double *v = src[i] + row * D;
+            double *dv = dV[i] + row * D;
+            const double *ki = k + (int64_t)i * D;
+            /* A2 */
+            double ds = alpha[i] * (da[i] - mean_da);
+            /* A1 */
+            for (int64_t d = 0; d < D; ++d) dq[d] += ds * ki[d];
+            /* RMS, with dk = ds q~ */
+            double v_dot_dk = 0.0;
+            for (int64_t d = 0; d < D; ++d) v_dot_dk += v[d] * ds * q_eff[d];
+            double c = r[i] * r[i] * r[i] / (double)D * v_dot_dk;
+            for (int64_t d = 0; d < D; ++d) dv[d] = alpha[i] * g[d] + r[i] * ds * q_eff[d] - c * v[d];
+        }
+    }
+    for (int64_t d = 0; d < D; ++d) {
+        dw[d] = dq[d] * (gamma ? gamma[d] : 1.0);
+        if (dgamma) dgamma[d] = dq[d] * w[d];
+    }
+    free(q_eff); free(dq); free(k); free(r); free(s); free(alpha); free(da);
+    return 0;
+}
+
 /* ---------------------------------------------------------------------- */
 /* Online-softmax statistics (eq. OS1, OS2, single_source_stats).          */
 /* A state is the triple (m, numer[D], denom) with h = numer / denom.      */

@@ -347,6 +347,78 @@ def test_normed_chain_equals_normed_naive_stack():
 
 
 # --------------------------------------------------------------------------
+# Backward of the depth aggregation (the operator's forward/backward,
+# "Depth attention 与 online merge reference", "公开实现边界")
+# --------------------------------------------------------------------------
+def test_backward_closed_form_two_sources():
+    # D = 1, eps = 0: RMS(v) = sign(v), so with v0 = 1, v1 = -2 and q~ = ln(3)/2 the scores are
+    # +-ln(3)/2, alpha = (3/4, 1/4), h = 1/4.  With dh = 1: da = (1, -2), sum alpha da = 1/4,
+    # ds = (3/4 * 3/4, 1/4 * -9/4) = (9/16, -9/16), dq~ = 9/16 * 1 + (-9/16) * (-1) = 9/8.
+    # The scores do not depend on |v| (D = 1, eps = 0), so dv is the direct term alpha dh.
+    q = math.log(3) / 2
+    dV, dw, dg = oracle.depth_aggregate_backward([[[1.0]], [[-2.0]]], [q / 2], [2.0], 0.0, [[1.0]])
+    assert np.allclose(dV.ravel(), [0.75, 0.25], rtol=0, atol=1e-15)
+    assert np.allclose(dw, [9 / 8 * 2.0], rtol=0, atol=1e-14)          # dw = dq~ * gamma
+    assert np.allclose(dg, [9 / 8 * q / 2], rtol=0, atol=1e-14)        # dgamma = dq~ * w
+
+
+def test_backward_matches_central_differences_of_the_forward():
+    rng = np.random.default_rng(18)
+    n, R, D, eps = 3, 2, 5, 1e-2
+    V = rng.normal(size=(n, R, D)) * rng.uniform(0.5, 3, size=(n, 1, 1))
+    w, gam = rng.normal(0, 0.7, size=D), rng.normal(1, 0.2, size=D)
+    dh = rng.normal(size=(R, D))
+
+    def loss(V_, w_, g_):
+        h, _, _ = oracle.depth_aggregate(V_, w_, g_, eps)
+        return float(np.sum(dh * h))
+
+    dV, dw, dg = oracle.depth_aggregate_backward(list(V), w, gam, eps, dh)
+    step = 1e-6
+    num = np.zeros_like(V)
+    for idx in np.ndindex(V.shape):
+        Vp, Vm = V.copy(), V.copy()
+        Vp[idx] += step
+        Vm[idx] -= step
+        num[idx] = (loss(Vp, w, gam) - loss(Vm, w, gam)) / (2 * step)
+    assert np.allclose(dV, num, rtol=0, atol=1e-8)
+    for arr, grad, which in ((w, dw, "w"), (gam, dg, "gamma")):
+        num = np.zeros(D)
+        for d in range(D):
+            ap, am = arr.copy(), arr.copy()
+            ap[d] += step
+            am[d] -= step
+            args_p = (V, ap, gam) if which == "w" else (V, w, ap)
+            args_m = (V, am, gam) if which == "w" else (V, w, am)
+            num[d] = (loss(*args_p) - loss(*args_m)) / (2 * step)
+        assert np.allclose(grad, num, rtol=0, atol=1e-8), which
+
+
+def test_backward_invariants():
+    rng = np.random.default_rng(19)
+    n, R, D = 4, 3, 16
+    V = rng.normal(size=(n, R, D)) * rng.uniform(0.5, 8, size=(n, 1, 1))
+    w, gam = rng.normal(0, 0.3, size=D), rng.normal(1, 0.1, size=D)
+    dh = rng.normal(size=(R, D))
+    # one source: h = v whatever the query -> dv = dh exactly, no query gradient
+    dV1, dw1, dg1 = oracle.depth_aggregate_backward([V[0]], w, gam, 1e-8, dh)
+    assert np.array_equal(dV1[0], dh) and not np.any(dw1) and not np.any(dg1)
+    # no upstream gradient -> no gradient
+    dV0, dw0, _ = oracle.depth_aggregate_backward(list(V), w, gam, 1e-8, np.zeros((R, D)))
+    assert not np.any(dV0) and not np.any(dw0)
+    # eps = 0: each score is invariant to the scale of its own source, so the radial part of
+    # dv_i is only the direct term: sum_i v_i . dv_i = sum_i alpha_i dh . v_i = dh . h
+    dV, _, _ = oracle.depth_aggregate_backward(list(V), w, gam, 0.0, dh)
+    h, _, _ = oracle.depth_aggregate(V, w, gam, 0.0)
+    assert np.allclose(np.einsum("nrd,nrd->r", V, dV), np.sum(dh * h, axis=1), rtol=1e-12, atol=0)
+    # identical sources: equal scores whatever the query, so alpha = 1/n and every ds is 0:
+    # no query gradient, and each source gets dh / n
+    same = [V[0]] * n
+    dVs, dws, _ = oracle.depth_aggregate_backward(same, w, gam, 1e-8, dh)
+    assert np.allclose(dws, 0.0, atol=1e-15) and np.allclose(dVs, dh / n, rtol=0, atol=1e-15)
+
+
+# --------------------------------------------------------------------------
 # Rounding to the I/O dtype
 # --------------------------------------------------------------------------
 def test_bf16_rounding_ties_and_ranges():

@@ -279,6 +279,7 @@ def run_two_phase(args, wl, dev, rank, world):
     # pass, final partial (the new block summary) -> pinned host, every step.
     e2e = run_two_phase_e2e(args, wl, dev, inp, n_blocks, world)
     decode = run_decode(dev) if wl.name == "two_phase_bf16" and not args.rows else None
+    backward = run_backward(dev) if wl.name == "two_phase_bf16" and not args.rows else None
 
     res = {
         "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
@@ -297,6 +298,7 @@ def run_two_phase(args, wl, dev, rank, world):
         "unfused": unfused,
         "prenorm": prenorm,
         "decode": decode,
+        "backward": backward,
         "e2e": e2e,
         "gpu_launches": K * blk.launches_per_run,
         "clocks": clk,
@@ -393,6 +395,42 @@ def run_two_phase_e2e(args, wl, dev, inp, n_blocks, world):
     return {"value": round(tokens / (ms * 1e-3), 1), "unit": "tokens/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": K,
             "ms_per_step": round(ms / K, 4)}
+
+
+def run_backward(dev, reps: int = 20):
+    """Backward of the block_single_bf16 aggregation (10 x [4, 4096, 2048] bf16):
+    source, query and gain gradients; L2 flushed before each timed call."""
+    from transformer_depth_wise_gb300 import api
+    wl = wk.WORKLOADS["block_single_bf16"]
+    inp = wk.single_aggregation_inputs(wl, device=dev)
+    dh = wk.upstream_grad(wk.generator(wl.seed + 11, dev), (wl.B, wl.T, wl.D), wl.dtype, dev)
+    grads = [torch.empty_like(s) for s in inp["sources"]]
+    ws = torch.empty((api.depth_aggregate_backward_workspace_rows(wl.D, wl.dtype), wl.D), dtype=torch.float32,
+                     device=dev)
+    call = lambda: api.depth_aggregate_backward(inp["sources"], inp["query"], inp["gain"], inp["eps"], dh,  # noqa
+                                                grad_sources=grads, workspace=ws)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    for _ in range(3):
+        call()
+    ts = []
+    for _ in range(reps):
+        flush.fill_(1)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        call()
+        b.record()
+        torch.cuda.synchronize(dev)
+        ts.append(a.elapsed_time(b))
+    ms = statistics.median(ts)
+    rows = wl.B * wl.T
+    byts = accounting.aggregate_backward_bytes(wl.n, rows, wl.D, 2)
+    peak, src = measured_peak()
+    gbs = byts / (ms * 1e-3) / 1e9
+    del inp, grads, ws, flush, dh
+    return {"workload": wl.name, "ms": round(ms, 5), "tokens_per_s": round(rows / (ms * 1e-3), 1),
+            "algorithmic_bytes": byts, "achieved_gbs": round(gbs, 1), "frac": round(gbs / peak, 4),
+            "peak_source": src, "launches": 2,
+            "timing": "backward kernel + partial-sum reduce, median of %d, L2 flushed before each" % reps}
 
 
 def run_single(args, wl, dev, world):

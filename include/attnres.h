@@ -115,6 +115,51 @@ int attnres_block_phase2_merge(const void *inter_out, const float *inter_lse, co
                                void *stream);
 
 /*
+ * Backward of the depth aggregation (eq. A1-A3 of "Attention Residual 深度残差"
+ * in reverse: the operator's forward/backward by recomputation that
+ * "Attention Residuals：当网络深度也拥有寻址能力" describes in sections "Depth
+ * attention 与 online merge reference" and "公开实现边界").  For the upstream
+ * gradient dh of h = attnres_depth_aggregate(sources, query, gain, eps), per
+ * token row, with r_i = (mean_d v_i^2 + eps)^(-1/2), s_i = r_i (w~ . v_i),
+ * alpha = softmax(s) and ds_i = alpha_i (dh . v_i - sum_j alpha_j dh . v_j):
+ *   grad_sources[i] (=, or += with accumulate = 1)
+ *             alpha_i dh + ds_i r_i w~ - (ds_i s_i r_i^2 / D) v_i
+ *   grad_query = dw~ (.) gain,  grad_gain = dw~ (.) query,
+ *   dw~ = sum over all rows and sources of ds_i r_i v_i.
+ * The softmax is recomputed from the sources; nothing from the forward is
+ * needed.  fp32 arithmetic; grad_sources in the source dtype, rounded once.
+ *   sources, n, B, T, D, dtype, query, gain, eps: as attnres_depth_aggregate
+ *   grad_out     device [B,T,D] dh (source dtype)
+ *   grad_sources host array of n device pointers [B,T,D]; must not alias the
+ *                sources or grad_out
+ *   accumulate   0: overwrite grad_sources; 1: add to them
+ *   grad_query   device fp32 [D] or NULL;  grad_gain  device fp32 [D] or NULL
+ *                (with gain == NULL the gain is one and grad_gain = dw~ (.) query)
+ *   workspace    device fp32 [workspace_rows, D], caller-owned scratch for
+ *                the per-CTA partial sums of dw~; required when grad_query or
+ *                grad_gain is given, else unused (may be NULL).  Fewer rows than
+ *                attnres_depth_aggregate_backward_workspace_rows() reports run
+ *                fewer CTAs (at least 1 and 8 for narrow rows: ATTNRES_ERR_CAPACITY
+ *                below that).  Its contents on entry do not matter.
+ * The sum over rows runs in a fixed order: results are reproducible for
+ * the same inputs and workspace_rows on the same device.
+ * B*T == 0: grad_query / grad_gain are set to zero, nothing else is touched.
+ * D limits: as attnres_depth_aggregate (up to 1024 16-byte vectors per row).
+ */
+int attnres_depth_aggregate_backward(const void *const *sources, int n, int64_t B, int64_t T, int64_t D,
+                                     int dtype, const float *query, const float *gain, float eps,
+                                     const void *grad_out, void *const *grad_sources, int accumulate,
+                                     float *grad_query, float *grad_gain, float *workspace,
+                                     int64_t workspace_rows, void *stream);
+
+/*
+ * Workspace rows with which attnres_depth_aggregate_backward fills the
+ * current device (resident CTAs x SMs x rows per CTA) for this D and dtype;
+ * a negative status on a bad argument or CUDA error.  Host-only query.
+ */
+int64_t attnres_depth_aggregate_backward_workspace_rows(int64_t D, int dtype);
+
+/*
  * Running intra-block partial update ("forward_naive": partial = out, or
  * partial + out) with the benchmark recipes' synthetic sublayer
  * f(h) = 0.5 * tanh(u (.) h) standing in for the model's attention / FFN:

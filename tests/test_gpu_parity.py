@@ -155,6 +155,87 @@ def test_aggregate_block_single_full_size_sampled(gpu):
 
 
 # --------------------------------------------------------------------------
+# Backward of the depth aggregation
+# --------------------------------------------------------------------------
+# Gradient bounds, against the gradient's own scale (the inputs are the same
+# bytes on both sides; only fp32 against fp64 arithmetic differs):
+# - source gradients: fp32 2e-5 * max|g| (dots over D <= 8192 terms, typical
+#   error sqrt(D) * 2^-24 ~ 5e-6, times 4); bf16 8e-3 * max|g| (one rounding
+#   of the stored gradient, as the forward outputs);
+# - query / gain gradients: 2e-4 * max|g| (fp32 partial sums over up to
+#   1e5 row-source terms, then over the partial rows).
+GRAD_TOL = {torch.float32: 2e-5, torch.bfloat16: 8e-3}
+GRAD_SUM_TOL = 2e-4
+
+
+def _bwd_case(gpu, dtype, D, n, rows, seed, accumulate=False):
+    g = wk.generator(seed, gpu)
+    srcs, _ = wk.scaled_normal_sources(g, n, (1, rows, D), 0.5, 8.0, dtype, gpu)
+    W, G = wk.queries_and_gains(g, 1, D, gpu)
+    dh = wk.upstream_grad(g, (1, rows, D), dtype, gpu)
+    prior = [wk.upstream_grad(g, (1, rows, D), dtype, gpu) for _ in range(n)] if accumulate else None
+    gs = [p.clone() for p in prior] if accumulate else None
+    gs, gq, gg = api.depth_aggregate_backward(srcs, W[0], G[0], 1e-8, dh, grad_sources=gs, accumulate=accumulate)
+    dV, dw, dg = oracle.depth_aggregate_backward([f64(s).reshape(rows, D) for s in srcs], f64(W[0]), f64(G[0]),
+                                                 1e-8, f64(dh).reshape(rows, D))
+    if accumulate:
+        dV = np.stack([oracle.round_to(f64(p).reshape(rows, D) + dV[i], ODT[dtype]) for i, p in enumerate(prior)])
+    else:
+        dV = oracle.round_to(dV, ODT[dtype])
+    check(torch.stack(gs).reshape(n, rows, D), dV, GRAD_TOL[dtype] * np.abs(dV).max(), "grad sources")
+    check(gq, dw, GRAD_SUM_TOL * np.abs(dw).max(), "grad query")
+    check(gg, dg, GRAD_SUM_TOL * np.abs(dg).max(), "grad gain")
+    return srcs, W, G, dh, gs, gq, gg
+
+
+@pytest.mark.parametrize("dtype,D,n,rows", [
+    (torch.bfloat16, 16, 3, 33), (torch.float32, 64, 5, 20), (torch.bfloat16, 512, 7, 45),
+    (torch.float32, 256, 2, 70), (torch.bfloat16, 2048, 10, 37), (torch.bfloat16, 8192, 4, 9),
+    (torch.float32, 4096, 17, 13), (torch.bfloat16, 1024, 256, 3), (torch.bfloat16, 4096, 9, 130),
+])
+def test_aggregate_backward_small(gpu, dtype, D, n, rows):
+    _bwd_case(gpu, dtype, D, n, rows, D + n + rows)
+
+
+def test_aggregate_backward_accumulate_and_special_cases(gpu):
+    _bwd_case(gpu, torch.bfloat16, 2048, 6, 21, 5, accumulate=True)
+    _bwd_case(gpu, torch.float32, 64, 3, 50, 6, accumulate=True)
+    # one source: alpha = 1 and ds = 0 exactly -> the gradient is dh, bitwise; no query gradient
+    g = wk.generator(7, gpu)
+    (v,), _ = wk.scaled_normal_sources(g, 1, (2, 9, 1024), 0.5, 8.0, torch.bfloat16, gpu)
+    W, G = wk.queries_and_gains(g, 1, 1024, gpu)
+    dh = wk.upstream_grad(g, (2, 9, 1024), torch.bfloat16, gpu)
+    (gv,), gq, gg = api.depth_aggregate_backward([v], W[0], G[0], 1e-8, dh)
+    assert torch.equal(gv, dh) and not torch.any(gq) and not torch.any(gg)
+    # empty: the parameter gradients are zero
+    e = torch.empty((0, 5, 1024), dtype=torch.bfloat16, device=gpu)
+    _, gq, gg = api.depth_aggregate_backward([e, e], W[0], G[0], 1e-8, e, grad_sources=[e.clone(), e.clone()])
+    assert not torch.any(gq) and not torch.any(gg)
+
+
+def test_aggregate_backward_full_size_sampled(gpu):
+    wl = wk.WORKLOADS["block_single_bf16"]               # 10 x [4, 4096, 2048] bf16
+    inp = wk.single_aggregation_inputs(wl, device=gpu)
+    dh = wk.upstream_grad(wk.generator(4242, gpu), (wl.B, wl.T, wl.D), wl.dtype, gpu)
+    gs, gq, gg = api.depth_aggregate_backward(inp["sources"], inp["query"], inp["gain"], inp["eps"], dh)
+    rows = sample_rows(wl.B, wl.T, 24, 7)
+    dV, _, _ = oracle.depth_aggregate_backward([f64(pick(s, rows, wl.D)) for s in inp["sources"]],
+                                               f64(inp["query"]), f64(inp["gain"]), inp["eps"],
+                                               f64(pick(dh, rows, wl.D)))
+    got = np.stack([f64(pick(x, rows, wl.D)) for x in gs])
+    dV = oracle.round_to(dV, oracle.BF16)
+    check(got, dV, GRAD_TOL[torch.bfloat16] * np.abs(dV).max(), "cfg2 grad sources")
+    # the query gradient sums over every row: the sum over two halves must agree,
+    # and a second call gives the same bits (fixed reduction order)
+    half = wl.B // 2
+    parts = [api.depth_aggregate_backward([s[sl] for s in inp["sources"]], inp["query"], inp["gain"], inp["eps"],
+                                          dh[sl])[1] for sl in (slice(0, half), slice(half, wl.B))]
+    check(gq, f64(parts[0] + parts[1]), GRAD_SUM_TOL * float(gq.abs().max()), "cfg2 grad query split")
+    _, gq2, gg2 = api.depth_aggregate_backward(inp["sources"], inp["query"], inp["gain"], inp["eps"], dh)
+    assert torch.equal(gq, gq2) and torch.equal(gg, gg2)
+
+
+# --------------------------------------------------------------------------
 # two-phase Block: phase 1, phase 2 merge, partial update, one block chain
 # --------------------------------------------------------------------------
 @pytest.mark.parametrize("dtype,D,n,S,rows", [

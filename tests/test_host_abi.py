@@ -19,7 +19,7 @@ OK, NULL, SHAPE, DTYPE, ALIGN, MANY, CUDA, CAP, VALUE = 0, -1, -2, -3, -4, -5, -
 
 def declared_symbols():
     text = open(os.path.join(ROOT, "include", "attnres.h")).read()
-    return sorted(set(re.findall(r"^(?:int|const char \*)\s*(attnres_\w+)\(", text, re.M)))
+    return sorted(set(re.findall(r"^(?:int|int64_t|const char \*)\s*(attnres_\w+)\(", text, re.M)))
 
 
 def test_library_exports_every_declared_symbol():
@@ -121,6 +121,32 @@ def test_merge_and_update_argument_checks():
     assert u(FAKE, None, FAKE, 1, 0, 64, 1, FAKE, None) == OK
 
 
+def test_backward_argument_checks():
+    L = _lib.lib()
+    arr = _lib.ptr_array([FAKE] * 3)
+    garr = _lib.ptr_array([FAKE + 4096] * 3)
+
+    def bwd(n=3, B=1, D=64, dtype=1, q=FAKE, dh=FAKE, g=garr, acc=0, gq=FAKE, ws=FAKE, wsr=64, eps=1e-8):
+        return L.attnres_depth_aggregate_backward(arr, n, B, 2, D, dtype, q, None, eps, dh, g, acc, gq, None,
+                                                  ws, wsr, None)
+
+    assert bwd(q=None) == NULL
+    assert bwd(dh=None) == NULL
+    assert bwd(g=None) == NULL
+    assert bwd(ws=None) == NULL                          # a query gradient needs the workspace
+    assert bwd(wsr=0) == CAP
+    assert bwd(acc=2) == VALUE
+    assert bwd(eps=-1.0) == VALUE
+    assert bwd(n=0) == SHAPE
+    assert bwd(n=257) == MANY
+    assert bwd(D=36) == ALIGN
+    assert bwd(D=16384) == SHAPE                         # beyond the kernel family (bf16: 8192)
+    assert bwd(gq=FAKE + 4) == ALIGN
+    assert bwd(dh=FAKE + 8) == ALIGN
+    assert L.attnres_depth_aggregate_backward_workspace_rows(16384, 1) == SHAPE
+    assert L.attnres_depth_aggregate_backward_workspace_rows(64, 7) == DTYPE
+
+
 def test_full_stack_argument_checks():
     L = _lib.lib()
     f = L.attnres_full_stack_forward
@@ -206,6 +232,9 @@ def test_golden_prefill_cache():
 def test_kernel_byte_accounting_by_hand():
     # Block single aggregation [4,4096,2048] bf16, n = 10: 11 rows of 4 KiB per token.
     assert accounting.aggregate_bytes(10, 4 * 4096, 2048, 2) == 11 * 16384 * 4096
+    # Backward of that aggregation: 11 rows read, 10 written (+10 read when accumulating).
+    assert accounting.aggregate_backward_bytes(10, 4 * 4096, 2048, 2) == 21 * 16384 * 4096
+    assert accounting.aggregate_backward_bytes(10, 4 * 4096, 2048, 2, True) == 31 * 16384 * 4096
     # Two-phase block, 9 summaries [8,4096,4096] bf16, S = 24.
     b = accounting.two_phase_block_bytes(9, 24, 32768, 4096, 2)
     assert b["phase1"] == 32768 * (33 * 8192 + 24 * 4)

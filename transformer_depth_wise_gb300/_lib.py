@@ -45,6 +45,9 @@ SIGNATURES = {
     "attnres_block_merge_update": (_int, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _int, _vp, _vp, _f,
                                           _vp, _vp, _vp, _vp, _f, _vp, _vp]),
     "attnres_rms_norm": (_int, [_vp, _i64, _i64, _i64, _int, _vp, _f, _vp, _vp]),
+    "attnres_depth_aggregate_backward": (_int, [_vp, _int, _i64, _i64, _i64, _int, _vp, _vp, _f, _vp, _vp,
+                                                _int, _vp, _vp, _vp, _i64, _vp]),
+    "attnres_depth_aggregate_backward_workspace_rows": (_i64, [_i64, _int]),
     "attnres_full_stack_forward": (_int, [_pp, _int, _i64, _i64, _i64, _int, _vp, _vp, _vp, _f, _vp,
                                           _vp]),
     "attnres_block_schedule": (_int, [_int, _int, _ip, _ip, _int]),

@@ -15,6 +15,13 @@ def aggregate_bytes(n: int, rows: int, D: int, elt: int, stats: bool = False) ->
     return rows * (n + 1) * D * elt + (rows * 8 if stats else 0)
 
 
+def aggregate_backward_bytes(n: int, rows: int, D: int, elt: int, accumulate: bool = False) -> int:
+    """Backward of one aggregation: read n sources and dh, write n source
+    gradients (and read them first when accumulating).  The [D] query and
+    gain gradients and the per-CTA partials are negligible and not counted."""
+    return rows * ((n + 1) + n + (n if accumulate else 0)) * D * elt
+
+
 def phase1_bytes(n: int, S: int, rows: int, D: int, elt: int, with_max: bool = False) -> int:
     """Phase 1: read n summaries once, write S outputs and S lse (and S max) per token."""
     return rows * ((n + S) * D * elt + S * 4 * (2 if with_max else 1))

@@ -85,6 +85,47 @@ def depth_aggregate(sources, query, gain=None, eps: float = 1e-8, out=None, stat
     return (out, m, lse) if stats else out
 
 
+def depth_aggregate_backward_workspace_rows(D: int, dtype) -> int:
+    """Rows of the fp32 [rows, D] workspace that let the backward fill the current GPU."""
+    code = 1 if dtype == torch.bfloat16 else 0
+    r = int(_lib.lib().attnres_depth_aggregate_backward_workspace_rows(int(D), code))
+    if r < 0:
+        _lib.check("attnres_depth_aggregate_backward_workspace_rows", r)
+    return r
+
+
+def depth_aggregate_backward(sources, query, gain, eps: float, grad_out, grad_sources=None,
+                             accumulate: bool = False, want_query: bool = True, want_gain: bool = True,
+                             workspace=None):
+    """Gradients of h = depth_aggregate(sources, query, gain, eps) for the upstream dh = grad_out.
+
+    Returns (grad_sources list, grad_query [D] fp32 or None, grad_gain [D] fp32 or None).
+    accumulate=True adds into the given grad_sources.  workspace: fp32 [rows, D]
+    (allocated here when None and a parameter gradient is wanted).
+    """
+    srcs = [_cuda(s, "sources[i]") for s in sources]
+    B, T, D = _btd(srcs[0])
+    _cuda(grad_out, "grad_out")
+    dev = srcs[0].device
+    if grad_sources is None:
+        if accumulate:
+            raise ValueError("accumulate=True needs grad_sources")
+        grad_sources = [torch.empty_like(s) for s in srcs]
+    gq = torch.empty(D, dtype=torch.float32, device=dev) if want_query else None
+    gg = torch.empty(D, dtype=torch.float32, device=dev) if want_gain else None
+    if (want_query or want_gain) and workspace is None:
+        rows = depth_aggregate_backward_workspace_rows(D, srcs[0].dtype)
+        workspace = torch.empty((rows, D), dtype=torch.float32, device=dev)
+    arr = _lib.ptr_array([s.data_ptr() for s in srcs])
+    garr = _lib.ptr_array([g.data_ptr() for g in grad_sources])
+    rc = _lib.lib().attnres_depth_aggregate_backward(
+        arr, len(srcs), B, T, D, _code(srcs[0]), _ptr(query), _ptr(gain), float(eps), grad_out.data_ptr(),
+        garr, 1 if accumulate else 0, _ptr(gq), _ptr(gg), _ptr(workspace),
+        0 if workspace is None else workspace.shape[0], _stream(grad_out))
+    _lib.check("attnres_depth_aggregate_backward", rc)
+    return grad_sources, gq, gg
+
+
 def block_phase1(blocks, queries, gains=None, eps: float = 1e-8, out=None, out_max=None,
                  out_lse=None, want_max: bool = False):
     """Phase 1: S queries [S, D] over n summaries; returns (o [S,B,T,D], m or None, lse [S,B,T])."""

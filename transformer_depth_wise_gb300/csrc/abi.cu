@@ -171,6 +171,58 @@ int attnres_rms_norm(const void *x, int64_t B, int64_t T, int64_t D, int dtype, 
   return cuda_status(launch_rms_norm(a));
 }
 
+int attnres_depth_aggregate_backward(const void *const *sources, int n, int64_t B, int64_t T, int64_t D,
+                                     int dtype, const float *query, const float *gain, float eps,
+                                     const void *grad_out, void *const *grad_sources, int accumulate,
+                                     float *grad_query, float *grad_gain, float *workspace,
+                                     int64_t workspace_rows, void *stream) {
+  int64_t rows = 0;
+  int st = check_rows(B, T, D, dtype, rows);
+  if (st) return st;
+  if (n < 1) return ATTNRES_ERR_SHAPE;
+  if (n > ATTNRES_MAX_SOURCES) return ATTNRES_ERR_TOO_MANY_SOURCES;
+  if ((st = check_eps(eps))) return st;
+  if (accumulate != 0 && accumulate != 1) return ATTNRES_ERR_VALUE;
+  if (!aggregate_backward_supported((int)D, dtype)) return ATTNRES_ERR_SHAPE;
+  const bool want_q = grad_query || grad_gain;
+  if (!query) return ATTNRES_ERR_NULL;
+  if ((grad_query && !aligned16(grad_query)) || (grad_gain && !aligned16(grad_gain)) || !aligned16(query) ||
+      (gain && !aligned16(gain)))
+    return ATTNRES_ERR_ALIGNMENT;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (rows == 0) {  // no token rows: the parameter gradients are zero, nothing else is touched
+    if (grad_query && cudaMemsetAsync(grad_query, 0, (size_t)D * sizeof(float), s) != cudaSuccess)
+      return ATTNRES_ERR_CUDA;
+    if (grad_gain && cudaMemsetAsync(grad_gain, 0, (size_t)D * sizeof(float), s) != cudaSuccess)
+      return ATTNRES_ERR_CUDA;
+    return ATTNRES_OK;
+  }
+  if (!sources || !grad_out || !grad_sources) return ATTNRES_ERR_NULL;
+  for (int i = 0; i < n; ++i) {
+    if (!sources[i] || !grad_sources[i]) return ATTNRES_ERR_NULL;
+    if (!aligned16(sources[i]) || !aligned16(grad_sources[i])) return ATTNRES_ERR_ALIGNMENT;
+  }
+  if (!aligned16(grad_out)) return ATTNRES_ERR_ALIGNMENT;
+  if (want_q) {
+    if (!workspace) return ATTNRES_ERR_NULL;
+    if (!aligned16(workspace)) return ATTNRES_ERR_ALIGNMENT;
+    if (workspace_rows < aggregate_backward_rows_per_partial((int)D, dtype)) return ATTNRES_ERR_CAPACITY;
+  }
+  AggregateBackwardArgs a{sources, n, rows, (int)D, dtype, query, gain, eps, grad_out, grad_sources,
+                          accumulate != 0, grad_query, grad_gain, workspace, workspace_rows, s};
+  return cuda_status(launch_aggregate_backward(a));
+}
+
+int64_t attnres_depth_aggregate_backward_workspace_rows(int64_t D, int dtype) {
+  int64_t rows = 0;
+  int st = check_rows(1, 1, D, dtype, rows);
+  if (st) return st;
+  if (!aggregate_backward_supported((int)D, dtype)) return ATTNRES_ERR_SHAPE;
+  int64_t p = 0;
+  if (aggregate_backward_workspace_rows((int)D, dtype, p) != cudaSuccess) return ATTNRES_ERR_CUDA;
+  return p;
+}
+
 int attnres_partial_update(const void *h, const void *partial_in, const float *u, int64_t B,
                            int64_t T, int64_t D, int dtype, void *partial_out, void *stream) {
   int64_t rows = 0;

@@ -29,6 +29,29 @@ struct AggregateArgs {
 bool aggregate_supported(int D, int dtype);
 cudaError_t launch_aggregate(const AggregateArgs &a);
 
+struct AggregateBackwardArgs {
+  const void *const *sources;  // n device pointers [rows, D]
+  int n;
+  int64_t rows;
+  int D;
+  int dtype;
+  const float *query;
+  const float *gain;           // or nullptr
+  float eps;
+  const void *grad_out;        // [rows, D] dh
+  void *const *grad_sources;   // n device pointers [rows, D]
+  bool accumulate;             // grad_sources[i] += (else =)
+  float *grad_query;           // [D] or nullptr
+  float *grad_gain;            // [D] or nullptr
+  float *workspace;            // [workspace_rows, D] fp32 partials (needed with grad_query / grad_gain)
+  int64_t workspace_rows;
+  cudaStream_t stream;
+};
+bool aggregate_backward_supported(int D, int dtype);
+int aggregate_backward_rows_per_partial(int D, int dtype);
+cudaError_t aggregate_backward_workspace_rows(int D, int dtype, int64_t &rows);
+cudaError_t launch_aggregate_backward(const AggregateBackwardArgs &a);
+
 struct MergeArgs {
   const void *inter_out;       // [rows, D]
   const float *inter_lse;      // [rows]

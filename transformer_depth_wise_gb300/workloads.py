@@ -100,6 +100,11 @@ def sublayer_u(g: torch.Generator, count: int, D: int, device="cpu"):
     return torch.empty((count, D), dtype=torch.float32, device=device).normal_(1.0, 0.25, generator=g)
 
 
+def upstream_grad(g: torch.Generator, shape, dtype, device) -> torch.Tensor:
+    """The gradient arriving at an aggregation's output in a backward pass: N(0, 1)."""
+    return torch.empty(shape, dtype=torch.float32, device=device).normal_(0.0, 1.0, generator=g).to(dtype)
+
+
 def single_aggregation_inputs(wl: Workload, rows: int | None = None, device="cpu",
                               zero_query=False, n: int | None = None):
     """Inputs of one depth aggregation: dict(sources, query [D], gain [D], eps)."""

@@ -222,7 +222,7 @@ def test_aggregate_backward_full_size_sampled(gpu):
     dV, _, _ = oracle.depth_aggregate_backward([f64(pick(s, rows, wl.D)) for s in inp["sources"]],
                                                f64(inp["query"]), f64(inp["gain"]), inp["eps"],
                                                f64(pick(dh, rows, wl.D)))
-    got = np.stack([f64(pick(x, rows, wl.D)) for x in gs])
+    got = torch.stack([pick(x, rows, wl.D) for x in gs])
     dV = oracle.round_to(dV, oracle.BF16)
     check(got, dV, GRAD_TOL[torch.bfloat16] * np.abs(dV).max(), "cfg2 grad sources")
     # the query gradient sums over every row: the sum over two halves must agree,

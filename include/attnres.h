@@ -55,7 +55,8 @@ typedef enum {
     ATTNRES_ERR_CUDA = -6,             /* a kernel launch failed                     */
     ATTNRES_ERR_CAPACITY = -7,         /* a host output buffer is too small          */
     ATTNRES_ERR_VALUE = -8,            /* eps negative / not finite, block size 0    */
-    ATTNRES_ERR_TIMEOUT = -9           /* a kernel wait gave up (see below)          */
+    ATTNRES_ERR_TIMEOUT = -9,          /* a kernel wait gave up (see below)          */
+    ATTNRES_ERR_SCRATCH = -10          /* request exceeds the library's fixed scratch */
 } attnres_status_t;
 
 /* Most sources one aggregation may read (Full stack: L + 1 <= this). */
@@ -151,6 +152,37 @@ int attnres_depth_aggregate_backward(const void *const *sources, int n, int64_t 
                                      const void *grad_out, void *const *grad_sources, int accumulate,
                                      float *grad_query, float *grad_gain, float *workspace,
                                      int64_t workspace_rows, void *stream);
+
+/*
+ * attnres_depth_aggregate_backward without a workspace argument: the same
+ * gradients (same arguments minus workspace / workspace_rows), for callers
+ * that cannot allocate device memory -- for example a host program whose
+ * device memory is all handed out by its own pool, or a real-time loop that
+ * may not stall on the implicit synchronisation of cudaMalloc / cudaFree.
+ * The pages have no counterpart of this call; it exists only for them.
+ *   Scratch: the per-CTA partial sums of the query gradient live in one
+ *   fixed 8 MiB device array inside this library (2^21 floats; every GPU
+ *   that loads the library holds it until the process exits).  A call uses
+ *   floor(2^21 / D) partial rows of it; a request whose D needs more rows
+ *   than that (more than 2^18 features for rows owned by one CTA, 2^18 / 8
+ *   for narrow rows) is refused with ATTNRES_ERR_SCRATCH.  Every supported
+ *   D fits.  Nothing in the array has to start at zero: each partial row a
+ *   call sums is written earlier in the same call.
+ *   Set-up: the first call on a device looks up the array's device address
+ *   (with that device current); make that first call before any stream
+ *   capture.
+ *   Calls share the array: two calls whose kernels overlap on the GPU (other
+ *   streams, other host threads) race on it and give wrong query and gain
+ *   gradients.  Calls in one stream are ordered and safe.
+ * Nothing here allocates: no cudaMalloc, no cudaFree, no allocating library
+ * routine.  Same status codes as attnres_depth_aggregate_backward, plus
+ * ATTNRES_ERR_SCRATCH.
+ */
+int attnres_depth_aggregate_backward_noalloc(const void *const *sources, int n, int64_t B, int64_t T,
+                                             int64_t D, int dtype, const float *query, const float *gain,
+                                             float eps, const void *grad_out, void *const *grad_sources,
+                                             int accumulate, float *grad_query, float *grad_gain,
+                                             void *stream);
 
 /*
  * Workspace rows with which attnres_depth_aggregate_backward fills the

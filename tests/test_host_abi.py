@@ -143,6 +143,10 @@ def test_backward_argument_checks():
     assert bwd(D=16384) == SHAPE                         # beyond the kernel family (bf16: 8192)
     assert bwd(gq=FAKE + 4) == ALIGN
     assert bwd(dh=FAKE + 8) == ALIGN
+    na = L.attnres_depth_aggregate_backward_noalloc
+    assert na(arr, 3, 1, 2, 16384, 1, FAKE, None, 1e-8, FAKE, garr, 0, FAKE, None, None) == SHAPE
+    assert na(arr, 3, 1, 2, 64, 5, FAKE, None, 1e-8, FAKE, garr, 0, FAKE, None, None) == DTYPE
+    assert na(arr, 3, 1, 2, 64, 1, None, None, 1e-8, FAKE, garr, 0, None, None, None) == NULL
     assert L.attnres_depth_aggregate_backward_workspace_rows(16384, 1) == SHAPE
     assert L.attnres_depth_aggregate_backward_workspace_rows(64, 7) == DTYPE
 

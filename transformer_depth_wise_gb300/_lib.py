@@ -28,6 +28,7 @@ STATUS = {
     -7: "ATTNRES_ERR_CAPACITY",
     -8: "ATTNRES_ERR_VALUE",
     -9: "ATTNRES_ERR_TIMEOUT",
+    -10: "ATTNRES_ERR_SCRATCH",
 }
 
 # Every symbol include/attnres.h declares, with its ctypes signature.
@@ -48,6 +49,8 @@ SIGNATURES = {
     "attnres_depth_aggregate_backward": (_int, [_vp, _int, _i64, _i64, _i64, _int, _vp, _vp, _f, _vp, _vp,
                                                 _int, _vp, _vp, _vp, _i64, _vp]),
     "attnres_depth_aggregate_backward_workspace_rows": (_i64, [_i64, _int]),
+    "attnres_depth_aggregate_backward_noalloc": (_int, [_vp, _int, _i64, _i64, _i64, _int, _vp, _vp, _f, _vp,
+                                                        _vp, _int, _vp, _vp, _vp]),
     "attnres_full_stack_forward": (_int, [_pp, _int, _i64, _i64, _i64, _int, _vp, _vp, _vp, _f, _vp,
                                           _vp]),
     "attnres_block_schedule": (_int, [_int, _int, _ip, _ip, _int]),

@@ -63,6 +63,7 @@ const char *attnres_status_string(int status) {
     case ATTNRES_ERR_CAPACITY: return "a host output buffer is too small";
     case ATTNRES_ERR_VALUE: return "a value is invalid (eps negative or not finite, block size 0)";
     case ATTNRES_ERR_TIMEOUT: return "a kernel wait ran out of time and gave up (results invalid)";
+    case ATTNRES_ERR_SCRATCH: return "the request needs more than the library's fixed scratch";
     default: return "unknown status";
   }
 }
@@ -211,6 +212,26 @@ int attnres_depth_aggregate_backward(const void *const *sources, int n, int64_t 
   AggregateBackwardArgs a{sources, n, rows, (int)D, dtype, query, gain, eps, grad_out, grad_sources,
                           accumulate != 0, grad_query, grad_gain, workspace, workspace_rows, s};
   return cuda_status(launch_aggregate_backward(a));
+}
+
+int attnres_depth_aggregate_backward_noalloc(const void *const *sources, int n, int64_t B, int64_t T,
+                                             int64_t D, int dtype, const float *query, const float *gain,
+                                             float eps, const void *grad_out, void *const *grad_sources,
+                                             int accumulate, float *grad_query, float *grad_gain,
+                                             void *stream) {
+  int64_t rows = 0;
+  int st = check_rows(B, T, D, dtype, rows);
+  if (st) return st;
+  if (!aggregate_backward_supported((int)D, dtype)) return ATTNRES_ERR_SHAPE;
+  float *scratch = nullptr;
+  int64_t scratch_rows = 0;
+  if (grad_query || grad_gain) {
+    scratch_rows = noalloc_scratch_floats() / D;
+    if (scratch_rows < aggregate_backward_rows_per_partial((int)D, dtype)) return ATTNRES_ERR_SCRATCH;
+    if (noalloc_scratch(scratch) != cudaSuccess) return ATTNRES_ERR_CUDA;
+  }
+  return attnres_depth_aggregate_backward(sources, n, B, T, D, dtype, query, gain, eps, grad_out, grad_sources,
+                                          accumulate, grad_query, grad_gain, scratch, scratch_rows, stream);
 }
 
 int64_t attnres_depth_aggregate_backward_workspace_rows(int64_t D, int dtype) {

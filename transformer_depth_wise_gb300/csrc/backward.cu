@@ -353,6 +353,35 @@ cudaError_t rows_for(const Cfg &c, int64_t &rows) {
 
 }  // namespace
 
+// ---------------------------------------------------------------------------
+// Fixed scratch for the allocation-free entry point: room for the partial
+// rows of the query gradient, shared by every call of that entry point.
+// ---------------------------------------------------------------------------
+constexpr int64_t kNoAllocScratchFloats = (int64_t)1 << 21;   // 8 MiB
+static __device__ __align__(256) float g_noalloc_scratch[kNoAllocScratchFloats];
+
+int64_t noalloc_scratch_floats() { return kNoAllocScratchFloats; }
+
+// Device address of the scratch array on the current device.  Host code
+// cannot use the symbol itself as a device pointer; the address is looked
+// up once per device (with that device current) and cached.
+cudaError_t noalloc_scratch(float *&ptr) {
+  static float *cache[64] = {};
+  ptr = nullptr;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!cache[dev]) {
+    void *p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return e;
+    cache[dev] = static_cast<float *>(p);
+  }
+  ptr = cache[dev];
+  return cudaSuccess;
+}
+
 bool aggregate_backward_supported(int D, int dtype) {
   Cfg c;
   return choose(D, dtype, c);

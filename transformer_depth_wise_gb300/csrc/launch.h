@@ -51,6 +51,8 @@ bool aggregate_backward_supported(int D, int dtype);
 int aggregate_backward_rows_per_partial(int D, int dtype);
 cudaError_t aggregate_backward_workspace_rows(int D, int dtype, int64_t &rows);
 cudaError_t launch_aggregate_backward(const AggregateBackwardArgs &a);
+int64_t noalloc_scratch_floats();
+cudaError_t noalloc_scratch(float *&ptr);  // fixed scratch of the current device
 
 struct MergeArgs {
   const void *inter_out;       // [rows, D]

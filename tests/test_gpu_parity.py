@@ -303,8 +303,28 @@ def test_partial_update(gpu):
         check(pin.reshape(rows, D), want, TOL[dtype] * vmax([p]), "update in place")
 
 
+def test_synthetic_sublayer_nonlinearity_error_bound(gpu):
+    # 0.5 tanh(z) is formed as 0.5 - 1 / (e^{2z} + 1) with fast exp / reciprocal: its absolute
+    # error must stay near fp32 rounding over the whole range, tails and tiny arguments included.
+    z = np.concatenate([np.linspace(-60.0, 60.0, 120000), np.linspace(-1e-3, 1e-3, 4001),
+                        np.array([0.0, 1e-30, -1e-30, 88.0, -88.0, 200.0, -200.0])])
+    D = 256
+    R = (z.size + D - 1) // D
+    zz = np.zeros(R * D)
+    zz[: z.size] = z
+    h = torch.tensor(zz, dtype=torch.float32, device=gpu).reshape(1, R, D)
+    u = torch.ones(D, dtype=torch.float32, device=gpu)
+    y = api.partial_update(h, None, u)                       # first sublayer: p = f(h) exactly once
+    want = 0.5 * np.tanh(f64(h).reshape(-1))
+    err = np.abs(f64(y).reshape(-1) - want).max()
+    assert err <= 3e-7, err
+
+
 def test_merge_update_fused_step(gpu):
-    for dtype, D, rows in ((torch.bfloat16, 4096, 45), (torch.float32, 256, 70), (torch.bfloat16, 16, 33)):
+    # rows of 128..512 vectors take the cp.async ring kernel (4096 bf16, 2048 fp32, 1032 bf16 =
+    # 129 vectors, not a multiple of a warp); the others the register kernel
+    for dtype, D, rows in ((torch.bfloat16, 4096, 45), (torch.float32, 256, 70), (torch.bfloat16, 16, 33),
+                           (torch.float32, 2048, 37), (torch.bfloat16, 1032, 300), (torch.bfloat16, 7168, 5)):
         for synth, with_pin in ((True, True), (True, False), (False, True)):
             g = wk.generator(D + rows + 3 * synth + with_pin, gpu)
             (o, pin, sub), _ = wk.scaled_normal_sources(g, 3, (1, rows, D), 0.5, 3.0, dtype, gpu)

@@ -173,7 +173,7 @@ aggregate_kernel(const __grid_constant__ AggParams p) {
 #pragma unroll
         for (int e = 0; e < EPV; ++e) {
           h[e] = acc[k * EPV + e] * inv;
-          if (FUSED_F) h[e] = 0.5f * tanhf(ue[k * EPV + e] * h[e]);
+          if (FUSED_F) h[e] = half_tanh(ue[k * EPV + e] * h[e]);
         }
         st_vec(static_cast<char *>(p.out) + row_off + (size_t)(lt + k * tpr) * 16, E::pack(h));
       }

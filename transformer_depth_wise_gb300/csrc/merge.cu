@@ -232,7 +232,7 @@ merge_update_kernel(const __grid_constant__ MergeUpdateParams P) {
       }
 #pragma unroll
       for (int e = 0; e < EPV; ++e) {
-        const float out = SYNTH ? 0.5f * tanhf((valid[kk] ? uu[e] : 0.f) * xs[e]) : xs[e];
+        const float out = SYNTH ? half_tanh((valid[kk] ? uu[e] : 0.f) * xs[e]) : xs[e];
         y[e] = xp[e] + out;
       }
       pn[kk] = E::pack(y);              // the stored (rounded) partial
@@ -449,10 +449,10 @@ partial_update_kernel(const void *__restrict__ h, const void *pin, const float *
 #pragma unroll
       for (int e4 = 0; e4 < EPV; e4 += 4) {
         const float4 u4 = ld_f4(u + j * EPV + e4);
-        y[e4 + 0] = xp[e4 + 0] + 0.5f * tanhf(u4.x * xh[e4 + 0]);
-        y[e4 + 1] = xp[e4 + 1] + 0.5f * tanhf(u4.y * xh[e4 + 1]);
-        y[e4 + 2] = xp[e4 + 2] + 0.5f * tanhf(u4.z * xh[e4 + 2]);
-        y[e4 + 3] = xp[e4 + 3] + 0.5f * tanhf(u4.w * xh[e4 + 3]);
+        y[e4 + 0] = xp[e4 + 0] + half_tanh(u4.x * xh[e4 + 0]);
+        y[e4 + 1] = xp[e4 + 1] + half_tanh(u4.y * xh[e4 + 1]);
+        y[e4 + 2] = xp[e4 + 2] + half_tanh(u4.z * xh[e4 + 2]);
+        y[e4 + 3] = xp[e4 + 3] + half_tanh(u4.w * xh[e4 + 3]);
       }
       st_vec(static_cast<uint4 *>(pout) + v, E::pack(y));
     }

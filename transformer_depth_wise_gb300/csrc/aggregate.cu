@@ -186,176 +186,6 @@ aggregate_kernel(const __grid_constant__ AggParams p) {
 }
 
 // ---------------------------------------------------------------------------
-// Rows owned by a whole CTA (more than 64 vectors): wide source groups.
-// Each thread owns VPT vectors; a group of G sources (G = 16 with one vector
-// per thread, 8 with two) is loaded at once, so a row of up to G sources
-// costs one HBM round trip.  The 2G partial sums (w~.v and v.v per source)
-// are reduced with a warp reduce-scatter (lane l ends with the warp's sum
-// of value l: 31 shuffles for all of them), one shared-memory exchange
-// between warps and one barrier per group.
-// ---------------------------------------------------------------------------
-template <int V>  // V = 16 or 32 values per lane
-__device__ __forceinline__ float warp_reduce_scatter(const float (&a)[V]) {
-  const int lane = threadIdx.x & 31;
-  float b[16];
-  if (V == 32) {
-    const bool up = lane & 16;
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const float send = up ? a[i] : a[i + 16 % V];
-      const float keep = up ? a[i + 16 % V] : a[i];
-      b[i] = keep + __shfl_xor_sync(0xffffffffu, send, 16);
-    }
-  } else {
-#pragma unroll
-    for (int i = 0; i < 16; ++i) b[i] = a[i % V] + __shfl_xor_sync(0xffffffffu, a[i % V], 16);
-  }
-#pragma unroll
-  for (int o = 8; o > 0; o >>= 1) {
-    const bool up = lane & o;
-#pragma unroll
-    for (int i = 0; i < o; ++i) {
-      const float send = up ? b[i] : b[i + o];
-      const float keep = up ? b[i + o] : b[i];
-      b[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
-    }
-  }
-  return b[0];  // lane l: value l (V = 32) or l % 16 (V = 16)
-}
-
-template <typename T, int VPT, int G, bool FUSED_F>
-__global__ void __launch_bounds__(512)
-aggregate_cta_kernel(const __grid_constant__ AggParams p) {
-  using E = Elt<T>;
-  constexpr int EPV = E::EPV;
-  constexpr int NE = VPT * EPV;
-  constexpr int V = 2 * G;
-  static_assert(V == 16 || V == 32, "two sums per source, 16 or 32 per group");
-  __shared__ float red[2][16][V];
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
-  const int tpr = blockDim.x;
-
-  float qe[NE];
-  float ue[FUSED_F ? NE : 1];
-  bool valid[VPT];
-#pragma unroll
-  for (int k = 0; k < VPT; ++k) {
-    const int j = tid + k * tpr;
-    valid[k] = j < p.nvec;
-#pragma unroll
-    for (int e4 = 0; e4 < EPV; e4 += 4) {
-      float4 w4 = make_float4(0.f, 0.f, 0.f, 0.f), g4 = make_float4(1.f, 1.f, 1.f, 1.f);
-      float4 u4 = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (valid[k]) {
-        w4 = ld_f4(p.q + j * EPV + e4);
-        if (p.g) g4 = ld_f4(p.g + j * EPV + e4);
-        if (FUSED_F) u4 = ld_f4(p.u + j * EPV + e4);
-      }
-      qe[k * EPV + e4 + 0] = w4.x * g4.x;
-      qe[k * EPV + e4 + 1] = w4.y * g4.y;
-      qe[k * EPV + e4 + 2] = w4.z * g4.z;
-      qe[k * EPV + e4 + 3] = w4.w * g4.w;
-      if (FUSED_F) {
-        ue[k * EPV + e4 + 0] = u4.x; ue[k * EPV + e4 + 1] = u4.y;
-        ue[k * EPV + e4 + 2] = u4.z; ue[k * EPV + e4 + 3] = u4.w;
-      }
-    }
-  }
-
-  const size_t row_bytes = (size_t)p.D * sizeof(T);
-  int parity = 0;
-  for (int64_t row = blockIdx.x; row < p.rows; row += gridDim.x) {
-    const size_t row_off = (size_t)row * row_bytes;
-    float acc[NE];
-#pragma unroll
-    for (int e = 0; e < NE; ++e) acc[e] = 0.f;
-    float m = -INFINITY, den = 0.f;
-
-    for (int i0 = 0; i0 < p.n; i0 += G) {
-      uint4 buf[G][VPT];
-#pragma unroll
-      for (int g = 0; g < G; ++g)
-#pragma unroll
-        for (int k = 0; k < VPT; ++k) {
-          buf[g][k] = make_uint4(0u, 0u, 0u, 0u);
-          if (i0 + g < p.n && valid[k])
-            buf[g][k] = ld_stream(static_cast<const char *>(p.src[i0 + g]) + row_off + (size_t)(tid + k * tpr) * 16);
-        }
-      float part[V];
-#pragma unroll
-      for (int g = 0; g < G; ++g) {
-        float dot = 0.f, ss = 0.f;
-#pragma unroll
-        for (int k = 0; k < VPT; ++k) {
-          float x[EPV];
-          E::unpack(buf[g][k], x);
-#pragma unroll
-          for (int e = 0; e < EPV; ++e) {
-            dot = fmaf(qe[k * EPV + e], x[e], dot);
-            ss = fmaf(x[e], x[e], ss);
-          }
-        }
-        part[2 * g] = dot;
-        part[2 * g + 1] = ss;
-      }
-      const float mine = warp_reduce_scatter<V>(part);
-      if (lane < V) red[parity][warp][lane] = mine;
-      __syncthreads();
-      float tot = 0.f;                         // lane l (< V): CTA-wide value l
-      for (int w = 0; w < nwarps; ++w) tot += red[parity][w][lane % V];
-      parity ^= 1;
-      // lane 2g holds dot_g, lane 2g + 1 holds ss_g
-      const float ss_next = __shfl_down_sync(0xffffffffu, tot, 1);
-      const float s_lane = tot * rsqrtf(fmaf(ss_next, p.inv_D, p.eps));  // valid on even lanes
-      float s[G];
-      float gmax = -INFINITY;
-#pragma unroll
-      for (int g = 0; g < G; ++g) {
-        s[g] = __shfl_sync(0xffffffffu, s_lane, 2 * g);
-        if (i0 + g < p.n) gmax = fmaxf(gmax, s[g]);
-      }
-      const float m_new = fmaxf(m, gmax);
-      const float scale = expf(m - m_new);  // 0 on the first group (m = -inf)
-      den *= scale;
-#pragma unroll
-      for (int e = 0; e < NE; ++e) acc[e] *= scale;
-#pragma unroll
-      for (int g = 0; g < G; ++g) {
-        if (i0 + g < p.n) {
-          const float w = expf(s[g] - m_new);
-          den += w;
-#pragma unroll
-          for (int k = 0; k < VPT; ++k) {
-            float x[EPV];
-            E::unpack(buf[g][k], x);
-#pragma unroll
-            for (int e = 0; e < EPV; ++e) acc[k * EPV + e] = fmaf(w, x[e], acc[k * EPV + e]);
-          }
-        }
-      }
-      m = m_new;
-    }
-
-    const float inv = 1.f / den;
-#pragma unroll
-    for (int k = 0; k < VPT; ++k) {
-      if (!valid[k]) continue;
-      float h[EPV];
-#pragma unroll
-      for (int e = 0; e < EPV; ++e) {
-        h[e] = acc[k * EPV + e] * inv;
-        if (FUSED_F) h[e] = half_tanh(ue[k * EPV + e] * h[e]);
-      }
-      st_vec(static_cast<char *>(p.out) + row_off + (size_t)(tid + k * tpr) * 16, E::pack(h));
-    }
-    if (tid == 0) {
-      if (p.out_lse) p.out_lse[row] = m + logf(den);
-      if (p.out_max) p.out_max[row] = m;
-    }
-  }
-}
-
-// ---------------------------------------------------------------------------
 // Launch configuration
 // ---------------------------------------------------------------------------
 namespace {
@@ -376,11 +206,7 @@ bool choose(int D, int dtype, Cfg &c) {
     c = {2, team, 256};
     return true;
   }
-  if (nvec <= 512) {  // one vector per thread, groups of 16 sources
-    c = {1, 0, (nvec + 31) / 32 * 32};
-    return true;
-  }
-  if (nvec <= 1024) {  // two vectors per thread, groups of 8 sources
+  if (nvec <= 1024) {
     c = {2, 0, ((nvec + 1) / 2 + 31) / 32 * 32};
     return true;
   }
@@ -407,33 +233,9 @@ cudaError_t run(const AggParams &p, const Cfg &c, cudaStream_t st) {
   return cudaGetLastError();
 }
 
-template <typename T, int VPT, int G, bool F>
-cudaError_t run_cta(const AggParams &p, const Cfg &c, cudaStream_t st) {
-  auto kern = aggregate_cta_kernel<T, VPT, G, F>;
-  static int occ[16] = {0};  // resident CTAs per SM, per device
-  int dev = 0;
-  cudaGetDevice(&dev);
-  int &o = occ[dev & 15];
-  if (o == 0) {
-    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, kern, c.threads, 0);
-    if (e != cudaSuccess) return e;
-    if (o < 1) o = 1;
-  }
-  const int64_t cap = (int64_t)o * sm_count();
-  const int grid = (int)(p.rows < cap ? p.rows : cap);
-  kern<<<grid, c.threads, 0, st>>>(p);
-  return cudaGetLastError();
-}
-
 template <typename T, bool F>
 cudaError_t dispatch(const AggParams &p, const Cfg &c, cudaStream_t st) {
-  // Wide groups without register spills: bf16 rows unpack to twice the
-  // registers of fp32 ones, so bf16 takes groups of 8 (and the narrow-group
-  // kernel beyond 512 vectors), fp32 groups of 16 (8 with two vectors).
-  if (c.team == 0) {
-    if constexpr (sizeof(T) == 2) return c.vpt == 1 ? run_cta<T, 1, 8, F>(p, c, st) : run<T, 2, 0, F>(p, c, st);
-    else return c.vpt == 1 ? run_cta<T, 1, 16, F>(p, c, st) : run_cta<T, 2, 8, F>(p, c, st);
-  }
+  if (c.team == 0) return run<T, 2, 0, F>(p, c, st);
   switch (c.team) {
     case 4: return run<T, 2, 4, F>(p, c, st);
     case 8: return run<T, 2, 8, F>(p, c, st);

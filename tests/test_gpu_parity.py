@@ -81,6 +81,8 @@ CASES = [  # (dtype, D, n, rows) -- covers warp teams of 4..32 lanes and CTA tea
     (torch.bfloat16, 2048, 10, 300), (torch.bfloat16, 4096, 9, 41), (torch.bfloat16, 7168, 10, 17),
     (torch.bfloat16, 8192, 3, 5), (torch.float32, 4, 2, 9), (torch.float32, 12, 5, 50),
     (torch.float32, 256, 5, 64), (torch.float32, 264, 6, 31), (torch.float32, 4096, 4, 13),
+    # several source groups with a ragged tail, and a Full-stack-sized source list
+    (torch.float32, 1024, 37, 7), (torch.float32, 2056, 19, 21), (torch.bfloat16, 2048, 187, 6),
 ]
 
 

@@ -87,6 +87,19 @@ aggregate_kernel(const __grid_constant__ AggParams p) {
   int parity = 0;
   // Every team of the CTA runs the same number of iterations (rows past the
   // end are masked), so warp shuffles and barriers stay uniform.
+  // L2 lookahead: the team walks (row, source) in order; before loading a
+  // group it asks L2 for the source rows kAhead positions further on
+  // (crossing into the team's next rows), one bulk prefetch per source row,
+  // lanes in turn.  No registers are held for them, the L2 footprint is
+  // kAhead rows per team, and the group loads then hit L2.
+  constexpr int kAhead = 2 * G;
+  auto prefetch_src = [&](int64_t rgp, int i) {   // source i of the team's row group rgp
+    const int64_t r = rgp * teams_per_cta + team;
+    if (rgp < groups && r < p.rows && i < p.n)
+      prefetch_l2_bulk(static_cast<const char *>(p.src[i]) + (size_t)r * row_bytes, (uint32_t)row_bytes);
+  };
+  for (int pos = lt; pos < kAhead; pos += tpr)
+    prefetch_src(blockIdx.x + (int64_t)(pos / p.n) * gridDim.x, pos % p.n);
   for (int64_t rg = blockIdx.x; rg < groups; rg += gridDim.x) {
     const int64_t row = rg * teams_per_cta + team;
     const bool row_ok = row < p.rows;
@@ -97,6 +110,10 @@ aggregate_kernel(const __grid_constant__ AggParams p) {
     float m = -INFINITY, den = 0.f;
 
     for (int i0 = 0; i0 < p.n; i0 += G) {
+      for (int g = lt; g < G; g += tpr) {  // kAhead sources past this group's g-th
+        const int pos = i0 + kAhead + g;     // counted from the start of this row
+        prefetch_src(rg + (int64_t)(pos / p.n) * gridDim.x, pos % p.n);
+      }
       uint4 buf[G][VPT];
 #pragma unroll
       for (int g = 0; g < G; ++g) {

@@ -129,6 +129,12 @@ __device__ __forceinline__ float half_tanh(float z) {
   return 0.5f - __fdividef(1.f, __expf(2.f * z) + 1.f);
 }
 
+// Ask L2 to fetch `bytes` (a multiple of 16) from a 16-byte aligned global
+// address, without staging anything on the SM: one instruction per row.
+__device__ __forceinline__ void prefetch_l2_bulk(const void *gmem, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(gmem), "r"(bytes) : "memory");
+}
+
 }  // namespace attnres
 
 // ---------------------------------------------------------------------------

@@ -342,8 +342,18 @@ merge_update_kernel(const __grid_constant__ MergeUpdateParams P) {
     if (row_ok && lt == 0 && p.lse_out) p.lse_out[row] = M + logf(a + c);
   };
 
+  // One row ahead, three threads of the team ask L2 for the next row's o,
+  // p_in and sub (one bulk prefetch each): its loads then find it in L2.
+  auto prefetch_row = [&](int64_t k) {
+    const int64_t row = ((int64_t)blockIdx.x + k * gridDim.x) * teams_per_cta + team;
+    if (k >= my_groups || row >= p.rows || lt >= 3) return;
+    const void *base = lt == 0 ? p.o : (lt == 1 ? P.p_in : P.sub);
+    if (base) prefetch_l2_bulk(static_cast<const char *>(base) + (size_t)row * row_bytes, (uint32_t)row_bytes);
+  };
+  prefetch_row(0);
   for (int64_t k = 0; k < my_groups; ++k) {
     uint4 ov[VPT], pv[VPT], sv[VPT];
+    prefetch_row(k + 1);
     load_row(k, ov, pv, sv);
     process(k, ov, pv, sv);
   }

@@ -54,7 +54,10 @@ aggregate_kernel(const __grid_constant__ AggParams p) {
   const int teams_per_cta = TEAM ? blockDim.x / TEAM : 1;
   const int team = TEAM ? threadIdx.x / TEAM : 0;
 
-  // Folded query w~ = w (.) gamma for this thread's elements (and u).
+  // Folded query w~ = w (.) gamma for this thread's elements, as packed
+  // pairs (and u).
+  using PR = Pairs<T>;
+  constexpr int NP = PR::NP;
   float qe[NE];
   float ue[FUSED_F ? NE : 1];
   bool valid[VPT];
@@ -82,6 +85,10 @@ aggregate_kernel(const __grid_constant__ AggParams p) {
     }
   }
 
+  uint64_t qp[VPT * NP];
+#pragma unroll
+  for (int j = 0; j < VPT * NP; ++j) qp[j] = pair(qe[2 * j], qe[2 * j + 1]);
+
   const size_t row_bytes = (size_t)p.D * sizeof(T);
   const int64_t groups = (p.rows + teams_per_cta - 1) / teams_per_cta;
   int parity = 0;
@@ -104,9 +111,9 @@ aggregate_kernel(const __grid_constant__ AggParams p) {
     const int64_t row = rg * teams_per_cta + team;
     const bool row_ok = row < p.rows;
     const size_t row_off = (size_t)row * row_bytes;
-    float acc[NE];
+    uint64_t acc[VPT * NP];
 #pragma unroll
-    for (int e = 0; e < NE; ++e) acc[e] = 0.f;
+    for (int j = 0; j < VPT * NP; ++j) acc[j] = 0ull;
     float m = -INFINITY, den = 0.f;
 
     for (int i0 = 0; i0 < p.n; i0 += G) {
@@ -128,25 +135,25 @@ aggregate_kernel(const __grid_constant__ AggParams p) {
       float part[2 * G];
 #pragma unroll
       for (int g = 0; g < G; ++g) {
-        float dot = 0.f, ss = 0.f;
+        uint64_t dot = 0ull, ss = 0ull;
 #pragma unroll
         for (int k = 0; k < VPT; ++k) {
-          float x[EPV];
-          E::unpack(buf[g][k], x);
+          uint64_t x[NP];
+          PR::split(buf[g][k], x);
 #pragma unroll
-          for (int e = 0; e < EPV; ++e) {
-            dot = fmaf(qe[k * EPV + e], x[e], dot);
-            ss = fmaf(x[e], x[e], ss);
+          for (int j = 0; j < NP; ++j) {
+            fma_pair(dot, qp[k * NP + j], x[j]);
+            fma_pair(ss, x[j], x[j]);
           }
         }
-        part[2 * g] = dot;
-        part[2 * g + 1] = ss;
+        part[2 * g] = pair_sum(dot);
+        part[2 * g + 1] = pair_sum(ss);
       }
       if (TEAM) {
 #pragma unroll
         for (int t = 0; t < 2 * G; ++t) part[t] = team_sum_shfl<TEAM ? TEAM : 1>(part[t]);
       } else {
-        cta_sum<2 * G>(part, red, parity);
+        cta_sum_rs<2 * G>(part, red, parity);
         parity ^= 1;
       }
       float s[G];
@@ -162,19 +169,21 @@ aggregate_kernel(const __grid_constant__ AggParams p) {
       const float m_new = fmaxf(m, gmax);
       const float scale = expf(m - m_new);  // 0 on the first group (m = -inf)
       den *= scale;
+      const uint64_t scale2 = pair(scale, scale);
 #pragma unroll
-      for (int e = 0; e < NE; ++e) acc[e] *= scale;
+      for (int j = 0; j < VPT * NP; ++j) scale_pair(acc[j], scale2);
 #pragma unroll
       for (int g = 0; g < G; ++g) {
         if (i0 + g < p.n) {
           const float w = expf(s[g] - m_new);
           den += w;
+          const uint64_t w2 = pair(w, w);
 #pragma unroll
           for (int k = 0; k < VPT; ++k) {
-            float x[EPV];
-            E::unpack(buf[g][k], x);
+            uint64_t x[NP];
+            PR::split(buf[g][k], x);
 #pragma unroll
-            for (int e = 0; e < EPV; ++e) acc[k * EPV + e] = fmaf(w, x[e], acc[k * EPV + e]);
+            for (int j = 0; j < NP; ++j) fma_pair(acc[k * NP + j], w2, x[j]);
           }
         }
       }
@@ -188,8 +197,10 @@ aggregate_kernel(const __grid_constant__ AggParams p) {
         if (!valid[k]) continue;
         float h[EPV];
 #pragma unroll
+        for (int j = 0; j < NP; ++j) unpair(acc[k * NP + j], h[2 * j], h[2 * j + 1]);
+#pragma unroll
         for (int e = 0; e < EPV; ++e) {
-          h[e] = acc[k * EPV + e] * inv;
+          h[e] = h[e] * inv;
           if (FUSED_F) h[e] = half_tanh(ue[k * EPV + e] * h[e]);
         }
         st_vec(static_cast<char *>(p.out) + row_off + (size_t)(lt + k * tpr) * 16, E::pack(h));

@@ -135,6 +135,85 @@ __device__ __forceinline__ void prefetch_l2_bulk(const void *gmem, uint32_t byte
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(gmem), "r"(bytes) : "memory");
 }
 
+// ---------------------------------------------------------------------------
+// Packed fp32 pairs (one 64-bit register, fma.rn.f32x2 = two FMAs per
+// instruction) and the element pairs of a 16-byte vector.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint64_t pair(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void unpair(uint64_t v, float &lo, float &hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ float pair_sum(uint64_t v) {
+  float lo, hi;
+  unpair(v, lo, hi);
+  return lo + hi;
+}
+__device__ __forceinline__ void fma_pair(uint64_t &acc, uint64_t a, uint64_t b) {
+  asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(a), "l"(b));
+}
+__device__ __forceinline__ void scale_pair(uint64_t &acc, uint64_t s) {
+  asm("fma.rn.f32x2 %0, %0, %1, %2;" : "+l"(acc) : "l"(s), "l"(0ull));
+}
+
+template <typename T> struct Pairs;
+template <> struct Pairs<float> {
+  static constexpr int NP = 2;  // pairs per 16-byte vector
+  static __device__ __forceinline__ void split(const uint4 &v, uint64_t *x) {
+    x[0] = ((uint64_t)v.y << 32) | v.x;
+    x[1] = ((uint64_t)v.w << 32) | v.z;
+  }
+};
+template <> struct Pairs<__nv_bfloat16> {
+  static constexpr int NP = 4;
+  static __device__ __forceinline__ void split(const uint4 &v, uint64_t *x) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) x[i] = ((uint64_t)(w[i] & 0xffff0000u) << 32) | (uint64_t)(w[i] << 16);
+  }
+};
+
+// Sum of K (a power of two, <= 32) values over a whole CTA, every thread
+// getting all K totals.  Each warp reduce-scatters (butterflies down to K
+// lanes' worth, then halving steps: lane l ends with the warp's total of
+// value l % K, 31 shuffles for K = 32 and fewer for smaller K instead of
+// 5 K), lanes < K publish to red[parity][warp][K], one barrier, each lane
+// adds the warps' totals of its value, and K shuffles hand every total to
+// every lane.  Alternating `parity` between calls saves a second barrier.
+template <int K>
+__device__ __forceinline__ void cta_sum_rs(float (&v)[K], float *red /*[2][32][K]*/, int parity) {
+  static_assert(K >= 1 && K <= 32 && (K & (K - 1)) == 0, "K: power of two <= 32");
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+  float b[K];
+#pragma unroll
+  for (int i = 0; i < K; ++i) b[i] = v[i];
+#pragma unroll
+  for (int o = 16; o >= K; o >>= 1) {  // plain butterflies over the lane bits no value is kept by
+#pragma unroll
+    for (int i = 0; i < K; ++i) b[i] += __shfl_xor_sync(0xffffffffu, b[i], o);
+  }
+#pragma unroll
+  for (int o = K / 2; o > 0; o >>= 1) {  // halving: keep the upper or lower half
+    const bool up = lane & o;
+#pragma unroll
+    for (int i = 0; i < o; ++i) {
+      const float send = up ? b[i] : b[i + o];
+      const float keep = up ? b[i + o] : b[i];
+      b[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+    }
+  }
+  float *slot = red + parity * 32 * K;
+  if (lane < K) slot[warp * K + lane] = b[0];
+  __syncthreads();
+  float t = 0.f;
+  for (int w = 0; w < nwarps; ++w) t += slot[w * K + (lane & (K - 1))];
+#pragma unroll
+  for (int i = 0; i < K; ++i) v[i] = __shfl_sync(0xffffffffu, t, i);
+}
+
 }  // namespace attnres
 
 // ---------------------------------------------------------------------------

@@ -80,6 +80,8 @@ def _load():
                                                        c_dbl, _D, _D]),
             "oracle_full_stack_forward": (c_int, [c_int, i64, i64, _D, _D, _D, _D, c_dbl, c_int,
                                                   _D, _D]),
+            "oracle_full_stack_two_phase": (c_int, [c_int, c_int, i64, i64, _D, _D, _D, _D, c_dbl, c_int,
+                                                    _D, _D]),
             "oracle_atomic_block_size": (c_int, [c_int, c_int, c_int]),
             "oracle_block_schedule": (c_int, [c_int, c_int, _I, _I, c_int]),
         }
@@ -344,6 +346,21 @@ def full_stack_forward(v0, W, G, U, eps: float, dtype: int):
 # --------------------------------------------------------------------------
 # Bookkeeping
 # --------------------------------------------------------------------------
+def full_stack_two_phase(v0, W, G, U, S: int, eps: float, dtype: int):
+    """Full stack with the two-phase schedule of block size S: returns (V [L+1, R, D], y [R, D])."""
+    v0 = _arr(v0)
+    R, D = v0.reshape(-1, v0.shape[-1]).shape
+    U = _arr(U)
+    L = U.shape[0]
+    W = _arr(W)
+    G = None if G is None else _arr(G)
+    V = np.empty((L + 1, R, D))
+    y = np.empty((R, D))
+    _check(_load().oracle_full_stack_two_phase(L, int(S), R, D, _p(v0), _p(W), _p(G), _p(U), float(eps),
+                                               int(dtype), _p(V), _p(y)))
+    return V, y
+
+
 def atomic_block_size(num_hidden_layers: int, attnres_block_size=None) -> int:
     has = attnres_block_size is not None
     return int(_load().oracle_atomic_block_size(int(num_hidden_layers), int(has),

@@ -577,6 +577,87 @@ int oracle_full_stack_forward(int L, int64_t R, int64_t D, const double *v0, con
     return rc;
 }
 
+/*
+ * Full stack with the two-phase schedule (a schedule block size S: the
+ * remark under "_run_block_two_phase" that Full AttnRes runs two-phase when
+ * schedule_block_size is given, and the (S+N)d residual I/O of "推理：block
+ * representations 像一份 depth KV cache").  Sublayers are taken S at a time;
+ * for the block of sublayers l = start+1 .. min(start+S, L):
+ *   phase 1: for every l of the block, the OS1 state of query l over the
+ *            sources completed before the block, v_0 .. v_start, handed over
+ *            normalised as (lse_l, o_l, 1);
+ *   phase 2: in order, h_l = that state merged (OS2) with each intra-block
+ *            source v_{start+1} .. v_{l-1} (single_source_stats), and
+ *            v_l = f_l(h_l) with the synthetic sublayer.
+ * The final aggregate is the plain one over v_0 .. v_L.  Rounding follows
+ * what the GPU path materialises: o_l to the I/O dtype (lse as fp32) and
+ * v_l to the I/O dtype; h_l stays unrounded (f is fused).  In the F64 mode
+ * nothing is rounded and the result equals oracle_full_stack_forward's.
+ * Arguments as oracle_full_stack_forward, plus S >= 1.
+ */
+int oracle_full_stack_two_phase(int L, int S, int64_t R, int64_t D, const double *v0, const double *W,
+                                const double *G, const double *U, double eps, int dtype,
+                                double *V_out, double *y)
+{
+    if (L < 1 || S < 1 || R < 0 || D < 1) return -1;
+    int64_t RD = R * D;
+    const double **srcs = malloc(sizeof(double *) * (size_t)(L + 1));
+    const double **rows = malloc(sizeof(double *) * (size_t)(L + 1));
+    double *O = malloc(sizeof(double) * (size_t)S * (size_t)RD);
+    double *LSE = malloc(sizeof(double) * (size_t)S * (size_t)R);
+    double *q_eff = malloc(sizeof(double) * (size_t)D);
+    double *numer = malloc(sizeof(double) * (size_t)D);
+    double *np = malloc(sizeof(double) * (size_t)D);
+    double *nm = malloc(sizeof(double) * (size_t)D);
+    double *h = malloc(sizeof(double) * (size_t)RD);
+    int rc = 0;
+    if (!srcs || !rows || !O || !LSE || !q_eff || !numer || !np || !nm || !h) { rc = -1; goto done; }
+    memcpy(V_out, v0, sizeof(double) * (size_t)RD);
+    for (int l = 0; l <= L; ++l) srcs[l] = V_out + (int64_t)l * RD;
+    for (int start = 0; start < L; start += S) {
+        int end = start + S < L ? start + S : L;          /* sublayers start+1 .. end */
+        /* phase 1: every query of the block over v_0 .. v_start */
+        for (int l = start + 1; l <= end; ++l) {
+            int s = l - start - 1;
+            oracle_fold_query(D, W + (int64_t)(l - 1) * D, G ? G + (int64_t)(l - 1) * D : NULL, q_eff);
+            for (int64_t r = 0; r < R; ++r) {
+                double m1, d1;
+                for (int i = 0; i <= start; ++i) rows[i] = srcs[i] + r * D;
+                oracle_os1_stats(start + 1, D, rows, q_eff, eps, &m1, numer, &d1);
+                double *o = O + ((int64_t)s * R + r) * D;
+                for (int64_t d = 0; d < D; ++d) o[d] = oracle_round(numer[d] / d1, dtype);
+                LSE[(int64_t)s * R + r] = oracle_round(m1 + log(d1), dtype == ORACLE_F64 ? ORACLE_F64 : ORACLE_F32);
+            }
+        }
+        /* phase 2: in order, merge the intra-block sources, then the sublayer */
+        for (int l = start + 1; l <= end; ++l) {
+            int s = l - start - 1;
+            oracle_fold_query(D, W + (int64_t)(l - 1) * D, G ? G + (int64_t)(l - 1) * D : NULL, q_eff);
+            for (int64_t r = 0; r < R; ++r) {
+                double m = LSE[(int64_t)s * R + r], den = 1.0;
+                for (int64_t d = 0; d < D; ++d) numer[d] = O[((int64_t)s * R + r) * D + d];
+                for (int j = start + 1; j < l; ++j) {
+                    double mp, dp, mm, dm;
+                    oracle_single_source_stats(D, srcs[j] + r * D, q_eff, eps, &mp, np, &dp);
+                    oracle_os2_merge(D, m, numer, den, mp, np, dp, &mm, nm, &dm);
+                    m = mm;
+                    den = dm;
+                    memcpy(numer, nm, sizeof(double) * (size_t)D);
+                }
+                for (int64_t d = 0; d < D; ++d) h[r * D + d] = numer[d] / den;
+            }
+            double *vl = V_out + (int64_t)l * RD;
+            oracle_synthetic_sublayer(R, D, U + (int64_t)(l - 1) * D, h, vl);
+            for (int64_t k = 0; k < RD; ++k) vl[k] = oracle_round(vl[k], dtype);
+        }
+    }
+    rc = oracle_depth_aggregate_list(L + 1, R, D, srcs, W + (int64_t)L * D,
+                                     G ? G + (int64_t)L * D : NULL, eps, y, NULL, NULL);
+done:
+    free(srcs); free(rows); free(O); free(LSE); free(q_eff); free(numer); free(np); free(nm); free(h);
+    return rc;
+}
+
 /* ---------------------------------------------------------------------- */
 /* Bookkeeping ("forward_naive" source lists, "atomic_block_size").        */
 /* ---------------------------------------------------------------------- */

@@ -273,6 +273,33 @@ def test_full_stack_first_layers_by_hand():
     assert np.allclose(y, (v0 + v1 + v2 + v3) / 4, atol=1e-15)
 
 
+@pytest.mark.parametrize("S", [1, 2, 3, 5, 7, 9, 12])
+def test_full_two_phase_schedule_equals_the_naive_full_stack(S):
+    # Phase 1 over the completed sources + OS2 merges of the intra-block ones reach,
+    # in exact arithmetic, the direct aggregation over every earlier source.
+    rng = np.random.default_rng(20 + S)
+    L, R, D = 9, 3, 8
+    v0 = rng.normal(size=(R, D)) * 2
+    W, G = rng.normal(0, 0.5, size=(L + 1, D)), rng.normal(1, 0.1, size=(L + 1, D))
+    U = rng.normal(1, 0.25, size=(L, D))
+    V0, y0 = oracle.full_stack_forward(v0, W, G, U, 1e-8, oracle.F64)
+    V1, y1 = oracle.full_stack_two_phase(v0, W, G, U, S, 1e-8, oracle.F64)
+    assert np.allclose(V1, V0, rtol=0, atol=1e-12)
+    assert np.allclose(y1, y0, rtol=0, atol=1e-12)
+
+
+def test_full_two_phase_rounds_what_it_materialises():
+    rng = np.random.default_rng(30)
+    L, R, D = 7, 2, 16
+    v0 = oracle.round_to(rng.normal(size=(R, D)), oracle.BF16)
+    W, G = rng.normal(0, 0.5, size=(L + 1, D)), rng.normal(1, 0.1, size=(L + 1, D))
+    U = rng.normal(1, 0.25, size=(L, D))
+    V, y = oracle.full_stack_two_phase(v0, W, G, U, 3, 1e-8, oracle.BF16)
+    assert np.array_equal(V, oracle.round_to(V, oracle.BF16))       # every v_l is a bf16 tensor
+    Vn, yn = oracle.full_stack_forward(v0, W, G, U, 1e-8, oracle.BF16)
+    assert np.allclose(V, Vn, atol=0.02) and np.allclose(y, yn, atol=0.02)  # a few bf16 ulps apart
+
+
 def test_chain_rounding_points():
     # The two-phase chain rounds o, h and p to the I/O dtype; in F64 mode it is exact
     # and must equal the unrounded two-phase recurrence of one block.

@@ -486,6 +486,25 @@ def run_full_stack(args, wl, dev, world):
     byts = accounting.full_stack_bytes(wl.L, rows, wl.D, 2)
     peak, src = measured_peak()
     gbs = byts / (ms * 1e-3) / 1e9
+    # The same stack with the two-phase schedule of block size S.
+    S = args.schedule_block_size
+    ws = torch.empty(int(api._lib.lib().attnres_full_stack_two_phase_workspace_bytes(
+        wl.L, S, 1, rows, wl.D, 1)), dtype=torch.uint8, device=dev)
+    for _ in range(args.warmup):
+        api.full_stack_two_phase(inp["v0"], inp["queries"], inp["gains"], inp["u"], S, inp["eps"], srcs, y, ws)
+    torch.cuda.synchronize(dev)
+    a.record()
+    for _ in range(args.steps):
+        api.full_stack_two_phase(inp["v0"], inp["queries"], inp["gains"], inp["u"], S, inp["eps"], srcs, y, ws)
+    b.record()
+    torch.cuda.synchronize(dev)
+    ms2 = a.elapsed_time(b) / args.steps
+    b2 = accounting.full_two_phase_bytes(wl.L, S, rows, wl.D, 2)
+    two_phase = {"schedule_block_size": S, "ms_per_step": round(ms2, 4),
+                 "tokens_per_s": round(rows / (ms2 * 1e-3), 1), "algorithmic_bytes": b2,
+                 "achieved_gbs": round(b2 / (ms2 * 1e-3) / 1e9, 1), "frac": round(b2 / (ms2 * 1e-3) / 1e9 / peak, 4),
+                 "speedup_vs_naive": round(ms / ms2, 3)}
+    del ws
     return {"metric": "Full AttnRes stack forward tokens/s", "value": round(rows / (ms * 1e-3), 1),
             "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
@@ -493,7 +512,8 @@ def run_full_stack(args, wl, dev, world):
             "config": {"workload": wl.name, "rows": rows, "D": wl.D, "L": wl.L},
             "roofline": {"bound": "hbm", "kernel": "aggregate (fused f)", "achieved": round(gbs, 1),
                          "peak": peak, "unit": "GB/s", "frac": round(gbs / peak, 4),
-                         "traffic": None, "peak_source": src}}
+                         "traffic": None, "peak_source": src},
+            "two_phase": two_phase}
 
 
 def cpu_baseline_block(wl):
@@ -511,6 +531,8 @@ def main():
     ap.add_argument("--workload", default="two_phase_bf16", choices=sorted(wk.WORKLOADS))
     ap.add_argument("--rows", type=int, default=0, help="shrink to B=1, T=rows (profiling)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--schedule-block-size", type=int, default=14,
+                    help="Full stack: block size S of the two-phase schedule timed beside the plain stack")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     wl = wk.WORKLOADS[args.workload]

@@ -271,6 +271,37 @@ int attnres_full_stack_forward(void *const *sources, int L, int64_t B, int64_t T
                                float eps, void *y_out, void *stream);
 
 /*
+ * The same Full stack with the two-phase schedule of block size S (Full
+ * AttnRes run two-phase when a schedule block size is given: the remark
+ * under "_run_block_two_phase" in "Attention Residual 深度残差", and the (S+N)d
+ * residual I/O of "推理：block representations 像一份 depth KV cache" in
+ * "Attention Residuals：当网络深度也拥有寻址能力").  For each block of
+ * sublayers l = start+1 .. min(start+S, L):
+ *   phase 1: the block's queries over v_0 .. v_start in one pass (the
+ *            normalised output o_l and lse_l of every sublayer of the block);
+ *   phase 2: in order, h_l = o_l's state merged online with the intra-block
+ *            sources v_{start+1} .. v_{l-1}; v_l = f_l(h_l) (fused, as above).
+ * Then y as above.  The same result as attnres_full_stack_forward up to
+ * rounding: o_l is stored in the source dtype (lse fp32) in between.
+ *   sources, L, B, T, D, dtype, queries, gains, u, eps, y_out: as above
+ *   S          1 .. ATTNRES_MAX_QUERIES
+ *   workspace  device, 256-byte aligned, at least
+ *              attnres_full_stack_two_phase_workspace_bytes() bytes (the
+ *              phase-1 outputs of one block and, for blocks past ten
+ *              sources, their scores); contents on entry do not matter
+ * Blocks with up to ten sources use the phase-1 kernels of
+ * attnres_block_phase1; wider ones need bf16 and D a multiple of 64 up to
+ * 2048 (else ATTNRES_ERR_SHAPE, checked before anything runs).
+ */
+int attnres_full_stack_two_phase(void *const *sources, int L, int S, int64_t B, int64_t T, int64_t D,
+                                 int dtype, const float *queries, const float *gains, const float *u,
+                                 float eps, void *y_out, void *workspace, int64_t workspace_bytes,
+                                 void *stream);
+
+/* Workspace bytes attnres_full_stack_two_phase needs (negative status on bad shapes). */
+int64_t attnres_full_stack_two_phase_workspace_bytes(int L, int S, int64_t B, int64_t T, int64_t D, int dtype);
+
+/*
  * Host-only bookkeeping ("BlockAttnResStack.forward_naive"): the sources each
  * atomic sublayer attends over, for num_atomic sublayers in blocks of
  * block_size.  Block 0 is the embedding; a block boundary falls after

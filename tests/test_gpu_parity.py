@@ -16,7 +16,7 @@ import pytest
 import torch
 
 import oracle
-from transformer_depth_wise_gb300 import api
+from transformer_depth_wise_gb300 import _lib, api
 from transformer_depth_wise_gb300 import workloads as wk
 
 pytestmark = pytest.mark.gpu
@@ -525,6 +525,52 @@ def test_full_stack_config_full_size_sampled(gpu):
                                       f64(inp["gains"]), f64(inp["u"]), inp["eps"], oracle.BF16)
     tol = TOL[torch.bfloat16] * float(inp["v0"].abs().max())
     for l in (1, 2, 50, 186):
+        check(pick(srcs[l], rows, wl.D), V[l], tol, f"v_{l}")
+    check(pick(y, rows, wl.D), oy, tol, "y")
+
+
+# Full stack with the two-phase schedule: blocks up to ten sources take the
+# block phase-1 kernels, wider ones the raw-score path (scores ten at a time,
+# softmax, outputs over all sources); the oracle rounds o_l and v_l where the
+# GPU stores them.
+@pytest.mark.parametrize("S,D,L,rows", [(4, 1024, 23, 130), (12, 2048, 30, 70), (1, 512, 14, 64),
+                                        (40, 1024, 25, 50), (24, 2048, 27, 129)])
+def test_full_two_phase_small(gpu, S, D, L, rows):
+    wl = wk.WORKLOADS["full_stack_bf16"]
+    inp = wk.full_stack_inputs(wl, rows=rows, device=gpu, L=L, D=D)
+    y, srcs = api.full_stack_two_phase(inp["v0"], inp["queries"], inp["gains"], inp["u"], S, inp["eps"])
+    V, oy = oracle.full_stack_two_phase(f64(inp["v0"]).reshape(rows, D), f64(inp["queries"]), f64(inp["gains"]),
+                                        f64(inp["u"]), S, inp["eps"], oracle.BF16)
+    tol = TOL[torch.bfloat16] * float(inp["v0"].abs().max())
+    for l in range(1, L + 1):
+        check(srcs[l].reshape(rows, D), V[l], tol, f"S={S} v_{l}")
+    check(y.reshape(rows, D), oracle.round_to(oy, oracle.BF16), tol, f"S={S} y")
+
+
+def test_full_two_phase_shape_limits(gpu):
+    # fp32 works while every block has at most ten sources; wider blocks need bf16
+    wl = wk.WORKLOADS["full_stack_bf16"]
+    inp = wk.full_stack_inputs(wl, rows=20, device=gpu, L=9, D=256)
+    v0 = inp["v0"].float()
+    y, srcs = api.full_stack_two_phase(v0, inp["queries"], inp["gains"], inp["u"], 3, inp["eps"])
+    V, oy = oracle.full_stack_two_phase(f64(v0).reshape(20, 256), f64(inp["queries"]), f64(inp["gains"]),
+                                        f64(inp["u"]), 3, inp["eps"], oracle.F32)
+    check(y.reshape(20, 256), oracle.round_to(oy, oracle.F32), TOL[torch.float32] * float(v0.abs().max()), "fp32 y")
+    inp = wk.full_stack_inputs(wl, rows=20, device=gpu, L=25, D=256)
+    with pytest.raises(_lib.AttnResError):
+        api.full_stack_two_phase(inp["v0"].float(), inp["queries"], inp["gains"], inp["u"], 3, inp["eps"])
+
+
+def test_full_two_phase_config_full_size_sampled(gpu):
+    wl = wk.WORKLOADS["full_stack_bf16"]                 # [1, 2048, 2048], L = 186
+    inp = wk.full_stack_inputs(wl, device=gpu)
+    S = 14
+    y, srcs = api.full_stack_two_phase(inp["v0"], inp["queries"], inp["gains"], inp["u"], S, inp["eps"])
+    rows = sample_rows(wl.B, wl.T, 6, 8)
+    V, oy = oracle.full_stack_two_phase(f64(pick(inp["v0"], rows, wl.D)), f64(inp["queries"]), f64(inp["gains"]),
+                                        f64(inp["u"]), S, inp["eps"], oracle.BF16)
+    tol = TOL[torch.bfloat16] * float(inp["v0"].abs().max())
+    for l in (1, 14, 15, 29, 100, 186):
         check(pick(srcs[l], rows, wl.D), V[l], tol, f"v_{l}")
     check(pick(y, rows, wl.D), oy, tol, "y")
 

@@ -249,5 +249,13 @@ def test_kernel_byte_accounting_by_hand():
     # fused: 117 row transfers per token after phase 1, against 140 unfused
     assert (fb["merges"] + fb["updates"]) // 32768 // 8192 == 117
     assert (b["merges"] + b["updates"]) // 32768 // 8192 == 140
+    # Full two-phase, S = L: one block, phase 1 over v_0 only (1 read + L writes + lse),
+    # sublayer j reads o, lse and j intra sources and writes v_l; then the final L+1 + 1.
+    L = 5
+    want = (1 + L) * 4096 + L * 4 + sum((j + 2) * 4096 + 4 for j in range(L)) + (L + 2) * 4096
+    assert accounting.full_two_phase_bytes(L, L, 1, 2048, 2) == want
+    # S = 1 gives back the naive stack's source reads (plus the o row and lse written and read)
+    naive = accounting.full_stack_bytes(186, 1, 2048, 2)
+    assert accounting.full_two_phase_bytes(186, 1, 1, 2048, 2) == naive + 186 * (2 * 4096 + 8)
     # Full stack, 186 sublayers: 17391 + 187 reads and 187 writes per token row.
     assert accounting.full_stack_bytes(186, 2048, 2048, 2) == 2048 * (17391 + 187 + 187) * 4096

@@ -49,6 +49,9 @@ SIGNATURES = {
     "attnres_depth_aggregate_backward": (_int, [_vp, _int, _i64, _i64, _i64, _int, _vp, _vp, _f, _vp, _vp,
                                                 _int, _vp, _vp, _vp, _i64, _vp]),
     "attnres_depth_aggregate_backward_workspace_rows": (_i64, [_i64, _int]),
+    "attnres_full_stack_two_phase": (_int, [_vp, _int, _int, _i64, _i64, _i64, _int, _vp, _vp, _vp, _f, _vp,
+                                            _vp, _i64, _vp]),
+    "attnres_full_stack_two_phase_workspace_bytes": (_i64, [_int, _int, _i64, _i64, _i64, _int]),
     "attnres_depth_aggregate_backward_noalloc": (_int, [_vp, _int, _i64, _i64, _i64, _int, _vp, _vp, _f, _vp,
                                                         _vp, _int, _vp, _vp, _vp]),
     "attnres_full_stack_forward": (_int, [_pp, _int, _i64, _i64, _i64, _int, _vp, _vp, _vp, _f, _vp,

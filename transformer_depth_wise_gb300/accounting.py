@@ -66,6 +66,24 @@ def full_stack_bytes(L: int, rows: int, D: int, elt: int) -> int:
     return rows * (reads + writes) * D * elt
 
 
+def full_two_phase_bytes(L: int, S: int, rows: int, D: int, elt: int) -> int:
+    """Full stack with the two-phase schedule of block size S, f fused.
+
+    Per block of Sb sublayers after `start` completed ones: phase 1 reads the
+    start + 1 completed sources once and writes Sb outputs (+ Sb lse); sublayer
+    j of the block reads its output and lse and its j intra-block sources and
+    writes v_l.  Then the final aggregate reads L + 1 sources and writes y.
+    """
+    row = D * elt
+    total = 0
+    for start in range(0, L, S):
+        Sb = min(S, L - start)
+        total += (start + 1 + Sb) * row + Sb * 4
+        total += sum((1 + j + 1) * row + 4 for j in range(Sb))
+    total += (L + 2) * row
+    return rows * total
+
+
 # ---------------------------------------------------------------------------
 # The pages' analytic models ("推理：block representations 像一份 depth KV cache")
 # ---------------------------------------------------------------------------

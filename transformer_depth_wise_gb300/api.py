@@ -196,6 +196,35 @@ def full_stack_forward(v0, queries, gains, u, eps: float = 1e-8, sources=None, y
     return y, sources
 
 
+def full_stack_two_phase(v0, queries, gains, u, S: int, eps: float = 1e-8, sources=None, y=None,
+                         workspace=None):
+    """The Full stack with the two-phase schedule of block size S; returns (y, [v_0..v_L]).
+
+    Same arguments as full_stack_forward (sources [L+1] with v_0 given,
+    v_1..v_L written); workspace is a uint8 CUDA tensor of the size
+    attnres_full_stack_two_phase_workspace_bytes reports (allocated when None).
+    """
+    _cuda(v0, "v0")
+    B, T, D = _btd(v0)
+    L = u.shape[0]
+    if sources is None:
+        sources = [v0] + [torch.empty_like(v0) for _ in range(L)]
+    if y is None:
+        y = torch.empty_like(v0)
+    L_lib = _lib.lib()
+    need = int(L_lib.attnres_full_stack_two_phase_workspace_bytes(L, int(S), B, T, D, _code(v0)))
+    if need < 0:
+        _lib.check("attnres_full_stack_two_phase_workspace_bytes", need)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=v0.device)
+    arr = _lib.ptr_array([s.data_ptr() for s in sources])
+    rc = L_lib.attnres_full_stack_two_phase(arr, L, int(S), B, T, D, _code(v0), _ptr(queries), _ptr(gains),
+                                            _ptr(u), float(eps), y.data_ptr(), workspace.data_ptr(),
+                                            workspace.numel(), _stream(y))
+    _lib.check("attnres_full_stack_two_phase", rc)
+    return y, sources
+
+
 def block_merge_update(inter_out, inter_lse, partial_in, sub_out, u, query, gain=None,
                        eps: float = 1e-8, partial_out=None, h_out=None, out_lse=None,
                        norm_weight=None, norm_eps: float = 1e-6, normed_out=None, write_h: bool = True):

@@ -292,6 +292,109 @@ int attnres_full_stack_forward(void *const *sources, int L, int64_t B, int64_t T
   return cuda_status(launch_aggregate(fin));
 }
 
+namespace {
+
+// Workspace layout of attnres_full_stack_two_phase: the phase-1 outputs of
+// one block [S, rows, D], their lse [S, rows] fp32, and the raw-score /
+// alpha buffer [rows, n, S] fp32 of the widest block (when it has more than
+// ten sources); each part 256-byte aligned.
+struct TwoPhaseLayout {
+  size_t o, lse, scores, total;
+};
+
+int64_t full_two_phase_widest(int L, int S) { return (int64_t)((L - 1) / S) * S + 1; }
+
+TwoPhaseLayout full_two_phase_layout(int L, int S, int64_t rows, int64_t D, int dtype) {
+  auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+  TwoPhaseLayout w;
+  const size_t elt = dtype == ATTNRES_BF16 ? 2 : 4;
+  w.o = 0;
+  w.lse = up((size_t)S * rows * D * elt);
+  w.scores = w.lse + up((size_t)S * rows * sizeof(float));
+  const int64_t n_max = full_two_phase_widest(L, S);
+  w.total = w.scores + (n_max > kP1TcMaxSources ? up((size_t)rows * n_max * S * sizeof(float)) : 0);
+  return w;
+}
+
+// Phase 1 of a block with n sources and Sb queries: which kernel family takes it.
+int full_two_phase_block_check(int n, int Sb, int64_t D, int dtype, int64_t rows) {
+  if (n <= kP1TcMaxSources) return phase1_check(n, (int)D, dtype, Sb);
+  return phase1_many_supported(n, (int)D, dtype, Sb, rows) ? ATTNRES_OK : ATTNRES_ERR_SHAPE;
+}
+
+}  // namespace
+
+int64_t attnres_full_stack_two_phase_workspace_bytes(int L, int S, int64_t B, int64_t T, int64_t D, int dtype) {
+  int64_t rows = 0;
+  int st = check_rows(B, T, D, dtype, rows);
+  if (st) return st;
+  if (L < 1 || S < 1) return ATTNRES_ERR_SHAPE;
+  return (int64_t)full_two_phase_layout(L, S, rows, D, dtype).total;
+}
+
+int attnres_full_stack_two_phase(void *const *sources, int L, int S, int64_t B, int64_t T, int64_t D,
+                                 int dtype, const float *queries, const float *gains, const float *u,
+                                 float eps, void *y_out, void *workspace, int64_t workspace_bytes,
+                                 void *stream) {
+  int64_t rows = 0;
+  int st = check_rows(B, T, D, dtype, rows);
+  if (st) return st;
+  if (L < 1 || S < 1 || S > ATTNRES_MAX_QUERIES) return ATTNRES_ERR_SHAPE;
+  if (L + 1 > ATTNRES_MAX_SOURCES) return ATTNRES_ERR_TOO_MANY_SOURCES;
+  if ((st = check_eps(eps))) return st;
+  if (!aggregate_supported((int)D, dtype)) return ATTNRES_ERR_SHAPE;
+  for (int start = 0; start < L; start += S) {
+    const int Sb = start + S < L ? S : L - start;
+    if ((st = full_two_phase_block_check(start + 1, Sb, D, dtype, rows))) return st;
+  }
+  if (rows == 0) return ATTNRES_OK;
+  if (!sources || !queries || !u || !y_out || !workspace) return ATTNRES_ERR_NULL;
+  for (int l = 0; l <= L; ++l) {
+    if (!sources[l]) return ATTNRES_ERR_NULL;
+    if (!aligned16(sources[l])) return ATTNRES_ERR_ALIGNMENT;
+  }
+  if (!aligned16(queries) || (gains && !aligned16(gains)) || !aligned16(u) || !aligned16(y_out) ||
+      (reinterpret_cast<uintptr_t>(workspace) & 255u))
+    return ATTNRES_ERR_ALIGNMENT;
+  const TwoPhaseLayout w = full_two_phase_layout(L, S, rows, D, dtype);
+  if (workspace_bytes < (int64_t)w.total) return ATTNRES_ERR_CAPACITY;
+  char *ws = static_cast<char *>(workspace);
+  void *o = ws + w.o;
+  float *lse = reinterpret_cast<float *>(ws + w.lse);
+  float *scores = reinterpret_cast<float *>(ws + w.scores);
+  const size_t o_step = (size_t)rows * D * (dtype == ATTNRES_BF16 ? 2 : 4);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const void *const *srcs = const_cast<const void *const *>(sources);
+  for (int start = 0; start < L; start += S) {
+    const int Sb = start + S < L ? S : L - start;   // sublayers start+1 .. start+Sb
+    const int n = start + 1;                         // sources completed before the block
+    const float *qb = queries + (size_t)start * D;
+    const float *gb = gains ? gains + (size_t)start * D : nullptr;
+    // phase 1: the block's Sb queries over v_0 .. v_start, one pass
+    if (n <= kP1TcMaxSources) {
+      Phase1Args a{srcs, n, rows, (int)D, dtype, qb, gb, Sb, eps, o, nullptr, lse, s};
+      if ((st = cuda_status(launch_phase1(a)))) return st;
+    } else {
+      Phase1ManyArgs a{srcs, n, rows, (int)D, qb, gb, Sb, eps, o, nullptr, lse, scores, s};
+      if ((st = cuda_status(launch_phase1_many(a)))) return st;
+    }
+    // phase 2: each sublayer merges its intra-block sources into its phase-1
+    // state, then applies f (fused) and stores v_l
+    for (int j = 0; j < Sb; ++j) {
+      const int l = start + 1 + j;
+      AggregateArgs a{srcs + start + 1, j, rows, (int)D, dtype, queries + (size_t)(l - 1) * D,
+                      gains ? gains + (size_t)(l - 1) * D : nullptr, u + (size_t)(l - 1) * D, eps,
+                      sources[l], nullptr, nullptr, s};
+      a.prior_o = static_cast<const char *>(o) + (size_t)j * o_step;
+      a.prior_lse = lse + (size_t)j * rows;
+      if ((st = cuda_status(launch_aggregate(a)))) return st;
+    }
+  }
+  AggregateArgs fin{srcs, L + 1, rows, (int)D, dtype, queries + (size_t)L * D,
+                    gains ? gains + (size_t)L * D : nullptr, nullptr, eps, y_out, nullptr, nullptr, s};
+  return cuda_status(launch_aggregate(fin));
+}
+
 int attnres_take_device_error(void) {
   if (cudaDeviceSynchronize() != cudaSuccess) return ATTNRES_ERR_CUDA;
   const unsigned int f = take_error_aggregate() | take_error_merge() | take_error_phase1() |

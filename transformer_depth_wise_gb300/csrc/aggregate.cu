@@ -34,6 +34,8 @@ struct AggParams {
   void *out;
   float *out_max;
   float *out_lse;
+  const void *prior_o;     // [rows, D] normalised prior state (o, lse), or nullptr
+  const float *prior_lse;  // [rows]
 };
 
 constexpr int kGroup = 4;  // sources per reduction step
@@ -100,13 +102,14 @@ aggregate_kernel(const __grid_constant__ AggParams p) {
   // lanes in turn.  No registers are held for them, the L2 footprint is
   // kAhead rows per team, and the group loads then hit L2.
   constexpr int kAhead = 2 * G;
-  auto prefetch_src = [&](int64_t rgp, int i) {   // source i of the team's row group rgp
+  auto prefetch_src = [&](int64_t rgp, int i) {   // source i of the team's row group rgp (n >= 1)
     const int64_t r = rgp * teams_per_cta + team;
     if (rgp < groups && r < p.rows && i < p.n)
       prefetch_l2_bulk(static_cast<const char *>(p.src[i]) + (size_t)r * row_bytes, (uint32_t)row_bytes);
   };
-  for (int pos = lt; pos < kAhead; pos += tpr)
-    prefetch_src(blockIdx.x + (int64_t)(pos / p.n) * gridDim.x, pos % p.n);
+  if (p.n > 0)
+    for (int pos = lt; pos < kAhead; pos += tpr)
+      prefetch_src(blockIdx.x + (int64_t)(pos / p.n) * gridDim.x, pos % p.n);
   for (int64_t rg = blockIdx.x; rg < groups; rg += gridDim.x) {
     const int64_t row = rg * teams_per_cta + team;
     const bool row_ok = row < p.rows;
@@ -115,6 +118,15 @@ aggregate_kernel(const __grid_constant__ AggParams p) {
 #pragma unroll
     for (int j = 0; j < VPT * NP; ++j) acc[j] = 0ull;
     float m = -INFINITY, den = 0.f;
+    if (p.prior_o) {  // start from the state (lse, o, 1): an earlier partial softmax
+      if (row_ok) m = p.prior_lse[row];
+      den = 1.f;
+#pragma unroll
+      for (int k = 0; k < VPT; ++k)
+        if (row_ok && valid[k])
+          PR::split(ld_stream(static_cast<const char *>(p.prior_o) + row_off + (size_t)(lt + k * tpr) * 16),
+                    acc + k * NP);
+    }
 
     for (int i0 = 0; i0 < p.n; i0 += G) {
       for (int g = lt; g < G; g += tpr) {  // kAhead sources past this group's g-th
@@ -296,6 +308,8 @@ cudaError_t launch_aggregate(const AggregateArgs &a) {
   p.out = a.out;
   p.out_max = a.out_max;
   p.out_lse = a.out_lse;
+  p.prior_o = a.prior_o;
+  p.prior_lse = a.prior_lse;
   const bool fused = a.u != nullptr;
   if (a.dtype == ATTNRES_BF16)
     return fused ? dispatch<__nv_bfloat16, true>(p, c, a.stream)

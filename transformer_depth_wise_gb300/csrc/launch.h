@@ -24,6 +24,10 @@ struct AggregateArgs {
   float *out_max;              // [rows] or nullptr
   float *out_lse;              // [rows] or nullptr
   cudaStream_t stream;
+  // Start every row from the normalised state (lse, o, 1) of an earlier
+  // partial softmax (then n may be 0): the merge of further sources into it.
+  const void *prior_o = nullptr;     // [rows, D]
+  const float *prior_lse = nullptr;  // [rows]
 };
 // Returns false when D is beyond what the kernel family covers.
 bool aggregate_supported(int D, int dtype);
@@ -138,6 +142,31 @@ cudaError_t launch_phase1(const Phase1Args &a);
 // Tensor-core phase 1 (bf16, D = 512 * {1,2,4,8}, n <= 9, S <= 24).
 bool phase1_tc_supported(int n, int D, int dtype, int S);
 cudaError_t launch_phase1_tc(const Phase1Args &a);
+
+// Phase 1 over any number of summaries (bf16): tensor-core scores ten
+// summaries per call into a raw-score buffer, a softmax over all of them,
+// then the outputs.  scores: [rows][n][S] fp32 scratch, left holding alpha.
+// Most summaries the fused phase-1 path takes in one pass (its TMEM holds
+// ten sources' scores); wider blocks go through the raw-score path below.
+constexpr int kP1TcMaxSources = 10;
+
+struct Phase1ManyArgs {
+  const void *const *blocks;
+  int n;
+  int64_t rows;
+  int D;
+  const float *queries;        // [S, D]
+  const float *gains;          // [S, D] or nullptr
+  int S;
+  float eps;
+  void *out;                   // [S, rows, D] bf16
+  float *out_max;              // [S, rows] or nullptr
+  float *out_lse;              // [S, rows]
+  float *scores;               // [rows, n, S]
+  cudaStream_t stream;
+};
+bool phase1_many_supported(int n, int D, int dtype, int S, int64_t rows);
+cudaError_t launch_phase1_many(const Phase1ManyArgs &a);
 
 // Read and clear the per-file flag that records a kernel wait that ran out
 // (non-zero: at least one wait gave up).

@@ -52,6 +52,7 @@ namespace tc {
 constexpr int kRows = 128;            // token rows per tile of kernel A (MMA M)
 constexpr int kKc = 64;               // features per chunk (one 128-byte swizzle row)
 constexpr int kMaxN = 10;             // summaries: TMEM columns n * 48 <= 480
+static_assert(kMaxN == kP1TcMaxSources, "one pass of the fused phase 1 takes ten summaries");
 constexpr int kMaxS = 24;             // queries
 constexpr int kNQ = 2 * kMaxS;        // B rows: hi parts at 0..S-1, lo parts at 24..24+S-1
 constexpr int kStages = 9;            // ring of (summary chunk 16 KB + query chunk 6 KB) stages
@@ -75,6 +76,11 @@ struct ParamsA {
   int64_t rows;
   int n, S, D;
   float eps, inv_D;
+  // Raw-score mode (sources past ten, taken ten at a time): write the scores
+  // s[row][raw_i0 + i][q] of this call's n summaries to raw ([rows][raw_n][S]
+  // fp32) and nothing else; the softmax over all of them runs afterwards.
+  float *raw;
+  int raw_n, raw_i0;
 };
 
 struct ParamsB {
@@ -318,6 +324,28 @@ __global__ void __launch_bounds__(kThreadsA, 1) p1_scores_kernel(const __grid_co
       float rinv[kMaxN];
 #pragma unroll
       for (int i = 0; i < kMaxN; ++i) rinv[i] = rsqrtf(fmaf(ss[i], p.inv_D, p.eps));
+      if (p.raw) {                                               // raw-score mode
+        const int64_t row = tile * kRows + r;
+        float c[kNQ];
+#pragma unroll
+        for (int i = 0; i < kMaxN; ++i) {
+          if (i >= n) continue;
+          tmem_ld16(taddr + i * kNQ, c);
+          tmem_ld16(taddr + i * kNQ + 16, c + 16);
+          tmem_ld16(taddr + i * kNQ + 32, c + 32);
+          asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+          if (row < p.rows) {
+            float *dst = p.raw + ((size_t)row * p.raw_n + p.raw_i0 + i) * S;
+#pragma unroll
+            for (int q = 0; q < kMaxS; ++q)
+              if (q < S) dst[q] = (c[q] + c[kMaxS + q]) * rinv[i];
+          }
+        }
+        asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) mbar_arrive(TFREE);
+        continue;
+      }
       float m[kMaxS], den[kMaxS];
 #pragma unroll
       for (int q = 0; q < kMaxS; ++q) { m[q] = -INFINITY; den[q] = 0.f; }
@@ -471,6 +499,101 @@ __global__ void __launch_bounds__(512, 1) p1_outputs_kernel(const __grid_constan
 }
 
 // -----------------------------------------------------------------------------
+// More than ten summaries: softmax over the raw scores, then the outputs
+// -----------------------------------------------------------------------------
+// One thread per (row, query): max, sum and normalisation over the n raw
+// scores (consecutive threads read consecutive queries), alpha written in
+// place; m and lse to their [S, rows] outputs.
+__global__ void __launch_bounds__(256)
+p1_many_softmax_kernel(float *scores, int64_t rows, int n, int S, float *out_max, float *out_lse) {
+  const int64_t total = rows * S;
+  for (int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; g < total; g += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t row = g / S;
+    const int q = (int)(g % S);
+    float *s = scores + (size_t)row * n * S + q;
+    float m = -INFINITY;
+    for (int i = 0; i < n; ++i) m = fmaxf(m, s[(size_t)i * S]);
+    float den = 0.f;
+    for (int i = 0; i < n; ++i) den += expf(s[(size_t)i * S] - m);
+    const float inv = 1.f / den;
+    for (int i = 0; i < n; ++i) s[(size_t)i * S] = expf(s[(size_t)i * S] - m) * inv;
+    out_lse[(size_t)q * rows + row] = m + logf(den);
+    if (out_max) out_max[(size_t)q * rows + row] = m;
+  }
+}
+
+struct ParamsB2 {
+  const void *src[kMaxSources];
+  const float *alpha;   // [rows][n][S]
+  void *out;            // [S, rows, D] bf16
+  int64_t rows;
+  int n, S, D;
+};
+
+// o_q = sum_i alpha_{q,i} v_i for any number of summaries: a CTA per token at
+// a time, each thread four features (8 bytes of every summary row) and the
+// S outputs' accumulators as packed pairs.  The token's alpha is staged in
+// shared memory as duplicated pairs (two queries per 16-byte read, feeding
+// four packed FMAs); its summary rows are asked into L2 32 ahead.
+constexpr int kB2Ahead = 32;
+
+__global__ void __launch_bounds__(512)
+p1_many_outputs_kernel(const __grid_constant__ ParamsB2 p) {
+  extern __shared__ uint64_t adup[];  // [n][Sp]
+  const int tid = threadIdx.x;
+  const int n = p.n, S = p.S, Sp = S + (S & 1);
+  const bool valid = tid * 4 < p.D;
+  const size_t row_bytes = (size_t)p.D * 2;
+  if (S & 1)
+    for (int i = tid; i < n; i += blockDim.x) adup[(size_t)i * Sp + S] = 0ull;
+  for (int64_t t = blockIdx.x; t < p.rows; t += gridDim.x) {
+    __syncthreads();                                   // the previous token's readers are done
+    if (tid < n && tid < kB2Ahead)
+      prefetch_l2_bulk(static_cast<const char *>(p.src[tid]) + (size_t)t * row_bytes, (uint32_t)row_bytes);
+    const float *at = p.alpha + (size_t)t * n * S;
+    for (int idx = tid; idx < n * S; idx += blockDim.x) {
+      const float a = at[idx];
+      adup[(size_t)(idx / S) * Sp + idx % S] = pair(a, a);
+    }
+    __syncthreads();
+    uint64_t acc[kMaxS][2];
+#pragma unroll
+    for (int q = 0; q < kMaxS; ++q) acc[q][0] = acc[q][1] = 0ull;
+    for (int i = 0; i < n; ++i) {
+      if (tid == 0 && i + kB2Ahead < n)
+        prefetch_l2_bulk(static_cast<const char *>(p.src[i + kB2Ahead]) + (size_t)t * row_bytes,
+                         (uint32_t)row_bytes);
+      uint2 w = make_uint2(0u, 0u);
+      if (valid) w = *reinterpret_cast<const uint2 *>(static_cast<const char *>(p.src[i]) + (size_t)t * row_bytes + (size_t)tid * 8);
+      const uint64_t x0 = ((uint64_t)(w.x & 0xffff0000u) << 32) | (uint64_t)(w.x << 16);
+      const uint64_t x1 = ((uint64_t)(w.y & 0xffff0000u) << 32) | (uint64_t)(w.y << 16);
+      const uint4 *ad = reinterpret_cast<const uint4 *>(adup + (size_t)i * Sp);
+#pragma unroll
+      for (int qq = 0; qq < kMaxS / 2; ++qq) {
+        if (2 * qq >= S) continue;
+        const uint4 a = ad[qq];
+        const uint64_t a0 = ((uint64_t)a.y << 32) | a.x, a1 = ((uint64_t)a.w << 32) | a.z;
+        fma_pair(acc[2 * qq][0], a0, x0);
+        fma_pair(acc[2 * qq][1], a0, x1);
+        fma_pair(acc[2 * qq + 1][0], a1, x0);
+        fma_pair(acc[2 * qq + 1][1], a1, x1);
+      }
+    }
+    if (valid) {
+#pragma unroll
+      for (int q = 0; q < kMaxS; ++q) {
+        if (q >= S) continue;
+        float y[4];
+        unpair(acc[q][0], y[0], y[1]);
+        unpair(acc[q][1], y[2], y[3]);
+        const uint2 v = make_uint2(Elt<__nv_bfloat16>::pack_word(y[0], y[1]), Elt<__nv_bfloat16>::pack_word(y[2], y[3]));
+        __stcs(reinterpret_cast<uint2 *>(static_cast<char *>(p.out) + ((size_t)q * p.rows + t) * row_bytes + (size_t)tid * 8), v);
+      }
+    }
+  }
+}
+
+// -----------------------------------------------------------------------------
 // Host side
 // -----------------------------------------------------------------------------
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -576,6 +699,100 @@ cudaError_t launch_phase1_tc(const Phase1Args &a) {
   const int64_t cap = (int64_t)occ * sm_count();
   const int64_t gb = a.rows < cap ? a.rows : cap;
   p1_outputs_kernel<<<(int)gb, threads, smem, a.stream>>>(pb);
+  return cudaGetLastError();
+}
+
+bool phase1_many_supported(int n, int D, int dtype, int S, int64_t rows) {
+  if (dtype != ATTNRES_BF16 || n < 1 || n > kMaxSources || S < 1 || S > tc::kMaxS) return false;
+  if (D % tc::kKc != 0 || D / 4 > 512) return false;           // the outputs kernel: 4 features per thread
+  if ((int64_t)S * rows < tc::kNQ) return false;               // room to park the query parts
+  if ((size_t)n * (S + (S & 1)) * 8 > 200 * 1024) return false;  // the token's alpha in shared memory
+  return tc::encode_fn() != nullptr;
+}
+
+cudaError_t launch_phase1_many(const Phase1ManyArgs &a) {
+  using namespace tc;
+  auto encode = encode_fn();
+  if (!encode) return cudaErrorNotSupported;
+  // the query parts, parked in the last 48 rows (of D) of the output buffer
+  __nv_bfloat16 *parts = static_cast<__nv_bfloat16 *>(a.out) + ((size_t)a.S * a.rows - kNQ) * a.D;
+  {
+    const int64_t total = (int64_t)kMaxS * a.D;
+    const int blocks = (int)((total + 255) / 256 < 4 * sm_count() ? (total + 255) / 256 : 4 * sm_count());
+    p1_qsplit_kernel<<<blocks, 256, 0, a.stream>>>(a.queries, a.gains, a.S, a.D, parts);
+    cudaError_t e0 = cudaGetLastError();
+    if (e0 != cudaSuccess) return e0;
+  }
+  ParamsA pa;
+  memset(&pa, 0, sizeof(pa));
+  {
+    cuuint64_t dims[2] = {(cuuint64_t)a.D, (cuuint64_t)kNQ};
+    cuuint64_t strides[1] = {(cuuint64_t)a.D * 2};
+    cuuint32_t box[2] = {kKc, kNQ};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = encode(&pa.qmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, parts, dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  }
+  pa.out = a.out;
+  pa.rows = a.rows;
+  pa.S = a.S;
+  pa.D = a.D;
+  pa.eps = a.eps;
+  pa.inv_D = 1.f / (float)a.D;
+  pa.raw = a.scores;
+  pa.raw_n = a.n;
+  cudaError_t e = cudaFuncSetAttribute(p1_scores_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)kSmemA);
+  if (e != cudaSuccess) return e;
+  const int64_t tiles = (a.rows + kRows - 1) / kRows;
+  const int64_t waves = (tiles + sm_count() - 1) / sm_count();
+  const int64_t ga = (tiles + waves - 1) / waves;
+  // raw scores, ten summaries per call
+  for (int i0 = 0; i0 < a.n; i0 += kMaxN) {
+    const int nc = a.n - i0 < kMaxN ? a.n - i0 : kMaxN;
+    for (int i = 0; i < nc; ++i) {
+      cuuint64_t dims[2] = {(cuuint64_t)a.D, (cuuint64_t)a.rows};
+      cuuint64_t strides[1] = {(cuuint64_t)a.D * 2};
+      cuuint32_t box[2] = {kKc, kRows};
+      cuuint32_t estr[2] = {1, 1};
+      CUresult r = encode(&pa.tmap[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(a.blocks[i0 + i]),
+                          dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+      if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    }
+    pa.n = nc;
+    pa.raw_i0 = i0;
+    p1_scores_kernel<<<(int)ga, kThreadsA, kSmemA, a.stream>>>(pa);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  {
+    const int64_t total = a.rows * a.S;
+    const int64_t blocks = (total + 255) / 256 < 8 * sm_count() ? (total + 255) / 256 : 8 * sm_count();
+    p1_many_softmax_kernel<<<(int)blocks, 256, 0, a.stream>>>(a.scores, a.rows, a.n, a.S, a.out_max, a.out_lse);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  ParamsB2 pb;
+  for (int i = 0; i < a.n; ++i) pb.src[i] = a.blocks[i];
+  pb.alpha = a.scores;
+  pb.out = a.out;
+  pb.rows = a.rows;
+  pb.n = a.n;
+  pb.S = a.S;
+  pb.D = a.D;
+  const int threads = (a.D / 4 + 31) / 32 * 32;
+  const size_t smem = (size_t)a.n * (a.S + (a.S & 1)) * 8;
+  e = cudaFuncSetAttribute(p1_many_outputs_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+  if (e != cudaSuccess) return e;
+  int occ = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, p1_many_outputs_kernel, threads, smem);
+  if (e != cudaSuccess) return e;
+  if (occ < 1) occ = 1;
+  const int64_t cap = (int64_t)occ * sm_count();
+  const int64_t gb = a.rows < cap ? a.rows : cap;
+  p1_many_outputs_kernel<<<(int)gb, threads, smem, a.stream>>>(pb);
   return cudaGetLastError();
 }
 

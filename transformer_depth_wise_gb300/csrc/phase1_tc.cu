@@ -67,8 +67,9 @@ constexpr int kThreadsA = kWarpsA * 32;
 constexpr uint32_t kOffBar = kStages * kStageBytes;
 constexpr uint32_t kSmemA = kOffBar + 64 * 8 + 1024;     // barriers + alignment slack
 
-struct ParamsA {
-  CUtensorMap tmap[kMaxN];            // one per summary: [rows, D] bf16, box 64 x 128
+template <int NM>
+struct ParamsAT {
+  CUtensorMap tmap[NM];               // one per summary: [rows, D] bf16, box 64 x 128
   CUtensorMap qmap;                   // parked query parts: [48, D] bf16, box 64 x 48
   void *out;                          // [S, rows, D] bf16 (alpha parked in o[0])
   float *out_max;                     // [S, rows] or nullptr
@@ -76,12 +77,20 @@ struct ParamsA {
   int64_t rows;
   int n, S, D;
   float eps, inv_D;
-  // Raw-score mode (sources past ten, taken ten at a time): write the scores
-  // s[row][raw_i0 + i][q] of this call's n summaries to raw ([rows][raw_n][S]
-  // fp32) and nothing else; the softmax over all of them runs afterwards.
+  // Raw-score mode (any number of summaries): the work items are (tile,
+  // chunk of ten summaries); each writes the scores s[row][i][q] of its
+  // chunk to raw ([rows][n][S] fp32) and nothing else; the softmax over all
+  // of them runs afterwards.  Without raw, n <= 10 and there is one chunk.
   float *raw;
-  int raw_n, raw_i0;
+  int raw_n, raw_off;                 // raw's summary count and this launch's first summary
 };
+// The fused path (up to ten summaries) and the raw-score path, which takes
+// up to kManyMaps summaries per launch (the tensor maps ride in the kernel
+// parameters: 128 bytes each, within the 32 KB parameter limit).
+constexpr int kManyMaps = 200;
+using ParamsA = ParamsAT<kMaxN>;
+using ParamsAMany = ParamsAT<kManyMaps>;
+static_assert(sizeof(ParamsAMany) <= 32764, "kernel parameters are limited to 32764 bytes");
 
 struct ParamsB {
   const void *src[kMaxN];
@@ -201,7 +210,8 @@ __global__ void __launch_bounds__(256) p1_qsplit_kernel(const float *__restrict_
 // -----------------------------------------------------------------------------
 // Kernel A: scores on tcgen05, softmax, alpha / m / lse
 // -----------------------------------------------------------------------------
-__global__ void __launch_bounds__(kThreadsA, 1) p1_scores_kernel(const __grid_constant__ ParamsA p) {
+template <int NM>
+__global__ void __launch_bounds__(kThreadsA, 1) p1_scores_kernel(const __grid_constant__ ParamsAT<NM> p) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char *sm = reinterpret_cast<unsigned char *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -233,8 +243,16 @@ __global__ void __launch_bounds__(kThreadsA, 1) p1_scores_kernel(const __grid_co
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   const uint32_t tmem_base = *tmem_slot;
 
+  // Work items: (tile of 128 rows, chunk of up to ten summaries), tile-minor.
   const int64_t tiles = (p.rows + kRows - 1) / kRows;
-  const int64_t my_tiles = tiles > (int64_t)blockIdx.x ? (tiles - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
+  const int64_t items = tiles * ((n + kMaxN - 1) / kMaxN);
+  const int64_t my_tiles = items > (int64_t)blockIdx.x ? (items - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
+  auto item_of = [&](int64_t tl, int64_t &tile, int &i0, int &nc) {
+    const int64_t item = (int64_t)blockIdx.x + tl * gridDim.x;
+    tile = item % tiles;
+    i0 = (int)(item / tiles) * kMaxN;
+    nc = n - i0 < kMaxN ? n - i0 : kMaxN;
+  };
   const int KC = p.D / kKc;
 
   if (warp == 4) {
@@ -245,14 +263,16 @@ __global__ void __launch_bounds__(kThreadsA, 1) p1_scores_kernel(const __grid_co
     if (lane == 0) {
       int64_t g = 0;
       for (int64_t tl = 0; tl < my_tiles; ++tl) {
-        const int64_t tile = blockIdx.x + tl * gridDim.x;
-        for (int i = 0; i < n; ++i)
+        int64_t tile;
+        int i0, nc;
+        item_of(tl, tile, i0, nc);
+        for (int i = 0; i < nc; ++i)
           for (int kc = 0; kc < KC; ++kc, ++g) {
             const int s = (int)(g % kStages);
             if (g >= kStages) wait_local(VEMPTY(s), (uint32_t)((g / kStages - 1) & 1));
             mbar_expect_tx(VFULL(s), kStageBytes);
             const uint32_t st = base + (uint32_t)s * kStageBytes;
-            tma_load_2d(st, &p.tmap[i], kc * kKc, (int)(tile * kRows), VFULL(s));
+            tma_load_2d(st, &p.tmap[i0 + i], kc * kKc, (int)(tile * kRows), VFULL(s));
             tma_load_2d(st + kVBytes, &p.qmap, kc * kKc, 0, VFULL(s));
           }
       }
@@ -268,7 +288,10 @@ __global__ void __launch_bounds__(kThreadsA, 1) p1_scores_kernel(const __grid_co
       for (int64_t tl = 0; tl < my_tiles; ++tl) {
         if (tl >= 1) wait_local(TFREE, (uint32_t)((tl - 1) & 1));   // epilogue read the last tile
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-        for (int i = 0; i < n; ++i)
+        int64_t tile;
+        int i0, nc;
+        item_of(tl, tile, i0, nc);
+        for (int i = 0; i < nc; ++i)
           for (int kc = 0; kc < KC; ++kc, ++g) {
             const int s = (int)(g % kStages);
             wait_local(VFULL(s), (uint32_t)((g / kStages) & 1));
@@ -291,13 +314,15 @@ __global__ void __launch_bounds__(kThreadsA, 1) p1_scores_kernel(const __grid_co
     const uint32_t taddr = tmem_base + ((uint32_t)(warp * 32) << 16);
     int64_t g = 0;
     for (int64_t tl = 0; tl < my_tiles; ++tl) {
-      const int64_t tile = blockIdx.x + tl * gridDim.x;
+      int64_t tile;
+      int i0, nc;
+      item_of(tl, tile, i0, nc);
       float ss[kMaxN];
 #pragma unroll
       for (int i = 0; i < kMaxN; ++i) ss[i] = 0.f;
 #pragma unroll
       for (int i = 0; i < kMaxN; ++i) {
-        if (i >= n) continue;
+        if (i >= nc) continue;
         for (int kc = 0; kc < KC; ++kc, ++g) {
           const int s = (int)(g % kStages);
           wait_local(VFULL(s), (uint32_t)((g / kStages) & 1));
@@ -329,13 +354,13 @@ __global__ void __launch_bounds__(kThreadsA, 1) p1_scores_kernel(const __grid_co
         float c[kNQ];
 #pragma unroll
         for (int i = 0; i < kMaxN; ++i) {
-          if (i >= n) continue;
+          if (i >= nc) continue;
           tmem_ld16(taddr + i * kNQ, c);
           tmem_ld16(taddr + i * kNQ + 16, c + 16);
           tmem_ld16(taddr + i * kNQ + 32, c + 32);
           asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
           if (row < p.rows) {
-            float *dst = p.raw + ((size_t)row * p.raw_n + p.raw_i0 + i) * S;
+            float *dst = p.raw + ((size_t)row * p.raw_n + p.raw_off + i0 + i) * S;
 #pragma unroll
             for (int q = 0; q < kMaxS; ++q)
               if (q < S) dst[q] = (c[q] + c[kMaxS + q]) * rinv[i];
@@ -352,7 +377,7 @@ __global__ void __launch_bounds__(kThreadsA, 1) p1_scores_kernel(const __grid_co
       float c[kNQ];
 #pragma unroll
       for (int i = 0; i < kMaxN; ++i) {                          // pass 1: max
-        if (i >= n) continue;
+        if (i >= nc) continue;
         tmem_ld16(taddr + i * kNQ, c);
         tmem_ld16(taddr + i * kNQ + 16, c + 16);
         tmem_ld16(taddr + i * kNQ + 32, c + 32);
@@ -362,7 +387,7 @@ __global__ void __launch_bounds__(kThreadsA, 1) p1_scores_kernel(const __grid_co
       }
 #pragma unroll
       for (int i = 0; i < kMaxN; ++i) {                          // pass 2: denominators
-        if (i >= n) continue;
+        if (i >= nc) continue;
         tmem_ld16(taddr + i * kNQ, c);
         tmem_ld16(taddr + i * kNQ + 16, c + 16);
         tmem_ld16(taddr + i * kNQ + 32, c + 32);
@@ -375,7 +400,7 @@ __global__ void __launch_bounds__(kThreadsA, 1) p1_scores_kernel(const __grid_co
       float *alpha = reinterpret_cast<float *>(static_cast<char *>(p.out) + (size_t)row * p.D * 2);
 #pragma unroll
       for (int i = 0; i < kMaxN; ++i) {                          // pass 3: alpha [n][S]
-        if (i >= n) continue;
+        if (i >= nc) continue;
         tmem_ld16(taddr + i * kNQ, c);
         tmem_ld16(taddr + i * kNQ + 16, c + 16);
         tmem_ld16(taddr + i * kNQ + 32, c + 32);
@@ -670,14 +695,14 @@ cudaError_t launch_phase1_tc(const Phase1Args &a) {
   pa.D = a.D;
   pa.eps = a.eps;
   pa.inv_D = 1.f / (float)a.D;
-  cudaError_t e = cudaFuncSetAttribute(p1_scores_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(p1_scores_kernel<kMaxN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)kSmemA);
   if (e != cudaSuccess) return e;
   // Every CTA gets the same number of tiles (no partly empty last wave).
   const int64_t tiles = (a.rows + kRows - 1) / kRows;
   const int64_t waves = (tiles + sm_count() - 1) / sm_count();
   const int64_t ga = (tiles + waves - 1) / waves;
-  p1_scores_kernel<<<(int)ga, kThreadsA, kSmemA, a.stream>>>(pa);
+  p1_scores_kernel<kMaxN><<<(int)ga, kThreadsA, kSmemA, a.stream>>>(pa);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   // Kernel B
   ParamsB pb;
@@ -723,7 +748,7 @@ cudaError_t launch_phase1_many(const Phase1ManyArgs &a) {
     cudaError_t e0 = cudaGetLastError();
     if (e0 != cudaSuccess) return e0;
   }
-  ParamsA pa;
+  ParamsAMany pa;
   memset(&pa, 0, sizeof(pa));
   {
     cuuint64_t dims[2] = {(cuuint64_t)a.D, (cuuint64_t)kNQ};
@@ -743,29 +768,31 @@ cudaError_t launch_phase1_many(const Phase1ManyArgs &a) {
   pa.inv_D = 1.f / (float)a.D;
   pa.raw = a.scores;
   pa.raw_n = a.n;
-  cudaError_t e = cudaFuncSetAttribute(p1_scores_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(p1_scores_kernel<kManyMaps>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)kSmemA);
   if (e != cudaSuccess) return e;
   const int64_t tiles = (a.rows + kRows - 1) / kRows;
-  const int64_t waves = (tiles + sm_count() - 1) / sm_count();
-  const int64_t ga = (tiles + waves - 1) / waves;
-  // raw scores, ten summaries per call
-  for (int i0 = 0; i0 < a.n; i0 += kMaxN) {
-    const int nc = a.n - i0 < kMaxN ? a.n - i0 : kMaxN;
-    for (int i = 0; i < nc; ++i) {
+  // Raw scores: one launch per kManyMaps summaries, its work items (tile,
+  // chunk of ten) spread evenly over the SMs.
+  for (int off = 0; off < a.n; off += kManyMaps) {
+    const int nl = a.n - off < kManyMaps ? a.n - off : kManyMaps;
+    for (int i = 0; i < nl; ++i) {
       cuuint64_t dims[2] = {(cuuint64_t)a.D, (cuuint64_t)a.rows};
       cuuint64_t strides[1] = {(cuuint64_t)a.D * 2};
       cuuint32_t box[2] = {kKc, kRows};
       cuuint32_t estr[2] = {1, 1};
-      CUresult r = encode(&pa.tmap[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(a.blocks[i0 + i]),
+      CUresult r = encode(&pa.tmap[i], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(a.blocks[off + i]),
                           dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                           CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
       if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
     }
-    pa.n = nc;
-    pa.raw_i0 = i0;
-    p1_scores_kernel<<<(int)ga, kThreadsA, kSmemA, a.stream>>>(pa);
+    pa.n = nl;
+    pa.raw_off = off;
+    const int64_t items = tiles * ((nl + kMaxN - 1) / kMaxN);
+    const int64_t waves = (items + sm_count() - 1) / sm_count();
+    const int64_t ga = (items + waves - 1) / waves;
+    p1_scores_kernel<kManyMaps><<<(int)ga, kThreadsA, kSmemA, a.stream>>>(pa);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   {

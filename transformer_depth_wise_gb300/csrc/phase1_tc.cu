@@ -559,7 +559,8 @@ struct ParamsB2 {
 // a time, each thread four features (8 bytes of every summary row) and the
 // S outputs' accumulators as packed pairs.  The token's alpha is staged in
 // shared memory as duplicated pairs (two queries per 16-byte read, feeding
-// four packed FMAs); its summary rows are asked into L2 32 ahead.
+// four packed FMAs); its summary rows are asked into L2 32 ahead and loaded
+// four at a time.
 constexpr int kB2Ahead = 32;
 
 __global__ void __launch_bounds__(512)
@@ -584,24 +585,35 @@ p1_many_outputs_kernel(const __grid_constant__ ParamsB2 p) {
     uint64_t acc[kMaxS][2];
 #pragma unroll
     for (int q = 0; q < kMaxS; ++q) acc[q][0] = acc[q][1] = 0ull;
-    for (int i = 0; i < n; ++i) {
-      if (tid == 0 && i + kB2Ahead < n)
-        prefetch_l2_bulk(static_cast<const char *>(p.src[i + kB2Ahead]) + (size_t)t * row_bytes,
+    constexpr int U = 4;  // summaries whose loads are in flight together
+    for (int i = 0; i < n; i += U) {
+      if (tid < U && i + kB2Ahead + tid < n)
+        prefetch_l2_bulk(static_cast<const char *>(p.src[i + kB2Ahead + tid]) + (size_t)t * row_bytes,
                          (uint32_t)row_bytes);
-      uint2 w = make_uint2(0u, 0u);
-      if (valid) w = *reinterpret_cast<const uint2 *>(static_cast<const char *>(p.src[i]) + (size_t)t * row_bytes + (size_t)tid * 8);
-      const uint64_t x0 = ((uint64_t)(w.x & 0xffff0000u) << 32) | (uint64_t)(w.x << 16);
-      const uint64_t x1 = ((uint64_t)(w.y & 0xffff0000u) << 32) | (uint64_t)(w.y << 16);
-      const uint4 *ad = reinterpret_cast<const uint4 *>(adup + (size_t)i * Sp);
+      uint2 w[U];
 #pragma unroll
-      for (int qq = 0; qq < kMaxS / 2; ++qq) {
-        if (2 * qq >= S) continue;
-        const uint4 a = ad[qq];
-        const uint64_t a0 = ((uint64_t)a.y << 32) | a.x, a1 = ((uint64_t)a.w << 32) | a.z;
-        fma_pair(acc[2 * qq][0], a0, x0);
-        fma_pair(acc[2 * qq][1], a0, x1);
-        fma_pair(acc[2 * qq + 1][0], a1, x0);
-        fma_pair(acc[2 * qq + 1][1], a1, x1);
+      for (int u = 0; u < U; ++u) {
+        w[u] = make_uint2(0u, 0u);
+        if (valid && i + u < n)
+          w[u] = *reinterpret_cast<const uint2 *>(static_cast<const char *>(p.src[i + u]) + (size_t)t * row_bytes +
+                                                  (size_t)tid * 8);
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        if (i + u >= n) break;
+        const uint64_t x0 = ((uint64_t)(w[u].x & 0xffff0000u) << 32) | (uint64_t)(w[u].x << 16);
+        const uint64_t x1 = ((uint64_t)(w[u].y & 0xffff0000u) << 32) | (uint64_t)(w[u].y << 16);
+        const uint4 *ad = reinterpret_cast<const uint4 *>(adup + (size_t)(i + u) * Sp);
+#pragma unroll
+        for (int qq = 0; qq < kMaxS / 2; ++qq) {
+          if (2 * qq >= S) continue;
+          const uint4 a = ad[qq];
+          const uint64_t a0 = ((uint64_t)a.y << 32) | a.x, a1 = ((uint64_t)a.w << 32) | a.z;
+          fma_pair(acc[2 * qq][0], a0, x0);
+          fma_pair(acc[2 * qq][1], a0, x1);
+          fma_pair(acc[2 * qq + 1][0], a1, x0);
+          fma_pair(acc[2 * qq + 1][1], a1, x1);
+        }
       }
     }
     if (valid) {

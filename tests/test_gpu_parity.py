@@ -533,8 +533,10 @@ def test_full_stack_config_full_size_sampled(gpu):
 # block phase-1 kernels, wider ones the raw-score path (scores ten at a time,
 # softmax, outputs over all sources); the oracle rounds o_l and v_l where the
 # GPU stores them.
+# Wide blocks with S <= 16 (and D a multiple of 256) take the tensor-core outputs kernel, wider S the packed-FMA one.
 @pytest.mark.parametrize("S,D,L,rows", [(4, 1024, 23, 130), (12, 2048, 30, 70), (1, 512, 14, 64),
-                                        (40, 1024, 25, 50), (24, 2048, 27, 129)])
+                                        (40, 1024, 25, 50), (24, 2048, 27, 129), (20, 1024, 45, 64),
+                                        (16, 256, 40, 33)])
 def test_full_two_phase_small(gpu, S, D, L, rows):
     wl = wk.WORKLOADS["full_stack_bf16"]
     inp = wk.full_stack_inputs(wl, rows=rows, device=gpu, L=L, D=D)

@@ -631,6 +631,150 @@ p1_many_outputs_kernel(const __grid_constant__ ParamsB2 p) {
 }
 
 // -----------------------------------------------------------------------------
+// Outputs for many summaries on tensor cores (S <= 16, D a multiple of 256 up
+// to 2048).  Per token, O[q][d] = sum_i alpha[q][i] v_i[d] is a dense
+// contraction with K = n: warp-level mma.m16n8k16 (bf16 in, fp32 accumulate),
+// M = 16 queries, N = 8 features per tile, K = 16 summaries per step.  The
+// summary rows are N-major (contiguous along d), which ldmatrix.trans turns
+// into the B fragments; alpha (fp32) is split into bf16 hi + lo, two MMAs per
+// tile, so it keeps about 16 significant bits.  The summary rows stream
+// through a two-slot cp.async ring, 16 rows per step (rows past n zero-filled);
+// each warp holds the accumulators of its 128 features across the steps.
+// -----------------------------------------------------------------------------
+constexpr int kTcK = 16;           // summaries per step (mma K)
+constexpr int kTcWarps = 16;       // 512 threads
+
+struct ParamsB3 {
+  const void *src[kMaxSources];
+  const float *alpha;   // [rows][n][S]
+  void *out;            // [S, rows, D] bf16
+  int64_t rows;
+  int n, S, D;
+};
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(addr));
+}
+__device__ __forceinline__ void mma_16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+               "{%8, %9}, {%0, %1, %2, %3};"
+               : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+               : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// 16-byte cp.async that reads `bytes` (16 or 0) and zero-fills the rest.
+__device__ __forceinline__ void cp_async16_zfill(void *smem, const void *gmem, uint32_t bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(smem)), "l"(gmem), "r"(bytes)
+               : "memory");
+}
+
+__host__ __device__ constexpr size_t tc_row_v(int D) { return (size_t)D * 2 + 16; }   // padded: no bank conflicts
+__host__ __device__ constexpr size_t tc_row_a(int n) { return (size_t)((n + kTcK - 1) / kTcK * kTcK) * 2 + 16; }
+__host__ __device__ constexpr size_t tc_smem(int n, int D) {
+  return 2 * (size_t)kTcK * tc_row_v(D) + 2 * 2 * (size_t)kTcK * tc_row_a(n);
+}
+
+__global__ void __launch_bounds__(kTcWarps * 32, 1)
+p1_many_outputs_tc_kernel(const __grid_constant__ ParamsB3 p) {
+  extern __shared__ __align__(16) unsigned char sm3[];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int n = p.n, S = p.S, D = p.D;
+  const int KS = (n + kTcK - 1) / kTcK, KP = KS * kTcK;
+  const size_t RV = tc_row_v(D), RA = tc_row_a(n);
+  unsigned char *vring = sm3;                                    // [2][16][RV]
+  unsigned char *abuf = sm3 + 2 * kTcK * RV;                     // [2 tokens][hi, lo][16][RA]
+  const size_t row_bytes = (size_t)D * 2;
+  const int chunks = D / 8;                                      // 16-byte chunks per row
+  const int ntw = D / 8 / kTcWarps;                              // n-tiles per warp (even, <= 16)
+  const int64_t my_tokens = p.rows > (int64_t)blockIdx.x ? (p.rows - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
+  const int64_t total = my_tokens * KS;
+
+  auto token = [&](int64_t j) { return (int64_t)blockIdx.x + j * gridDim.x; };
+  auto issue = [&](int64_t g) {                                  // step g: 16 summary rows -> slot g & 1
+    const int64_t t = token(g / KS);
+    const int kk = (int)(g % KS);
+    unsigned char *slot = vring + (size_t)(g & 1) * kTcK * RV;
+    for (int c = tid; c < kTcK * chunks; c += blockDim.x) {
+      const int r = c / chunks, ch = c % chunks, i = kk * kTcK + r;
+      const char *gp = static_cast<const char *>(p.src[i < n ? i : 0]) + (size_t)t * row_bytes + (size_t)ch * 16;
+      cp_async16_zfill(slot + (size_t)r * RV + (size_t)ch * 16, gp, i < n ? 16u : 0u);
+    }
+    cp_async_commit();
+  };
+  auto stage_alpha = [&](int64_t j) {                            // alpha of token j -> bf16 hi / lo [q][i]
+    const int64_t t = token(j);
+    unsigned char *ab = abuf + (size_t)(j & 1) * 2 * kTcK * RA;
+    const float *at = p.alpha + (size_t)t * n * S;
+    for (int idx = tid; idx < kTcK * KP; idx += blockDim.x) {
+      const int q = idx / KP, i = idx % KP;
+      const float a = (q < S && i < n) ? at[(size_t)i * S + q] : 0.f;
+      const __nv_bfloat16 hi = __float2bfloat16_rn(a);
+      const __nv_bfloat16 lo = __float2bfloat16_rn(a - __bfloat162float(hi));
+      *reinterpret_cast<__nv_bfloat16 *>(ab + (size_t)q * RA + (size_t)i * 2) = hi;
+      *reinterpret_cast<__nv_bfloat16 *>(ab + (size_t)(kTcK + q) * RA + (size_t)i * 2) = lo;
+    }
+  };
+
+  float c[16][4];
+  if (total > 0) {
+    stage_alpha(0);
+    issue(0);
+  }
+  for (int64_t g = 0; g < total; ++g) {
+    const int64_t j = g / KS;
+    const int kk = (int)(g % KS);
+    cp_async_wait<0>();
+    __syncthreads();             // step g's rows and token j's alpha are visible; slot (g + 1) & 1 is free
+    if (g + 1 < total) issue(g + 1);
+    if (kk == 0 && j + 1 < my_tokens) stage_alpha(j + 1);   // the other alpha buffer (last read by token j - 1)
+    if (kk == 0) {
+#pragma unroll
+      for (int nt = 0; nt < 16; ++nt) c[nt][0] = c[nt][1] = c[nt][2] = c[nt][3] = 0.f;
+    }
+    // A fragments (hi, lo) of this step: rows q, columns kk*16 .. +15
+    const unsigned char *ab = abuf + (size_t)(j & 1) * 2 * kTcK * RA;
+    const int mrow = (lane & 7) + ((lane >> 3) & 1) * 8, mcol = kk * kTcK + (lane >> 4) * 8;
+    uint32_t ahi[4], alo[4];
+    ldsm_x4(smem_u32(ab + (size_t)mrow * RA + (size_t)mcol * 2), ahi);
+    ldsm_x4(smem_u32(ab + (size_t)(kTcK + mrow) * RA + (size_t)mcol * 2), alo);
+    // B fragments from the slot: rows k (summaries), 8 features per tile; two tiles per ldmatrix
+    const unsigned char *slot = vring + (size_t)(g & 1) * kTcK * RV;
+    const int krow = (lane & 7) + ((lane >> 3) & 1) * 8, kcol = (lane >> 4) * 8;
+#pragma unroll
+    for (int pr = 0; pr < 8; ++pr) {
+      if (2 * pr >= ntw) break;
+      const int f0 = (warp * ntw + 2 * pr) * 8;
+      uint32_t b[4];
+      ldsm_x4_trans(smem_u32(slot + (size_t)krow * RV + (size_t)(f0 + kcol) * 2), b);
+      mma_16816(c[2 * pr], ahi, b[0], b[1]);
+      mma_16816(c[2 * pr], alo, b[0], b[1]);
+      mma_16816(c[2 * pr + 1], ahi, b[2], b[3]);
+      mma_16816(c[2 * pr + 1], alo, b[2], b[3]);
+    }
+    if (kk == KS - 1) {          // token done: rows q = lane/4 and lane/4 + 8, two features per tile
+      const int64_t t = token(j);
+      const int q0 = lane >> 2, fc = (lane & 3) * 2;
+#pragma unroll
+      for (int nt = 0; nt < 16; ++nt) {
+        if (nt >= ntw) break;
+        const int f = (warp * ntw + nt) * 8 + fc;
+        if (q0 < S)
+          __stcs(reinterpret_cast<uint32_t *>(static_cast<char *>(p.out) + ((size_t)q0 * p.rows + t) * row_bytes + (size_t)f * 2),
+                 Elt<__nv_bfloat16>::pack_word(c[nt][0], c[nt][1]));
+        if (q0 + 8 < S)
+          __stcs(reinterpret_cast<uint32_t *>(static_cast<char *>(p.out) + ((size_t)(q0 + 8) * p.rows + t) * row_bytes + (size_t)f * 2),
+                 Elt<__nv_bfloat16>::pack_word(c[nt][2], c[nt][3]));
+      }
+    }
+  }
+  cp_async_wait<0>();
+}
+
+// -----------------------------------------------------------------------------
 // Host side
 // -----------------------------------------------------------------------------
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -812,6 +956,23 @@ cudaError_t launch_phase1_many(const Phase1ManyArgs &a) {
     const int64_t blocks = (total + 255) / 256 < 8 * sm_count() ? (total + 255) / 256 : 8 * sm_count();
     p1_many_softmax_kernel<<<(int)blocks, 256, 0, a.stream>>>(a.scores, a.rows, a.n, a.S, a.out_max, a.out_lse);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  if (a.S <= kTcK && a.D % (8 * kTcWarps * 2) == 0 && a.D <= 8 * kTcWarps * 16 &&
+      tc_smem(a.n, a.D) <= 227 * 1024) {
+    ParamsB3 pc;
+    for (int i = 0; i < a.n; ++i) pc.src[i] = a.blocks[i];
+    pc.alpha = a.scores;
+    pc.out = a.out;
+    pc.rows = a.rows;
+    pc.n = a.n;
+    pc.S = a.S;
+    pc.D = a.D;
+    const size_t smem3 = tc_smem(a.n, a.D);
+    e = cudaFuncSetAttribute(p1_many_outputs_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem3);
+    if (e != cudaSuccess) return e;
+    const int64_t g3 = a.rows < sm_count() ? a.rows : sm_count();
+    p1_many_outputs_tc_kernel<<<(int)g3, kTcWarps * 32, smem3, a.stream>>>(pc);
+    return cudaGetLastError();
   }
   ParamsB2 pb;
   for (int i = 0; i < a.n; ++i) pb.src[i] = a.blocks[i];

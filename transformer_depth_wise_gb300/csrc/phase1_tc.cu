@@ -447,21 +447,6 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" :: "n"(N) : "memory"); }
 
-// Warp-level tensor-core helpers (ldmatrix, mma.m16n8k16 bf16 -> fp32).
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(addr));
-}
-__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t (&r)[4]) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(addr));
-}
-__device__ __forceinline__ void mma_16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
-  asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
-               "{%8, %9}, {%0, %1, %2, %3};"
-               : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-               : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
 __global__ void __launch_bounds__(512, 1) p1_outputs_kernel(const __grid_constant__ ParamsB p) {
   extern __shared__ uint4 vbuf[];                     // [kBStages][n][nvec] 16-byte chunks
   __shared__ __align__(16) float alpha[kBStages][2 * kMaxN * kMaxS];   // [n][Sp][2]
@@ -536,112 +521,6 @@ __global__ void __launch_bounds__(512, 1) p1_outputs_kernel(const __grid_constan
     }
     __syncthreads();    // every thread is done with stage `buf` before it is refilled
   }
-}
-
-// -----------------------------------------------------------------------------
-// Kernel B on tensor cores (D a multiple of 256): per token the outputs are a
-// dense contraction O[q][d] = sum_i alpha[q][i] v_i[d] with K = n <= 10:
-// warp-level mma.m16n8k16 (bf16 in, fp32 accumulate), M = 32 queries in two
-// tiles, K = 16 summaries (rows past n read a zero block), N = 8 features per
-// tile.  alpha (fp32, parked in o[0][t] by kernel A and staged with the rows)
-// is split into bf16 hi + lo per warp straight into the A fragments; the
-// summary rows (N-major) become B fragments through ldmatrix.trans.  Two
-// cp.async stages: token k + 1 lands while token k is formed.
-// -----------------------------------------------------------------------------
-constexpr int kBtcStages = 2;
-constexpr int kBtcWarps = 16;
-
-__host__ __device__ constexpr size_t btc_row(int D) { return (size_t)D * 2 + 16; }
-__host__ __device__ constexpr size_t btc_smem(int n, int D) {
-  return 16 + (size_t)kBtcStages * n * btc_row(D) + (size_t)kBtcStages * 2 * kMaxN * kMaxS * sizeof(float);
-}
-
-__global__ void __launch_bounds__(kBtcWarps * 32, 1) p1_outputs_tc_kernel(const __grid_constant__ ParamsB p) {
-  extern __shared__ __align__(16) unsigned char smb[];
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int n = p.n, S = p.S, D = p.D;
-  const size_t RV = btc_row(D), row_bytes = (size_t)D * 2;
-  unsigned char *zero = smb;                                        // 16 zero bytes
-  unsigned char *vb = smb + 16;                                     // [stage][n][RV]
-  float *alpha = reinterpret_cast<float *>(vb + (size_t)kBtcStages * n * RV);   // [stage][n][Sp][2]
-  const int Sp = S + (S & 1);
-  const int alpha_vecs = (2 * n * Sp) / 4;
-  const int chunks = D / 8;
-  const int ntw = chunks / kBtcWarps;                               // feature tiles per warp (even)
-  const int64_t my = p.rows > (int64_t)blockIdx.x ? (p.rows - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
-  if (tid == 0) *reinterpret_cast<uint4 *>(zero) = make_uint4(0u, 0u, 0u, 0u);
-
-  auto prefetch = [&](int64_t k, int buf) {
-    const int64_t t = blockIdx.x + k * gridDim.x;
-    for (int c = tid; c < n * chunks; c += blockDim.x) {
-      const int i = c / chunks, ch = c % chunks;
-      cp_async16(vb + ((size_t)buf * n + i) * RV + (size_t)ch * 16,
-                 static_cast<const char *>(p.src[i]) + (size_t)t * row_bytes + (size_t)ch * 16);
-    }
-    if (tid < alpha_vecs)
-      cp_async16(alpha + (size_t)buf * 2 * kMaxN * kMaxS + tid * 4,
-                 static_cast<const char *>(p.out) + (size_t)t * row_bytes + (size_t)tid * 16);
-    cp_async_commit();
-  };
-
-  if (my > 0) prefetch(0, 0);
-  else cp_async_commit();
-  const int g = lane >> 2, tig = lane & 3;
-  const int krow = (lane & 7) + ((lane >> 3) & 1) * 8, kcol = (lane >> 4) * 8;
-  for (int64_t k = 0; k < my; ++k) {
-    const int buf = (int)(k % kBtcStages);
-    const int64_t t = blockIdx.x + k * gridDim.x;
-    if (k + 1 < my) prefetch(k + 1, (int)((k + 1) % kBtcStages));
-    else cp_async_commit();
-    cp_async_wait<1>();
-    __syncthreads();    // token k's rows and alpha are in; alpha of t is read before o[0][t] is written
-    // A fragments: alpha[q][i] (query rows, summary columns) as bf16 hi + lo
-    const float *al = alpha + (size_t)buf * 2 * kMaxN * kMaxS;
-    auto av = [&](int q, int i) { return (q < S && i < n) ? al[(size_t)(i * Sp + q) * 2] : 0.f; };
-    uint32_t ahi[2][4], alo[2][4];
-#pragma unroll
-    for (int mt = 0; mt < 2; ++mt) {
-#pragma unroll
-      for (int r = 0; r < 4; ++r) {
-        const int q = mt * 16 + g + (r & 1) * 8, i = tig * 2 + (r >> 1) * 8;
-        const float x0 = av(q, i), x1 = av(q, i + 1);
-        const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
-        const __nv_bfloat162 l = __floats2bfloat162_rn(x0 - __low2float(h), x1 - __high2float(h));
-        ahi[mt][r] = *reinterpret_cast<const uint32_t *>(&h);
-        alo[mt][r] = *reinterpret_cast<const uint32_t *>(&l);
-      }
-    }
-    const unsigned char *rowp = krow < n ? vb + ((size_t)buf * n + krow) * RV : nullptr;
-    const size_t qstride = (size_t)p.rows * row_bytes;
-    char *dst = static_cast<char *>(p.out) + (size_t)t * row_bytes;
-    for (int pr = 0; pr < ntw; pr += 2) {
-      const int f0 = (warp * ntw + pr) * 8;
-      uint32_t b[4];
-      ldsm_x4_trans(smem_u32(rowp ? rowp + (size_t)(f0 + kcol) * 2 : zero), b);
-      float c[2][2][4];
-#pragma unroll
-      for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-        for (int tl = 0; tl < 2; ++tl) {
-          c[mt][tl][0] = c[mt][tl][1] = c[mt][tl][2] = c[mt][tl][3] = 0.f;
-          mma_16816(c[mt][tl], ahi[mt], b[2 * tl], b[2 * tl + 1]);
-          mma_16816(c[mt][tl], alo[mt], b[2 * tl], b[2 * tl + 1]);
-        }
-#pragma unroll
-      for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-        for (int tl = 0; tl < 2; ++tl) {
-          const size_t f = (size_t)(f0 + tl * 8 + tig * 2) * 2;
-          const int q0 = mt * 16 + g, q1 = q0 + 8;
-          if (q0 < S) __stcs(reinterpret_cast<uint32_t *>(dst + (size_t)q0 * qstride + f),
-                             Elt<__nv_bfloat16>::pack_word(c[mt][tl][0], c[mt][tl][1]));
-          if (q1 < S) __stcs(reinterpret_cast<uint32_t *>(dst + (size_t)q1 * qstride + f),
-                             Elt<__nv_bfloat16>::pack_word(c[mt][tl][2], c[mt][tl][3]));
-        }
-    }
-    __syncthreads();    // every warp is done with stage `buf` before it is refilled
-  }
-  cp_async_wait<0>();
 }
 
 // -----------------------------------------------------------------------------
@@ -773,6 +652,20 @@ struct ParamsB3 {
   int n, S, D;
 };
 
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(addr));
+}
+__device__ __forceinline__ void mma_16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+               "{%8, %9}, {%0, %1, %2, %3};"
+               : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+               : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
 // 16-byte cp.async that reads `bytes` (16 or 0) and zero-fills the rest.
 __device__ __forceinline__ void cp_async16_zfill(void *smem, const void *gmem, uint32_t bytes) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(smem)), "l"(gmem), "r"(bytes)
@@ -967,7 +860,7 @@ cudaError_t launch_phase1_tc(const Phase1Args &a) {
   const int64_t ga = (tiles + waves - 1) / waves;
   p1_scores_kernel<kMaxN><<<(int)ga, kThreadsA, kSmemA, a.stream>>>(pa);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  // Kernel B (tensor cores when D is a multiple of 256 and its stages fit)
+  // Kernel B
   ParamsB pb;
   for (int i = 0; i < a.n; ++i) pb.src[i] = a.blocks[i];
   pb.out = a.out;
@@ -976,14 +869,6 @@ cudaError_t launch_phase1_tc(const Phase1Args &a) {
   pb.S = a.S;
   pb.D = a.D;
   pb.nvec = a.D / 8;
-  if (a.D % (8 * kBtcWarps * 2) == 0 && btc_smem(a.n, a.D) <= 227 * 1024) {
-    const size_t smtc = btc_smem(a.n, a.D);
-    e = cudaFuncSetAttribute(p1_outputs_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smtc);
-    if (e != cudaSuccess) return e;
-    const int64_t gbt = a.rows < sm_count() ? a.rows : sm_count();
-    p1_outputs_tc_kernel<<<(int)gbt, kBtcWarps * 32, smtc, a.stream>>>(pb);
-    return cudaGetLastError();
-  }
   const int threads = (pb.nvec + 31) / 32 * 32;
   const size_t smem = smem_b(a.n, a.D);
   e = cudaFuncSetAttribute(p1_outputs_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

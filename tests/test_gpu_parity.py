@@ -249,6 +249,8 @@ def test_aggregate_backward_full_size_sampled(gpu):
     # general kernel: other D, n > 9, fp32
     (torch.bfloat16, 7168, 9, 4, 9), (torch.float32, 256, 5, 7, 66), (torch.bfloat16, 64, 1, 3, 20),
     (torch.bfloat16, 2048, 16, 2, 11), (torch.bfloat16, 4096, 10, 24, 21),
+    # tensor-core path with rows formed in two pieces (D > 4096)
+    (torch.bfloat16, 7168, 9, 24, 37), (torch.bfloat16, 8192, 5, 7, 130), (torch.bfloat16, 5120, 9, 24, 19),
 ])
 def test_phase1_small(gpu, dtype, D, n, S, rows):
     g = wk.generator(D + n + S, gpu)

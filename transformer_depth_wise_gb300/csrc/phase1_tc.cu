@@ -97,6 +97,7 @@ struct ParamsB {
   void *out;
   int64_t rows;
   int n, S, D, nvec;
+  int parts, nvp;   // a row is formed in `parts` pieces of nvp 16-byte chunks (D > 4096: two)
 };
 
 // --- small PTX wrappers ------------------------------------------------------
@@ -448,23 +449,27 @@ template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" :: "n"(N) : "memory"); }
 
 __global__ void __launch_bounds__(512, 1) p1_outputs_kernel(const __grid_constant__ ParamsB p) {
-  extern __shared__ uint4 vbuf[];                     // [kBStages][n][nvec] 16-byte chunks
+  extern __shared__ uint4 vbuf[];                     // [kBStages][n][nvp] 16-byte chunks
   __shared__ __align__(16) float alpha[kBStages][2 * kMaxN * kMaxS];   // [n][Sp][2]
   const int tid = threadIdx.x;
-  const int n = p.n, S = p.S, nvec = p.nvec;
+  const int n = p.n, S = p.S, nvp = p.nvp, parts = p.parts;
   const size_t row_bytes = (size_t)p.D * 2;
-  const int64_t my = p.rows > (int64_t)blockIdx.x ? (p.rows - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
+  // Items are (token, piece), the pieces of a token consecutive on the same
+  // CTA: the first piece brings in alpha (parked in o[0][t], which that piece
+  // then overwrites), the next one reads it from the first piece's stage.
+  const int64_t my = (p.rows > (int64_t)blockIdx.x ? (p.rows - blockIdx.x + gridDim.x - 1) / gridDim.x : 0) * parts;
   const int Sp = S + (S & 1);                          // queries per alpha row (even)
   const int alpha_vecs = (2 * n * Sp) / 4;
 
   auto prefetch = [&](int64_t k, int buf) {
-    const int64_t t = blockIdx.x + k * gridDim.x;
-    if (tid < nvec) {
+    const int64_t t = blockIdx.x + (k / parts) * gridDim.x;
+    const int part = (int)(k % parts);
+    if (tid < nvp) {
       for (int i = 0; i < n; ++i)
-        cp_async16(&vbuf[(size_t)(buf * n + i) * nvec + tid],
-                   static_cast<const char *>(p.src[i]) + (size_t)t * row_bytes + (size_t)tid * 16);
+        cp_async16(&vbuf[(size_t)(buf * n + i) * nvp + tid],
+                   static_cast<const char *>(p.src[i]) + (size_t)t * row_bytes + (size_t)(part * nvp + tid) * 16);
     }
-    if (tid < alpha_vecs)
+    if (part == 0 && tid < alpha_vecs)
       cp_async16(&alpha[buf][tid * 4], static_cast<const char *>(p.out) + (size_t)t * row_bytes + (size_t)tid * 16);
     cp_async_commit();
   };
@@ -476,25 +481,28 @@ __global__ void __launch_bounds__(512, 1) p1_outputs_kernel(const __grid_constan
   }
   for (int64_t k = 0; k < my; ++k) {
     const int buf = (int)(k % kBStages);
-    const int64_t t = blockIdx.x + k * gridDim.x;
+    const int64_t t = blockIdx.x + (k / parts) * gridDim.x;
+    const int part = (int)(k % parts);
     if (k + kBStages - 1 < my) prefetch(k + kBStages - 1, (int)((k + kBStages - 1) % kBStages));
     else cp_async_commit();
     cp_async_wait<kBStages - 1>();
     __syncthreads();    // stage `buf` complete for every thread; alpha of t read before o[0][t] is written
-    if (tid < nvec) {
+    if (tid < nvp) {
       uint64_t xp[kMaxN][4];                        // the row chunk of every summary, as fp32 pairs
 #pragma unroll
       for (int i = 0; i < kMaxN; ++i) {
         if (i < n) {
           float x[8];
-          Elt<__nv_bfloat16>::unpack(vbuf[(size_t)(buf * n + i) * nvec + tid], x);
+          Elt<__nv_bfloat16>::unpack(vbuf[(size_t)(buf * n + i) * nvp + tid], x);
 #pragma unroll
           for (int m = 0; m < 4; ++m) xp[i][m] = pk(x[2 * m], x[2 * m + 1]);
         }
       }
-      char *dst = static_cast<char *>(p.out) + (size_t)t * row_bytes + (size_t)tid * 16;
+      char *dst = static_cast<char *>(p.out) + (size_t)t * row_bytes + (size_t)(part * nvp + tid) * 16;
       const size_t qstride = (size_t)p.rows * row_bytes;
-      const float *al = alpha[buf];
+      // alpha came with the token's first piece (k - part); the stages in
+      // between carry no alpha, so its buffer is intact
+      const float *al = alpha[(k - part) % kBStages];
       for (int q = 0; q < S; q += 2) {              // queries in pairs
         uint64_t acc0[4] = {0, 0, 0, 0}, acc1[4] = {0, 0, 0, 0};
 #pragma unroll
@@ -798,9 +806,11 @@ size_t smem_b(int n, int D) { return (size_t)kBStages * n * (D / 8) * 16; }
 
 bool phase1_tc_supported(int n, int D, int dtype, int S) {
   if (dtype != ATTNRES_BF16 || n < 1 || n > tc::kMaxN || S < 1 || S > tc::kMaxS) return false;
-  if (D % tc::kKc != 0 || D > 4096) return false;            // kernel B: one thread per 16 bytes
-  if ((size_t)(S + (S & 1)) * n * 8 > (size_t)D * 2) return false;   // alpha fits in o[0]'s row
-  if (tc::smem_b(n, D) + sizeof(float) * tc::kBStages * 2 * tc::kMaxN * tc::kMaxS > 227 * 1024)
+  if (D % tc::kKc != 0 || D > 8192) return false;            // kernel B: a thread per 16 bytes of a row piece
+  const int parts = D > 4096 ? 2 : 1;
+  // alpha fits in o[0]'s row, inside the first piece of it
+  if ((size_t)(S + (S & 1)) * n * 8 > (size_t)D * 2 / parts) return false;
+  if (tc::smem_b(n, D / parts) + sizeof(float) * tc::kBStages * 2 * tc::kMaxN * tc::kMaxS > 227 * 1024)
     return false;
   return tc::encode_fn() != nullptr;
 }
@@ -869,8 +879,10 @@ cudaError_t launch_phase1_tc(const Phase1Args &a) {
   pb.S = a.S;
   pb.D = a.D;
   pb.nvec = a.D / 8;
-  const int threads = (pb.nvec + 31) / 32 * 32;
-  const size_t smem = smem_b(a.n, a.D);
+  pb.parts = a.D > 4096 ? 2 : 1;
+  pb.nvp = pb.nvec / pb.parts;
+  const int threads = (pb.nvp + 31) / 32 * 32;
+  const size_t smem = smem_b(a.n, a.D / pb.parts);
   e = cudaFuncSetAttribute(p1_outputs_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   int occ = 0;

@@ -241,16 +241,15 @@ def test_aggregate_backward_full_size_sampled(gpu):
 # two-phase Block: phase 1, phase 2 merge, partial update, one block chain
 # --------------------------------------------------------------------------
 @pytest.mark.parametrize("dtype,D,n,S,rows", [
-    # tensor-core kernel (bf16, D = 512 x {1, 2, 4, 8}, n <= 9, S <= 24): clusters of
-    # 1..8 CTAs, one / several / ragged 8-token tiles
+    # tensor-core path (bf16, D a multiple of 64, n <= 10, S <= 24, at least 512 rows): one / several / ragged
+    # 128-row tiles; rows wider than 4096 formed in two pieces
+    (torch.bfloat16, 512, 9, 24, 600), (torch.bfloat16, 1024, 5, 7, 520), (torch.bfloat16, 2048, 9, 24, 700),
+    (torch.bfloat16, 4096, 9, 24, 520), (torch.bfloat16, 4096, 2, 3, 1000), (torch.bfloat16, 4096, 8, 24, 4103),
+    (torch.bfloat16, 7168, 9, 24, 530), (torch.bfloat16, 8192, 5, 7, 515), (torch.bfloat16, 5120, 9, 24, 600),
+    # general kernel: few rows, n > 10, fp32
     (torch.bfloat16, 512, 1, 1, 1), (torch.bfloat16, 512, 9, 24, 37), (torch.bfloat16, 512, 3, 5, 130),
-    (torch.bfloat16, 1024, 5, 7, 130), (torch.bfloat16, 2048, 9, 24, 64), (torch.bfloat16, 4096, 9, 24, 37),
-    (torch.bfloat16, 4096, 9, 24, 8), (torch.bfloat16, 4096, 2, 3, 1000), (torch.bfloat16, 4096, 8, 24, 4103),
-    # general kernel: other D, n > 9, fp32
-    (torch.bfloat16, 7168, 9, 4, 9), (torch.float32, 256, 5, 7, 66), (torch.bfloat16, 64, 1, 3, 20),
-    (torch.bfloat16, 2048, 16, 2, 11), (torch.bfloat16, 4096, 10, 24, 21),
-    # tensor-core path with rows formed in two pieces (D > 4096)
-    (torch.bfloat16, 7168, 9, 24, 37), (torch.bfloat16, 8192, 5, 7, 130), (torch.bfloat16, 5120, 9, 24, 19),
+    (torch.bfloat16, 4096, 9, 24, 8), (torch.bfloat16, 7168, 9, 4, 9), (torch.float32, 256, 5, 7, 66),
+    (torch.bfloat16, 64, 1, 3, 20), (torch.bfloat16, 2048, 16, 2, 11), (torch.bfloat16, 4096, 10, 24, 21),
 ])
 def test_phase1_small(gpu, dtype, D, n, S, rows):
     g = wk.generator(D + n + S, gpu)

@@ -206,8 +206,10 @@ int phase1_check(int n, int D, int dtype, int S) {
 
 cudaError_t launch_phase1(const Phase1Args &a) {
   // The tensor-core path parks the split queries in the last 48 D-rows of
-  // `out`, which must not overlap out[0] (where it parks alpha).
-  if (phase1_tc_supported(a.n, a.D, a.dtype, a.S) && (int64_t)(a.S - 1) * a.rows >= 48)
+  // `out`, which must not overlap out[0] (where it parks alpha).  Its scores
+  // kernel works on 128-row tiles, one CTA each: below four tiles the
+  // one-CTA-per-row kernel spreads wider and is faster.
+  if (phase1_tc_supported(a.n, a.D, a.dtype, a.S) && (int64_t)(a.S - 1) * a.rows >= 48 && a.rows >= 512)
     return launch_phase1_tc(a);
   Cfg c;
   if (!choose(a.n, a.D, a.dtype, c)) return cudaErrorInvalidValue;

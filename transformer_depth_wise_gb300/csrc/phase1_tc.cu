@@ -448,11 +448,13 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" :: "n"(N) : "memory"); }
 
+template <int PARTS>
 __global__ void __launch_bounds__(512, 1) p1_outputs_kernel(const __grid_constant__ ParamsB p) {
   extern __shared__ uint4 vbuf[];                     // [kBStages][n][nvp] 16-byte chunks
   __shared__ __align__(16) float alpha[kBStages][2 * kMaxN * kMaxS];   // [n][Sp][2]
   const int tid = threadIdx.x;
-  const int n = p.n, S = p.S, nvp = p.nvp, parts = p.parts;
+  const int n = p.n, S = p.S, nvp = p.nvp;
+  constexpr int parts = PARTS;
   const size_t row_bytes = (size_t)p.D * 2;
   // Items are (token, piece), the pieces of a token consecutive on the same
   // CTA: the first piece brings in alpha (parked in o[0][t], which that piece
@@ -883,15 +885,16 @@ cudaError_t launch_phase1_tc(const Phase1Args &a) {
   pb.nvp = pb.nvec / pb.parts;
   const int threads = (pb.nvp + 31) / 32 * 32;
   const size_t smem = smem_b(a.n, a.D / pb.parts);
-  e = cudaFuncSetAttribute(p1_outputs_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  auto kern = pb.parts == 2 ? p1_outputs_kernel<2> : p1_outputs_kernel<1>;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   int occ = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, p1_outputs_kernel, threads, smem);
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, threads, smem);
   if (e != cudaSuccess) return e;
   if (occ < 1) occ = 1;
   const int64_t cap = (int64_t)occ * sm_count();
   const int64_t gb = a.rows < cap ? a.rows : cap;
-  p1_outputs_kernel<<<(int)gb, threads, smem, a.stream>>>(pb);
+  kern<<<(int)gb, threads, smem, a.stream>>>(pb);
   return cudaGetLastError();
 }
 

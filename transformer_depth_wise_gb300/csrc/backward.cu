@@ -64,7 +64,8 @@ aggregate_backward_kernel(const __grid_constant__ BwdParams p) {
   constexpr int GA = kBwdGroupA, GB = kBwdGroupB;
   constexpr int TPC = TEAM ? kBwdTeams : 1;
   constexpr int W = TEAM ? TEAM : 32;     // lanes that run the per-row softmax
-  __shared__ float red[TEAM ? 1 : 2 * 32 * 3 * GA];
+  constexpr int KR = 4 * GA;               // per-source sums, padded to a power of two (3 used of 4)
+  __shared__ float red[TEAM ? 1 : 2 * 32 * KR];
   __shared__ float coef[TPC][kMaxSources][3];
 
   const int tpr = TEAM ? TEAM : blockDim.x;
@@ -91,9 +92,16 @@ aggregate_backward_kernel(const __grid_constant__ BwdParams p) {
       qe[k * EPV + e4 + 3] = w4.w * g4.w;
     }
   }
-  float acc[NE];
+  // As packed fp32 pairs (two FMAs per instruction): the folded query and
+  // the query-gradient accumulator.
+  using PR = Pairs<T>;
+  constexpr int NP = PR::NP;
+  uint64_t qp[VPT * NP], accp[VPT * NP];
 #pragma unroll
-  for (int e = 0; e < NE; ++e) acc[e] = 0.f;
+  for (int j = 0; j < VPT * NP; ++j) {
+    qp[j] = pair(qe[2 * j], qe[2 * j + 1]);
+    accp[j] = 0ull;
+  }
 
   const size_t row_bytes = (size_t)p.nvec * 16;
   const int64_t groups = (p.rows + TPC - 1) / TPC;
@@ -103,13 +111,13 @@ aggregate_backward_kernel(const __grid_constant__ BwdParams p) {
     const bool row_ok = row < p.rows;
     const size_t row_off = (size_t)row * row_bytes;
 
-    float gh[NE];  // dh of this row
+    uint64_t gp[VPT * NP];  // dh of this row, as pairs
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
       uint4 x = make_uint4(0u, 0u, 0u, 0u);
       if (row_ok && valid[k])
         x = ld_stream(static_cast<const char *>(p.dh) + row_off + (size_t)(lt + k * tpr) * 16);
-      E::unpack(x, gh + k * EPV);
+      PR::split(x, gp + k * NP);
     }
 
     // Pass A: sum v^2, w~ . v and dh . v for every source.
@@ -124,36 +132,42 @@ aggregate_backward_kernel(const __grid_constant__ BwdParams p) {
             v[j][k] = ld_stream(static_cast<const char *>(p.src[i0 + j]) + row_off +
                                 (size_t)(lt + k * tpr) * 16);
         }
-      float part[3 * GA];
+      float part[KR];
 #pragma unroll
-      for (int j = 0; j < 3 * GA; ++j) part[j] = 0.f;
-#pragma unroll
-      for (int j = 0; j < GA; ++j)
+      for (int j = 0; j < GA; ++j) {
+        uint64_t ss = 0ull, dq = 0ull, dg = 0ull;
 #pragma unroll
         for (int k = 0; k < VPT; ++k) {
-          float x[EPV];
-          E::unpack(v[j][k], x);
+          uint64_t x[NP];
+          PR::split(v[j][k], x);
 #pragma unroll
-          for (int e = 0; e < EPV; ++e) {
-            part[3 * j + 0] = fmaf(x[e], x[e], part[3 * j + 0]);
-            part[3 * j + 1] = fmaf(qe[k * EPV + e], x[e], part[3 * j + 1]);
-            part[3 * j + 2] = fmaf(gh[k * EPV + e], x[e], part[3 * j + 2]);
+          for (int m = 0; m < NP; ++m) {
+            fma_pair(ss, x[m], x[m]);
+            fma_pair(dq, qp[k * NP + m], x[m]);
+            fma_pair(dg, gp[k * NP + m], x[m]);
           }
         }
+        part[4 * j + 0] = pair_sum(ss);
+        part[4 * j + 1] = pair_sum(dq);
+        part[4 * j + 2] = pair_sum(dg);
+        part[4 * j + 3] = 0.f;
+      }
       if (TEAM) {
 #pragma unroll
-        for (int j = 0; j < 3 * GA; ++j) part[j] = team_sum_shfl<TEAM ? TEAM : 1>(part[j]);
+        for (int j = 0; j < GA; ++j)
+#pragma unroll
+          for (int m = 0; m < 3; ++m) part[4 * j + m] = team_sum_shfl<TEAM ? TEAM : 1>(part[4 * j + m]);
       } else {
-        cta_sum<3 * GA>(part, red, parity);
+        cta_sum_rs<KR>(part, red, parity);
         parity ^= 1;
       }
       if (lt == 0) {
 #pragma unroll
         for (int j = 0; j < GA; ++j)
           if (i0 + j < p.n) {
-            cf[i0 + j][0] = part[3 * j + 0];
-            cf[i0 + j][1] = part[3 * j + 1];
-            cf[i0 + j][2] = part[3 * j + 2];
+            cf[i0 + j][0] = part[4 * j + 0];
+            cf[i0 + j][1] = part[4 * j + 1];
+            cf[i0 + j][2] = part[4 * j + 2];
           }
       }
     }
@@ -209,17 +223,28 @@ aggregate_backward_kernel(const __grid_constant__ BwdParams p) {
       for (int j = 0; j < GB; ++j) {
         if (i0 + j >= p.n || !row_ok) continue;
         const float a = cf[i0 + j][0], b = cf[i0 + j][1], c = cf[i0 + j][2];
+        const uint64_t a2 = pair(a, a), b2 = pair(b, b), nc2 = pair(-c, -c);
 #pragma unroll
         for (int k = 0; k < VPT; ++k) {
           if (!valid[k]) continue;
-          float x[EPV], o[EPV];
-          E::unpack(v[j][k], x);
-          if (p.accumulate) E::unpack(din[j][k], o);
+          uint64_t x[NP], d[NP];
+          PR::split(v[j][k], x);
 #pragma unroll
-          for (int e = 0; e < EPV; ++e) {
-            const float d = fmaf(a, gh[k * EPV + e], fmaf(b, qe[k * EPV + e], -c * x[e]));
-            o[e] = p.accumulate ? o[e] + d : d;
-            acc[k * EPV + e] = fmaf(b, x[e], acc[k * EPV + e]);
+          for (int m = 0; m < NP; ++m) {
+            d[m] = 0ull;
+            fma_pair(d[m], nc2, x[m]);               // -c v
+            fma_pair(d[m], b2, qp[k * NP + m]);      // + (ds r) w~
+            fma_pair(d[m], a2, gp[k * NP + m]);      // + alpha dh
+            fma_pair(accp[k * NP + m], b2, x[m]);    // dw~ += (ds r) v
+          }
+          float o[EPV];
+#pragma unroll
+          for (int m = 0; m < NP; ++m) unpair(d[m], o[2 * m], o[2 * m + 1]);
+          if (p.accumulate) {
+            float w[EPV];
+            E::unpack(din[j][k], w);
+#pragma unroll
+            for (int e = 0; e < EPV; ++e) o[e] += w[e];
           }
           st_vec(static_cast<char *>(p.dsrc[i0 + j]) + row_off + (size_t)(lt + k * tpr) * 16, E::pack(o));
         }
@@ -234,10 +259,12 @@ aggregate_backward_kernel(const __grid_constant__ BwdParams p) {
     for (int k = 0; k < VPT; ++k) {
       if (!valid[k]) continue;
       float *d = dst + (lt + k * tpr) * EPV;
+      float w[EPV];
+#pragma unroll
+      for (int m = 0; m < NP; ++m) unpair(accp[k * NP + m], w[2 * m], w[2 * m + 1]);
 #pragma unroll
       for (int e4 = 0; e4 < EPV; e4 += 4)
-        *reinterpret_cast<float4 *>(d + e4) =
-            make_float4(acc[k * EPV + e4], acc[k * EPV + e4 + 1], acc[k * EPV + e4 + 2], acc[k * EPV + e4 + 3]);
+        *reinterpret_cast<float4 *>(d + e4) = make_float4(w[e4], w[e4 + 1], w[e4 + 2], w[e4 + 3]);
     }
   }
 }

@@ -492,14 +492,8 @@ __global__ void __launch_bounds__(512, 1) p1_outputs_kernel(const __grid_constan
     if (tid < nvp) {
       uint64_t xp[kMaxN][4];                        // the row chunk of every summary, as fp32 pairs
 #pragma unroll
-      for (int i = 0; i < kMaxN; ++i) {
-        if (i < n) {
-          float x[8];
-          Elt<__nv_bfloat16>::unpack(vbuf[(size_t)(buf * n + i) * nvp + tid], x);
-#pragma unroll
-          for (int m = 0; m < 4; ++m) xp[i][m] = pk(x[2 * m], x[2 * m + 1]);
-        }
-      }
+      for (int i = 0; i < kMaxN; ++i)
+        if (i < n) Pairs<__nv_bfloat16>::split(vbuf[(size_t)(buf * n + i) * nvp + tid], xp[i]);
       char *dst = static_cast<char *>(p.out) + (size_t)t * row_bytes + (size_t)(part * nvp + tid) * 16;
       const size_t qstride = (size_t)p.rows * row_bytes;
       // alpha came with the token's first piece (k - part); the stages in
@@ -510,8 +504,9 @@ __global__ void __launch_bounds__(512, 1) p1_outputs_kernel(const __grid_constan
 #pragma unroll
         for (int i = 0; i < kMaxN; ++i) {
           if (i < n) {
-            const float4 a = *reinterpret_cast<const float4 *>(al + 2 * (i * Sp + q));
-            const uint64_t a0 = pk(a.x, a.y), a1 = pk(a.z, a.w);
+            // alpha of queries q and q + 1, each already a duplicated pair
+            const ulonglong2 a = *reinterpret_cast<const ulonglong2 *>(al + 2 * (i * Sp + q));
+            const uint64_t a0 = a.x, a1 = a.y;
 #pragma unroll
             for (int m = 0; m < 4; ++m) {
               fma2(acc0[m], a0, xp[i][m]);

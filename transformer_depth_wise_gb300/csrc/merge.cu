@@ -611,6 +611,9 @@ cudaError_t dispatch_norm(const RmsNormArgs &a, const Cfg &c) {
 cudaError_t launch_merge_update(const MergeUpdateArgs &a) {
   Cfg c;
   if (!choose(a.D, a.dtype, c)) return cudaErrorInvalidValue;
+  // Few rows (decode): two vectors per thread, twice the threads on each row.
+  if (c.team == 0 && a.rows <= 4 * sm_count() && (a.D / epv_of(a.dtype) + 1) / 2 <= 512)
+    c = {2, 0, ((a.D / epv_of(a.dtype) + 1) / 2 + 31) / 32 * 32};
   MergeUpdateParams P;
   P.m.o = a.inter_out;
   P.m.lse = a.inter_lse;

@@ -246,11 +246,10 @@ def test_aggregate_backward_full_size_sampled(gpu):
     (torch.bfloat16, 512, 9, 24, 600), (torch.bfloat16, 1024, 5, 7, 520), (torch.bfloat16, 2048, 9, 24, 700),
     (torch.bfloat16, 4096, 9, 24, 520), (torch.bfloat16, 4096, 2, 3, 1000), (torch.bfloat16, 4096, 8, 24, 4103),
     (torch.bfloat16, 7168, 9, 24, 530), (torch.bfloat16, 8192, 5, 7, 515), (torch.bfloat16, 5120, 9, 24, 600),
-    # summaries that fit in L2: one aggregation launch over (row, query) pairs
+    # the per-row kernel: few rows, fp32, n > 10
     (torch.bfloat16, 512, 1, 1, 1), (torch.bfloat16, 512, 9, 24, 37), (torch.bfloat16, 512, 3, 5, 130),
     (torch.bfloat16, 4096, 9, 24, 8), (torch.bfloat16, 7168, 9, 4, 9), (torch.float32, 256, 5, 7, 66),
     (torch.bfloat16, 64, 1, 3, 20), (torch.bfloat16, 2048, 16, 2, 11), (torch.bfloat16, 4096, 10, 24, 21),
-    # the per-row kernel: beyond L2 and outside the tensor-core path (fp32, n > 10)
     (torch.float32, 2048, 5, 7, 1600), (torch.bfloat16, 2048, 16, 2, 900),
 ])
 def test_phase1_small(gpu, dtype, D, n, S, rows):

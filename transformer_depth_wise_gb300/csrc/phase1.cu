@@ -211,16 +211,6 @@ cudaError_t launch_phase1(const Phase1Args &a) {
   // one-CTA-per-row kernel spreads wider and is faster.
   if (phase1_tc_supported(a.n, a.D, a.dtype, a.S) && (int64_t)(a.S - 1) * a.rows >= 48 && a.rows >= 512)
     return launch_phase1_tc(a);
-  // Summaries that stay in L2 (decode-sized problems): one aggregation launch
-  // over (row, query) pairs; each summary row comes from HBM once and from L2
-  // for the other queries, and no CTA walks the queries one after another.
-  if ((size_t)a.rows * a.n * a.D * (a.dtype == ATTNRES_BF16 ? 2 : 4) <= ((size_t)48 << 20) &&
-      aggregate_supported(a.D, a.dtype)) {
-    AggregateArgs g{a.blocks, a.n, a.rows, a.D, a.dtype, a.queries, a.gains, nullptr, a.eps, a.out,
-                    a.out_max, a.out_lse, a.stream};
-    g.nq = a.S;
-    return launch_aggregate(g);
-  }
   Cfg c;
   if (!choose(a.n, a.D, a.dtype, c)) return cudaErrorInvalidValue;
   P1Params p;

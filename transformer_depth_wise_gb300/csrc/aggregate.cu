@@ -55,14 +55,6 @@ aggregate_kernel(const __grid_constant__ AggParams p) {
   const int lt = TEAM ? (threadIdx.x % TEAM) : threadIdx.x;
   const int teams_per_cta = TEAM ? blockDim.x / TEAM : 1;
   const int team = TEAM ? threadIdx.x / TEAM : 0;
-  // blockIdx.y picks one of several queries over the same sources (phase 1
-  // of a problem small enough to stay in L2): its query, gain and outputs.
-  const size_t qy = blockIdx.y;
-  const float *qsel = p.q + qy * p.D;
-  const float *gsel = p.g ? p.g + qy * p.D : nullptr;
-  char *osel = static_cast<char *>(p.out) + qy * (size_t)p.rows * p.D * sizeof(T);
-  float *lse_sel = p.out_lse ? p.out_lse + qy * p.rows : nullptr;
-  float *max_sel = p.out_max ? p.out_max + qy * p.rows : nullptr;
 
   // Folded query w~ = w (.) gamma for this thread's elements, as packed
   // pairs (and u).
@@ -80,8 +72,8 @@ aggregate_kernel(const __grid_constant__ AggParams p) {
       float4 w4 = make_float4(0.f, 0.f, 0.f, 0.f), g4 = make_float4(1.f, 1.f, 1.f, 1.f);
       float4 u4 = make_float4(0.f, 0.f, 0.f, 0.f);
       if (valid[k]) {
-        w4 = ld_f4(qsel + j * EPV + e4);
-        if (gsel) g4 = ld_f4(gsel + j * EPV + e4);
+        w4 = ld_f4(p.q + j * EPV + e4);
+        if (p.g) g4 = ld_f4(p.g + j * EPV + e4);
         if (FUSED_F) u4 = ld_f4(p.u + j * EPV + e4);
       }
       qe[k * EPV + e4 + 0] = w4.x * g4.x;
@@ -223,11 +215,11 @@ aggregate_kernel(const __grid_constant__ AggParams p) {
           h[e] = h[e] * inv;
           if (FUSED_F) h[e] = half_tanh(ue[k * EPV + e] * h[e]);
         }
-        st_vec(osel + row_off + (size_t)(lt + k * tpr) * 16, E::pack(h));
+        st_vec(static_cast<char *>(p.out) + row_off + (size_t)(lt + k * tpr) * 16, E::pack(h));
       }
       if (lt == 0) {
-        if (lse_sel) lse_sel[row] = m + logf(den);
-        if (max_sel) max_sel[row] = m;
+        if (p.out_lse) p.out_lse[row] = m + logf(den);
+        if (p.out_max) p.out_max[row] = m;
       }
     }
   }
@@ -262,7 +254,7 @@ bool choose(int D, int dtype, Cfg &c) {
 }
 
 template <typename T, int VPT, int TEAM, bool F>
-cudaError_t run(const AggParams &p, const Cfg &c, cudaStream_t st, int nq) {
+cudaError_t run(const AggParams &p, const Cfg &c, cudaStream_t st) {
   auto kern = aggregate_kernel<T, VPT, TEAM, F>;
   static int occ[16] = {0};  // resident CTAs per SM, per device
   int dev = 0;
@@ -277,18 +269,18 @@ cudaError_t run(const AggParams &p, const Cfg &c, cudaStream_t st, int nq) {
   const int64_t groups = (p.rows + per_cta - 1) / per_cta;
   const int64_t cap = (int64_t)o * sm_count();
   const int grid = (int)(groups < cap ? groups : cap);
-  kern<<<dim3(grid, nq), c.threads, 0, st>>>(p);
+  kern<<<grid, c.threads, 0, st>>>(p);
   return cudaGetLastError();
 }
 
 template <typename T, bool F>
-cudaError_t dispatch(const AggParams &p, const Cfg &c, cudaStream_t st, int nq) {
-  if (c.team == 0) return run<T, 2, 0, F>(p, c, st, nq);
+cudaError_t dispatch(const AggParams &p, const Cfg &c, cudaStream_t st) {
+  if (c.team == 0) return run<T, 2, 0, F>(p, c, st);
   switch (c.team) {
-    case 4: return run<T, 2, 4, F>(p, c, st, nq);
-    case 8: return run<T, 2, 8, F>(p, c, st, nq);
-    case 16: return run<T, 2, 16, F>(p, c, st, nq);
-    default: return run<T, 2, 32, F>(p, c, st, nq);
+    case 4: return run<T, 2, 4, F>(p, c, st);
+    case 8: return run<T, 2, 8, F>(p, c, st);
+    case 16: return run<T, 2, 16, F>(p, c, st);
+    default: return run<T, 2, 32, F>(p, c, st);
   }
 }
 
@@ -320,9 +312,9 @@ cudaError_t launch_aggregate(const AggregateArgs &a) {
   p.prior_lse = a.prior_lse;
   const bool fused = a.u != nullptr;
   if (a.dtype == ATTNRES_BF16)
-    return fused ? dispatch<__nv_bfloat16, true>(p, c, a.stream, a.nq)
-                 : dispatch<__nv_bfloat16, false>(p, c, a.stream, a.nq);
-  return fused ? dispatch<float, true>(p, c, a.stream, a.nq) : dispatch<float, false>(p, c, a.stream, a.nq);
+    return fused ? dispatch<__nv_bfloat16, true>(p, c, a.stream)
+                 : dispatch<__nv_bfloat16, false>(p, c, a.stream);
+  return fused ? dispatch<float, true>(p, c, a.stream) : dispatch<float, false>(p, c, a.stream);
 }
 
 }  // namespace attnres

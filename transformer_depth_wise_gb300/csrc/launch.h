@@ -28,9 +28,6 @@ struct AggregateArgs {
   // partial softmax (then n may be 0): the merge of further sources into it.
   const void *prior_o = nullptr;     // [rows, D]
   const float *prior_lse = nullptr;  // [rows]
-  // nq > 1: nq queries (query/gain rows of D) over the same sources at once,
-  // outputs [nq, rows, D] and stats [nq, rows] (phase 1 of a small problem).
-  int nq = 1;
 };
 // Returns false when D is beyond what the kernel family covers.
 bool aggregate_supported(int D, int dtype);

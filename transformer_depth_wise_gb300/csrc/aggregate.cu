@@ -310,8 +310,7 @@ aggregate_ring_kernel(const __grid_constant__ AggParams p) {
       for (int g = 0; g < G; ++g) {
         int sl = cons_slot + g;
         if (sl >= RING) sl -= RING;
-        // threads past the row's last vector copy nothing: they contribute zeros
-        buf[g] = (g < g_n && valid) ? ring[(size_t)sl * nt + tid] : make_uint4(0u, 0u, 0u, 0u);
+        buf[g] = g < g_n ? ring[(size_t)sl * nt + tid] : make_uint4(0u, 0u, 0u, 0u);
       }
       cons_slot += g_n;
       if (cons_slot >= RING) cons_slot -= RING;

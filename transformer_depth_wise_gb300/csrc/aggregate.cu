@@ -226,162 +226,6 @@ aggregate_kernel(const __grid_constant__ AggParams p) {
 }
 
 // ---------------------------------------------------------------------------
-// Rows owned by a CTA with one 16-byte vector per thread (65..512 vectors):
-// the same online softmax, with the loads decoupled from the reductions.
-// Each thread streams its own vector of every source row into its own slots
-// of a shared-memory ring (cp.async, one commit group per source row), RING
-// source rows ahead along the CTA's (row, source) sequence -- across row
-// boundaries.  A thread only ever reads back its own slots, so waiting on
-// its own copy groups is enough: no barrier guards the ring, and the loads
-// keep running while the CTA reduces a group.  About 128 KB per SM stays in
-// flight, twice what a register-held group allows.
-// ---------------------------------------------------------------------------
-template <typename T, int RING, bool FUSED_F>
-__global__ void __launch_bounds__(512)
-aggregate_ring_kernel(const __grid_constant__ AggParams p) {
-  using E = Elt<T>;
-  using PR = Pairs<T>;
-  constexpr int EPV = E::EPV;
-  constexpr int NP = PR::NP;
-  constexpr int G = kGroup;
-  static_assert(RING > G, "the ring holds more than one group");
-  __shared__ float red[2 * 32 * 2 * G];
-  extern __shared__ uint4 ring[];            // [RING][blockDim.x]
-  const int tid = threadIdx.x, nt = blockDim.x;
-  const bool valid = tid < p.nvec;
-
-  uint64_t qp[NP];
-  float ue[FUSED_F ? EPV : 1];
-  {
-    float qe[EPV];
-#pragma unroll
-    for (int e4 = 0; e4 < EPV; e4 += 4) {
-      float4 w4 = make_float4(0.f, 0.f, 0.f, 0.f), g4 = make_float4(1.f, 1.f, 1.f, 1.f);
-      float4 u4 = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (valid) {
-        w4 = ld_f4(p.q + tid * EPV + e4);
-        if (p.g) g4 = ld_f4(p.g + tid * EPV + e4);
-        if (FUSED_F) u4 = ld_f4(p.u + tid * EPV + e4);
-      }
-      qe[e4 + 0] = w4.x * g4.x; qe[e4 + 1] = w4.y * g4.y; qe[e4 + 2] = w4.z * g4.z; qe[e4 + 3] = w4.w * g4.w;
-      if (FUSED_F) { ue[e4 + 0] = u4.x; ue[e4 + 1] = u4.y; ue[e4 + 2] = u4.z; ue[e4 + 3] = u4.w; }
-    }
-#pragma unroll
-    for (int j = 0; j < NP; ++j) qp[j] = pair(qe[2 * j], qe[2 * j + 1]);
-  }
-
-  const size_t row_bytes = (size_t)p.D * sizeof(T);
-  const int n = p.n;
-  const int64_t my_rows = p.rows > (int64_t)blockIdx.x ? (p.rows - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
-  // The issue cursor walks (row k, source i) with its ring slot; no divisions.
-  int64_t iss_k = 0;
-  int iss_i = 0, iss_slot = 0;
-  auto issue = [&]() {                      // the next position -> its slot (an empty group past the end)
-    if (iss_k < my_rows && valid)
-      cp_async_16(&ring[(size_t)iss_slot * nt + tid],
-                  static_cast<const char *>(p.src[iss_i]) + (size_t)((int64_t)blockIdx.x + iss_k * gridDim.x) * row_bytes +
-                      (size_t)tid * 16);
-    cp_async_commit_group();
-    if (++iss_i == n) { iss_i = 0; ++iss_k; }
-    if (++iss_slot == RING) iss_slot = 0;
-  };
-#pragma unroll 1
-  for (int s = 0; s < RING; ++s) issue();
-
-  int cons_slot = 0;                        // ring slot of the next position to consume
-  int parity = 0;
-  for (int64_t k = 0; k < my_rows; ++k) {
-    const int64_t row = (int64_t)blockIdx.x + k * gridDim.x;
-    const size_t row_off = (size_t)row * row_bytes;
-    uint64_t acc[NP];
-#pragma unroll
-    for (int j = 0; j < NP; ++j) acc[j] = 0ull;
-    float m = -INFINITY, den = 0.f;
-    if (p.prior_o) {  // start from the state (lse, o, 1) of an earlier partial softmax
-      m = p.prior_lse[row];
-      den = 1.f;
-      if (valid) PR::split(ld_stream(static_cast<const char *>(p.prior_o) + row_off + (size_t)tid * 16), acc);
-    }
-    for (int i0 = 0; i0 < n; i0 += G) {
-      const int g_n = n - i0 < G ? n - i0 : G;
-      cp_async_wait_group<RING - G>();      // the next G positions have landed
-      uint4 buf[G];
-#pragma unroll
-      for (int g = 0; g < G; ++g) {
-        int sl = cons_slot + g;
-        if (sl >= RING) sl -= RING;
-        buf[g] = g < g_n ? ring[(size_t)sl * nt + tid] : make_uint4(0u, 0u, 0u, 0u);
-      }
-      cons_slot += g_n;
-      if (cons_slot >= RING) cons_slot -= RING;
-      for (int g = 0; g < g_n; ++g) issue();  // refill the slots just read, RING ahead
-      float part[2 * G];
-#pragma unroll
-      for (int g = 0; g < G; ++g) {
-        uint64_t dot = 0ull, ss = 0ull;
-        uint64_t x[NP];
-        PR::split(buf[g], x);
-#pragma unroll
-        for (int j = 0; j < NP; ++j) {
-          fma_pair(dot, qp[j], x[j]);
-          fma_pair(ss, x[j], x[j]);
-        }
-        part[2 * g] = pair_sum(dot);
-        part[2 * g + 1] = pair_sum(ss);
-      }
-      cta_sum_rs<2 * G>(part, red, parity);
-      parity ^= 1;
-      float s[G];
-      float gmax = -INFINITY;
-#pragma unroll
-      for (int g = 0; g < G; ++g) {
-        s[g] = -INFINITY;
-        if (g < g_n) {
-          s[g] = part[2 * g] * rsqrtf(fmaf(part[2 * g + 1], p.inv_D, p.eps));
-          gmax = fmaxf(gmax, s[g]);
-        }
-      }
-      const float m_new = fmaxf(m, gmax);
-      const float scale = expf(m - m_new);
-      den *= scale;
-      const uint64_t scale2 = pair(scale, scale);
-#pragma unroll
-      for (int j = 0; j < NP; ++j) scale_pair(acc[j], scale2);
-#pragma unroll
-      for (int g = 0; g < G; ++g) {
-        if (g < g_n) {
-          const float w = expf(s[g] - m_new);
-          den += w;
-          const uint64_t w2 = pair(w, w);
-          uint64_t x[NP];
-          PR::split(buf[g], x);
-#pragma unroll
-          for (int j = 0; j < NP; ++j) fma_pair(acc[j], w2, x[j]);
-        }
-      }
-      m = m_new;
-    }
-    if (valid) {
-      const float inv = 1.f / den;
-      float h[EPV];
-#pragma unroll
-      for (int j = 0; j < NP; ++j) unpair(acc[j], h[2 * j], h[2 * j + 1]);
-#pragma unroll
-      for (int e = 0; e < EPV; ++e) {
-        h[e] *= inv;
-        if (FUSED_F) h[e] = half_tanh(ue[e] * h[e]);
-      }
-      st_vec(static_cast<char *>(p.out) + row_off + (size_t)tid * 16, E::pack(h));
-    }
-    if (tid == 0) {
-      if (p.out_lse) p.out_lse[row] = m + logf(den);
-      if (p.out_max) p.out_max[row] = m;
-    }
-  }
-  cp_async_wait_group<0>();
-}
-
-// ---------------------------------------------------------------------------
 // Launch configuration
 // ---------------------------------------------------------------------------
 namespace {
@@ -429,37 +273,8 @@ cudaError_t run(const AggParams &p, const Cfg &c, cudaStream_t st) {
   return cudaGetLastError();
 }
 
-constexpr int kAggRing = 24;   // source rows in flight per thread
-
-template <typename T, bool F>
-cudaError_t run_ring(const AggParams &p, cudaStream_t st) {
-  auto kern = aggregate_ring_kernel<T, kAggRing, F>;
-  const int threads = (p.nvec + 31) / 32 * 32;
-  const size_t smem = (size_t)kAggRing * threads * 16;
-  struct Entry { int dev, threads, occ; };
-  static Entry cache[16];
-  static int used = 0;
-  int dev = 0, o = 0;
-  cudaGetDevice(&dev);
-  for (int i = 0; i < used; ++i)
-    if (cache[i].dev == dev && cache[i].threads == threads) o = cache[i].occ;
-  if (o == 0) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kAggRing * 512 * 16);
-    if (e != cudaSuccess) return e;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, kern, threads, smem);
-    if (e != cudaSuccess) return e;
-    if (o < 1) o = 1;
-    if (used < 16) cache[used++] = {dev, threads, o};
-  }
-  const int64_t cap = (int64_t)o * sm_count();
-  const int grid = (int)(p.rows < cap ? p.rows : cap);
-  kern<<<grid, threads, smem, st>>>(p);
-  return cudaGetLastError();
-}
-
 template <typename T, bool F>
 cudaError_t dispatch(const AggParams &p, const Cfg &c, cudaStream_t st) {
-  if (c.team == 0 && p.nvec <= 512 && p.n > 0) return run_ring<T, F>(p, st);
   if (c.team == 0) return run<T, 2, 0, F>(p, c, st);
   switch (c.team) {
     case 4: return run<T, 2, 4, F>(p, c, st);

@@ -135,20 +135,6 @@ __device__ __forceinline__ void prefetch_l2_bulk(const void *gmem, uint32_t byte
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(gmem), "r"(bytes) : "memory");
 }
 
-// Asynchronous 16-byte global -> shared copy (L2 only), its commit and a
-// wait for all but the N most recent committed groups of this thread.
-__device__ __forceinline__ void cp_async_16(void *smem, const void *gmem) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
-                   static_cast<uint32_t>(__cvta_generic_to_shared(smem))),
-               "l"(gmem)
-               : "memory");
-}
-__device__ __forceinline__ void cp_async_commit_group() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait_group() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-
 // ---------------------------------------------------------------------------
 // Packed fp32 pairs (one 64-bit register, fma.rn.f32x2 = two FMAs per
 // instruction) and the element pairs of a 16-byte vector.

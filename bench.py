@@ -537,10 +537,11 @@ def main():
     args.warmup = max(args.warmup, 3)
     wl = wk.WORKLOADS[args.workload]
 
-    rank, local, world = dist_setup()
-
     if args.impl == "reference":
-        # The reference arm is the fp64 CPU oracle, on rank 0 only.
+        # The reference arm is the fp64 CPU oracle, on rank 0 only; under torchrun the
+        # other ranks exit at once, and no process group is formed for it.
+        rank = int(os.environ.get("RANK", "0"))
+        world = int(os.environ.get("WORLD_SIZE", "1"))
         if rank == 0:
             rates = []
             for _ in range(args.warmup):
@@ -564,6 +565,7 @@ def main():
             print(json.dumps(line), flush=True)
         return
 
+    rank, local, world = dist_setup()
     if not torch.cuda.is_available():
         raise SystemExit("bench.py needs a CUDA GPU (the CUDA path has no CPU fallback)")
     dev = torch.device("cuda", local)

@@ -42,7 +42,6 @@ __global__ void __launch_bounds__(512, 1)
 phase1_kernel(const __grid_constant__ P1Params p) {
   using E = Elt<T>;
   constexpr int EPV = E::EPV;
-  constexpr int NE = VPT * EPV;
   constexpr int NM = kP1MaxN;
   extern __shared__ uint4 stage[];  // [n][VPT][blockDim.x], thread-private slots
   __shared__ float red[2 * 32 * NM];
@@ -74,44 +73,52 @@ phase1_kernel(const __grid_constant__ P1Params p) {
         }
       }
     }
-    cta_sum<NM>(rinv, red, parity);
+    cta_sum_rs<NM>(rinv, red, parity);
     parity ^= 1;
 #pragma unroll
     for (int i = 0; i < NM; ++i) rinv[i] = rsqrtf(fmaf(rinv[i], p.inv_D, p.eps));
 
-    for (int s = 0; s < p.S; ++s) {
-      float qe[NE];
+    // The folded query of query s, as packed pairs; the next query's is
+    // loaded while the current one is formed (its latency is hidden).
+    using PR = Pairs<T>;
+    constexpr int NP = PR::NP;
+    auto load_q = [&](int s, uint64_t (&qp)[VPT * NP]) {
 #pragma unroll
       for (int k = 0; k < VPT; ++k) {
         const int j = tid + k * nt;
 #pragma unroll
         for (int e4 = 0; e4 < EPV; e4 += 4) {
           float4 w4 = make_float4(0.f, 0.f, 0.f, 0.f), g4 = make_float4(1.f, 1.f, 1.f, 1.f);
-          if (valid[k]) {
+          if (valid[k] && s < p.S) {
             w4 = ld_f4(p.q + (size_t)s * p.D + j * EPV + e4);
             if (p.g) g4 = ld_f4(p.g + (size_t)s * p.D + j * EPV + e4);
           }
-          qe[k * EPV + e4 + 0] = w4.x * g4.x;
-          qe[k * EPV + e4 + 1] = w4.y * g4.y;
-          qe[k * EPV + e4 + 2] = w4.z * g4.z;
-          qe[k * EPV + e4 + 3] = w4.w * g4.w;
+          qp[k * NP + e4 / 2] = pair(w4.x * g4.x, w4.y * g4.y);
+          qp[k * NP + e4 / 2 + 1] = pair(w4.z * g4.z, w4.w * g4.w);
         }
       }
+    };
+    uint64_t qcur[VPT * NP], qnext[VPT * NP];
+    load_q(0, qcur);
+    for (int s = 0; s < p.S; ++s) {
+      load_q(s + 1, qnext);
       float dots[NM];
 #pragma unroll
       for (int i = 0; i < NM; ++i) {
         dots[i] = 0.f;
         if (i < p.n) {
+          uint64_t d2 = 0ull;
 #pragma unroll
           for (int k = 0; k < VPT; ++k) {
-            float x[EPV];
-            E::unpack(stage[(i * VPT + k) * nt + tid], x);
+            uint64_t x[NP];
+            PR::split(stage[(i * VPT + k) * nt + tid], x);
 #pragma unroll
-            for (int e = 0; e < EPV; ++e) dots[i] = fmaf(qe[k * EPV + e], x[e], dots[i]);
+            for (int m = 0; m < NP; ++m) fma_pair(d2, qcur[k * NP + m], x[m]);
           }
+          dots[i] = pair_sum(d2);
         }
       }
-      cta_sum<NM>(dots, red, parity);
+      cta_sum_rs<NM>(dots, red, parity);
       parity ^= 1;
       float m = -INFINITY;
 #pragma unroll
@@ -130,25 +137,31 @@ phase1_kernel(const __grid_constant__ P1Params p) {
 #pragma unroll
       for (int k = 0; k < VPT; ++k) {
         if (!valid[k]) continue;
-        float h[EPV];
+        uint64_t h2[NP];
 #pragma unroll
-        for (int e = 0; e < EPV; ++e) h[e] = 0.f;
+        for (int m2 = 0; m2 < NP; ++m2) h2[m2] = 0ull;
 #pragma unroll
         for (int i = 0; i < NM; ++i) {
           if (i < p.n) {
-            float x[EPV];
-            E::unpack(stage[(i * VPT + k) * nt + tid], x);
+            uint64_t x[NP];
+            PR::split(stage[(i * VPT + k) * nt + tid], x);
             const float a = dots[i] * inv;
+            const uint64_t a2 = pair(a, a);
 #pragma unroll
-            for (int e = 0; e < EPV; ++e) h[e] = fmaf(a, x[e], h[e]);
+            for (int m2 = 0; m2 < NP; ++m2) fma_pair(h2[m2], a2, x[m2]);
           }
         }
+        float h[EPV];
+#pragma unroll
+        for (int m2 = 0; m2 < NP; ++m2) unpair(h2[m2], h[2 * m2], h[2 * m2 + 1]);
         st_stream(orow + (size_t)(tid + k * nt) * 16, E::pack(h));
       }
       if (tid == 0) {
         p.out_lse[(size_t)s * p.rows + row] = m + logf(den);
         if (p.out_max) p.out_max[(size_t)s * p.rows + row] = m;
       }
+#pragma unroll
+      for (int j = 0; j < VPT * NP; ++j) qcur[j] = qnext[j];
     }
   }
 }

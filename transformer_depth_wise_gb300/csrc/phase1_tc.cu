@@ -169,19 +169,6 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float *v) {
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-// Packed fp32 pairs (fma.rn.f32x2): two lanes of work per instruction.
-__device__ __forceinline__ uint64_t pk(float lo, float hi) {
-  uint64_t r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
-  return r;
-}
-__device__ __forceinline__ void upk(uint64_t v, float &lo, float &hi) {
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-}
-__device__ __forceinline__ void fma2(uint64_t &acc, uint64_t a, uint64_t x) {
-  asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(a), "l"(x));
-}
-
 // Byte offset of 16-byte chunk `j` of row `r` inside a 1024-byte, 8-row atom
 // written by TMA (or by hand) with the 128-byte swizzle.
 __device__ __forceinline__ uint32_t swz(uint32_t r, uint32_t j) { return r * 128u + ((j ^ (r & 7u)) << 4); }
@@ -509,16 +496,16 @@ __global__ void __launch_bounds__(512, 1) p1_outputs_kernel(const __grid_constan
             const uint64_t a0 = a.x, a1 = a.y;
 #pragma unroll
             for (int m = 0; m < 4; ++m) {
-              fma2(acc0[m], a0, xp[i][m]);
-              fma2(acc1[m], a1, xp[i][m]);
+              fma_pair(acc0[m], a0, xp[i][m]);
+              fma_pair(acc1[m], a1, xp[i][m]);
             }
           }
         }
         float h0[8], h1[8];
 #pragma unroll
         for (int m = 0; m < 4; ++m) {
-          upk(acc0[m], h0[2 * m], h0[2 * m + 1]);
-          upk(acc1[m], h1[2 * m], h1[2 * m + 1]);
+          unpair(acc0[m], h0[2 * m], h0[2 * m + 1]);
+          unpair(acc1[m], h1[2 * m], h1[2 * m + 1]);
         }
         st_stream(dst + (size_t)q * qstride, Elt<__nv_bfloat16>::pack(h0));
         if (q + 1 < S) st_stream(dst + (size_t)(q + 1) * qstride, Elt<__nv_bfloat16>::pack(h1));

@@ -226,6 +226,209 @@ aggregate_kernel(const __grid_constant__ AggParams p) {
 }
 
 // ---------------------------------------------------------------------------
+// Pipelined variant: rows of more than 64 vectors, n >= 1.
+// ---------------------------------------------------------------------------
+// A CTA owns one token row at a time and each thread VPT 16-byte vectors of
+// it.  Sources go in groups of two; the thread's slices of the next group are
+// loaded into a second register set while the current group is reduced and
+// folded in, so loads stay in flight through the arithmetic.  The folded
+// query lives in shared memory (read once per vector for both sources of a
+// group), which leaves the registers to the loads in flight and the
+// accumulator.  The arithmetic is that of aggregate_kernel.
+// TPR > 0: rows that exactly fill a CTA of TPR threads (nvec == TPR * VPT),
+// so the per-vector offsets are constants and every vector is valid.
+template <typename T, bool FUSED_F, int G, int VPT, int TPR>
+__global__ void __launch_bounds__(TPR ? TPR : 256, TPR ? 512 / (TPR ? TPR : 512) : 2)
+aggregate_pipe_kernel(const __grid_constant__ AggParams p) {
+  using E = Elt<T>;
+  constexpr int EPV = E::EPV;
+  static_assert(VPT >= 1 && VPT <= 4, "VPT: 1..4 vectors per thread");
+  using PR = Pairs<T>;
+  constexpr int NP = PR::NP;
+  constexpr int Q4 = EPV / 4;               // float4 of w~ per vector
+  extern __shared__ float4 qs[];            // [Q4][nvec]: w~ = w (.) gamma
+  __shared__ float red[2 * 32 * 2 * G];
+
+  const int tid = threadIdx.x, tpr = TPR ? TPR : blockDim.x;
+  const int nvec = TPR ? TPR * VPT : p.nvec;
+  for (int idx = tid; idx < nvec * Q4; idx += tpr) {
+    const int j = idx / Q4, e4 = (idx % Q4) * 4;
+    const float4 w4 = ld_f4(p.q + j * EPV + e4);
+    const float4 g4 = p.g ? ld_f4(p.g + j * EPV + e4) : make_float4(1.f, 1.f, 1.f, 1.f);
+    qs[(e4 / 4) * nvec + j] = make_float4(w4.x * g4.x, w4.y * g4.y, w4.z * g4.z, w4.w * g4.w);
+  }
+  __syncthreads();
+  bool valid[VPT];
+#pragma unroll
+  for (int k = 0; k < VPT; ++k) valid[k] = TPR ? true : tid + k * tpr < nvec;
+  const float4 *qt = qs + tid;  // this thread's vectors of w~: qt[c * nvec + k * tpr]
+
+  const size_t row_bytes = (size_t)p.D * sizeof(T);
+  const int ngr = (p.n + G - 1) / G;  // groups per row
+  const int64_t my_rows = p.rows > (int64_t)blockIdx.x ? (p.rows - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+  const int64_t total = my_rows * ngr;
+
+  // Loader cursor: the group whose slices are loaded next.
+  int lgi = 0;
+  int64_t lrow = blockIdx.x;
+  auto load_next = [&](uint4 (&buf)[G][VPT]) {
+    const size_t off = (size_t)lrow * row_bytes + (size_t)tid * 16;
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      const int i = lgi * G + g;
+      if (TPR) {
+        const char *base = static_cast<const char *>(p.src[i < p.n ? i : 0]) + off;
+        if (i < p.n) {
+          buf[g][0] = ld_stream_at<0>(base);
+          if (VPT > 1) buf[g][1 % VPT] = ld_stream_at<(TPR ? TPR : 1) * 16>(base);
+          if (VPT > 2) buf[g][2 % VPT] = ld_stream_at<(TPR ? TPR : 1) * 32>(base);
+          if (VPT > 3) buf[g][3 % VPT] = ld_stream_at<(TPR ? TPR : 1) * 48>(base);
+        } else {
+#pragma unroll
+          for (int k = 0; k < VPT; ++k) buf[g][k] = make_uint4(0u, 0u, 0u, 0u);
+        }
+      } else {
+#pragma unroll
+        for (int k = 0; k < VPT; ++k) {
+          buf[g][k] = make_uint4(0u, 0u, 0u, 0u);
+          if (i < p.n && valid[k])
+            buf[g][k] = ld_stream(static_cast<const char *>(p.src[i]) + off + (size_t)k * tpr * 16);
+        }
+      }
+    }
+    if (++lgi == ngr) { lgi = 0; lrow += gridDim.x; }
+  };
+
+  // Processing cursor and the row's online-softmax state.
+  int cgi = 0, parity = 0;
+  int64_t crow = blockIdx.x;
+  float m = -INFINITY, den = 0.f;
+  uint64_t acc[VPT * NP];
+  auto process = [&](const uint4 (&buf)[G][VPT]) {
+    const size_t row_off = (size_t)crow * row_bytes;
+    if (cgi == 0) {  // a new row: empty state, or the prior state (lse, o, 1)
+      m = -INFINITY;
+      den = 0.f;
+#pragma unroll
+      for (int j = 0; j < VPT * NP; ++j) acc[j] = 0ull;
+      if (p.prior_o) {
+        m = p.prior_lse[crow];
+        den = 1.f;
+#pragma unroll
+        for (int k = 0; k < VPT; ++k)
+          if (valid[k])
+            PR::split(ld_stream(static_cast<const char *>(p.prior_o) + row_off + (size_t)(tid + k * tpr) * 16),
+                      acc + k * NP);
+      }
+    }
+    const int i0 = cgi * G;
+    uint64_t dot[G], ss[G];
+#pragma unroll
+    for (int g = 0; g < G; ++g) dot[g] = ss[g] = 0ull;
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+      if (!valid[k]) continue;
+      uint64_t qp[NP];
+#pragma unroll
+      for (int c = 0; c < Q4; ++c) {
+        const float4 q4 = qt[c * nvec + k * tpr];
+        qp[2 * c] = pair(q4.x, q4.y);
+        qp[2 * c + 1] = pair(q4.z, q4.w);
+      }
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        uint64_t x[NP];
+        PR::split(buf[g][k], x);
+#pragma unroll
+        for (int j = 0; j < NP; ++j) {
+          fma_pair(dot[g], qp[j], x[j]);
+          fma_pair(ss[g], x[j], x[j]);
+        }
+      }
+    }
+    float part[2 * G];
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      part[2 * g] = pair_sum(dot[g]);
+      part[2 * g + 1] = pair_sum(ss[g]);
+    }
+    cta_sum_rs<2 * G>(part, red, parity);
+    parity ^= 1;
+    float s[G];
+    float gmax = -INFINITY;
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      s[g] = -INFINITY;
+      if (i0 + g < p.n) {
+        s[g] = part[2 * g] * rsqrtf(fmaf(part[2 * g + 1], p.inv_D, p.eps));
+        gmax = fmaxf(gmax, s[g]);
+      }
+    }
+    const float m_new = fmaxf(m, gmax);
+    const float scale = expf(m - m_new);  // 0 on a row's first group without a prior (m = -inf)
+    den *= scale;
+    const uint64_t scale2 = pair(scale, scale);
+#pragma unroll
+    for (int j = 0; j < VPT * NP; ++j) scale_pair(acc[j], scale2);
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      if (i0 + g < p.n) {
+        const float w = expf(s[g] - m_new);
+        den += w;
+        const uint64_t w2 = pair(w, w);
+#pragma unroll
+        for (int k = 0; k < VPT; ++k) {
+          uint64_t x[NP];
+          PR::split(buf[g][k], x);
+#pragma unroll
+          for (int j = 0; j < NP; ++j) fma_pair(acc[k * NP + j], w2, x[j]);
+        }
+      }
+    }
+    m = m_new;
+    if (cgi == ngr - 1) {  // the row's last group: normalise and store
+      const float inv = 1.f / den;
+#pragma unroll
+      for (int k = 0; k < VPT; ++k) {
+        if (!valid[k]) continue;
+        const int j = tid + k * tpr;
+        float h[EPV];
+#pragma unroll
+        for (int jj = 0; jj < NP; ++jj) unpair(acc[k * NP + jj], h[2 * jj], h[2 * jj + 1]);
+#pragma unroll
+        for (int e4 = 0; e4 < EPV; e4 += 4) {
+          float4 u4 = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (FUSED_F) u4 = ld_f4(p.u + j * EPV + e4);
+          const float uu[4] = {u4.x, u4.y, u4.z, u4.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            h[e4 + e] *= inv;
+            if (FUSED_F) h[e4 + e] = half_tanh(uu[e] * h[e4 + e]);
+          }
+        }
+        st_vec(static_cast<char *>(p.out) + row_off + (size_t)j * 16, E::pack(h));
+      }
+      if (tid == 0) {
+        if (p.out_lse) p.out_lse[crow] = m + logf(den);
+        if (p.out_max) p.out_max[crow] = m;
+      }
+    }
+    if (++cgi == ngr) { cgi = 0; crow += gridDim.x; }
+  };
+
+  // Two register sets in turn: group q + 1 loads while group q is processed.
+  uint4 ba[G][VPT], bb[G][VPT];
+  if (total > 0) load_next(ba);
+  for (int64_t q = 0; q < total; q += 2) {
+    if (q + 1 < total) load_next(bb);
+    process(ba);
+    if (q + 1 >= total) break;
+    if (q + 2 < total) load_next(ba);
+    process(bb);
+  }
+}
+
+// ---------------------------------------------------------------------------
 // Launch configuration
 // ---------------------------------------------------------------------------
 namespace {
@@ -284,6 +487,81 @@ cudaError_t dispatch(const AggParams &p, const Cfg &c, cudaStream_t st) {
   }
 }
 
+// The pipelined kernel: n >= 1 sources and rows of more than 64 vectors (the
+// lane-team kernel takes shorter rows; a prior state with no further source
+// goes to aggregate_kernel).  Two shapes, measured on a GB300 for D = 2048:
+// groups of 2 sources with 4 vectors per thread (64-thread CTAs for D =
+// 2048) win once there are rows enough for every CTA of the grid to take
+// several (from 32 rows per SM; e.g. 5.5 against 5.1 TB/s at 16384 rows and
+// n = 10), groups of 4 with 2 vectors per thread (twice the threads per row)
+// below that (e.g. 4.2 against 4.0 TB/s at 2048 rows and n = 187).  A CTA
+// of ceil(nvec / vpt) threads, rounded up to whole warps, per row; rows that
+// fill it exactly take the kernel with that thread count built in.
+struct PipeCfg {
+  int g, vpt, threads;
+  int tpr;  // the built-in thread count, or 0 (general kernel)
+};
+
+bool choose_pipe(int n, int64_t rows, int D, int dtype, PipeCfg &c) {
+  const int nvec = D / epv_of(dtype);
+  if (n < 1 || nvec <= 64) return false;
+  auto threads_for = [&](int vpt) { return ((nvec + vpt - 1) / vpt + 31) / 32 * 32; };
+  const bool many_rows = rows >= 32 * (int64_t)sm_count();
+  if (!many_rows && threads_for(2) <= 256) {
+    c.g = 4;
+    c.vpt = 2;
+  } else {
+    c.g = 2;
+    c.vpt = 4;
+  }
+  c.threads = threads_for(c.vpt);
+  if (c.threads > 256) return false;
+  const bool exact = nvec == c.threads * c.vpt;
+  c.tpr = 0;
+  if (exact) {
+    const int built[] = {64, 128, 256};
+    for (int b : built)
+      if (b == c.threads) c.tpr = b;
+  }
+  return true;
+}
+
+template <typename T, bool F, int G, int VPT, int TPR>
+cudaError_t run_pipe(const AggParams &p, int threads, cudaStream_t st) {
+  auto kern = aggregate_pipe_kernel<T, F, G, VPT, TPR>;
+  const size_t smem = (size_t)p.D * sizeof(float);  // w~
+  if (smem > 48 * 1024) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+  }
+  int occ = 0;
+  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, threads, smem);
+  if (e != cudaSuccess) return e;
+  if (occ < 1) occ = 1;
+  const int64_t cap = (int64_t)occ * sm_count();
+  const int grid = (int)(p.rows < cap ? p.rows : cap);
+  kern<<<grid, threads, smem, st>>>(p);
+  return cudaGetLastError();
+}
+
+template <typename T, bool F>
+cudaError_t dispatch_pipe(const AggParams &p, const PipeCfg &c, cudaStream_t st) {
+  if (c.g == 4) {
+    switch (c.tpr) {
+      case 64: return run_pipe<T, F, 4, 2, 64>(p, c.threads, st);
+      case 128: return run_pipe<T, F, 4, 2, 128>(p, c.threads, st);
+      case 256: return run_pipe<T, F, 4, 2, 256>(p, c.threads, st);
+      default: return run_pipe<T, F, 4, 2, 0>(p, c.threads, st);
+    }
+  }
+  switch (c.tpr) {
+    case 64: return run_pipe<T, F, 2, 4, 64>(p, c.threads, st);
+    case 128: return run_pipe<T, F, 2, 4, 128>(p, c.threads, st);
+    case 256: return run_pipe<T, F, 2, 4, 256>(p, c.threads, st);
+    default: return run_pipe<T, F, 2, 4, 0>(p, c.threads, st);
+  }
+}
+
 }  // namespace
 
 bool aggregate_supported(int D, int dtype) {
@@ -311,6 +589,13 @@ cudaError_t launch_aggregate(const AggregateArgs &a) {
   p.prior_o = a.prior_o;
   p.prior_lse = a.prior_lse;
   const bool fused = a.u != nullptr;
+  PipeCfg pc;
+  if (choose_pipe(a.n, a.rows, a.D, a.dtype, pc)) {
+    if (a.dtype == ATTNRES_BF16)
+      return fused ? dispatch_pipe<__nv_bfloat16, true>(p, pc, a.stream)
+                   : dispatch_pipe<__nv_bfloat16, false>(p, pc, a.stream);
+    return fused ? dispatch_pipe<float, true>(p, pc, a.stream) : dispatch_pipe<float, false>(p, pc, a.stream);
+  }
   if (a.dtype == ATTNRES_BF16)
     return fused ? dispatch<__nv_bfloat16, true>(p, c, a.stream)
                  : dispatch<__nv_bfloat16, false>(p, c, a.stream);

@@ -72,6 +72,16 @@ __device__ __forceinline__ uint4 ld_stream(const void *p) {
   return v;
 }
 
+// The same at a constant byte offset from `p`, folded into the instruction.
+template <int OFF>
+__device__ __forceinline__ uint4 ld_stream_at(const void *p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4+%5];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p), "n"(OFF));
+  return v;
+}
+
 // Plain 16-byte load through L1 (small, reused operands: queries, gains, u).
 __device__ __forceinline__ float4 ld_f4(const float *p) {
   return __ldg(reinterpret_cast<const float4 *>(p));

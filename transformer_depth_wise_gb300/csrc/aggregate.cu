@@ -276,24 +276,11 @@ aggregate_pipe_kernel(const __grid_constant__ AggParams p) {
 #pragma unroll
     for (int g = 0; g < G; ++g) {
       const int i = lgi * G + g;
-      if (TPR) {
-        const char *base = static_cast<const char *>(p.src[i < p.n ? i : 0]) + off;
-        if (i < p.n) {
-          buf[g][0] = ld_stream_at<0>(base);
-          if (VPT > 1) buf[g][1 % VPT] = ld_stream_at<(TPR ? TPR : 1) * 16>(base);
-          if (VPT > 2) buf[g][2 % VPT] = ld_stream_at<(TPR ? TPR : 1) * 32>(base);
-          if (VPT > 3) buf[g][3 % VPT] = ld_stream_at<(TPR ? TPR : 1) * 48>(base);
-        } else {
+      const char *base = static_cast<const char *>(p.src[i < p.n ? i : 0]) + off;
 #pragma unroll
-          for (int k = 0; k < VPT; ++k) buf[g][k] = make_uint4(0u, 0u, 0u, 0u);
-        }
-      } else {
-#pragma unroll
-        for (int k = 0; k < VPT; ++k) {
-          buf[g][k] = make_uint4(0u, 0u, 0u, 0u);
-          if (i < p.n && valid[k])
-            buf[g][k] = ld_stream(static_cast<const char *>(p.src[i]) + off + (size_t)k * tpr * 16);
-        }
+      for (int k = 0; k < VPT; ++k) {
+        buf[g][k] = make_uint4(0u, 0u, 0u, 0u);
+        if (i < p.n && valid[k]) buf[g][k] = ld_stream_vec<TPR>(base, k, tpr);
       }
     }
     if (++lgi == ngr) { lgi = 0; lrow += gridDim.x; }

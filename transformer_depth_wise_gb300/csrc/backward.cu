@@ -54,9 +54,11 @@ __device__ __forceinline__ float lanes_max(float v) {
 }
 
 // TEAM > 0: TEAM lanes of a warp own a row (kBwdTeams rows per CTA).
-// TEAM == 0: the whole CTA owns a row.
-template <typename T, int VPT, int TEAM>
-__global__ void __launch_bounds__(TEAM ? kBwdTeams * TEAM : 512)
+// TEAM == 0: the whole CTA owns a row; with TPR > 0 rows that exactly fill a
+// CTA of TPR threads (nvec == TPR * VPT), so the per-vector offsets are
+// constants and every vector is valid.
+template <typename T, int VPT, int TEAM, int TPR>
+__global__ void __launch_bounds__(TEAM ? kBwdTeams * TEAM : (TPR ? TPR : 512), TPR ? 512 / (TPR ? TPR : 512) : 1)
 aggregate_backward_kernel(const __grid_constant__ BwdParams p) {
   using E = Elt<T>;
   constexpr int EPV = E::EPV;
@@ -68,7 +70,8 @@ aggregate_backward_kernel(const __grid_constant__ BwdParams p) {
   __shared__ float red[TEAM ? 1 : 2 * 32 * KR];
   __shared__ float coef[TPC][kMaxSources][3];
 
-  const int tpr = TEAM ? TEAM : blockDim.x;
+  static_assert(TPR == 0 || TEAM == 0, "a built-in thread count is for CTA teams");
+  const int tpr = TPR ? TPR : (TEAM ? TEAM : blockDim.x);
   const int lt = TEAM ? (threadIdx.x % TEAM) : threadIdx.x;
   const int team = TEAM ? threadIdx.x / TEAM : 0;
   float(*cf)[3] = coef[team];
@@ -78,7 +81,7 @@ aggregate_backward_kernel(const __grid_constant__ BwdParams p) {
 #pragma unroll
   for (int k = 0; k < VPT; ++k) {
     const int j = lt + k * tpr;
-    valid[k] = j < p.nvec;
+    valid[k] = TPR ? true : j < p.nvec;
 #pragma unroll
     for (int e4 = 0; e4 < EPV; e4 += 4) {
       float4 w4 = make_float4(0.f, 0.f, 0.f, 0.f), g4 = make_float4(1.f, 1.f, 1.f, 1.f);
@@ -111,12 +114,12 @@ aggregate_backward_kernel(const __grid_constant__ BwdParams p) {
     const bool row_ok = row < p.rows;
     const size_t row_off = (size_t)row * row_bytes;
 
+    const size_t thr_off = row_off + (size_t)lt * 16;  // this thread's first vector of the row
     uint64_t gp[VPT * NP];  // dh of this row, as pairs
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
       uint4 x = make_uint4(0u, 0u, 0u, 0u);
-      if (row_ok && valid[k])
-        x = ld_stream(static_cast<const char *>(p.dh) + row_off + (size_t)(lt + k * tpr) * 16);
+      if (row_ok && valid[k]) x = ld_stream_vec<TPR>(static_cast<const char *>(p.dh) + thr_off, k, tpr);
       PR::split(x, gp + k * NP);
     }
 
@@ -129,8 +132,7 @@ aggregate_backward_kernel(const __grid_constant__ BwdParams p) {
         for (int k = 0; k < VPT; ++k) {
           v[j][k] = make_uint4(0u, 0u, 0u, 0u);
           if (i0 + j < p.n && row_ok && valid[k])
-            v[j][k] = ld_stream(static_cast<const char *>(p.src[i0 + j]) + row_off +
-                                (size_t)(lt + k * tpr) * 16);
+            v[j][k] = ld_stream_vec<TPR>(static_cast<const char *>(p.src[i0 + j]) + thr_off, k, tpr);
         }
       float part[KR];
 #pragma unroll
@@ -214,9 +216,10 @@ aggregate_backward_kernel(const __grid_constant__ BwdParams p) {
         for (int k = 0; k < VPT; ++k) {
           v[j][k] = din[j][k] = make_uint4(0u, 0u, 0u, 0u);
           if (i0 + j < p.n && row_ok && valid[k]) {
-            const size_t off = row_off + (size_t)(lt + k * tpr) * 16;
-            v[j][k] = ld_stream(static_cast<const char *>(p.src[i0 + j]) + off);
-            if (p.accumulate) din[j][k] = *reinterpret_cast<const uint4 *>(static_cast<const char *>(p.dsrc[i0 + j]) + off);
+            v[j][k] = ld_stream_vec<TPR>(static_cast<const char *>(p.src[i0 + j]) + thr_off, k, tpr);
+            if (p.accumulate)
+              din[j][k] = *reinterpret_cast<const uint4 *>(static_cast<const char *>(p.dsrc[i0 + j]) + thr_off +
+                                                           (size_t)k * tpr * 16);
           }
         }
 #pragma unroll
@@ -246,7 +249,7 @@ aggregate_backward_kernel(const __grid_constant__ BwdParams p) {
 #pragma unroll
             for (int e = 0; e < EPV; ++e) o[e] += w[e];
           }
-          st_vec(static_cast<char *>(p.dsrc[i0 + j]) + row_off + (size_t)(lt + k * tpr) * 16, E::pack(o));
+          st_vec(static_cast<char *>(p.dsrc[i0 + j]) + thr_off + (size_t)k * tpr * 16, E::pack(o));
         }
       }
     }
@@ -298,6 +301,7 @@ int epv_of(int dtype) { return dtype == ATTNRES_BF16 ? 8 : 4; }
 
 struct Cfg {
   int team, threads;
+  int tpr;  // CTA teams: the built-in thread count (rows that fill the CTA exactly), or 0
 };
 
 bool choose(int D, int dtype, Cfg &c) {
@@ -305,25 +309,27 @@ bool choose(int D, int dtype, Cfg &c) {
   if (nvec <= 64) {
     int need = (nvec + 1) / 2, team = 4;
     while (team < need) team *= 2;
-    c = {team, kBwdTeams * team};
+    c = {team, kBwdTeams * team, 0};
     return true;
   }
   if (nvec <= 1024) {
-    c = {0, ((nvec + 1) / 2 + 31) / 32 * 32};
+    const int threads = ((nvec + 1) / 2 + 31) / 32 * 32;
+    const bool exact = nvec == 2 * threads;
+    c = {0, threads, exact && (threads == 64 || threads == 128 || threads == 256) ? threads : 0};
     return true;
   }
   return false;
 }
 
 // Resident CTAs per SM of one instantiation on the current device.
-template <typename T, int TEAM>
+template <typename T, int TEAM, int TPR>
 cudaError_t occupancy(const Cfg &c, int &o) {
   static int occ[16] = {0};
   int dev = 0;
   cudaGetDevice(&dev);
   int &slot = occ[dev & 15];
   if (slot == 0) {
-    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&slot, aggregate_backward_kernel<T, 2, TEAM>,
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&slot, aggregate_backward_kernel<T, 2, TEAM, TPR>,
                                                                   c.threads, 0);
     if (e != cudaSuccess) return e;
     if (slot < 1) slot = 1;
@@ -332,11 +338,11 @@ cudaError_t occupancy(const Cfg &c, int &o) {
   return cudaSuccess;
 }
 
-template <typename T, int TEAM>
+template <typename T, int TEAM, int TPR>
 cudaError_t run(const BwdParams &p0, const AggregateBackwardArgs &a, const Cfg &c) {
   constexpr int TPC = TEAM ? kBwdTeams : 1;
   int o = 0;
-  cudaError_t e = occupancy<T, TEAM>(c, o);
+  cudaError_t e = occupancy<T, TEAM, TPR>(c, o);
   if (e != cudaSuccess) return e;
   BwdParams p = p0;
   const int64_t groups = (a.rows + TPC - 1) / TPC;
@@ -344,7 +350,7 @@ cudaError_t run(const BwdParams &p0, const AggregateBackwardArgs &a, const Cfg &
   if (groups < grid) grid = groups;
   if (p.ws && a.workspace_rows / TPC < grid) grid = a.workspace_rows / TPC;
   if (grid < 1) return cudaErrorInvalidValue;
-  aggregate_backward_kernel<T, 2, TEAM><<<(int)grid, c.threads, 0, a.stream>>>(p);
+  aggregate_backward_kernel<T, 2, TEAM, TPR><<<(int)grid, c.threads, 0, a.stream>>>(p);
   e = cudaGetLastError();
   if (e != cudaSuccess || !p.ws) return e;
   aggregate_backward_reduce_kernel<<<(a.D + 31) / 32, 256, 0, a.stream>>>(
@@ -355,11 +361,17 @@ cudaError_t run(const BwdParams &p0, const AggregateBackwardArgs &a, const Cfg &
 template <typename T>
 cudaError_t dispatch(const BwdParams &p, const AggregateBackwardArgs &a, const Cfg &c) {
   switch (c.team) {
-    case 0: return run<T, 0>(p, a, c);
-    case 4: return run<T, 4>(p, a, c);
-    case 8: return run<T, 8>(p, a, c);
-    case 16: return run<T, 16>(p, a, c);
-    default: return run<T, 32>(p, a, c);
+    case 0:
+      switch (c.tpr) {
+        case 64: return run<T, 0, 64>(p, a, c);
+        case 128: return run<T, 0, 128>(p, a, c);
+        case 256: return run<T, 0, 256>(p, a, c);
+        default: return run<T, 0, 0>(p, a, c);
+      }
+    case 4: return run<T, 4, 0>(p, a, c);
+    case 8: return run<T, 8, 0>(p, a, c);
+    case 16: return run<T, 16, 0>(p, a, c);
+    default: return run<T, 32, 0>(p, a, c);
   }
 }
 
@@ -368,11 +380,18 @@ cudaError_t rows_for(const Cfg &c, int64_t &rows) {
   int o = 0;
   cudaError_t e = cudaSuccess;
   switch (c.team) {
-    case 0: e = occupancy<T, 0>(c, o); break;
-    case 4: e = occupancy<T, 4>(c, o); break;
-    case 8: e = occupancy<T, 8>(c, o); break;
-    case 16: e = occupancy<T, 16>(c, o); break;
-    default: e = occupancy<T, 32>(c, o); break;
+    case 0:
+      switch (c.tpr) {
+        case 64: e = occupancy<T, 0, 64>(c, o); break;
+        case 128: e = occupancy<T, 0, 128>(c, o); break;
+        case 256: e = occupancy<T, 0, 256>(c, o); break;
+        default: e = occupancy<T, 0, 0>(c, o); break;
+      }
+      break;
+    case 4: e = occupancy<T, 4, 0>(c, o); break;
+    case 8: e = occupancy<T, 8, 0>(c, o); break;
+    case 16: e = occupancy<T, 16, 0>(c, o); break;
+    default: e = occupancy<T, 32, 0>(c, o); break;
   }
   rows = (int64_t)o * sm_count() * (c.team ? kBwdTeams : 1);
   return e;

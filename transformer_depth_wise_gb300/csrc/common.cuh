@@ -82,6 +82,23 @@ __device__ __forceinline__ uint4 ld_stream_at(const void *p) {
   return v;
 }
 
+// Vector k (0..3) of a thread's slice of a row: `base` points at the thread's
+// first vector and the slice's vectors lie tpr * 16 bytes apart.  With the
+// thread count TPR built in, the offset is folded into the load; in unrolled
+// loops k is a constant and the switch disappears.
+template <int TPR>
+__device__ __forceinline__ uint4 ld_stream_vec(const char *base, int k, int tpr) {
+  if (TPR > 0) {
+    switch (k) {
+      case 0: return ld_stream_at<0>(base);
+      case 1: return ld_stream_at<TPR * 16>(base);
+      case 2: return ld_stream_at<TPR * 32>(base);
+      default: return ld_stream_at<TPR * 48>(base);
+    }
+  }
+  return ld_stream(base + (size_t)k * tpr * 16);
+}
+
 // Plain 16-byte load through L1 (small, reused operands: queries, gains, u).
 __device__ __forceinline__ float4 ld_f4(const float *p) {
   return __ldg(reinterpret_cast<const float4 *>(p));

@@ -456,15 +456,19 @@ def run_single(args, wl, dev, world):
     ms = statistics.median(times)
     peak, src = measured_peak()
     gbs = byts / (ms * 1e-3) / 1e9
+    n_src = len(inp["sources"])
+    del inp, out, flush
+    backward = run_backward(dev) if wl.name == "block_single_bf16" and not args.rows else None
     return {"metric": "depth aggregation tokens/s", "value": round(rows / (ms * 1e-3), 1),
             "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16" if wl.dtype == torch.bfloat16 else "f32",
             "data": "synthetic", "config": {"workload": wl.name, "rows": rows, "D": wl.D,
-                                            "n": len(inp["sources"]), "l2": "flushed between launches"},
+                                            "n": n_src, "l2": "flushed between launches"},
             "roofline": {"bound": "hbm", "kernel": "aggregate", "achieved": round(gbs, 1),
                          "peak": peak, "unit": "GB/s", "frac": round(gbs / peak, 4),
-                         "traffic": None, "peak_source": src}}
+                         "traffic": None, "peak_source": src},
+            "backward": backward}
 
 
 def run_full_stack(args, wl, dev, world):

@@ -109,6 +109,10 @@ aggregate_backward_kernel(const __grid_constant__ BwdParams p) {
   const size_t row_bytes = (size_t)p.nvec * 16;
   const int64_t groups = (p.rows + TPC - 1) / TPC;
   int parity = 0;
+  // Pass A's reads of the sources are read again by pass B a few
+  // microseconds later: they stay in L2 (evict_last); pass B's reads and the
+  // gradients it writes are last uses (evict_first).
+  const uint64_t keep = l2_policy_keep(), drop = l2_policy_drop();
   for (int64_t rg = blockIdx.x; rg < groups; rg += gridDim.x) {
     const int64_t row = rg * TPC + team;
     const bool row_ok = row < p.rows;
@@ -132,7 +136,7 @@ aggregate_backward_kernel(const __grid_constant__ BwdParams p) {
         for (int k = 0; k < VPT; ++k) {
           v[j][k] = make_uint4(0u, 0u, 0u, 0u);
           if (i0 + j < p.n && row_ok && valid[k])
-            v[j][k] = ld_stream_vec<TPR>(static_cast<const char *>(p.src[i0 + j]) + thr_off, k, tpr);
+            v[j][k] = ld_hint_vec<TPR>(static_cast<const char *>(p.src[i0 + j]) + thr_off, k, tpr, keep);
         }
       float part[KR];
 #pragma unroll
@@ -216,7 +220,7 @@ aggregate_backward_kernel(const __grid_constant__ BwdParams p) {
         for (int k = 0; k < VPT; ++k) {
           v[j][k] = din[j][k] = make_uint4(0u, 0u, 0u, 0u);
           if (i0 + j < p.n && row_ok && valid[k]) {
-            v[j][k] = ld_stream_vec<TPR>(static_cast<const char *>(p.src[i0 + j]) + thr_off, k, tpr);
+            v[j][k] = ld_hint_vec<TPR>(static_cast<const char *>(p.src[i0 + j]) + thr_off, k, tpr, drop);
             if (p.accumulate)
               din[j][k] = *reinterpret_cast<const uint4 *>(static_cast<const char *>(p.dsrc[i0 + j]) + thr_off +
                                                            (size_t)k * tpr * 16);
@@ -249,7 +253,7 @@ aggregate_backward_kernel(const __grid_constant__ BwdParams p) {
 #pragma unroll
             for (int e = 0; e < EPV; ++e) o[e] += w[e];
           }
-          st_vec(static_cast<char *>(p.dsrc[i0 + j]) + thr_off + (size_t)k * tpr * 16, E::pack(o));
+          st_hint(static_cast<char *>(p.dsrc[i0 + j]) + thr_off + (size_t)k * tpr * 16, E::pack(o), drop);
         }
       }
     }

@@ -82,6 +82,54 @@ __device__ __forceinline__ uint4 ld_stream_at(const void *p) {
   return v;
 }
 
+// L2 eviction policies (createpolicy, sm_80+) for loads and stores with an
+// explicit cache hint: data read again soon is kept (evict_last), data used
+// for the last time goes first (evict_first).
+__device__ __forceinline__ uint64_t l2_policy_keep() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ uint64_t l2_policy_drop() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+// 16-byte read-only load, no L1 allocation, with an L2 policy.
+__device__ __forceinline__ uint4 ld_hint(const void *p, uint64_t policy) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p), "l"(policy));
+  return v;
+}
+template <int OFF>
+__device__ __forceinline__ uint4 ld_hint_at(const void *p, uint64_t policy) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4+%5], %6;"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p), "n"(OFF), "l"(policy));
+  return v;
+}
+// 16-byte store with an L2 policy.
+__device__ __forceinline__ void st_hint(void *p, const uint4 &v, uint64_t policy) {
+  asm volatile("st.global.L2::cache_hint.v4.u32 [%0], {%1,%2,%3,%4}, %5;"
+               :: "l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "l"(policy) : "memory");
+}
+// Vector k (0..3) of a thread's slice with an L2 policy (as ld_stream_vec).
+template <int TPR>
+__device__ __forceinline__ uint4 ld_hint_vec(const char *base, int k, int tpr, uint64_t policy) {
+  if (TPR > 0) {
+    switch (k) {
+      case 0: return ld_hint_at<0>(base, policy);
+      case 1: return ld_hint_at<TPR * 16>(base, policy);
+      case 2: return ld_hint_at<TPR * 32>(base, policy);
+      default: return ld_hint_at<TPR * 48>(base, policy);
+    }
+  }
+  return ld_hint(base + (size_t)k * tpr * 16, policy);
+}
+
 // Vector k (0..3) of a thread's slice of a row: `base` points at the thread's
 // first vector and the slice's vectors lie tpr * 16 bytes apart.  With the
 // thread count TPR built in, the offset is folded into the load; in unrolled

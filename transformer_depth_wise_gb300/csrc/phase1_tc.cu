@@ -244,29 +244,37 @@ __global__ void __launch_bounds__(kThreadsA, 1) p1_scores_kernel(const __grid_co
   const int KC = p.D / kKc;
 
   if (warp == 4) {
-    // ---------------- TMA producer: (tile, summary, chunk) stages ----------------
+    // ---------------- TMA producers: (tile, summary, chunk) stages ----------------
     // Each stage carries 64 features of one summary for the tile's 128 rows
     // and the same 64 features of the query parts.  Walking the features of
     // one summary in order keeps consecutive stages on neighbouring bytes.
-    if (lane == 0) {
-      int64_t g = 0;
+    // The bulk copies one thread issues complete one after another (about
+    // 0.4 us each on GB300, whatever their size), so every stage has a
+    // producer lane of its own: lane s issues each use of stage s.  All lanes
+    // walk the same sequence; the stage's empty barrier orders its uses.
+    if (lane < kStages) {
+      int64_t g = 0, last = -1;
+      int s = 0;  // g % kStages
       for (int64_t tl = 0; tl < my_tiles; ++tl) {
         int64_t tile;
         int i0, nc;
         item_of(tl, tile, i0, nc);
         for (int i = 0; i < nc; ++i)
           for (int kc = 0; kc < KC; ++kc, ++g) {
-            const int s = (int)(g % kStages);
-            if (g >= kStages) wait_local(VEMPTY(s), (uint32_t)((g / kStages - 1) & 1));
-            mbar_expect_tx(VFULL(s), kStageBytes);
-            const uint32_t st = base + (uint32_t)s * kStageBytes;
-            tma_load_2d(st, &p.tmap[i0 + i], kc * kKc, (int)(tile * kRows), VFULL(s));
-            tma_load_2d(st + kVBytes, &p.qmap, kc * kKc, 0, VFULL(s));
+            if (s == lane) {
+              if (g >= kStages) wait_local(VEMPTY(s), (uint32_t)((g / kStages - 1) & 1));
+              mbar_expect_tx(VFULL(s), kStageBytes);
+              const uint32_t st = base + (uint32_t)s * kStageBytes;
+              tma_load_2d(st, &p.tmap[i0 + i], kc * kKc, (int)(tile * kRows), VFULL(s));
+              tma_load_2d(st + kVBytes, &p.qmap, kc * kKc, 0, VFULL(s));
+              last = g;
+            }
+            if (++s == kStages) s = 0;
           }
       }
-      // the last stages have landed before the CTA may exit
-      for (int64_t k = g - kStages < 0 ? 0 : g - kStages; k < g; ++k)
-        wait_local(VFULL((int)(k % kStages)), (uint32_t)((k / kStages) & 1));
+      // this lane's last stage has landed before the CTA may exit (its
+      // earlier uses were consumed before the stage was refilled)
+      if (last >= 0) wait_local(VFULL(lane), (uint32_t)((last / kStages) & 1));
     }
   } else if (warp == 5) {
     // ---------------- MMA issuer ----------------
@@ -435,12 +443,17 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 template <int N>
 __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" :: "n"(N) : "memory"); }
 
-template <int PARTS>
+// NS, SQ > 0: the number of summaries and of queries built in (the loops
+// over them unroll fully and every alpha load has a constant offset);
+// 0: taken from the parameters.
+template <int PARTS, int NS, int SQ>
 __global__ void __launch_bounds__(512, 1) p1_outputs_kernel(const __grid_constant__ ParamsB p) {
   extern __shared__ uint4 vbuf[];                     // [kBStages][n][nvp] 16-byte chunks
   __shared__ __align__(16) float alpha[kBStages][2 * kMaxN * kMaxS];   // [n][Sp][2]
+  static_assert(NS <= kMaxN && SQ <= kMaxS, "built-in shape within the kernel's limits");
+  constexpr int kQUnroll = 1;  // unrolling the query pairs spills at 128 registers
   const int tid = threadIdx.x;
-  const int n = p.n, S = p.S, nvp = p.nvp;
+  const int n = NS ? NS : p.n, S = SQ ? SQ : p.S, nvp = p.nvp;
   constexpr int parts = PARTS;
   const size_t row_bytes = (size_t)p.D * 2;
   // Items are (token, piece), the pieces of a token consecutive on the same
@@ -486,6 +499,7 @@ __global__ void __launch_bounds__(512, 1) p1_outputs_kernel(const __grid_constan
       // alpha came with the token's first piece (k - part); the stages in
       // between carry no alpha, so its buffer is intact
       const float *al = alpha[(k - part) % kBStages];
+#pragma unroll kQUnroll
       for (int q = 0; q < S; q += 2) {              // queries in pairs
         uint64_t acc0[4] = {0, 0, 0, 0}, acc1[4] = {0, 0, 0, 0};
 #pragma unroll
@@ -867,7 +881,11 @@ cudaError_t launch_phase1_tc(const Phase1Args &a) {
   pb.nvp = pb.nvec / pb.parts;
   const int threads = (pb.nvp + 31) / 32 * 32;
   const size_t smem = smem_b(a.n, a.D / pb.parts);
-  auto kern = pb.parts == 2 ? p1_outputs_kernel<2> : p1_outputs_kernel<1>;
+  // The two-phase Block shape of the pages (9 summaries, 24 queries) has
+  // its instantiation with both built in.
+  const bool built = a.n == 9 && a.S == 24;
+  auto kern = pb.parts == 2 ? (built ? p1_outputs_kernel<2, 9, 24> : p1_outputs_kernel<2, 0, 0>)
+                            : (built ? p1_outputs_kernel<1, 9, 24> : p1_outputs_kernel<1, 0, 0>);
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   int occ = 0;

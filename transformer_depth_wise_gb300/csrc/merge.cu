@@ -153,7 +153,10 @@ struct MergeUpdateParams {
   void *y;             // RMSNorm(h) (.) nw, [rows, D] (NORM)
 };
 
-template <typename T, int VPT, int TEAM, bool SYNTH, bool NORM>
+// TPR > 0 (CTA teams): rows that exactly fill a CTA of TPR threads (nvec ==
+// TPR * VPT), so the per-vector offsets are constants and every vector is
+// valid.
+template <typename T, int VPT, int TEAM, bool SYNTH, bool NORM, int TPR>
 __global__ void __launch_bounds__(TEAM ? 256 : 512)
 merge_update_kernel(const __grid_constant__ MergeUpdateParams P) {
   using E = Elt<T>;
@@ -161,7 +164,10 @@ merge_update_kernel(const __grid_constant__ MergeUpdateParams P) {
   __shared__ float red[TEAM ? 1 : 2 * 32 * 2];
   __shared__ float red_n[(TEAM || !NORM) ? 1 : 2 * 32];
   const MergeParams &p = P.m;
-  const int tpr = TEAM ? TEAM : blockDim.x;
+  static_assert(TPR == 0 || TEAM == 0, "a built-in thread count is for CTA teams");
+  const int tpr = TPR ? TPR : (TEAM ? TEAM : blockDim.x);
+  // 16-byte vectors per row (read from the parameters where not built in)
+  auto nvec = [&]() { return TPR ? TPR * VPT : p.nvec; };
   const int lt = TEAM ? (threadIdx.x % TEAM) : threadIdx.x;
   const int teams_per_cta = TEAM ? blockDim.x / TEAM : 1;
   const int team = TEAM ? threadIdx.x / TEAM : 0;
@@ -174,20 +180,20 @@ merge_update_kernel(const __grid_constant__ MergeUpdateParams P) {
   extern __shared__ float4 qu[];   // [EPV/4][nvec] q~, then u (SYNTH), then the norm weight (NORM)
   constexpr int Q4 = EPV / 4;
   constexpr int NW_AT = SYNTH ? 2 * Q4 : Q4;
-  for (int idx = threadIdx.x; idx < p.nvec * Q4; idx += blockDim.x) {
+  for (int idx = threadIdx.x; idx < nvec() * Q4; idx += blockDim.x) {
     const int j = idx / Q4, e4 = (idx % Q4) * 4;
     const float4 w4 = ld_f4(p.q + j * EPV + e4);
     const float4 g4 = p.g ? ld_f4(p.g + j * EPV + e4) : make_float4(1.f, 1.f, 1.f, 1.f);
-    qu[(e4 / 4) * p.nvec + j] = make_float4(w4.x * g4.x, w4.y * g4.y, w4.z * g4.z, w4.w * g4.w);
-    if (SYNTH) qu[(Q4 + e4 / 4) * p.nvec + j] = ld_f4(P.u + j * EPV + e4);
-    if (NORM) qu[(NW_AT + e4 / 4) * p.nvec + j] = ld_f4(P.nw + j * EPV + e4);
+    qu[(e4 / 4) * nvec() + j] = make_float4(w4.x * g4.x, w4.y * g4.y, w4.z * g4.z, w4.w * g4.w);
+    if (SYNTH) qu[(Q4 + e4 / 4) * nvec() + j] = ld_f4(P.u + j * EPV + e4);
+    if (NORM) qu[(NW_AT + e4 / 4) * nvec() + j] = ld_f4(P.nw + j * EPV + e4);
   }
   __syncthreads();
   bool valid[VPT];
 #pragma unroll
-  for (int k = 0; k < VPT; ++k) valid[k] = lt + k * tpr < p.nvec;
+  for (int k = 0; k < VPT; ++k) valid[k] = TPR ? true : lt + k * tpr < nvec();
   auto qv = [&](int k, int e) -> float {           // element e of this thread's vector k of w~
-    const float4 v = qu[(e >> 2) * p.nvec + lt + k * tpr];
+    const float4 v = qu[(e >> 2) * nvec() + lt + k * tpr];
     return (e & 3) == 0 ? v.x : (e & 3) == 1 ? v.y : (e & 3) == 2 ? v.z : v.w;
   };
 
@@ -203,7 +209,8 @@ merge_update_kernel(const __grid_constant__ MergeUpdateParams P) {
       ov[kk] = pv[kk] = sv[kk] = make_uint4(0u, 0u, 0u, 0u);
       const size_t off = (size_t)row * row_bytes + (size_t)(lt + kk * tpr) * 16;
       if (row_ok && valid[kk]) {
-        ov[kk] = ld_stream(static_cast<const char *>(p.o) + off);
+        ov[kk] = TPR ? ld_stream_vec<TPR>(static_cast<const char *>(p.o) + (size_t)row * row_bytes + (size_t)lt * 16, kk, tpr)
+                     : ld_stream(static_cast<const char *>(p.o) + off);
         // p_in and sub may be overwritten by this kernel: coherent loads
         if (has_pin) pv[kk] = *reinterpret_cast<const uint4 *>(static_cast<const char *>(P.p_in) + off);
         sv[kk] = *reinterpret_cast<const uint4 *>(static_cast<const char *>(P.sub) + off);
@@ -226,7 +233,7 @@ merge_update_kernel(const __grid_constant__ MergeUpdateParams P) {
       if (SYNTH && valid[kk]) {
 #pragma unroll
         for (int e4 = 0; e4 < EPV; e4 += 4) {
-          const float4 v = qu[(Q4 + e4 / 4) * p.nvec + lt + kk * tpr];
+          const float4 v = qu[(Q4 + e4 / 4) * nvec() + lt + kk * tpr];
           uu[e4] = v.x; uu[e4 + 1] = v.y; uu[e4 + 2] = v.z; uu[e4 + 3] = v.w;
         }
       }
@@ -241,7 +248,7 @@ merge_update_kernel(const __grid_constant__ MergeUpdateParams P) {
       E::unpack_again(pn[kk], x);
 #pragma unroll
       for (int e4 = 0; e4 < EPV; e4 += 4) {
-        const float4 q4 = qu[(e4 / 4) * p.nvec + lt + kk * tpr];
+        const float4 q4 = qu[(e4 / 4) * nvec() + lt + kk * tpr];
         part[0] = fmaf(q4.x, x[e4], part[0]);
         part[0] = fmaf(q4.y, x[e4 + 1], part[0]);
         part[0] = fmaf(q4.z, x[e4 + 2], part[0]);
@@ -329,7 +336,7 @@ merge_update_kernel(const __grid_constant__ MergeUpdateParams P) {
           E::unpack_again(pn[kk], xp);
 #pragma unroll
           for (int e4 = 0; e4 < EPV; e4 += 4) {
-            const float4 w4 = qu[(NW_AT + e4 / 4) * p.nvec + lt + kk * tpr];
+            const float4 w4 = qu[(NW_AT + e4 / 4) * nvec() + lt + kk * tpr];
             y[e4 + 0] = fmaf(wa, xo[e4 + 0], wc * xp[e4 + 0]) * rn * w4.x;
             y[e4 + 1] = fmaf(wa, xo[e4 + 1], wc * xp[e4 + 1]) * rn * w4.y;
             y[e4 + 2] = fmaf(wa, xo[e4 + 2], wc * xp[e4 + 2]) * rn * w4.z;
@@ -529,9 +536,9 @@ cudaError_t dispatch(const MergeParams &p, const Cfg &c, cudaStream_t st) {
 // supported row (2048 vectors).
 constexpr int mu_max_smem(bool norm) { return (norm ? 3 : 2) * 2048 * 8 * (int)sizeof(float); }
 
-template <typename T, int VPT, int TEAM, bool SYNTH, bool NORM>
+template <typename T, int VPT, int TEAM, bool SYNTH, bool NORM, int TPR = 0>
 cudaError_t run_mu(const MergeUpdateParams &P, const Cfg &c, cudaStream_t st) {
-  auto kern = merge_update_kernel<T, VPT, TEAM, SYNTH, NORM>;
+  auto kern = merge_update_kernel<T, VPT, TEAM, SYNTH, NORM, TPR>;
   const size_t smem = (size_t)P.m.D * sizeof(float) * (1 + (SYNTH ? 1 : 0) + (NORM ? 1 : 0));
   struct Entry { int dev; size_t smem; int occ; };
   static Entry cache[16];
@@ -558,6 +565,20 @@ cudaError_t run_mu(const MergeUpdateParams &P, const Cfg &c, cudaStream_t st) {
 
 template <typename T, bool SYNTH, bool NORM>
 cudaError_t dispatch_mu(const MergeUpdateParams &P, const Cfg &c, cudaStream_t st) {
+  // Rows that fill the CTA exactly run with its width built in, except the
+  // plain step on 128 threads (D = 4096 bf16), where measured on a GB300 it
+  // was slower (0.238 against 0.211 ms); with the pre-norm on the same rows
+  // it is faster (0.232 against 0.266 ms), and so on 224 threads (D = 7168:
+  // 0.736 against 0.776 ms).
+  const bool exact = c.team == 0 && P.m.nvec == c.threads * c.vpt && (NORM || c.threads != 128);
+  if (exact && c.vpt == 4) {
+    switch (c.threads) {
+      case 128: return run_mu<T, 4, 0, SYNTH, NORM, 128>(P, c, st);
+      case 224: return run_mu<T, 4, 0, SYNTH, NORM, 224>(P, c, st);
+      case 256: return run_mu<T, 4, 0, SYNTH, NORM, 256>(P, c, st);
+      default: break;
+    }
+  }
   switch (c.team) {
     case 0: return c.vpt == 2 ? run_mu<T, 2, 0, SYNTH, NORM>(P, c, st) : run_mu<T, 4, 0, SYNTH, NORM>(P, c, st);
     case 4: return run_mu<T, 2, 4, SYNTH, NORM>(P, c, st);

@@ -700,14 +700,27 @@ p1_many_outputs_tc_kernel(const __grid_constant__ ParamsB3 p) {
   const int64_t total = my_tokens * KS;
 
   auto token = [&](int64_t j) { return (int64_t)blockIdx.x + j * gridDim.x; };
+  // When the CTA width is a multiple of the chunks per row, a thread's chunk
+  // column is fixed and its rows step by a constant (no division per copy).
+  const bool whole_rows = blockDim.x % chunks == 0;
+  const int rstep = whole_rows ? blockDim.x / chunks : 0, r0 = tid / chunks, ch0 = tid % chunks;
   auto issue = [&](int64_t g) {                                  // step g: 16 summary rows -> slot g & 1
     const int64_t t = token(g / KS);
     const int kk = (int)(g % KS);
     unsigned char *slot = vring + (size_t)(g & 1) * kTcK * RV;
-    for (int c = tid; c < kTcK * chunks; c += blockDim.x) {
-      const int r = c / chunks, ch = c % chunks, i = kk * kTcK + r;
-      const char *gp = static_cast<const char *>(p.src[i < n ? i : 0]) + (size_t)t * row_bytes + (size_t)ch * 16;
-      cp_async16_zfill(slot + (size_t)r * RV + (size_t)ch * 16, gp, i < n ? 16u : 0u);
+    if (whole_rows) {
+      const size_t goff = (size_t)t * row_bytes + (size_t)ch0 * 16;
+      for (int r = r0; r < kTcK; r += rstep) {
+        const int i = kk * kTcK + r;
+        const char *gp = static_cast<const char *>(p.src[i < n ? i : 0]) + goff;
+        cp_async16_zfill(slot + (size_t)r * RV + (size_t)ch0 * 16, gp, i < n ? 16u : 0u);
+      }
+    } else {
+      for (int c = tid; c < kTcK * chunks; c += blockDim.x) {
+        const int r = c / chunks, ch = c % chunks, i = kk * kTcK + r;
+        const char *gp = static_cast<const char *>(p.src[i < n ? i : 0]) + (size_t)t * row_bytes + (size_t)ch * 16;
+        cp_async16_zfill(slot + (size_t)r * RV + (size_t)ch * 16, gp, i < n ? 16u : 0u);
+      }
     }
     cp_async_commit();
   };

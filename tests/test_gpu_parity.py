@@ -156,6 +156,24 @@ def test_aggregate_block_single_full_size_sampled(gpu):
     check_stats(lse.reshape(-1)[torch.as_tensor(rows, device=gpu)], olse, "lse")
 
 
+# Shapes that reach the aggregation's instantiations with the CTA width
+# built in and the many-rows shape (from 32 rows per SM on a 152-SM GPU,
+# 4864 rows): rows that exactly fill 64, 128 or 256 threads, and a ragged
+# width for contrast; rows compared on a sample (rows are independent).
+@pytest.mark.parametrize("dtype,D,n,rows", [
+    (torch.bfloat16, 4096, 5, 4900), (torch.bfloat16, 1024, 7, 5000), (torch.bfloat16, 8192, 3, 4870),
+    (torch.float32, 2048, 4, 4900), (torch.bfloat16, 1024, 3, 2000), (torch.bfloat16, 2056, 6, 4900),
+])
+def test_aggregate_exact_widths_sampled(gpu, dtype, D, n, rows):
+    srcs, q, g = rand_sources(n, (1, rows, D), dtype, gpu, seed=D + 3 * n + rows)
+    out, m, lse = api.depth_aggregate(srcs, q, g, 1e-8, stats=True)
+    sample = sample_rows(1, rows, 40, D + rows)
+    V = np.stack([f64(pick(s, sample, D)) for s in srcs])
+    h, om, olse = oracle.depth_aggregate(V, f64(q), f64(g), 1e-8)
+    check(pick(out, sample, D), oracle.round_to(h, ODT[dtype]), TOL[dtype] * vmax(srcs), f"D={D} rows={rows}")
+    check_stats(lse.reshape(-1)[torch.as_tensor(sample, device=gpu)], olse, "lse")
+
+
 # --------------------------------------------------------------------------
 # Backward of the depth aggregation
 # --------------------------------------------------------------------------
@@ -397,6 +415,37 @@ def test_merge_update_with_prenorm(gpu):
             api.block_merge_update(o, lse, pi if with_pin else None, ys, u, W[0], G[0], 1e-8, partial_out=pi,
                                    norm_weight=Wn[0], norm_eps=1e-5, normed_out=ys, write_h=False)
             assert torch.equal(pi, p_out) and torch.equal(ys, y)
+
+
+@pytest.mark.parametrize("D,rows", [(4096, 700), (7168, 650), (8192, 620)])
+def test_merge_update_many_rows_sampled(gpu, D, rows):
+    """Past 4 rows per SM the fused step takes four vectors per thread; these
+    widths fill 128, 224 and 256 threads exactly, the instantiations with the
+    CTA width built in (with and without the pre-norm).  Sampled rows."""
+    dtype = torch.bfloat16
+    sample = sample_rows(1, rows, 24, D)
+    for norm in (True, False):
+        g = wk.generator(D + rows + 7 * norm, gpu)
+        (o, pin, sub), _ = wk.scaled_normal_sources(g, 3, (1, rows, D), 0.5, 3.0, dtype, gpu)
+        W, G = wk.queries_and_gains(g, 1, D, gpu)
+        _, Wn = wk.queries_and_gains(g, 1, D, gpu)
+        u = wk.sublayer_u(g, 1, D, gpu)[0].contiguous()
+        lse = torch.empty(rows, device=gpu).normal_(0.0, 2.0, generator=g)
+        kw = dict(norm_weight=Wn[0], norm_eps=1e-5) if norm else {}
+        res = api.block_merge_update(o, lse, pin, sub, u, W[0], G[0], 1e-8, **kw)
+        p_out, h = res[0], res[1]
+        idx = torch.as_tensor(sample, device=gpu)
+        subn = f64(pick(sub, sample, D))
+        want_p = oracle.round_to(f64(pick(pin, sample, D)) + oracle.synthetic_sublayer(f64(u), subn), ODT[dtype])
+        want_h, _ = oracle.block_phase2_merge(f64(pick(o, sample, D)), f64(lse[idx]), want_p, f64(W[0]),
+                                              f64(G[0]), 1e-8)
+        tol = TOL[dtype] * vmax([o, pin, sub])
+        check(pick(p_out, sample, D), want_p, tol, f"p D={D} norm={norm}")
+        check(pick(h, sample, D), oracle.round_to(want_h, ODT[dtype]), tol, f"h D={D} norm={norm}")
+        if norm:
+            want_y = oracle.rms_norm(want_h, f64(Wn[0]), 1e-5)
+            check(pick(res[2], sample, D), oracle.round_to(want_y, ODT[dtype]),
+                  TOL[dtype] * np.abs(want_y).max(), f"y D={D}")
 
 
 @pytest.mark.parametrize("fused", [True, False])

@@ -273,6 +273,17 @@ aggregate_pipe_kernel(const __grid_constant__ AggParams p) {
   int64_t lrow = blockIdx.x;
   auto load_next = [&](uint4 (&buf)[G][VPT]) {
     const size_t off = (size_t)lrow * row_bytes + (size_t)tid * 16;
+    // The shape for many rows (G = 2) also asks L2 for the group after this
+    // one, so its rows arrive while this one is processed: block_single 0.134
+    // -> 0.126 ms on a GB300.  The G = 4 shape (fewer rows, e.g. the Full
+    // stack's 2048) measured slower with it (27.2 -> 30.1 ms) and goes without.
+    if (G == 2 && tid < G) {
+      const bool wrap = lgi + 1 == ngr;
+      const int64_t frow = wrap ? lrow + gridDim.x : lrow;
+      const int fi = (wrap ? 0 : (lgi + 1) * G) + tid;
+      if (frow < p.rows && fi < p.n)
+        prefetch_l2_bulk(static_cast<const char *>(p.src[fi]) + (size_t)frow * row_bytes, (uint32_t)row_bytes);
+    }
 #pragma unroll
     for (int g = 0; g < G; ++g) {
       const int i = lgi * G + g;

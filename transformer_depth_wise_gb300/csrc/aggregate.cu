@@ -1,4 +1,4 @@
-// aggregate.cu -- depth aggregation kernel (eq. A1-A3 of "Attention Residual
+// aggregate.cu -- depth aggregation kernels (eq. A1-A3 of "Attention Residual
 // 深度残差", "DepthResidual.forward"), one pass over the sources.
 //
 // A "team" of threads owns one token row; each thread owns VPT 16-byte
@@ -10,9 +10,14 @@
 // acc[]) held in registers (eq. OS1 / OS2).  No [n, B, T] score tensor ever
 // exists; each source byte is read from HBM once.
 //
-// The same kernel, with u != nullptr, applies the synthetic sublayer
-// v = 0.5 tanh(u (.) h) to the fp32 h before the single rounding store: the
-// Full stack uses it so h_l never round-trips through memory.
+// aggregate_pipe_kernel takes rows of more than 64 vectors with at least one
+// source (the CTA is the team, the next group's loads in flight while the
+// current one is folded in); aggregate_kernel takes short rows (lane teams of
+// a warp) and a prior state with no further source.
+//
+// Both, with u != nullptr, apply the synthetic sublayer v = 0.5 tanh(u (.) h)
+// to the fp32 h before the single rounding store: the Full stack uses it so
+// h_l never round-trips through memory.
 #include "common.cuh"
 #include "launch.h"
 
@@ -229,11 +234,11 @@ aggregate_kernel(const __grid_constant__ AggParams p) {
 // Pipelined variant: rows of more than 64 vectors, n >= 1.
 // ---------------------------------------------------------------------------
 // A CTA owns one token row at a time and each thread VPT 16-byte vectors of
-// it.  Sources go in groups of two; the thread's slices of the next group are
-// loaded into a second register set while the current group is reduced and
-// folded in, so loads stay in flight through the arithmetic.  The folded
-// query lives in shared memory (read once per vector for both sources of a
-// group), which leaves the registers to the loads in flight and the
+// it.  Sources go in groups of G (2 or 4); the thread's slices of the next
+// group are loaded into a second register set while the current group is
+// reduced and folded in, so loads stay in flight through the arithmetic.  The
+// folded query lives in shared memory (read once per vector for all sources
+// of a group), which leaves the registers to the loads in flight and the
 // accumulator.  The arithmetic is that of aggregate_kernel.
 // TPR > 0: rows that exactly fill a CTA of TPR threads (nvec == TPR * VPT),
 // so the per-vector offsets are constants and every vector is valid.

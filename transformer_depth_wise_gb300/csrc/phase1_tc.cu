@@ -17,23 +17,28 @@
 // Kernel A (scores, tensor cores).  A CTA owns a tile of 128 token rows.
 // TMA streams each summary of the tile in 64-feature chunks (box 64 x 128,
 // 128-byte swizzle), one summary after the other, through a ring of
-// shared-memory stages; each stage also carries the parked query parts for
-// the same 64 features (box 64 x 48), the MMA's B operand (N = 48);
-// tcgen05.mma
-// accumulates, per summary i, the 128 x 48 partial scores in its own TMEM
-// columns [48 i, 48 i + 48).  Four warps (one thread per token row) read the
-// same stages to accumulate each row's sum of squares, then run the
-// epilogue: scores = (hi + lo) * rsqrt(ss / D + eps), the softmax over the n
-// summaries, m and lse to their outputs, and alpha (fp32, [n][Sp][2] with
-// Sp = S rounded up to even, each value twice) into the
-// first S*n*4 bytes of the token's own o[0] row -- a region kernel B reads
-// before it overwrites that row with o_0, so no scratch memory is needed.
+// shared-memory stages, each with a producer lane of its own; each stage
+// also carries the parked query parts for the same 64 features (box 64 x
+// 48), the MMA's B operand (N = 48).  tcgen05.mma accumulates, per summary
+// i, the 128 x 48 partial scores in its own TMEM columns [48 i, 48 i + 48).
+// Four warps (one thread per token row) read the same stages to accumulate
+// each row's sum of squares, then run the epilogue: scores = (hi + lo) *
+// rsqrt(ss / D + eps), the softmax over the n summaries, m and lse to their
+// outputs, and alpha (fp32, [n][Sp][2] with Sp = S rounded up to even, each
+// value twice) into the first S*n*4 bytes of the token's own o[0] row -- a
+// region kernel B reads before it overwrites that row with o_0, so no
+// scratch memory is needed.
 //
 // Kernel B (outputs).  A CTA owns one token at a time, one thread per 16-byte
-// chunk of the row (D <= 4096); cp.async double-buffers the next token's n
-// summary chunks and alpha (two tokens ahead) while the current token's S
-// outputs are formed,
-// two queries at a time, with packed fp32x2 FMAs and stored.
+// chunk of the row (rows wider than 4096 features in two pieces); a 3-stage
+// cp.async pipeline brings in the next tokens' n summary chunks and alpha
+// while the current token's S outputs are formed, two queries at a time,
+// with packed fp32x2 FMAs, and stored.  The pages' shape (9 summaries, 24
+// queries) has an instantiation with both counts built in.
+//
+// More than ten summaries (the Full two-phase schedule): kernel A in a
+// raw-score mode over work items (tile, ten summaries), a softmax kernel,
+// and a tensor-core outputs kernel (mma.sync, K = 16 summaries per step).
 //
 // Each summary byte is read twice (once per kernel); there is no cluster or
 // cross-CTA exchange.  Every in-kernel wait is bounded: one that runs out

@@ -71,6 +71,14 @@ constexpr int kWarpsA = 6;            // 0-3: sums of squares + epilogue, 4: TMA
 constexpr int kThreadsA = kWarpsA * 32;
 constexpr uint32_t kOffBar = kStages * kStageBytes;
 constexpr uint32_t kSmemA = kOffBar + 64 * 8 + 1024;     // barriers + alignment slack
+// Work items of CH summaries (10, or 5 in raw-score mode): the stage ring and
+// the TMEM columns of a CTA.  With five, a CTA takes 256 TMEM columns and
+// about 93 KB of shared memory, so two CTAs share an SM: the tensor-map
+// loads one CTA issues are served one box at a time (16 KB boxes stream at
+// 4.2 TB/s with one CTA per SM on GB300, 6.2 TB/s with two).
+__host__ __device__ constexpr int stages_a(int CH) { return CH == kMaxN ? kStages : 4; }
+__host__ __device__ constexpr uint32_t tmem_cols_a(int CH) { return CH * kNQ <= 256 ? 256u : 512u; }
+__host__ __device__ constexpr uint32_t smem_a(int CH) { return (uint32_t)stages_a(CH) * kStageBytes + 64 * 8 + 1024; }
 
 template <int NM>
 struct ParamsAT {
@@ -203,23 +211,27 @@ __global__ void __launch_bounds__(256) p1_qsplit_kernel(const float *__restrict_
 // -----------------------------------------------------------------------------
 // Kernel A: scores on tcgen05, softmax, alpha / m / lse
 // -----------------------------------------------------------------------------
-template <int NM>
-__global__ void __launch_bounds__(kThreadsA, 1) p1_scores_kernel(const __grid_constant__ ParamsAT<NM> p) {
+template <int NM, int CH = kMaxN>
+__global__ void __launch_bounds__(kThreadsA, CH == kMaxN ? 1 : 2) p1_scores_kernel(const __grid_constant__ ParamsAT<NM> p) {
+  static_assert(CH >= 1 && CH <= CH, "summaries per work item");
+  constexpr int ST = stages_a(CH);                 // stage ring
+  constexpr uint32_t TC = tmem_cols_a(CH);         // TMEM columns of this CTA
+  constexpr uint32_t OFF_BAR = (uint32_t)ST * kStageBytes;
   extern __shared__ unsigned char smem_raw[];
   unsigned char *sm = reinterpret_cast<unsigned char *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   const uint32_t base = smem_u32(sm);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n = p.n, S = p.S;
-  const uint32_t b0 = base + kOffBar;
+  const uint32_t b0 = base + OFF_BAR;
   auto VFULL = [&](int s) { return b0 + 8u * s; };
-  auto VEMPTY = [&](int s) { return b0 + 8u * (kStages + s); };
-  const uint32_t TDONE = b0 + 8u * (2 * kStages);
+  auto VEMPTY = [&](int s) { return b0 + 8u * (ST + s); };
+  const uint32_t TDONE = b0 + 8u * (2 * ST);
   const uint32_t TFREE = TDONE + 8u;
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + kOffBar + 8 * (2 * kStages + 2));
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + OFF_BAR + 8 * (2 * ST + 2));
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < ST; ++s) {
       mbar_init(VFULL(s), 1);
       mbar_init(VEMPTY(s), 1 + 4);    // the MMA's commit + the four row warps
     }
@@ -229,7 +241,7 @@ __global__ void __launch_bounds__(kThreadsA, 1) p1_scores_kernel(const __grid_co
   }
   if (warp == 5) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
-                 :: "r"(smem_u32(tmem_slot)), "r"(kTmemCols));
+                 :: "r"(smem_u32(tmem_slot)), "r"(TC));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
   __syncthreads();
@@ -238,13 +250,13 @@ __global__ void __launch_bounds__(kThreadsA, 1) p1_scores_kernel(const __grid_co
 
   // Work items: (tile of 128 rows, chunk of up to ten summaries), tile-minor.
   const int64_t tiles = (p.rows + kRows - 1) / kRows;
-  const int64_t items = tiles * ((n + kMaxN - 1) / kMaxN);
+  const int64_t items = tiles * ((n + CH - 1) / CH);
   const int64_t my_tiles = items > (int64_t)blockIdx.x ? (items - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
   auto item_of = [&](int64_t tl, int64_t &tile, int &i0, int &nc) {
     const int64_t item = (int64_t)blockIdx.x + tl * gridDim.x;
     tile = item % tiles;
-    i0 = (int)(item / tiles) * kMaxN;
-    nc = n - i0 < kMaxN ? n - i0 : kMaxN;
+    i0 = (int)(item / tiles) * CH;
+    nc = n - i0 < CH ? n - i0 : CH;
   };
   const int KC = p.D / kKc;
 
@@ -257,9 +269,9 @@ __global__ void __launch_bounds__(kThreadsA, 1) p1_scores_kernel(const __grid_co
     // 0.4 us each on GB300, whatever their size), so every stage has a
     // producer lane of its own: lane s issues each use of stage s.  All lanes
     // walk the same sequence; the stage's empty barrier orders its uses.
-    if (lane < kStages) {
+    if (lane < ST) {
       int64_t g = 0, last = -1;
-      int s = 0;  // g % kStages
+      int s = 0;  // g % ST
       for (int64_t tl = 0; tl < my_tiles; ++tl) {
         int64_t tile;
         int i0, nc;
@@ -267,19 +279,19 @@ __global__ void __launch_bounds__(kThreadsA, 1) p1_scores_kernel(const __grid_co
         for (int i = 0; i < nc; ++i)
           for (int kc = 0; kc < KC; ++kc, ++g) {
             if (s == lane) {
-              if (g >= kStages) wait_local(VEMPTY(s), (uint32_t)((g / kStages - 1) & 1));
+              if (g >= ST) wait_local(VEMPTY(s), (uint32_t)((g / ST - 1) & 1));
               mbar_expect_tx(VFULL(s), kStageBytes);
               const uint32_t st = base + (uint32_t)s * kStageBytes;
               tma_load_2d(st, &p.tmap[i0 + i], kc * kKc, (int)(tile * kRows), VFULL(s));
               tma_load_2d(st + kVBytes, &p.qmap, kc * kKc, 0, VFULL(s));
               last = g;
             }
-            if (++s == kStages) s = 0;
+            if (++s == ST) s = 0;
           }
       }
       // this lane's last stage has landed before the CTA may exit (its
       // earlier uses were consumed before the stage was refilled)
-      if (last >= 0) wait_local(VFULL(lane), (uint32_t)((last / kStages) & 1));
+      if (last >= 0) wait_local(VFULL(lane), (uint32_t)((last / ST) & 1));
     }
   } else if (warp == 5) {
     // ---------------- MMA issuer ----------------
@@ -294,8 +306,8 @@ __global__ void __launch_bounds__(kThreadsA, 1) p1_scores_kernel(const __grid_co
         item_of(tl, tile, i0, nc);
         for (int i = 0; i < nc; ++i)
           for (int kc = 0; kc < KC; ++kc, ++g) {
-            const int s = (int)(g % kStages);
-            wait_local(VFULL(s), (uint32_t)((g / kStages) & 1));
+            const int s = (int)(g % ST);
+            wait_local(VFULL(s), (uint32_t)((g / ST) & 1));
             asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
             const uint32_t st = base + (uint32_t)s * kStageBytes;
 #pragma unroll
@@ -318,15 +330,15 @@ __global__ void __launch_bounds__(kThreadsA, 1) p1_scores_kernel(const __grid_co
       int64_t tile;
       int i0, nc;
       item_of(tl, tile, i0, nc);
-      float ss[kMaxN];
+      float ss[CH];
 #pragma unroll
-      for (int i = 0; i < kMaxN; ++i) ss[i] = 0.f;
+      for (int i = 0; i < CH; ++i) ss[i] = 0.f;
 #pragma unroll
-      for (int i = 0; i < kMaxN; ++i) {
+      for (int i = 0; i < CH; ++i) {
         if (i >= nc) continue;
         for (int kc = 0; kc < KC; ++kc, ++g) {
-          const int s = (int)(g % kStages);
-          wait_local(VFULL(s), (uint32_t)((g / kStages) & 1));
+          const int s = (int)(g % ST);
+          wait_local(VFULL(s), (uint32_t)((g / ST) & 1));
           const unsigned char *row = sm + (uint32_t)s * kStageBytes;
           uint4 v[8];
 #pragma unroll
@@ -347,14 +359,14 @@ __global__ void __launch_bounds__(kThreadsA, 1) p1_scores_kernel(const __grid_co
       // epilogue: scores -> softmax over the n summaries -> alpha, m, lse
       wait_local(TDONE, (uint32_t)(tl & 1));
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-      float rinv[kMaxN];
+      float rinv[CH];
 #pragma unroll
-      for (int i = 0; i < kMaxN; ++i) rinv[i] = rsqrtf(fmaf(ss[i], p.inv_D, p.eps));
+      for (int i = 0; i < CH; ++i) rinv[i] = rsqrtf(fmaf(ss[i], p.inv_D, p.eps));
       if (p.raw) {                                               // raw-score mode
         const int64_t row = tile * kRows + r;
         float c[kNQ];
 #pragma unroll
-        for (int i = 0; i < kMaxN; ++i) {
+        for (int i = 0; i < CH; ++i) {
           if (i >= nc) continue;
           tmem_ld16(taddr + i * kNQ, c);
           tmem_ld16(taddr + i * kNQ + 16, c + 16);
@@ -377,7 +389,7 @@ __global__ void __launch_bounds__(kThreadsA, 1) p1_scores_kernel(const __grid_co
       for (int q = 0; q < kMaxS; ++q) { m[q] = -INFINITY; den[q] = 0.f; }
       float c[kNQ];
 #pragma unroll
-      for (int i = 0; i < kMaxN; ++i) {                          // pass 1: max
+      for (int i = 0; i < CH; ++i) {                          // pass 1: max
         if (i >= nc) continue;
         tmem_ld16(taddr + i * kNQ, c);
         tmem_ld16(taddr + i * kNQ + 16, c + 16);
@@ -387,7 +399,7 @@ __global__ void __launch_bounds__(kThreadsA, 1) p1_scores_kernel(const __grid_co
         for (int q = 0; q < kMaxS; ++q) m[q] = fmaxf(m[q], (c[q] + c[kMaxS + q]) * rinv[i]);
       }
 #pragma unroll
-      for (int i = 0; i < kMaxN; ++i) {                          // pass 2: denominators
+      for (int i = 0; i < CH; ++i) {                          // pass 2: denominators
         if (i >= nc) continue;
         tmem_ld16(taddr + i * kNQ, c);
         tmem_ld16(taddr + i * kNQ + 16, c + 16);
@@ -400,7 +412,7 @@ __global__ void __launch_bounds__(kThreadsA, 1) p1_scores_kernel(const __grid_co
       const bool row_ok = row < p.rows;
       float *alpha = reinterpret_cast<float *>(static_cast<char *>(p.out) + (size_t)row * p.D * 2);
 #pragma unroll
-      for (int i = 0; i < kMaxN; ++i) {                          // pass 3: alpha [n][S]
+      for (int i = 0; i < CH; ++i) {                          // pass 3: alpha [n][S]
         if (i >= nc) continue;
         tmem_ld16(taddr + i * kNQ, c);
         tmem_ld16(taddr + i * kNQ + 16, c + 16);
@@ -434,7 +446,7 @@ __global__ void __launch_bounds__(kThreadsA, 1) p1_scores_kernel(const __grid_co
   __syncthreads();
   if (warp == 5) {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" :: "r"(tmem_base), "r"(kTmemCols));
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" :: "r"(tmem_base), "r"(TC));
   }
 }
 
@@ -957,8 +969,9 @@ cudaError_t launch_phase1_many(const Phase1ManyArgs &a) {
   pa.inv_D = 1.f / (float)a.D;
   pa.raw = a.scores;
   pa.raw_n = a.n;
-  cudaError_t e = cudaFuncSetAttribute(p1_scores_kernel<kManyMaps>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)kSmemA);
+  constexpr int kManyCh = 5;   // summaries per work item here: two CTAs per SM
+  cudaError_t e = cudaFuncSetAttribute(p1_scores_kernel<kManyMaps, kManyCh>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_a(kManyCh));
   if (e != cudaSuccess) return e;
   const int64_t tiles = (a.rows + kRows - 1) / kRows;
   // Raw scores: one launch per kManyMaps summaries, its work items (tile,
@@ -978,10 +991,11 @@ cudaError_t launch_phase1_many(const Phase1ManyArgs &a) {
     }
     pa.n = nl;
     pa.raw_off = off;
-    const int64_t items = tiles * ((nl + kMaxN - 1) / kMaxN);
-    const int64_t waves = (items + sm_count() - 1) / sm_count();
+    const int64_t items = tiles * ((nl + kManyCh - 1) / kManyCh);
+    const int64_t slots = 2 * (int64_t)sm_count();   // resident CTAs
+    const int64_t waves = (items + slots - 1) / slots;
     const int64_t ga = (items + waves - 1) / waves;
-    p1_scores_kernel<kManyMaps><<<(int)ga, kThreadsA, kSmemA, a.stream>>>(pa);
+    p1_scores_kernel<kManyMaps, kManyCh><<<(int)ga, kThreadsA, smem_a(kManyCh), a.stream>>>(pa);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   {

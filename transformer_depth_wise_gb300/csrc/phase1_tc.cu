@@ -96,6 +96,7 @@ struct ParamsAT {
   // of them runs afterwards.  Without raw, n <= 10 and there is one chunk.
   float *raw;
   int raw_n, raw_off;                 // raw's summary count and this launch's first summary
+  int64_t raw_stride;                 // floats from one row's scores to the next (raw_n * S when packed)
 };
 // The fused path (up to ten summaries) and the raw-score path, which takes
 // up to kManyMaps summaries per launch (the tensor maps ride in the kernel
@@ -373,7 +374,7 @@ __global__ void __launch_bounds__(kThreadsA, CH == kMaxN ? 1 : 2) p1_scores_kern
           tmem_ld16(taddr + i * kNQ + 32, c + 32);
           asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
           if (row < p.rows) {
-            float *dst = p.raw + ((size_t)row * p.raw_n + p.raw_off + i0 + i) * S;
+            float *dst = p.raw + (size_t)row * p.raw_stride + (size_t)(p.raw_off + i0 + i) * S;
 #pragma unroll
             for (int q = 0; q < kMaxS; ++q)
               if (q < S) dst[q] = (c[q] + c[kMaxS + q]) * rinv[i];
@@ -543,6 +544,42 @@ __global__ void __launch_bounds__(512, 1) p1_outputs_kernel(const __grid_constan
       }
     }
     __syncthreads();    // every thread is done with stage `buf` before it is refilled
+  }
+}
+
+// -----------------------------------------------------------------------------
+// Up to ten summaries with the scores computed in raw mode: each token's raw
+// scores [n][S] sit in its o[1] row; one thread per (row, query) takes their
+// softmax, writes m and lse, and writes alpha into the token's o[0] row in
+// the layout the outputs kernel reads ([n][Sp][2], each value twice; the
+// pad query of an odd S gets zeros).  The outputs kernel then overwrites
+// both rows.
+// -----------------------------------------------------------------------------
+__global__ void __launch_bounds__(256)
+p1_park_softmax_kernel(const float *raw, float *alpha, int64_t row_floats, int64_t rows, int n, int S,
+                       float *out_max, float *out_lse) {
+  const int Sp = S + (S & 1);
+  const int64_t total = rows * Sp;
+  for (int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; g < total; g += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t row = g / Sp;
+    const int q = (int)(g % Sp);
+    float *al = alpha + (size_t)row * row_floats;
+    if (q >= S) {                                   // the pad query of an odd S
+      for (int i = 0; i < n; ++i) *reinterpret_cast<float2 *>(al + 2 * (i * Sp + q)) = make_float2(0.f, 0.f);
+      continue;
+    }
+    const float *s = raw + (size_t)row * row_floats + q;
+    float m = -INFINITY;
+    for (int i = 0; i < n; ++i) m = fmaxf(m, s[(size_t)i * S]);
+    float den = 0.f;
+    for (int i = 0; i < n; ++i) den += expf(s[(size_t)i * S] - m);
+    const float inv = 1.f / den;
+    for (int i = 0; i < n; ++i) {
+      const float a = expf(s[(size_t)i * S] - m) * inv;
+      *reinterpret_cast<float2 *>(al + 2 * (i * Sp + q)) = make_float2(a, a);
+    }
+    out_lse[(size_t)q * rows + row] = m + logf(den);
+    if (out_max) out_max[(size_t)q * rows + row] = m;
   }
 }
 
@@ -889,15 +926,45 @@ cudaError_t launch_phase1_tc(const Phase1Args &a) {
   pa.D = a.D;
   pa.eps = a.eps;
   pa.inv_D = 1.f / (float)a.D;
-  cudaError_t e = cudaFuncSetAttribute(p1_scores_kernel<kMaxN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)kSmemA);
-  if (e != cudaSuccess) return e;
-  // Every CTA gets the same number of tiles (no partly empty last wave).
+  cudaError_t e = cudaSuccess;
   const int64_t tiles = (a.rows + kRows - 1) / kRows;
-  const int64_t waves = (tiles + sm_count() - 1) / sm_count();
-  const int64_t ga = (tiles + waves - 1) / waves;
-  p1_scores_kernel<kMaxN><<<(int)ga, kThreadsA, kSmemA, a.stream>>>(pa);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  // Raw scores with five-summary items, two CTAs per SM (tensor-map loads
+  // are served one box at a time per CTA), when each token's o[1] row can
+  // hold its raw scores and lies before the parked query parts; then a
+  // softmax kernel writes alpha into o[0].  Otherwise the fused kernel: one
+  // CTA per SM, the softmax in its epilogue.
+  const size_t row_bytes = (size_t)a.D * 2;
+  if (a.S >= 3 && (int64_t)(a.S - 2) * a.rows >= kNQ && (size_t)a.n * a.S * 4 <= row_bytes) {
+    constexpr int kCh = 5;
+    float *raw = reinterpret_cast<float *>(static_cast<char *>(a.out) + (size_t)a.rows * row_bytes);  // o[1]
+    pa.raw = raw;
+    pa.raw_n = a.n;
+    pa.raw_off = 0;
+    pa.raw_stride = (int64_t)(row_bytes / 4);
+    e = cudaFuncSetAttribute(p1_scores_kernel<kMaxN, kCh>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem_a(kCh));
+    if (e != cudaSuccess) return e;
+    const int64_t items = tiles * ((a.n + kCh - 1) / kCh);
+    const int64_t slots = 2 * (int64_t)sm_count();
+    const int64_t waves = (items + slots - 1) / slots;
+    const int64_t ga = (items + waves - 1) / waves;
+    p1_scores_kernel<kMaxN, kCh><<<(int)ga, kThreadsA, smem_a(kCh), a.stream>>>(pa);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    const int64_t total = a.rows * (a.S + (a.S & 1));
+    const int64_t blocks = (total + 255) / 256 < 8 * sm_count() ? (total + 255) / 256 : 8 * sm_count();
+    p1_park_softmax_kernel<<<(int)blocks, 256, 0, a.stream>>>(raw, static_cast<float *>(a.out),
+                                                              (int64_t)(row_bytes / 4), a.rows, a.n, a.S,
+                                                              a.out_max, a.out_lse);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  } else {
+    e = cudaFuncSetAttribute(p1_scores_kernel<kMaxN>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemA);
+    if (e != cudaSuccess) return e;
+    // Every CTA gets the same number of tiles (no partly empty last wave).
+    const int64_t waves = (tiles + sm_count() - 1) / sm_count();
+    const int64_t ga = (tiles + waves - 1) / waves;
+    p1_scores_kernel<kMaxN><<<(int)ga, kThreadsA, kSmemA, a.stream>>>(pa);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
   // Kernel B
   ParamsB pb;
   for (int i = 0; i < a.n; ++i) pb.src[i] = a.blocks[i];
@@ -969,6 +1036,7 @@ cudaError_t launch_phase1_many(const Phase1ManyArgs &a) {
   pa.inv_D = 1.f / (float)a.D;
   pa.raw = a.scores;
   pa.raw_n = a.n;
+  pa.raw_stride = (int64_t)a.n * a.S;
   constexpr int kManyCh = 5;   // summaries per work item here: two CTAs per SM
   cudaError_t e = cudaFuncSetAttribute(p1_scores_kernel<kManyMaps, kManyCh>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_a(kManyCh));

@@ -90,7 +90,10 @@ int attnres_depth_aggregate(const void *const *sources, int n, int64_t B, int64_
  *   out      device [S,B,T,D] of `dtype`: out[s] = normalised output o_s
  *   out_lse  device fp32 [S,B,T], required (phase 2 consumes it)
  *   out_max  device fp32 [S,B,T], optional
- * Each summary is read from HBM once for all S queries.
+ * All S queries are served by one batched pass over the summaries: the
+ * per-token-row kernel (few rows, fp32, more than ten summaries) reads each
+ * summary once; the tensor-core kernels (bf16, at least 512 rows) read it
+ * twice, once for the scores and once for the outputs.
  */
 int attnres_block_phase1(const void *const *blocks, int n_blocks, int64_t B, int64_t T, int64_t D,
                          int dtype, const float *queries, const float *gains, int S, float eps,
@@ -168,9 +171,13 @@ int attnres_depth_aggregate_backward(const void *const *sources, int n, int64_t 
  *   for narrow rows) is refused with ATTNRES_ERR_SCRATCH.  Every supported
  *   D fits.  Nothing in the array has to start at zero: each partial row a
  *   call sums is written earlier in the same call.
- *   Set-up: the first call on a device looks up the array's device address
- *   (with that device current); make that first call before any stream
- *   capture.
+ *   Set-up: the first call on a device that needs the scratch (token rows
+ *   and a query or gain gradient) looks up the array's device address, with
+ *   that device current, and caches it; make that first call before any
+ *   stream capture.  A cudaDeviceReset unloads the library's device code:
+ *   the cached address is then stale, so do not call this entry point on a
+ *   device after resetting it.  All other arguments are checked before the
+ *   lookup, as in attnres_depth_aggregate_backward.
  *   Calls share the array: two calls whose kernels overlap on the GPU (other
  *   streams, other host threads) race on it and give wrong query and gain
  *   gradients.  Calls in one stream are ordered and safe.
@@ -329,15 +336,29 @@ int attnres_block_schedule(int num_atomic, int block_size, int *n_sources_per_la
 int attnres_atomic_block_size(int num_hidden_layers, int attnres_block_size);
 
 /*
- * Kernels that wait on in-kernel events (bulk-copy completion, peer CTAs of a
- * cluster) bound every wait to about 2 s; a wait that runs out records a
- * device-side flag and the kernel carries on to its end instead of hanging
- * (its results are then invalid).  This call synchronises the current
- * device, reads and clears those flags, and returns ATTNRES_ERR_TIMEOUT if
- * any was set since the previous call (ATTNRES_ERR_CUDA if the device
- * reports an error), else ATTNRES_OK.
+ * Kernels that wait on in-kernel events (bulk-copy and tensor-core
+ * completion) bound every wait.  A wait that runs out records a device-side
+ * flag; the part of the CTA that waited stops issuing work, every part
+ * waits (bounded again) for the copies and tensor-core operations it still
+ * has in flight, and the CTA ends: the kernel never hangs and leaves nothing
+ * running, but its results are invalid.  While the flag is set, later
+ * launches of those kernels skip their work, so every result of the calls
+ * that use them stays invalid until the error is taken.
+ * This call synchronises the current device, reads and clears those flags,
+ * and returns ATTNRES_ERR_TIMEOUT if any was set since the previous call
+ * (ATTNRES_ERR_CUDA if the device reports an error), else ATTNRES_OK.
  */
 int attnres_take_device_error(void);
+
+/*
+ * Diagnostics: the limit of those in-kernel waits, in SM clock cycles, for
+ * launches made after this call (process-wide; 0 restores the default of
+ * 4e9 cycles, about 2 s).  A very short limit makes waits run out on
+ * purpose, which exercises the give-up path above without a GPU fault.
+ * The final drain of a CTA's own operations in flight always keeps the
+ * default limit.  cycles < 0: ATTNRES_ERR_VALUE.
+ */
+int attnres_set_wait_limit(int64_t cycles);
 
 /* Static, human-readable name of a status code. */
 const char *attnres_status_string(int status);

@@ -39,6 +39,20 @@ def check(got, want, tol_abs, what=""):
     return err
 
 
+# Regression guard for the bf16 block chains, beside the benchmark spec's bound
+# (8e-3 * max|v| over the summaries, about 0.29 at their scale): one bf16 ulp
+# at the compared tensor's own largest magnitude.  The GPU and the oracle
+# round at the same points; they differ only where fp32 and fp64 land on
+# either side of a rounding boundary, so a few-percent error in one merge's
+# weights fails this bound long before the other.
+CHAIN_GUARD = 2.0 ** -7
+
+
+def check_chain(got, want, what=""):
+    bound = CHAIN_GUARD * float(np.abs(want).max())
+    return check(got, want, bound, what + " (regression guard)")
+
+
 STATS_TOL = 2e-5           # fp32 score arithmetic
 STATS_TOL_SPLIT_Q = 1e-4   # bf16 phase 1: query as bf16 hi + lo
 
@@ -269,6 +283,11 @@ def test_aggregate_backward_full_size_sampled(gpu):
     (torch.bfloat16, 4096, 9, 24, 8), (torch.bfloat16, 7168, 9, 4, 9), (torch.float32, 256, 5, 7, 66),
     (torch.bfloat16, 64, 1, 3, 20), (torch.bfloat16, 2048, 16, 2, 11), (torch.bfloat16, 4096, 10, 24, 21),
     (torch.float32, 2048, 5, 7, 1600), (torch.bfloat16, 2048, 16, 2, 900),
+    # S = 2 on the tensor-core path: the scores kernel with the softmax in its epilogue (ten
+    # summaries, one CTA per SM) writes alpha itself; and rows in two pieces with ten summaries
+    (torch.bfloat16, 4096, 9, 2, 600), (torch.bfloat16, 7168, 10, 2, 530), (torch.bfloat16, 1024, 10, 2, 1300),
+    # the largest S one call takes (the per-row kernel), bf16 and fp32
+    (torch.bfloat16, 1024, 5, 64, 40), (torch.float32, 512, 3, 64, 19), (torch.bfloat16, 4096, 9, 64, 7),
 ])
 def test_phase1_small(gpu, dtype, D, n, S, rows):
     g = wk.generator(D + n + S, gpu)
@@ -463,6 +482,8 @@ def test_two_phase_block_chain_with_prenorm(gpu, fused):
     # one bf16 rounding apart, inside the same bound
     check(Y.reshape(S, rows, D), OY, TOL[torch.bfloat16] * np.abs(OY).max(), "chain y")
     check(p.reshape(rows, D), OP, TOL[torch.bfloat16] * vmax(blocks), "chain p")
+    check_chain(Y.reshape(S, rows, D), OY, "chain y")
+    check_chain(p.reshape(rows, D), OP, "chain p")
 
 
 @pytest.mark.parametrize("fused", [True, False])
@@ -478,6 +499,8 @@ def test_two_phase_block_chain_small(gpu, fused):
     tol = TOL[torch.bfloat16] * vmax(blocks)
     check(H.reshape(S, rows, D), OH, tol, "chain h")
     check(p.reshape(rows, D), OP, tol, "chain p")
+    check_chain(H.reshape(S, rows, D), OH, "chain h")
+    check_chain(p.reshape(rows, D), OP, "chain p")
 
 
 @pytest.mark.parametrize("fused", [True, False])
@@ -492,6 +515,7 @@ def test_two_phase_block_chain_full_size_sampled(gpu, fused):
                                          f64(inp["queries"]), f64(inp["gains"]), f64(inp["u"]),
                                          inp["eps"], oracle.BF16)
     check(pick(p, rows, wl.D), OP, TOL[torch.bfloat16] * vmax(inp["blocks"]), "cfg3 chain")
+    check_chain(pick(p, rows, wl.D), OP, "cfg3 chain")
 
 
 @pytest.mark.parametrize("name", ["long_prefill_bf16", "decode_bf16"])
@@ -512,6 +536,7 @@ def test_d7168_configs_sampled(gpu, name):
                                          f64(tp["queries"]), f64(tp["gains"]), f64(tp["u"]),
                                          tp["eps"], oracle.BF16)
     check(pick(p, rows, wl.D), OP, TOL[torch.bfloat16] * vmax(tp["blocks"]), name + " chain")
+    check_chain(pick(p, rows, wl.D), OP, name + " chain")
 
 
 # --------------------------------------------------------------------------
@@ -535,6 +560,8 @@ def test_decode_overlap_and_graph(gpu):
     for p, H, name in ((p_eager, eager.h, "eager"), (p_ov, ov.h, "overlap")):
         check(pick(p, rows, wl.D), OP, tol, name + " p")
         check(H.reshape(wl.S, -1, wl.D)[:, ix], OH, tol, name + " h")
+        check_chain(pick(p, rows, wl.D), OP, name + " p")
+        check_chain(H.reshape(wl.S, -1, wl.D)[:, ix], OH, name + " h")
     # graphs replay exactly the eager launches: bitwise equal
     for blk, want in ((eager, p_eager), (ov, p_ov)):
         blk.capture()
@@ -587,7 +614,11 @@ def test_full_stack_config_full_size_sampled(gpu):
 # Wide blocks with S <= 16 (and D a multiple of 256) take the tensor-core outputs kernel, wider S the packed-FMA one.
 @pytest.mark.parametrize("S,D,L,rows", [(4, 1024, 23, 130), (12, 2048, 30, 70), (1, 512, 14, 64),
                                         (40, 1024, 25, 50), (24, 2048, 27, 129), (20, 1024, 45, 64),
-                                        (16, 256, 40, 33)])
+                                        (16, 256, 40, 33),
+                                        # S = 2 over 512+ rows: blocks of up to ten sources take the
+                                        # tensor-core phase 1 with the softmax in the scores kernel,
+                                        # wider ones the raw-score path
+                                        (2, 1024, 9, 600), (2, 512, 25, 520)])
 def test_full_two_phase_small(gpu, S, D, L, rows):
     wl = wk.WORKLOADS["full_stack_bf16"]
     inp = wk.full_stack_inputs(wl, rows=rows, device=gpu, L=L, D=D)
@@ -632,3 +663,34 @@ def test_no_kernel_wait_ran_out(gpu):
     """Every bounded in-kernel wait of the runs above completed in time."""
     from transformer_depth_wise_gb300 import _lib
     assert _lib.lib().attnres_take_device_error() == 0
+
+
+def test_wait_that_runs_out_reports_timeout(gpu):
+    """A bounded in-kernel wait that runs out, on purpose and without a fault:
+    with a limit of one clock cycle the tensor-core phase 1's waits give up
+    (each CTA takes several 128-row tiles, so at least its wait for the
+    epilogue of an earlier tile cannot have completed).  The part of a CTA
+    whose wait gave up stops, the CTA drains its copies and tensor-core
+    operations in flight, and attnres_take_device_error reports
+    ATTNRES_ERR_TIMEOUT.  The device stays usable: the same call with the
+    default limit then matches the oracle, with no error."""
+    L = _lib.lib()
+    D, n, S, rows = 2048, 9, 2, 128 * 152 * 2
+    g = wk.generator(99, gpu)
+    blocks, _ = wk.scaled_normal_sources(g, n, (1, rows, D), 0.5, 8.0, torch.bfloat16, gpu)
+    W, G = wk.queries_and_gains(g, S, D, gpu)
+    assert L.attnres_take_device_error() == 0
+    assert L.attnres_set_wait_limit(1) == 0
+    try:
+        api.block_phase1(blocks, W, G, 1e-8)
+        rc = L.attnres_take_device_error()
+    finally:
+        assert L.attnres_set_wait_limit(0) == 0
+    assert rc == -9, _lib.STATUS.get(rc, rc)                  # ATTNRES_ERR_TIMEOUT
+    o, _, lse = api.block_phase1(blocks, W, G, 1e-8)
+    assert L.attnres_take_device_error() == 0
+    sample = sample_rows(1, rows, 24, 99)
+    O, _, LSE = oracle.block_phase1([f64(pick(b, sample, D)) for b in blocks], f64(W), f64(G), 1e-8)
+    ix = torch.as_tensor(sample, device=gpu)
+    check(o.reshape(S, -1, D)[:, ix], O, TOL[torch.bfloat16] * vmax(blocks), "phase1 after a timeout")
+    check_stats(lse.reshape(S, -1)[:, ix], LSE, "lse after a timeout", STATS_TOL_SPLIT_Q)

@@ -147,8 +147,25 @@ def test_backward_argument_checks():
     assert na(arr, 3, 1, 2, 16384, 1, FAKE, None, 1e-8, FAKE, garr, 0, FAKE, None, None) == SHAPE
     assert na(arr, 3, 1, 2, 64, 5, FAKE, None, 1e-8, FAKE, garr, 0, FAKE, None, None) == DTYPE
     assert na(arr, 3, 1, 2, 64, 1, None, None, 1e-8, FAKE, garr, 0, None, None, None) == NULL
+    # every argument is checked before the scratch is looked up (a CUDA call,
+    # which fails here without a GPU): bad arguments report their own status
+    assert na(arr, 3, 1, 2, 64, 1, None, None, 1e-8, FAKE, garr, 0, FAKE, None, None) == NULL
+    assert na(arr, 3, 1, 2, 64, 1, FAKE, None, 1e-8, None, garr, 0, FAKE, None, None) == NULL
+    assert na(arr, 3, 1, 2, 64, 1, FAKE, None, 1e-8, FAKE + 8, garr, 0, FAKE, None, None) == ALIGN
+    assert na(arr, 3, 1, 2, 64, 1, FAKE, None, 1e-8, FAKE, garr, 0, FAKE + 4, None, None) == ALIGN
+    assert na(arr, 3, 1, 2, 64, 1, FAKE, None, -1.0, FAKE, garr, 0, FAKE, None, None) == VALUE
+    assert na(arr, 3, 1, 2, 64, 1, FAKE, None, 1e-8, FAKE, garr, 3, FAKE, None, None) == VALUE
+    assert na(arr, 0, 1, 2, 64, 1, FAKE, None, 1e-8, FAKE, garr, 0, FAKE, None, None) == SHAPE
+    assert na(arr, 257, 1, 2, 64, 1, FAKE, None, 1e-8, FAKE, garr, 0, FAKE, None, None) == MANY
     assert L.attnres_depth_aggregate_backward_workspace_rows(16384, 1) == SHAPE
     assert L.attnres_depth_aggregate_backward_workspace_rows(64, 7) == DTYPE
+
+
+def test_wait_limit_knob():
+    L = _lib.lib()
+    assert L.attnres_set_wait_limit(-1) == VALUE
+    assert L.attnres_set_wait_limit(1000) == OK
+    assert L.attnres_set_wait_limit(0) == OK                # back to the default
 
 
 def test_full_stack_argument_checks():

@@ -59,6 +59,7 @@ SIGNATURES = {
     "attnres_block_schedule": (_int, [_int, _int, _ip, _ip, _int]),
     "attnres_atomic_block_size": (_int, [_int, _int]),
     "attnres_take_device_error": (_int, []),
+    "attnres_set_wait_limit": (_int, [_i64]),
     "attnres_status_string": (ctypes.c_char_p, [_int]),
 }
 

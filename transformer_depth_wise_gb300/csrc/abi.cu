@@ -1,6 +1,7 @@
 // abi.cu -- the extern "C" entry points of libattnres.so (declared in
 // include/attnres.h): argument checks, then dispatch to the kernels.
 // Nothing here allocates device memory, synchronises, prints or aborts.
+#include <atomic>
 #include <cmath>
 #include <cstdint>
 
@@ -20,6 +21,15 @@ int sm_count() {
     c = v;
   }
   return c;
+}
+
+namespace {
+std::atomic<long long> g_wait_limit{0};   // 0: the default
+}  // namespace
+
+long long wait_limit_cycles() {
+  const long long v = g_wait_limit.load(std::memory_order_relaxed);
+  return v > 0 ? v : kDrainLimitCycles;
 }
 
 namespace {
@@ -43,6 +53,34 @@ int check_eps(float eps) {
 }
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? ATTNRES_OK : ATTNRES_ERR_CUDA; }
+
+// The checks both backward entry points make on everything but the workspace;
+// rows receives B*T.  With no token rows, only the query and the parameter
+// gradients must be valid (the data pointers of empty tensors may be NULL).
+int backward_checks(const void *const *sources, int n, int64_t B, int64_t T, int64_t D, int dtype,
+                    const float *query, const float *gain, float eps, const void *grad_out,
+                    void *const *grad_sources, int accumulate, const float *grad_query, const float *grad_gain,
+                    int64_t &rows) {
+  int st = check_rows(B, T, D, dtype, rows);
+  if (st) return st;
+  if (n < 1) return ATTNRES_ERR_SHAPE;
+  if (n > ATTNRES_MAX_SOURCES) return ATTNRES_ERR_TOO_MANY_SOURCES;
+  if ((st = check_eps(eps))) return st;
+  if (accumulate != 0 && accumulate != 1) return ATTNRES_ERR_VALUE;
+  if (!aggregate_backward_supported((int)D, dtype)) return ATTNRES_ERR_SHAPE;
+  if (!query) return ATTNRES_ERR_NULL;
+  if ((grad_query && !aligned16(grad_query)) || (grad_gain && !aligned16(grad_gain)) || !aligned16(query) ||
+      (gain && !aligned16(gain)))
+    return ATTNRES_ERR_ALIGNMENT;
+  if (rows == 0) return ATTNRES_OK;
+  if (!sources || !grad_out || !grad_sources) return ATTNRES_ERR_NULL;
+  for (int i = 0; i < n; ++i) {
+    if (!sources[i] || !grad_sources[i]) return ATTNRES_ERR_NULL;
+    if (!aligned16(sources[i]) || !aligned16(grad_sources[i])) return ATTNRES_ERR_ALIGNMENT;
+  }
+  if (!aligned16(grad_out)) return ATTNRES_ERR_ALIGNMENT;
+  return ATTNRES_OK;
+}
 
 }  // namespace
 }  // namespace attnres
@@ -178,18 +216,9 @@ int attnres_depth_aggregate_backward(const void *const *sources, int n, int64_t 
                                      float *grad_query, float *grad_gain, float *workspace,
                                      int64_t workspace_rows, void *stream) {
   int64_t rows = 0;
-  int st = check_rows(B, T, D, dtype, rows);
+  int st = backward_checks(sources, n, B, T, D, dtype, query, gain, eps, grad_out, grad_sources, accumulate,
+                           grad_query, grad_gain, rows);
   if (st) return st;
-  if (n < 1) return ATTNRES_ERR_SHAPE;
-  if (n > ATTNRES_MAX_SOURCES) return ATTNRES_ERR_TOO_MANY_SOURCES;
-  if ((st = check_eps(eps))) return st;
-  if (accumulate != 0 && accumulate != 1) return ATTNRES_ERR_VALUE;
-  if (!aggregate_backward_supported((int)D, dtype)) return ATTNRES_ERR_SHAPE;
-  const bool want_q = grad_query || grad_gain;
-  if (!query) return ATTNRES_ERR_NULL;
-  if ((grad_query && !aligned16(grad_query)) || (grad_gain && !aligned16(grad_gain)) || !aligned16(query) ||
-      (gain && !aligned16(gain)))
-    return ATTNRES_ERR_ALIGNMENT;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (rows == 0) {  // no token rows: the parameter gradients are zero, nothing else is touched
     if (grad_query && cudaMemsetAsync(grad_query, 0, (size_t)D * sizeof(float), s) != cudaSuccess)
@@ -198,13 +227,7 @@ int attnres_depth_aggregate_backward(const void *const *sources, int n, int64_t 
       return ATTNRES_ERR_CUDA;
     return ATTNRES_OK;
   }
-  if (!sources || !grad_out || !grad_sources) return ATTNRES_ERR_NULL;
-  for (int i = 0; i < n; ++i) {
-    if (!sources[i] || !grad_sources[i]) return ATTNRES_ERR_NULL;
-    if (!aligned16(sources[i]) || !aligned16(grad_sources[i])) return ATTNRES_ERR_ALIGNMENT;
-  }
-  if (!aligned16(grad_out)) return ATTNRES_ERR_ALIGNMENT;
-  if (want_q) {
+  if (grad_query || grad_gain) {
     if (!workspace) return ATTNRES_ERR_NULL;
     if (!aligned16(workspace)) return ATTNRES_ERR_ALIGNMENT;
     if (workspace_rows < aggregate_backward_rows_per_partial((int)D, dtype)) return ATTNRES_ERR_CAPACITY;
@@ -219,13 +242,16 @@ int attnres_depth_aggregate_backward_noalloc(const void *const *sources, int n, 
                                              float eps, const void *grad_out, void *const *grad_sources,
                                              int accumulate, float *grad_query, float *grad_gain,
                                              void *stream) {
+  // Every argument is checked before the scratch is looked up, so a bad
+  // argument reports its own status; empty inputs and calls without a
+  // parameter gradient need no scratch at all.
   int64_t rows = 0;
-  int st = check_rows(B, T, D, dtype, rows);
+  int st = backward_checks(sources, n, B, T, D, dtype, query, gain, eps, grad_out, grad_sources, accumulate,
+                           grad_query, grad_gain, rows);
   if (st) return st;
-  if (!aggregate_backward_supported((int)D, dtype)) return ATTNRES_ERR_SHAPE;
   float *scratch = nullptr;
   int64_t scratch_rows = 0;
-  if (grad_query || grad_gain) {
+  if (rows > 0 && (grad_query || grad_gain)) {
     scratch_rows = noalloc_scratch_floats() / D;
     if (scratch_rows < aggregate_backward_rows_per_partial((int)D, dtype)) return ATTNRES_ERR_SCRATCH;
     if (noalloc_scratch(scratch) != cudaSuccess) return ATTNRES_ERR_CUDA;
@@ -393,6 +419,12 @@ int attnres_full_stack_two_phase(void *const *sources, int L, int S, int64_t B, 
   AggregateArgs fin{srcs, L + 1, rows, (int)D, dtype, queries + (size_t)L * D,
                     gains ? gains + (size_t)L * D : nullptr, nullptr, eps, y_out, nullptr, nullptr, s};
   return cuda_status(launch_aggregate(fin));
+}
+
+int attnres_set_wait_limit(int64_t cycles) {
+  if (cycles < 0) return ATTNRES_ERR_VALUE;
+  g_wait_limit.store((long long)cycles, std::memory_order_relaxed);
+  return ATTNRES_OK;
 }
 
 int attnres_take_device_error(void) {

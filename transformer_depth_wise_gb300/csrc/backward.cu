@@ -21,6 +21,8 @@
 // the rows a team processes; each team writes its partial row [D] to the
 // caller's workspace and a second kernel sums the partials in a fixed order
 // (deterministic, no atomics).
+#include <atomic>
+
 #include "common.cuh"
 #include "launch.h"
 
@@ -414,21 +416,27 @@ int64_t noalloc_scratch_floats() { return kNoAllocScratchFloats; }
 
 // Device address of the scratch array on the current device.  Host code
 // cannot use the symbol itself as a device pointer; the address is looked
-// up once per device (with that device current) and cached.
+// up once per device (with that device current) and cached.  The slots are
+// atomic: two host threads making their first call on a device at the same
+// time may both look the address up, and both store the same value.  A
+// cudaDeviceReset unloads the library's device code, so the cached address
+// is stale afterwards (the header says so).
 cudaError_t noalloc_scratch(float *&ptr) {
-  static float *cache[64] = {};
+  static std::atomic<float *> cache[64];
   ptr = nullptr;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (!cache[dev]) {
-    void *p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+  float *p = cache[dev].load(std::memory_order_acquire);
+  if (!p) {
+    void *addr = nullptr;
+    e = cudaGetSymbolAddress(&addr, g_noalloc_scratch);
     if (e != cudaSuccess) return e;
-    cache[dev] = static_cast<float *>(p);
+    p = static_cast<float *>(addr);
+    cache[dev].store(p, std::memory_order_release);
   }
-  ptr = cache[dev];
+  ptr = p;
   return cudaSuccess;
 }
 

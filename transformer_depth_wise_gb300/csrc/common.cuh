@@ -296,15 +296,13 @@ __device__ __forceinline__ void cta_sum_rs(float (&v)[K], float *red /*[2][32][K
 // ---------------------------------------------------------------------------
 namespace attnres {
 
-// Upper bound on any single wait inside a kernel.  A wait that runs out sets
-// the translation unit's error flag and gives up instead of spinning forever.
-constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
-
-__device__ __forceinline__ unsigned long long globaltimer_ns() {
-  unsigned long long t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
+// Upper bound on any single wait inside a kernel, in SM clock cycles (about
+// 2 s at 2 GHz).  A wait that runs out sets the translation unit's error flag
+// and gives up instead of spinning forever.  The waits of a kernel's normal
+// work take their limit from the launch (attnres_set_wait_limit can shorten
+// it); the drain at a kernel's end, which waits for the CTA's own copies and
+// tensor-core operations still in flight, always uses this one.
+constexpr long long kDrainLimitCycles = 4000000000ll;
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -336,13 +334,17 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Wait for the phase of `parity` to complete; false if the time limit ran out.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+// Wait for the phase of `parity` to complete, for at most `limit` SM clock
+// cycles; false if the limit ran out (the caller then stops issuing work and
+// drains what it has in flight).  try_wait itself parks the thread for a
+// while, so the clock is read only between tries.
+__device__ __forceinline__ bool mbar_wait_for(uint32_t bar, uint32_t parity, long long limit) {
   if (mbar_try(bar, parity)) return true;
-  const unsigned long long t0 = globaltimer_ns();
-  while (!mbar_try(bar, parity))
-    if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
-  return true;
+  const long long t0 = clock64();
+  for (;;) {
+    if (mbar_try(bar, parity)) return true;
+    if (clock64() - t0 > limit) return false;
+  }
 }
 
 // 1-D bulk copy global -> shared (this CTA), completion counted on `bar`.

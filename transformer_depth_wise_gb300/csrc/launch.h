@@ -10,6 +10,10 @@ namespace attnres {
 // Streaming-multiprocessor count of the current device (cached per device).
 int sm_count();
 
+// SM clock cycles an in-kernel wait of a launch's work loop may take before
+// it gives up (attnres_set_wait_limit; about 2 s by default).
+long long wait_limit_cycles();
+
 struct AggregateArgs {
   const void *const *sources;  // host array of n device pointers
   int n;
@@ -139,13 +143,14 @@ struct Phase1Args {
 // Returns ATTNRES_OK or a (negative) status for shapes the kernels cannot take.
 int phase1_check(int n, int D, int dtype, int S);
 cudaError_t launch_phase1(const Phase1Args &a);
-// Tensor-core phase 1 (bf16, D = 512 * {1,2,4,8}, n <= 9, S <= 24).
+// Tensor-core phase 1 (bf16, D a multiple of 64 up to 8192, n <= 10, S <= 24).
 bool phase1_tc_supported(int n, int D, int dtype, int S);
 cudaError_t launch_phase1_tc(const Phase1Args &a);
 
-// Phase 1 over any number of summaries (bf16): tensor-core scores ten
-// summaries per call into a raw-score buffer, a softmax over all of them,
-// then the outputs.  scores: [rows][n][S] fp32 scratch, left holding alpha.
+// Phase 1 over any number of summaries (bf16): tensor-core scores, five
+// summaries per work item, into a raw-score buffer, a softmax over all of
+// them, then the outputs.  scores: [rows][n][S] fp32 scratch, left holding
+// alpha.
 // Most summaries the fused phase-1 path takes in one pass (its TMEM holds
 // ten sources' scores); wider blocks go through the raw-score path below.
 constexpr int kP1TcMaxSources = 10;

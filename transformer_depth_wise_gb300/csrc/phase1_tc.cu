@@ -36,13 +36,17 @@
 // with packed fp32x2 FMAs, and stored.  The pages' shape (9 summaries, 24
 // queries) has an instantiation with both counts built in.
 //
-// More than ten summaries (the Full two-phase schedule): kernel A in a
-// raw-score mode over work items (tile, ten summaries), a softmax kernel,
-// and a tensor-core outputs kernel (mma.sync, K = 16 summaries per step).
+// Raw-score mode.  With S >= 3 (and room in the token's o[1] row), and for
+// more than ten summaries (the Full two-phase schedule), kernel A runs over
+// work items (tile, five summaries) at two CTAs per SM and writes raw scores
+// only; a softmax kernel then turns them into alpha, m and lse.  Beyond ten
+// summaries the outputs come from a tensor-core kernel (mma.sync, K = 16
+// summaries per step) or, for S > 16, a packed-FMA kernel.
 //
 // Each summary byte is read twice (once per kernel); there is no cluster or
 // cross-CTA exchange.  Every in-kernel wait is bounded: one that runs out
-// records a flag and the kernel runs to its end.
+// records a flag, its role stops issuing work, and the CTA drains what it
+// has in flight before it ends.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -66,7 +70,6 @@ constexpr uint32_t kQBytes = kNQ * kKc * 2;
 constexpr uint32_t kStageBytes = kVBytes + kQBytes;   // both parts 1024-byte aligned
 constexpr int kTmemCols = 512;
 constexpr int kBStages = 3;           // kernel B: tokens in flight (cp.async stages)
-constexpr long long kWaitLimitCycles = 4000000000ll;   // ~2 s at 2 GHz: bound on any wait
 constexpr int kWarpsA = 6;            // 0-3: sums of squares + epilogue, 4: TMA, 5: MMA
 constexpr int kThreadsA = kWarpsA * 32;
 constexpr uint32_t kOffBar = kStages * kStageBytes;
@@ -91,12 +94,13 @@ struct ParamsAT {
   int n, S, D;
   float eps, inv_D;
   // Raw-score mode (any number of summaries): the work items are (tile,
-  // chunk of ten summaries); each writes the scores s[row][i][q] of its
+  // chunk of CH summaries); each writes the scores s[row][i][q] of its
   // chunk to raw ([rows][n][S] fp32) and nothing else; the softmax over all
   // of them runs afterwards.  Without raw, n <= 10 and there is one chunk.
   float *raw;
   int raw_n, raw_off;                 // raw's summary count and this launch's first summary
   int64_t raw_stride;                 // floats from one row's scores to the next (raw_n * S when packed)
+  long long wait_limit;               // SM clock cycles any wait of the work loop may take
 };
 // The fused path (up to ten summaries) and the raw-score path, which takes
 // up to kManyMaps summaries per launch (the tensor maps ride in the kernel
@@ -115,24 +119,26 @@ struct ParamsB {
 };
 
 // --- small PTX wrappers ------------------------------------------------------
-// After any wait in the process has run out, every later wait gives up at
-// once, so a broken run ends quickly instead of spending the limit per wait.
-__device__ __forceinline__ bool aborted() {
-  return *reinterpret_cast<volatile unsigned int *>(&g_error_flag) != 0;
+// Bounded waits.  A wait of the work loop that runs out raises the error flag
+// and returns false; the role that waited then stops issuing work (it never
+// signals a stage it did not consume, so no producer refills a stage that is
+// still being read), and every role that issued asynchronous work drains it
+// before the CTA ends (drain_wait, with the fixed drain limit): the TMA
+// producer lanes wait for their last copies to land, the MMA thread for its
+// last tensor-core operations to complete.  Only then is TMEM freed.
+__device__ __forceinline__ bool wait_local(uint32_t bar, uint32_t parity, long long limit) {
+  if (mbar_wait_for(bar, parity, limit)) return true;
+  raise_timeout();
+  return false;
 }
-__device__ __forceinline__ void wait_local(uint32_t bar, uint32_t parity) {
-  if (mbar_try(bar, parity)) return;
-  // try_wait already parks the thread for a while; the clock and the global
-  // abort flag are looked at only every 1024 tries, so a short wait costs
-  // no global-memory round trip.
-  const long long t0 = clock64();
-  for (uint32_t it = 1;; ++it) {
-    if (mbar_try(bar, parity)) return;
-    if ((it & 1023u) == 0) {
-      if (aborted()) return;
-      if (clock64() - t0 > kWaitLimitCycles) { raise_timeout(); return; }
-    }
-  }
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity) {
+  if (!mbar_wait_for(bar, parity, kDrainLimitCycles)) raise_timeout();
+}
+// The error flag as a launch finds it: set means a wait of an earlier launch
+// ran out and the host has not taken the error yet; such a launch issues
+// nothing (its results would be invalid as well).
+__device__ __forceinline__ bool error_pending() {
+  return *reinterpret_cast<volatile unsigned int *>(&g_error_flag) != 0;
 }
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, int x, int y,
@@ -229,17 +235,24 @@ __global__ void __launch_bounds__(kThreadsA, CH == kMaxN ? 1 : 2) p1_scores_kern
   auto VEMPTY = [&](int s) { return b0 + 8u * (ST + s); };
   const uint32_t TDONE = b0 + 8u * (2 * ST);
   const uint32_t TFREE = TDONE + 8u;
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + OFF_BAR + 8 * (2 * ST + 2));
+  const uint32_t MDRAIN = TFREE + 8u;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + OFF_BAR + 8 * (2 * ST + 3));
+  uint32_t *skip = tmem_slot + 1;
+  const long long lim = p.wait_limit;
 
   if (threadIdx.x == 0) {
+    *skip = error_pending() ? 1u : 0u;
     for (int s = 0; s < ST; ++s) {
       mbar_init(VFULL(s), 1);
       mbar_init(VEMPTY(s), 1 + 4);    // the MMA's commit + the four row warps
     }
     mbar_init(TDONE, 1);
     mbar_init(TFREE, 4);
+    mbar_init(MDRAIN, 1);
     fence_mbar_init();
   }
+  __syncthreads();
+  if (*skip) return;                  // nothing issued yet: no copy, no TMEM
   if (warp == 5) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
                  :: "r"(smem_u32(tmem_slot)), "r"(TC));
@@ -249,7 +262,7 @@ __global__ void __launch_bounds__(kThreadsA, CH == kMaxN ? 1 : 2) p1_scores_kern
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
   const uint32_t tmem_base = *tmem_slot;
 
-  // Work items: (tile of 128 rows, chunk of up to ten summaries), tile-minor.
+  // Work items: (tile of 128 rows, chunk of up to CH summaries), tile-minor.
   const int64_t tiles = (p.rows + kRows - 1) / kRows;
   const int64_t items = tiles * ((n + CH - 1) / CH);
   const int64_t my_tiles = items > (int64_t)blockIdx.x ? (items - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
@@ -273,14 +286,17 @@ __global__ void __launch_bounds__(kThreadsA, CH == kMaxN ? 1 : 2) p1_scores_kern
     if (lane < ST) {
       int64_t g = 0, last = -1;
       int s = 0;  // g % ST
-      for (int64_t tl = 0; tl < my_tiles; ++tl) {
+      bool ok = true;
+      for (int64_t tl = 0; tl < my_tiles && ok; ++tl) {
         int64_t tile;
         int i0, nc;
         item_of(tl, tile, i0, nc);
-        for (int i = 0; i < nc; ++i)
+        for (int i = 0; i < nc && ok; ++i)
           for (int kc = 0; kc < KC; ++kc, ++g) {
             if (s == lane) {
-              if (g >= ST) wait_local(VEMPTY(s), (uint32_t)((g / ST - 1) & 1));
+              // a stage is refilled only once every consumer is done with it
+              // (which they signal only after its copy has landed)
+              if (g >= ST && !wait_local(VEMPTY(s), (uint32_t)((g / ST - 1) & 1), lim)) { ok = false; break; }
               mbar_expect_tx(VFULL(s), kStageBytes);
               const uint32_t st = base + (uint32_t)s * kStageBytes;
               tma_load_2d(st, &p.tmap[i0 + i], kc * kKc, (int)(tile * kRows), VFULL(s));
@@ -290,25 +306,27 @@ __global__ void __launch_bounds__(kThreadsA, CH == kMaxN ? 1 : 2) p1_scores_kern
             if (++s == ST) s = 0;
           }
       }
-      // this lane's last stage has landed before the CTA may exit (its
-      // earlier uses were consumed before the stage was refilled)
-      if (last >= 0) wait_local(VFULL(lane), (uint32_t)((last / ST) & 1));
+      // drain: this lane's last copies have landed before the CTA may exit
+      // (its earlier uses of the stage landed before the stage was refilled)
+      if (last >= 0) drain_wait(VFULL(lane), (uint32_t)((last / ST) & 1));
     }
   } else if (warp == 5) {
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
       const uint32_t idesc = idesc_bf16(kRows, kNQ);
       int64_t g = 0;
-      for (int64_t tl = 0; tl < my_tiles; ++tl) {
-        if (tl >= 1) wait_local(TFREE, (uint32_t)((tl - 1) & 1));   // epilogue read the last tile
+      bool ok = true;
+      for (int64_t tl = 0; tl < my_tiles && ok; ++tl) {
+        // the epilogue has read the last tile's accumulators
+        if (tl >= 1 && !wait_local(TFREE, (uint32_t)((tl - 1) & 1), lim)) break;
         asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
         int64_t tile;
         int i0, nc;
         item_of(tl, tile, i0, nc);
-        for (int i = 0; i < nc; ++i)
+        for (int i = 0; i < nc && ok; ++i)
           for (int kc = 0; kc < KC; ++kc, ++g) {
             const int s = (int)(g % ST);
-            wait_local(VFULL(s), (uint32_t)((g / ST) & 1));
+            if (!wait_local(VFULL(s), (uint32_t)((g / ST) & 1), lim)) { ok = false; break; }
             asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
             const uint32_t st = base + (uint32_t)s * kStageBytes;
 #pragma unroll
@@ -319,15 +337,19 @@ __global__ void __launch_bounds__(kThreadsA, CH == kMaxN ? 1 : 2) p1_scores_kern
             }
             mma_commit(VEMPTY(s));
           }
-        mma_commit(TDONE);
+        if (ok) mma_commit(TDONE);
       }
+      // drain: every MMA this thread issued has completed
+      mma_commit(MDRAIN);
+      drain_wait(MDRAIN, 0);
     }
   } else {
     // ---------------- warps 0-3: row sums of squares, then the epilogue ----------------
     const int r = threadIdx.x;                                   // token row in the tile = TMEM lane
     const uint32_t taddr = tmem_base + ((uint32_t)(warp * 32) << 16);
     int64_t g = 0;
-    for (int64_t tl = 0; tl < my_tiles; ++tl) {
+    bool ok = true;
+    for (int64_t tl = 0; tl < my_tiles && ok; ++tl) {
       int64_t tile;
       int i0, nc;
       item_of(tl, tile, i0, nc);
@@ -336,10 +358,12 @@ __global__ void __launch_bounds__(kThreadsA, CH == kMaxN ? 1 : 2) p1_scores_kern
       for (int i = 0; i < CH; ++i) ss[i] = 0.f;
 #pragma unroll
       for (int i = 0; i < CH; ++i) {
-        if (i >= nc) continue;
+        if (i >= nc || !ok) continue;
         for (int kc = 0; kc < KC; ++kc, ++g) {
           const int s = (int)(g % ST);
-          wait_local(VFULL(s), (uint32_t)((g / ST) & 1));
+          // every lane waits; the warp goes on only if all of them saw the
+          // stage land (the code below syncs the warp)
+          if (!__all_sync(0xffffffffu, wait_local(VFULL(s), (uint32_t)((g / ST) & 1), lim))) { ok = false; break; }
           const unsigned char *row = sm + (uint32_t)s * kStageBytes;
           uint4 v[8];
 #pragma unroll
@@ -358,7 +382,7 @@ __global__ void __launch_bounds__(kThreadsA, CH == kMaxN ? 1 : 2) p1_scores_kern
         }
       }
       // epilogue: scores -> softmax over the n summaries -> alpha, m, lse
-      wait_local(TDONE, (uint32_t)(tl & 1));
+      if (!ok || !__all_sync(0xffffffffu, wait_local(TDONE, (uint32_t)(tl & 1), lim))) { ok = false; break; }
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
       float rinv[CH];
 #pragma unroll
@@ -926,6 +950,7 @@ cudaError_t launch_phase1_tc(const Phase1Args &a) {
   pa.D = a.D;
   pa.eps = a.eps;
   pa.inv_D = 1.f / (float)a.D;
+  pa.wait_limit = wait_limit_cycles();
   cudaError_t e = cudaSuccess;
   const int64_t tiles = (a.rows + kRows - 1) / kRows;
   // Raw scores with five-summary items, two CTAs per SM (tensor-map loads
@@ -1037,13 +1062,14 @@ cudaError_t launch_phase1_many(const Phase1ManyArgs &a) {
   pa.raw = a.scores;
   pa.raw_n = a.n;
   pa.raw_stride = (int64_t)a.n * a.S;
+  pa.wait_limit = wait_limit_cycles();
   constexpr int kManyCh = 5;   // summaries per work item here: two CTAs per SM
   cudaError_t e = cudaFuncSetAttribute(p1_scores_kernel<kManyMaps, kManyCh>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_a(kManyCh));
   if (e != cudaSuccess) return e;
   const int64_t tiles = (a.rows + kRows - 1) / kRows;
   // Raw scores: one launch per kManyMaps summaries, its work items (tile,
-  // chunk of ten) spread evenly over the SMs.
+  // chunk of five) spread evenly over the SMs.
   for (int off = 0; off < a.n; off += kManyMaps) {
     const int nl = a.n - off < kManyMaps ? a.n - off : kManyMaps;
     for (int i = 0; i < nl; ++i) {

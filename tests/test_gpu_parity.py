@@ -40,17 +40,25 @@ def check(got, want, tol_abs, what=""):
 
 
 # Regression guard for the bf16 block chains, beside the benchmark spec's bound
-# (8e-3 * max|v| over the summaries, about 0.29 at their scale): one bf16 ulp
-# at the compared tensor's own largest magnitude.  The GPU and the oracle
-# round at the same points; they differ only where fp32 and fp64 land on
-# either side of a rounding boundary, so a few-percent error in one merge's
-# weights fails this bound long before the other.
-CHAIN_GUARD = 2.0 ** -7
+# (8e-3 * max|v| over the summaries, about 0.29 at their scale).  The GPU and
+# the oracle round at the same points and differ only where fp32 and fp64
+# land on either side of a rounding boundary; such a flip in p_k carries on
+# through the later updates, so single elements can end a few ulps apart
+# (up to 2^-6 * max|p| has been seen over 100k sampled elements), but most
+# elements agree exactly.  The guard bounds the root-mean-square error by
+# 2^-8 of the compared tensor's own RMS: a few-percent error in one merge's
+# weights shifts most elements of every later sublayer by several ulps and
+# fails it, while the rare flips stay far below it.
+CHAIN_RMS_GUARD = 2.0 ** -8
 
 
 def check_chain(got, want, what=""):
-    bound = CHAIN_GUARD * float(np.abs(want).max())
-    return check(got, want, bound, what + " (regression guard)")
+    d = f64(got) - want
+    rms_err = float(np.sqrt(np.mean(d * d)))
+    rms = float(np.sqrt(np.mean(want * want)))
+    assert rms_err <= CHAIN_RMS_GUARD * rms, \
+        f"{what} (regression guard): rms err {rms_err:.3e} > {CHAIN_RMS_GUARD:.3g} * rms {rms:.3e}"
+    return rms_err
 
 
 STATS_TOL = 2e-5           # fp32 score arithmetic

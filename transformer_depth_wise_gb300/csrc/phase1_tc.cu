@@ -52,6 +52,7 @@
 
 #include "common.cuh"
 #include "launch.h"
+#include "tcgen05.cuh"
 
 ATTNRES_DEFINE_ERROR_FLAG(take_error_phase1_tc)
 
@@ -149,46 +150,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
       :: "r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar) : "memory");
 }
 
-// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups
-// `sbo` bytes apart (the leading offset is unused for this layout).
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t addr, uint32_t sbo) {
-  uint64_t d = 0;
-  d |= (uint64_t)((addr & 0x3FFFFu) >> 4);
-  d |= (uint64_t)1 << 16;                         // leading byte offset (unused): 16 B
-  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
-  d |= (uint64_t)1 << 46;                         // descriptor version (sm_100 family)
-  d |= (uint64_t)2 << 61;                         // 128-byte swizzle
-  return d;
-}
-
-// Instruction descriptor, kind::f16: bf16 A and B (both K-major), fp32 D.
-__host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
-}
-
-__device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t a, uint64_t b, uint32_t idesc,
-                                         uint32_t accumulate) {
-  asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}"
-      :: "r"(tmem_d), "l"(a), "l"(b), "r"(idesc), "r"(accumulate));
-}
-__device__ __forceinline__ void mma_commit(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
-               :: "r"(bar) : "memory");
-}
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float *v) {
-  uint32_t r[16];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr));
-#pragma unroll
-  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
-}
-
 // Byte offset of 16-byte chunk `j` of row `r` inside a 1024-byte, 8-row atom
 // written by TMA (or by hand) with the 128-byte swizzle.
 __device__ __forceinline__ uint32_t swz(uint32_t r, uint32_t j) { return r * 128u + ((j ^ (r & 7u)) << 4); }
@@ -254,12 +215,10 @@ __global__ void __launch_bounds__(kThreadsA, CH == kMaxN ? 1 : 2) p1_scores_kern
   __syncthreads();
   if (*skip) return;                  // nothing issued yet: no copy, no TMEM
   if (warp == 5) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
-                 :: "r"(smem_u32(tmem_slot)), "r"(TC));
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    tmem_alloc(smem_u32(tmem_slot), TC);
   }
   __syncthreads();
-  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+  tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
   // Work items: (tile of 128 rows, chunk of up to CH summaries), tile-minor.
@@ -319,7 +278,7 @@ __global__ void __launch_bounds__(kThreadsA, CH == kMaxN ? 1 : 2) p1_scores_kern
       for (int64_t tl = 0; tl < my_tiles && ok; ++tl) {
         // the epilogue has read the last tile's accumulators
         if (tl >= 1 && !wait_local(TFREE, (uint32_t)((tl - 1) & 1), lim)) break;
-        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+        tc_fence_after();
         int64_t tile;
         int i0, nc;
         item_of(tl, tile, i0, nc);
@@ -327,7 +286,7 @@ __global__ void __launch_bounds__(kThreadsA, CH == kMaxN ? 1 : 2) p1_scores_kern
           for (int kc = 0; kc < KC; ++kc, ++g) {
             const int s = (int)(g % ST);
             if (!wait_local(VFULL(s), (uint32_t)((g / ST) & 1), lim)) { ok = false; break; }
-            asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+            tc_fence_after();
             const uint32_t st = base + (uint32_t)s * kStageBytes;
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
@@ -383,7 +342,7 @@ __global__ void __launch_bounds__(kThreadsA, CH == kMaxN ? 1 : 2) p1_scores_kern
       }
       // epilogue: scores -> softmax over the n summaries -> alpha, m, lse
       if (!ok || !__all_sync(0xffffffffu, wait_local(TDONE, (uint32_t)(tl & 1), lim))) { ok = false; break; }
-      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      tc_fence_after();
       float rinv[CH];
 #pragma unroll
       for (int i = 0; i < CH; ++i) rinv[i] = rsqrtf(fmaf(ss[i], p.inv_D, p.eps));
@@ -396,7 +355,7 @@ __global__ void __launch_bounds__(kThreadsA, CH == kMaxN ? 1 : 2) p1_scores_kern
           tmem_ld16(taddr + i * kNQ, c);
           tmem_ld16(taddr + i * kNQ + 16, c + 16);
           tmem_ld16(taddr + i * kNQ + 32, c + 32);
-          asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+          tmem_wait_ld();
           if (row < p.rows) {
             float *dst = p.raw + (size_t)row * p.raw_stride + (size_t)(p.raw_off + i0 + i) * S;
 #pragma unroll
@@ -404,7 +363,7 @@ __global__ void __launch_bounds__(kThreadsA, CH == kMaxN ? 1 : 2) p1_scores_kern
               if (q < S) dst[q] = (c[q] + c[kMaxS + q]) * rinv[i];
           }
         }
-        asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+        tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(TFREE);
         continue;
@@ -419,7 +378,7 @@ __global__ void __launch_bounds__(kThreadsA, CH == kMaxN ? 1 : 2) p1_scores_kern
         tmem_ld16(taddr + i * kNQ, c);
         tmem_ld16(taddr + i * kNQ + 16, c + 16);
         tmem_ld16(taddr + i * kNQ + 32, c + 32);
-        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+        tmem_wait_ld();
 #pragma unroll
         for (int q = 0; q < kMaxS; ++q) m[q] = fmaxf(m[q], (c[q] + c[kMaxS + q]) * rinv[i]);
       }
@@ -429,7 +388,7 @@ __global__ void __launch_bounds__(kThreadsA, CH == kMaxN ? 1 : 2) p1_scores_kern
         tmem_ld16(taddr + i * kNQ, c);
         tmem_ld16(taddr + i * kNQ + 16, c + 16);
         tmem_ld16(taddr + i * kNQ + 32, c + 32);
-        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+        tmem_wait_ld();
 #pragma unroll
         for (int q = 0; q < kMaxS; ++q) den[q] += expf((c[q] + c[kMaxS + q]) * rinv[i] - m[q]);
       }
@@ -442,7 +401,7 @@ __global__ void __launch_bounds__(kThreadsA, CH == kMaxN ? 1 : 2) p1_scores_kern
         tmem_ld16(taddr + i * kNQ, c);
         tmem_ld16(taddr + i * kNQ + 16, c + 16);
         tmem_ld16(taddr + i * kNQ + 32, c + 32);
-        asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+        tmem_wait_ld();
         float a[kMaxS];
 #pragma unroll
         for (int q = 0; q < kMaxS; ++q) a[q] = expf((c[q] + c[kMaxS + q]) * rinv[i] - m[q]) / den[q];
@@ -454,7 +413,7 @@ __global__ void __launch_bounds__(kThreadsA, CH == kMaxN ? 1 : 2) p1_scores_kern
               *reinterpret_cast<float4 *>(alpha + 2 * (i * Sp + q)) = make_float4(a[q], a[q], a[q + 1], a[q + 1]);
         }
       }
-      asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+      tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(TFREE);
       if (row_ok) {
@@ -470,8 +429,8 @@ __global__ void __launch_bounds__(kThreadsA, CH == kMaxN ? 1 : 2) p1_scores_kern
   }
   __syncthreads();
   if (warp == 5) {
-    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" :: "r"(tmem_base), "r"(TC));
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TC);
   }
 }
 

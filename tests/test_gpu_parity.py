@@ -296,6 +296,10 @@ def test_aggregate_backward_full_size_sampled(gpu):
     (torch.bfloat16, 4096, 9, 2, 600), (torch.bfloat16, 7168, 10, 2, 530), (torch.bfloat16, 1024, 10, 2, 1300),
     # the largest S one call takes (the per-row kernel), bf16 and fp32
     (torch.bfloat16, 1024, 5, 64, 40), (torch.float32, 512, 3, 64, 19), (torch.bfloat16, 4096, 9, 64, 7),
+    # few rows (64..511) on the tensor cores with the scores split over feature slices: the decode
+    # shape, one partly filled tile, an odd S (pad query), ten summaries at S = 3
+    (torch.bfloat16, 7168, 9, 24, 256), (torch.bfloat16, 4096, 9, 24, 100), (torch.bfloat16, 2048, 5, 7, 300),
+    (torch.bfloat16, 1024, 10, 3, 64),
 ])
 def test_phase1_small(gpu, dtype, D, n, S, rows):
     g = wk.generator(D + n + S, gpu)

@@ -146,6 +146,9 @@ cudaError_t launch_phase1(const Phase1Args &a);
 // Tensor-core phase 1 (bf16, D a multiple of 64 up to 8192, n <= 10, S <= 24).
 bool phase1_tc_supported(int n, int D, int dtype, int S);
 cudaError_t launch_phase1_tc(const Phase1Args &a);
+// Feature slices the tensor-core path splits the scores into for few token
+// rows (partial sums in the tokens' o[1] rows), or 1 when it does not.
+int split_parts(const Phase1Args &a);
 
 // Phase 1 over any number of summaries (bf16): tensor-core scores, five
 // summaries per work item, into a raw-score buffer, a softmax over all of

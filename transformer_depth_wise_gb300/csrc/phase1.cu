@@ -20,6 +20,7 @@ ATTNRES_DEFINE_ERROR_FLAG(take_error_phase1)
 namespace attnres {
 
 constexpr int kP1MaxN = 16;  // summaries per phase-1 call (this kernel)
+constexpr int64_t kSplitMinRows = 64;   // token rows from which the split tensor-core path is taken
 
 struct P1Params {
   const void *src[kP1MaxN];
@@ -224,9 +225,12 @@ int phase1_check(int n, int D, int dtype, int S) {
 cudaError_t launch_phase1(const Phase1Args &a) {
   // The tensor-core path parks the split queries in the last 48 D-rows of
   // `out`, which must not overlap out[0] (where it parks alpha).  Its scores
-  // kernel works on 128-row tiles, one CTA each: below four tiles the
-  // one-CTA-per-row kernel spreads wider and is faster.
-  if (phase1_tc_supported(a.n, a.D, a.dtype, a.S) && (int64_t)(a.S - 1) * a.rows >= 48 && a.rows >= 512)
+  // kernel works on 128-row tiles; from 512 rows its work items (tile, five
+  // summaries) fill the GPU.  With fewer rows (from kSplitMinRows) it splits
+  // the scores over slices of the features instead (split_parts), so that a
+  // decode batch still fills it; below that the one-CTA-per-row kernel.
+  if (phase1_tc_supported(a.n, a.D, a.dtype, a.S) && (int64_t)(a.S - 1) * a.rows >= 48 &&
+      (a.rows >= 512 || (a.rows >= kSplitMinRows && split_parts(a) > 1)))
     return launch_phase1_tc(a);
   Cfg c;
   if (!choose(a.n, a.D, a.dtype, c)) return cudaErrorInvalidValue;

@@ -101,6 +101,11 @@ struct ParamsAT {
   float *raw;
   int raw_n, raw_off;                 // raw's summary count and this launch's first summary
   int64_t raw_stride;                 // floats from one row's scores to the next (raw_n * S when packed)
+  // Split mode (few token rows, raw set): the work items are (tile, chunk
+  // of CH summaries, part kp of kparts slices of the features); each writes
+  // its partial dot products and partial sums of squares, unnormalised, to
+  // slot kp of the row's raw area: [kp][n S dots, then n sums of squares].
+  int kparts;                         // 1: every item covers all of D
   long long wait_limit;               // SM clock cycles any wait of the work loop may take
 };
 // The fused path (up to ten summaries) and the raw-score path, which takes
@@ -223,15 +228,19 @@ __global__ void __launch_bounds__(kThreadsA, CH == kMaxN ? 1 : 2) p1_scores_kern
 
   // Work items: (tile of 128 rows, chunk of up to CH summaries), tile-minor.
   const int64_t tiles = (p.rows + kRows - 1) / kRows;
-  const int64_t items = tiles * ((n + CH - 1) / CH);
+  const int kparts = p.kparts;
+  const int64_t items = tiles * ((n + CH - 1) / CH) * kparts;
   const int64_t my_tiles = items > (int64_t)blockIdx.x ? (items - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
-  auto item_of = [&](int64_t tl, int64_t &tile, int &i0, int &nc) {
+  const int KCP = p.D / kKc / kparts;                 // 64-feature chunks per item
+  // item -> (tile, first summary i0 and count nc, feature chunks [kc0, kc0 + KCP))
+  auto item_of = [&](int64_t tl, int64_t &tile, int &i0, int &nc, int &kc0) {
     const int64_t item = (int64_t)blockIdx.x + tl * gridDim.x;
     tile = item % tiles;
-    i0 = (int)(item / tiles) * CH;
+    const int64_t rest = item / tiles;
+    kc0 = (int)(rest % kparts) * KCP;
+    i0 = (int)(rest / kparts) * CH;
     nc = n - i0 < CH ? n - i0 : CH;
   };
-  const int KC = p.D / kKc;
 
   if (warp == 4) {
     // ---------------- TMA producers: (tile, summary, chunk) stages ----------------
@@ -248,10 +257,10 @@ __global__ void __launch_bounds__(kThreadsA, CH == kMaxN ? 1 : 2) p1_scores_kern
       bool ok = true;
       for (int64_t tl = 0; tl < my_tiles && ok; ++tl) {
         int64_t tile;
-        int i0, nc;
-        item_of(tl, tile, i0, nc);
+        int i0, nc, kc0;
+        item_of(tl, tile, i0, nc, kc0);
         for (int i = 0; i < nc && ok; ++i)
-          for (int kc = 0; kc < KC; ++kc, ++g) {
+          for (int kc = kc0; kc < kc0 + KCP; ++kc, ++g) {
             if (s == lane) {
               // a stage is refilled only once every consumer is done with it
               // (which they signal only after its copy has landed)
@@ -280,10 +289,10 @@ __global__ void __launch_bounds__(kThreadsA, CH == kMaxN ? 1 : 2) p1_scores_kern
         if (tl >= 1 && !wait_local(TFREE, (uint32_t)((tl - 1) & 1), lim)) break;
         tc_fence_after();
         int64_t tile;
-        int i0, nc;
-        item_of(tl, tile, i0, nc);
+        int i0, nc, kc0;
+        item_of(tl, tile, i0, nc, kc0);
         for (int i = 0; i < nc && ok; ++i)
-          for (int kc = 0; kc < KC; ++kc, ++g) {
+          for (int kc = kc0; kc < kc0 + KCP; ++kc, ++g) {
             const int s = (int)(g % ST);
             if (!wait_local(VFULL(s), (uint32_t)((g / ST) & 1), lim)) { ok = false; break; }
             tc_fence_after();
@@ -292,7 +301,7 @@ __global__ void __launch_bounds__(kThreadsA, CH == kMaxN ? 1 : 2) p1_scores_kern
             for (int kk = 0; kk < 4; ++kk) {
               const uint64_t a = sw128_desc(st + kk * 32u, 1024u);
               const uint64_t b = sw128_desc(st + kVBytes + kk * 32u, 1024u);
-              mma_bf16(tmem_base + (uint32_t)(i * kNQ), a, b, idesc, (kc | kk) != 0);
+              mma_bf16(tmem_base + (uint32_t)(i * kNQ), a, b, idesc, (kc > kc0 || kk != 0) ? 1u : 0u);
             }
             mma_commit(VEMPTY(s));
           }
@@ -310,15 +319,15 @@ __global__ void __launch_bounds__(kThreadsA, CH == kMaxN ? 1 : 2) p1_scores_kern
     bool ok = true;
     for (int64_t tl = 0; tl < my_tiles && ok; ++tl) {
       int64_t tile;
-      int i0, nc;
-      item_of(tl, tile, i0, nc);
+      int i0, nc, kc0;
+      item_of(tl, tile, i0, nc, kc0);
       float ss[CH];
 #pragma unroll
       for (int i = 0; i < CH; ++i) ss[i] = 0.f;
 #pragma unroll
       for (int i = 0; i < CH; ++i) {
         if (i >= nc || !ok) continue;
-        for (int kc = 0; kc < KC; ++kc, ++g) {
+        for (int kc = kc0; kc < kc0 + KCP; ++kc, ++g) {
           const int s = (int)(g % ST);
           // every lane waits; the warp goes on only if all of them saw the
           // stage land (the code below syncs the warp)
@@ -346,6 +355,29 @@ __global__ void __launch_bounds__(kThreadsA, CH == kMaxN ? 1 : 2) p1_scores_kern
       float rinv[CH];
 #pragma unroll
       for (int i = 0; i < CH; ++i) rinv[i] = rsqrtf(fmaf(ss[i], p.inv_D, p.eps));
+      if (kparts > 1) {                                          // split mode: partials
+        const int64_t row = tile * kRows + r;
+        float c[kNQ];
+        float *slot = p.raw + (size_t)row * p.raw_stride + (size_t)(kc0 / KCP) * (size_t)(n * S + n);
+#pragma unroll
+        for (int i = 0; i < CH; ++i) {
+          if (i >= nc) continue;
+          tmem_ld16(taddr + i * kNQ, c);
+          tmem_ld16(taddr + i * kNQ + 16, c + 16);
+          tmem_ld16(taddr + i * kNQ + 32, c + 32);
+          tmem_wait_ld();
+          if (row < p.rows) {
+#pragma unroll
+            for (int q = 0; q < kMaxS; ++q)
+              if (q < S) slot[(size_t)(i0 + i) * S + q] = c[q] + c[kMaxS + q];
+            slot[(size_t)n * S + i0 + i] = ss[i];
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(TFREE);
+        continue;
+      }
       if (p.raw) {                                               // raw-score mode
         const int64_t row = tile * kRows + r;
         float c[kNQ];
@@ -561,6 +593,59 @@ p1_park_softmax_kernel(const float *raw, float *alpha, int64_t row_floats, int64
       const float a = expf(s[(size_t)i * S] - m) * inv;
       *reinterpret_cast<float2 *>(al + 2 * (i * Sp + q)) = make_float2(a, a);
     }
+    out_lse[(size_t)q * rows + row] = m + logf(den);
+    if (out_max) out_max[(size_t)q * rows + row] = m;
+  }
+}
+
+// -----------------------------------------------------------------------------
+// Split mode: each token's o[1] row holds kparts slots of partial dot
+// products [n][S] and partial sums of squares [n] over slices of the
+// features.  One thread per (row, query) adds them up in slot order, forms
+// the scores, takes their softmax, writes m and lse, and writes alpha into
+// the token's o[0] row in the layout the outputs kernel reads.
+// -----------------------------------------------------------------------------
+__global__ void __launch_bounds__(256)
+p1_split_softmax_kernel(const float *raw, float *alpha, int64_t row_floats, int64_t rows, int n, int S, int kparts,
+                        float inv_D, float eps, float *out_max, float *out_lse) {
+  const int Sp = S + (S & 1);
+  const int64_t total = rows * Sp;
+  const int slot = n * S + n;
+  for (int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; g < total; g += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t row = g / Sp;
+    const int q = (int)(g % Sp);
+    float *al = alpha + (size_t)row * row_floats;
+    if (q >= S) {                                   // the pad query of an odd S
+      for (int i = 0; i < n; ++i) *reinterpret_cast<float2 *>(al + 2 * (i * Sp + q)) = make_float2(0.f, 0.f);
+      continue;
+    }
+    const float *pr = raw + (size_t)row * row_floats;
+    float sc[kMaxN];
+    float m = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < kMaxN; ++i) {
+      sc[i] = -INFINITY;
+      if (i < n) {
+        float dot = 0.f, ss = 0.f;
+        for (int kp = 0; kp < kparts; ++kp) {
+          dot += pr[(size_t)kp * slot + (size_t)i * S + q];
+          ss += pr[(size_t)kp * slot + (size_t)n * S + i];
+        }
+        sc[i] = dot * rsqrtf(fmaf(ss, inv_D, eps));
+        m = fmaxf(m, sc[i]);
+      }
+    }
+    float den = 0.f;
+#pragma unroll
+    for (int i = 0; i < kMaxN; ++i)
+      if (i < n) den += expf(sc[i] - m);
+    const float inv = 1.f / den;
+#pragma unroll
+    for (int i = 0; i < kMaxN; ++i)
+      if (i < n) {
+        const float a = expf(sc[i] - m) * inv;
+        *reinterpret_cast<float2 *>(al + 2 * (i * Sp + q)) = make_float2(a, a);
+      }
     out_lse[(size_t)q * rows + row] = m + logf(den);
     if (out_max) out_max[(size_t)q * rows + row] = m;
   }
@@ -863,6 +948,24 @@ bool phase1_tc_supported(int n, int D, int dtype, int S) {
   return tc::encode_fn() != nullptr;
 }
 
+// Feature slices for split mode, or 1 when it does not apply: only when the
+// normal work items (128-row tiles x five summaries) would leave most SMs
+// idle, and only with room in o[1] for the partials of every slice (o[1]
+// must lie before the parked query parts).  The largest divisor of the
+// 64-feature chunk count that keeps the items within two per SM.
+int split_parts(const Phase1Args &a) {
+  using namespace tc;
+  const int64_t tiles = (a.rows + kRows - 1) / kRows;
+  if (a.S < 3 || (int64_t)(a.S - 2) * a.rows < kNQ) return 1;
+  if (tiles * ((a.n + 4) / 5) >= sm_count()) return 1;
+  const int KC = a.D / kKc;
+  const int64_t slots = 2 * (int64_t)sm_count();
+  const size_t per_part = (size_t)(a.n * a.S + a.n) * 4;
+  for (int kp = KC; kp >= 2; --kp)
+    if (KC % kp == 0 && tiles * a.n * kp <= slots && (size_t)kp * per_part <= (size_t)a.D * 2) return kp;
+  return 1;
+}
+
 cudaError_t launch_phase1_tc(const Phase1Args &a) {
   using namespace tc;
   auto encode = encode_fn();
@@ -909,15 +1012,44 @@ cudaError_t launch_phase1_tc(const Phase1Args &a) {
   pa.D = a.D;
   pa.eps = a.eps;
   pa.inv_D = 1.f / (float)a.D;
+  pa.kparts = 1;
   pa.wait_limit = wait_limit_cycles();
   cudaError_t e = cudaSuccess;
   const int64_t tiles = (a.rows + kRows - 1) / kRows;
+  const size_t row_bytes = (size_t)a.D * 2;
+  const int kparts = split_parts(a);
+  if (kparts > 1) {
+    // Split mode: items (tile, one summary, 1/kparts of the features) fill
+    // the GPU where (tile, five summaries) would leave it idle; partials in
+    // o[1], then their sum and softmax, then the outputs kernel below.
+    constexpr int kCh = 1;
+    float *raw = reinterpret_cast<float *>(static_cast<char *>(a.out) + (size_t)a.rows * row_bytes);  // o[1]
+    pa.raw = raw;
+    pa.raw_n = a.n;
+    pa.raw_off = 0;
+    pa.raw_stride = (int64_t)(row_bytes / 4);
+    pa.kparts = kparts;
+    e = cudaFuncSetAttribute(p1_scores_kernel<kMaxN, kCh>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem_a(kCh));
+    if (e != cudaSuccess) return e;
+    const int64_t items = tiles * a.n * kparts;
+    const int64_t slots = 2 * (int64_t)sm_count();
+    const int64_t waves = (items + slots - 1) / slots;
+    const int64_t ga = (items + waves - 1) / waves;
+    p1_scores_kernel<kMaxN, kCh><<<(int)ga, kThreadsA, smem_a(kCh), a.stream>>>(pa);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    const int64_t total = a.rows * (a.S + (a.S & 1));
+    const int64_t blocks = (total + 255) / 256 < 8 * sm_count() ? (total + 255) / 256 : 8 * sm_count();
+    p1_split_softmax_kernel<<<(int)blocks, 256, 0, a.stream>>>(raw, static_cast<float *>(a.out),
+                                                               (int64_t)(row_bytes / 4), a.rows, a.n, a.S, kparts,
+                                                               pa.inv_D, a.eps, a.out_max, a.out_lse);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  } else
   // Raw scores with five-summary items, two CTAs per SM (tensor-map loads
   // are served one box at a time per CTA), when each token's o[1] row can
   // hold its raw scores and lies before the parked query parts; then a
   // softmax kernel writes alpha into o[0].  Otherwise the fused kernel: one
   // CTA per SM, the softmax in its epilogue.
-  const size_t row_bytes = (size_t)a.D * 2;
   if (a.S >= 3 && (int64_t)(a.S - 2) * a.rows >= kNQ && (size_t)a.n * a.S * 4 <= row_bytes) {
     constexpr int kCh = 5;
     float *raw = reinterpret_cast<float *>(static_cast<char *>(a.out) + (size_t)a.rows * row_bytes);  // o[1]
@@ -1021,6 +1153,7 @@ cudaError_t launch_phase1_many(const Phase1ManyArgs &a) {
   pa.raw = a.scores;
   pa.raw_n = a.n;
   pa.raw_stride = (int64_t)a.n * a.S;
+  pa.kparts = 1;
   pa.wait_limit = wait_limit_cycles();
   constexpr int kManyCh = 5;   // summaries per work item here: two CTAs per SM
   cudaError_t e = cudaFuncSetAttribute(p1_scores_kernel<kManyMaps, kManyCh>,

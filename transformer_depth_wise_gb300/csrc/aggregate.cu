@@ -50,6 +50,8 @@ constexpr int kGroup = 4;  // sources per reduction step
 template <typename T, int VPT, int TEAM, bool FUSED_F>
 __global__ void __launch_bounds__(TEAM ? 256 : 512)
 aggregate_kernel(const __grid_constant__ AggParams p) {
+  grid_dependency_wait();
+  allow_dependents();
   using E = Elt<T>;
   constexpr int EPV = E::EPV;
   constexpr int NE = VPT * EPV;
@@ -245,6 +247,8 @@ aggregate_kernel(const __grid_constant__ AggParams p) {
 template <typename T, bool FUSED_F, int G, int VPT, int TPR>
 __global__ void __launch_bounds__(TPR ? TPR : 256, TPR ? 512 / (TPR ? TPR : 512) : 2)
 aggregate_pipe_kernel(const __grid_constant__ AggParams p) {
+  grid_dependency_wait();
+  allow_dependents();
   using E = Elt<T>;
   constexpr int EPV = E::EPV;
   static_assert(VPT >= 1 && VPT <= 4, "VPT: 1..4 vectors per thread");
@@ -475,7 +479,8 @@ cudaError_t run(const AggParams &p, const Cfg &c, cudaStream_t st) {
   const int64_t groups = (p.rows + per_cta - 1) / per_cta;
   const int64_t cap = (int64_t)o * sm_count();
   const int grid = (int)(groups < cap ? groups : cap);
-  kern<<<grid, c.threads, 0, st>>>(p);
+  if (cudaError_t le = launch_dependent(kern, dim3((unsigned)(grid)), dim3(c.threads), 0, st, p); le != cudaSuccess)
+    return le;
   return cudaGetLastError();
 }
 
@@ -543,7 +548,9 @@ cudaError_t run_pipe(const AggParams &p, int threads, cudaStream_t st) {
   if (occ < 1) occ = 1;
   const int64_t cap = (int64_t)occ * sm_count();
   const int grid = (int)(p.rows < cap ? p.rows : cap);
-  kern<<<grid, threads, smem, st>>>(p);
+  if (cudaError_t le = launch_dependent(kern, dim3((unsigned)(grid)), dim3(threads), smem, st,
+                                        p); le != cudaSuccess)
+    return le;
   return cudaGetLastError();
 }
 

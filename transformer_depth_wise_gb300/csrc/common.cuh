@@ -211,6 +211,38 @@ __device__ __forceinline__ void prefetch_l2_bulk(const void *gmem, uint32_t byte
 }
 
 // ---------------------------------------------------------------------------
+// Programmatic dependent launch.  A kernel launched with launch_dependent()
+// may start while the kernel before it on the stream is still running: it
+// does its setup that reads only constant parameters (staging a query in
+// shared memory, barrier set-up), then calls grid_dependency_wait(), which
+// returns once the earlier grid has completed and its writes are visible.
+// Every access to data another kernel writes or reads comes after that call.
+// allow_dependents() lets the next kernel on the stream start its set-up
+// now, instead of after this grid has exited.  Both are no-ops for a kernel
+// launched without the attribute.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void allow_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// Launch `kern` so that it may overlap the end of the previous kernel on the
+// stream (it must call grid_dependency_wait() before touching shared data).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_dependent(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                                    Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, static_cast<Args &&>(args)...);
+}
+
+// ---------------------------------------------------------------------------
 // Packed fp32 pairs (one 64-bit register, fma.rn.f32x2 = two FMAs per
 // instruction) and the element pairs of a 16-byte vector.
 // ---------------------------------------------------------------------------

@@ -32,6 +32,8 @@ struct MergeParams {
 template <typename T, int VPT, int TEAM>
 __global__ void __launch_bounds__(TEAM ? 256 : 512)
 merge_kernel(const __grid_constant__ MergeParams p) {
+  grid_dependency_wait();
+  allow_dependents();
   using E = Elt<T>;
   constexpr int EPV = E::EPV;
   constexpr int NE = VPT * EPV;
@@ -159,6 +161,8 @@ struct MergeUpdateParams {
 template <typename T, int VPT, int TEAM, bool SYNTH, bool NORM, int TPR>
 __global__ void __launch_bounds__(TEAM ? 256 : 512)
 merge_update_kernel(const __grid_constant__ MergeUpdateParams P) {
+  grid_dependency_wait();
+  allow_dependents();
   using E = Elt<T>;
   constexpr int EPV = E::EPV;
   __shared__ float red[TEAM ? 1 : 2 * 32 * 2];
@@ -180,22 +184,26 @@ merge_update_kernel(const __grid_constant__ MergeUpdateParams P) {
   extern __shared__ float4 qu[];   // [EPV/4][nvec] q~, then u (SYNTH), then the norm weight (NORM)
   constexpr int Q4 = EPV / 4;
   constexpr int NW_AT = SYNTH ? 2 * Q4 : Q4;
-  for (int idx = threadIdx.x; idx < nvec() * Q4; idx += blockDim.x) {
-    const int j = idx / Q4, e4 = (idx % Q4) * 4;
-    const float4 w4 = ld_f4(p.q + j * EPV + e4);
-    const float4 g4 = p.g ? ld_f4(p.g + j * EPV + e4) : make_float4(1.f, 1.f, 1.f, 1.f);
-    qu[(e4 / 4) * nvec() + j] = make_float4(w4.x * g4.x, w4.y * g4.y, w4.z * g4.z, w4.w * g4.w);
-    if (SYNTH) qu[(Q4 + e4 / 4) * nvec() + j] = ld_f4(P.u + j * EPV + e4);
-    if (NORM) qu[(NW_AT + e4 / 4) * nvec() + j] = ld_f4(P.nw + j * EPV + e4);
-  }
-  __syncthreads();
+  // With two vectors a thread on whole-CTA rows (the few-rows launch, as in
+  // decode, one row a CTA) the staging follows the CTA's first row loads, so
+  // their latencies overlap instead of adding up; elsewhere it comes first,
+  // which holds fewer registers across it.
+  constexpr bool kLateStage = VPT == 2 && TEAM == 0 && TPR == 0;
+  auto stage_query = [&]() {
+    for (int idx = threadIdx.x; idx < nvec() * Q4; idx += blockDim.x) {
+      const int j = idx / Q4, e4 = (idx % Q4) * 4;
+      const float4 w4 = ld_f4(p.q + j * EPV + e4);
+      const float4 g4 = p.g ? ld_f4(p.g + j * EPV + e4) : make_float4(1.f, 1.f, 1.f, 1.f);
+      qu[(e4 / 4) * nvec() + j] = make_float4(w4.x * g4.x, w4.y * g4.y, w4.z * g4.z, w4.w * g4.w);
+      if (SYNTH) qu[(Q4 + e4 / 4) * nvec() + j] = ld_f4(P.u + j * EPV + e4);
+      if (NORM) qu[(NW_AT + e4 / 4) * nvec() + j] = ld_f4(P.nw + j * EPV + e4);
+    }
+    __syncthreads();
+  };
+  if (!kLateStage) stage_query();
   bool valid[VPT];
 #pragma unroll
   for (int k = 0; k < VPT; ++k) valid[k] = TPR ? true : lt + k * tpr < nvec();
-  auto qv = [&](int k, int e) -> float {           // element e of this thread's vector k of w~
-    const float4 v = qu[(e >> 2) * nvec() + lt + k * tpr];
-    return (e & 3) == 0 ? v.x : (e & 3) == 1 ? v.y : (e & 3) == 2 ? v.z : v.w;
-  };
 
   const size_t row_bytes = (size_t)p.D * sizeof(T);
   const int64_t groups = (p.rows + teams_per_cta - 1) / teams_per_cta;
@@ -358,10 +366,12 @@ merge_update_kernel(const __grid_constant__ MergeUpdateParams P) {
     if (base) prefetch_l2_bulk(static_cast<const char *>(base) + (size_t)row * row_bytes, (uint32_t)row_bytes);
   };
   prefetch_row(0);
+  // my_groups depends on the CTA alone, so the staging barrier is uniform.
   for (int64_t k = 0; k < my_groups; ++k) {
     uint4 ov[VPT], pv[VPT], sv[VPT];
     prefetch_row(k + 1);
     load_row(k, ov, pv, sv);
+    if (kLateStage && k == 0) stage_query();
     process(k, ov, pv, sv);
   }
 }
@@ -375,6 +385,8 @@ template <typename T, int VPT, int TEAM>
 __global__ void __launch_bounds__(TEAM ? 256 : 512)
 rms_norm_kernel(const void *x, const float *__restrict__ w, void *y, int64_t rows, int nvec,
                 float inv_D, float eps) {
+  grid_dependency_wait();
+  allow_dependents();
   using E = Elt<T>;
   constexpr int EPV = E::EPV;
   __shared__ float red[TEAM ? 1 : 2 * 32];
@@ -438,6 +450,8 @@ partial_update_kernel(const void *__restrict__ h, const void *pin, const float *
                       void *pout, int64_t total_vec, int nvec) {
   // pin may alias pout (in-place update): every vector is read, then written,
   // by the same thread, and pin is read through the coherent path.
+  grid_dependency_wait();
+  allow_dependents();
   using E = Elt<T>;
   constexpr int EPV = E::EPV;
   constexpr int U = 4;
@@ -515,8 +529,7 @@ cudaError_t run(const MergeParams &p, const Cfg &c, cudaStream_t st) {
   const int64_t groups = (p.rows + per_cta - 1) / per_cta;
   const int64_t cap = (int64_t)o * sm_count();
   const int grid = (int)(groups < cap ? groups : cap);
-  kern<<<grid, c.threads, 0, st>>>(p);
-  return cudaGetLastError();
+  return launch_dependent(kern, dim3(grid), dim3(c.threads), 0, st, p);
 }
 
 template <typename T>
@@ -559,8 +572,7 @@ cudaError_t run_mu(const MergeUpdateParams &P, const Cfg &c, cudaStream_t st) {
   const int64_t groups = (P.m.rows + per_cta - 1) / per_cta;
   const int64_t cap = (int64_t)o * sm_count();
   const int grid = (int)(groups < cap ? groups : cap);
-  kern<<<grid, c.threads, smem, st>>>(P);
-  return cudaGetLastError();
+  return launch_dependent(kern, dim3(grid), dim3(c.threads), smem, st, P);
 }
 
 template <typename T, bool SYNTH, bool NORM>
@@ -611,9 +623,8 @@ cudaError_t run_norm(const RmsNormArgs &a, const Cfg &c) {
   const int64_t groups = (a.rows + per_cta - 1) / per_cta;
   const int64_t cap = (int64_t)o * sm_count();
   const int grid = (int)(groups < cap ? groups : cap);
-  kern<<<grid, c.threads, 0, a.stream>>>(a.x, a.weight, a.y, a.rows, a.D / epv_of(a.dtype),
-                                         1.f / (float)a.D, a.eps);
-  return cudaGetLastError();
+  return launch_dependent(kern, dim3(grid), dim3(c.threads), 0, a.stream, a.x, a.weight, a.y, a.rows,
+                          a.D / epv_of(a.dtype), 1.f / (float)a.D, a.eps);
 }
 
 template <typename T>
@@ -703,12 +714,10 @@ cudaError_t launch_partial_update(const PartialUpdateArgs &a) {
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
   if (a.dtype == ATTNRES_BF16)
-    partial_update_kernel<__nv_bfloat16><<<(int)blocks, threads, 0, a.stream>>>(
-        a.h, a.partial_in, a.u, a.partial_out, total, nvec);
-  else
-    partial_update_kernel<float><<<(int)blocks, threads, 0, a.stream>>>(
-        a.h, a.partial_in, a.u, a.partial_out, total, nvec);
-  return cudaGetLastError();
+    return launch_dependent(partial_update_kernel<__nv_bfloat16>, dim3((unsigned)blocks), dim3(threads), 0, a.stream,
+                            a.h, a.partial_in, a.u, a.partial_out, total, nvec);
+  return launch_dependent(partial_update_kernel<float>, dim3((unsigned)blocks), dim3(threads), 0, a.stream, a.h,
+                          a.partial_in, a.u, a.partial_out, total, nvec);
 }
 
 }  // namespace attnres

@@ -43,6 +43,8 @@ struct P1Params {
 template <typename T, int VPT, int NS>
 __global__ void __launch_bounds__(512, 1)
 phase1_kernel(const __grid_constant__ P1Params p) {
+  grid_dependency_wait();
+  allow_dependents();
   using E = Elt<T>;
   constexpr int EPV = E::EPV;
   constexpr int NM = kP1MaxN;
@@ -208,7 +210,9 @@ cudaError_t run(const P1Params &p, const Cfg &c, cudaStream_t st) {
   if (occ < 1) occ = 1;
   const int64_t cap = (int64_t)occ * sm_count();
   const int grid = (int)(p.rows < cap ? p.rows : cap);
-  kern<<<grid, c.threads, c.smem, st>>>(p);
+  if (cudaError_t le = launch_dependent(kern, dim3((unsigned)(grid)), dim3(c.threads), c.smem, st,
+                                        p); le != cudaSuccess)
+    return le;
   return cudaGetLastError();
 }
 

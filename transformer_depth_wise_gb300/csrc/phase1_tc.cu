@@ -166,6 +166,8 @@ __device__ __forceinline__ uint32_t swz(uint32_t r, uint32_t j) { return r * 128
 __global__ void __launch_bounds__(256) p1_qsplit_kernel(const float *__restrict__ q,
                                                         const float *__restrict__ g, int S, int D,
                                                         __nv_bfloat16 *__restrict__ parts) {
+  grid_dependency_wait();
+  allow_dependents();
   const int64_t total = (int64_t)kMaxS * D;
   for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
        idx += (int64_t)gridDim.x * blockDim.x) {
@@ -186,6 +188,8 @@ __global__ void __launch_bounds__(256) p1_qsplit_kernel(const float *__restrict_
 // -----------------------------------------------------------------------------
 template <int NM, int CH = kMaxN>
 __global__ void __launch_bounds__(kThreadsA, CH == kMaxN ? 1 : 2) p1_scores_kernel(const __grid_constant__ ParamsAT<NM> p) {
+  grid_dependency_wait();
+  allow_dependents();
   static_assert(CH >= 1 && CH <= CH, "summaries per work item");
   constexpr int ST = stages_a(CH);                 // stage ring
   constexpr uint32_t TC = tmem_cols_a(CH);         // TMEM columns of this CTA
@@ -481,6 +485,8 @@ __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_gr
 // 0: taken from the parameters.
 template <int PARTS, int NS, int SQ>
 __global__ void __launch_bounds__(512, 1) p1_outputs_kernel(const __grid_constant__ ParamsB p) {
+  grid_dependency_wait();
+  allow_dependents();
   extern __shared__ uint4 vbuf[];                     // [kBStages][n][nvp] 16-byte chunks
   __shared__ __align__(16) float alpha[kBStages][2 * kMaxN * kMaxS];   // [n][Sp][2]
   static_assert(NS <= kMaxN && SQ <= kMaxS, "built-in shape within the kernel's limits");
@@ -573,6 +579,8 @@ __global__ void __launch_bounds__(512, 1) p1_outputs_kernel(const __grid_constan
 __global__ void __launch_bounds__(256)
 p1_park_softmax_kernel(const float *raw, float *alpha, int64_t row_floats, int64_t rows, int n, int S,
                        float *out_max, float *out_lse) {
+  grid_dependency_wait();
+  allow_dependents();
   const int Sp = S + (S & 1);
   const int64_t total = rows * Sp;
   for (int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; g < total; g += (int64_t)gridDim.x * blockDim.x) {
@@ -601,53 +609,70 @@ p1_park_softmax_kernel(const float *raw, float *alpha, int64_t row_floats, int64
 // -----------------------------------------------------------------------------
 // Split mode: each token's o[1] row holds kparts slots of partial dot
 // products [n][S] and partial sums of squares [n] over slices of the
-// features.  One thread per (row, query) adds them up in slot order, forms
-// the scores, takes their softmax, writes m and lse, and writes alpha into
-// the token's o[0] row in the layout the outputs kernel reads.
+// features.  One CTA per token: thread (i, q) adds up its kparts partials in
+// slot order (consecutive threads read consecutive queries), the first n
+// threads the sums of squares; then thread q takes the softmax over the n
+// scores, writes m and lse, and writes alpha into the token's o[0] row in
+// the layout the outputs kernel reads.
 // -----------------------------------------------------------------------------
-__global__ void __launch_bounds__(256)
+constexpr int kSplitThreads = 256;
+static_assert(kSplitThreads >= kMaxN * kMaxS, "one thread per (summary, query)");
+
+__global__ void __launch_bounds__(kSplitThreads)
 p1_split_softmax_kernel(const float *raw, float *alpha, int64_t row_floats, int64_t rows, int n, int S, int kparts,
                         float inv_D, float eps, float *out_max, float *out_lse) {
+  grid_dependency_wait();
+  allow_dependents();
+  __shared__ float dots[kMaxN * kMaxS];
+  __shared__ float rn[kMaxN];
+  const int tid = threadIdx.x;
   const int Sp = S + (S & 1);
-  const int64_t total = rows * Sp;
   const int slot = n * S + n;
-  for (int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; g < total; g += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t row = g / Sp;
-    const int q = (int)(g % Sp);
-    float *al = alpha + (size_t)row * row_floats;
-    if (q >= S) {                                   // the pad query of an odd S
-      for (int i = 0; i < n; ++i) *reinterpret_cast<float2 *>(al + 2 * (i * Sp + q)) = make_float2(0.f, 0.f);
-      continue;
-    }
+  for (int64_t row = blockIdx.x; row < rows; row += gridDim.x) {
     const float *pr = raw + (size_t)row * row_floats;
-    float sc[kMaxN];
-    float m = -INFINITY;
+    if (tid < n * S) {
+      float d = 0.f;
+      for (int kp = 0; kp < kparts; ++kp) d += pr[(size_t)kp * slot + tid];
+      dots[tid] = d;
+    }
+    if (tid < n) {
+      float ss = 0.f;
+      for (int kp = 0; kp < kparts; ++kp) ss += pr[(size_t)kp * slot + (size_t)n * S + tid];
+      rn[tid] = rsqrtf(fmaf(ss, inv_D, eps));
+    }
+    __syncthreads();
+    if (tid < Sp) {
+      const int q = tid;
+      float *al = alpha + (size_t)row * row_floats;
+      if (q >= S) {                                   // the pad query of an odd S
+        for (int i = 0; i < n; ++i) *reinterpret_cast<float2 *>(al + 2 * (i * Sp + q)) = make_float2(0.f, 0.f);
+      } else {
+        float sc[kMaxN];
+        float m = -INFINITY;
 #pragma unroll
-    for (int i = 0; i < kMaxN; ++i) {
-      sc[i] = -INFINITY;
-      if (i < n) {
-        float dot = 0.f, ss = 0.f;
-        for (int kp = 0; kp < kparts; ++kp) {
-          dot += pr[(size_t)kp * slot + (size_t)i * S + q];
-          ss += pr[(size_t)kp * slot + (size_t)n * S + i];
+        for (int i = 0; i < kMaxN; ++i) {
+          sc[i] = -INFINITY;
+          if (i < n) {
+            sc[i] = dots[i * S + q] * rn[i];
+            m = fmaxf(m, sc[i]);
+          }
         }
-        sc[i] = dot * rsqrtf(fmaf(ss, inv_D, eps));
-        m = fmaxf(m, sc[i]);
+        float den = 0.f;
+#pragma unroll
+        for (int i = 0; i < kMaxN; ++i)
+          if (i < n) den += expf(sc[i] - m);
+        const float inv = 1.f / den;
+#pragma unroll
+        for (int i = 0; i < kMaxN; ++i)
+          if (i < n) {
+            const float a = expf(sc[i] - m) * inv;
+            *reinterpret_cast<float2 *>(al + 2 * (i * Sp + q)) = make_float2(a, a);
+          }
+        out_lse[(size_t)q * rows + row] = m + logf(den);
+        if (out_max) out_max[(size_t)q * rows + row] = m;
       }
     }
-    float den = 0.f;
-#pragma unroll
-    for (int i = 0; i < kMaxN; ++i)
-      if (i < n) den += expf(sc[i] - m);
-    const float inv = 1.f / den;
-#pragma unroll
-    for (int i = 0; i < kMaxN; ++i)
-      if (i < n) {
-        const float a = expf(sc[i] - m) * inv;
-        *reinterpret_cast<float2 *>(al + 2 * (i * Sp + q)) = make_float2(a, a);
-      }
-    out_lse[(size_t)q * rows + row] = m + logf(den);
-    if (out_max) out_max[(size_t)q * rows + row] = m;
+    __syncthreads();                                  // the next token's partials reuse the buffers
   }
 }
 
@@ -659,6 +684,8 @@ p1_split_softmax_kernel(const float *raw, float *alpha, int64_t row_floats, int6
 // place; m and lse to their [S, rows] outputs.
 __global__ void __launch_bounds__(256)
 p1_many_softmax_kernel(float *scores, int64_t rows, int n, int S, float *out_max, float *out_lse) {
+  grid_dependency_wait();
+  allow_dependents();
   const int64_t total = rows * S;
   for (int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; g < total; g += (int64_t)gridDim.x * blockDim.x) {
     const int64_t row = g / S;
@@ -693,6 +720,8 @@ constexpr int kB2Ahead = 32;
 
 __global__ void __launch_bounds__(512)
 p1_many_outputs_kernel(const __grid_constant__ ParamsB2 p) {
+  grid_dependency_wait();
+  allow_dependents();
   extern __shared__ uint64_t adup[];  // [n][Sp]
   const int tid = threadIdx.x;
   const int n = p.n, S = p.S, Sp = S + (S & 1);
@@ -808,6 +837,8 @@ __host__ __device__ constexpr size_t tc_smem(int n, int D) {
 
 __global__ void __launch_bounds__(kTcWarps * 32, 1)
 p1_many_outputs_tc_kernel(const __grid_constant__ ParamsB3 p) {
+  grid_dependency_wait();
+  allow_dependents();
   extern __shared__ __align__(16) unsigned char sm3[];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int n = p.n, S = p.S, D = p.D;
@@ -989,7 +1020,9 @@ cudaError_t launch_phase1_tc(const Phase1Args &a) {
   {
     const int64_t total = (int64_t)kMaxS * a.D;
     const int blocks = (int)((total + 255) / 256 < 4 * sm_count() ? (total + 255) / 256 : 4 * sm_count());
-    p1_qsplit_kernel<<<blocks, 256, 0, a.stream>>>(a.queries, a.gains, a.S, a.D, parts);
+    if (cudaError_t le = launch_dependent(p1_qsplit_kernel, dim3((unsigned)(blocks)), dim3(256), 0, a.stream,
+                                          a.queries, a.gains, a.S, a.D, parts); le != cudaSuccess)
+      return le;
     cudaError_t e0 = cudaGetLastError();
     if (e0 != cudaSuccess) return e0;
   }
@@ -1036,14 +1069,15 @@ cudaError_t launch_phase1_tc(const Phase1Args &a) {
     const int64_t slots = 2 * (int64_t)sm_count();
     const int64_t waves = (items + slots - 1) / slots;
     const int64_t ga = (items + waves - 1) / waves;
-    p1_scores_kernel<kMaxN, kCh><<<(int)ga, kThreadsA, smem_a(kCh), a.stream>>>(pa);
+    if (cudaError_t le = launch_dependent((p1_scores_kernel<kMaxN, kCh>), dim3((unsigned)(ga)), dim3(kThreadsA),
+                                          smem_a(kCh), a.stream, pa); le != cudaSuccess)
+      return le;
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    const int64_t total = a.rows * (a.S + (a.S & 1));
-    const int64_t blocks = (total + 255) / 256 < 8 * sm_count() ? (total + 255) / 256 : 8 * sm_count();
-    p1_split_softmax_kernel<<<(int)blocks, 256, 0, a.stream>>>(raw, static_cast<float *>(a.out),
-                                                               (int64_t)(row_bytes / 4), a.rows, a.n, a.S, kparts,
-                                                               pa.inv_D, a.eps, a.out_max, a.out_lse);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    const int64_t blocks = a.rows < 8 * (int64_t)sm_count() ? a.rows : 8 * (int64_t)sm_count();
+    e = launch_dependent(p1_split_softmax_kernel, dim3((unsigned)blocks), dim3(kSplitThreads), 0, a.stream,
+                         (const float *)raw, static_cast<float *>(a.out), (int64_t)(row_bytes / 4), a.rows, a.n, a.S,
+                         kparts, pa.inv_D, a.eps, a.out_max, a.out_lse);
+    if (e != cudaSuccess) return e;
   } else
   // Raw scores with five-summary items, two CTAs per SM (tensor-map loads
   // are served one box at a time per CTA), when each token's o[1] row can
@@ -1064,21 +1098,25 @@ cudaError_t launch_phase1_tc(const Phase1Args &a) {
     const int64_t slots = 2 * (int64_t)sm_count();
     const int64_t waves = (items + slots - 1) / slots;
     const int64_t ga = (items + waves - 1) / waves;
-    p1_scores_kernel<kMaxN, kCh><<<(int)ga, kThreadsA, smem_a(kCh), a.stream>>>(pa);
+    if (cudaError_t le = launch_dependent((p1_scores_kernel<kMaxN, kCh>), dim3((unsigned)(ga)), dim3(kThreadsA),
+                                          smem_a(kCh), a.stream, pa); le != cudaSuccess)
+      return le;
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     const int64_t total = a.rows * (a.S + (a.S & 1));
     const int64_t blocks = (total + 255) / 256 < 8 * sm_count() ? (total + 255) / 256 : 8 * sm_count();
-    p1_park_softmax_kernel<<<(int)blocks, 256, 0, a.stream>>>(raw, static_cast<float *>(a.out),
-                                                              (int64_t)(row_bytes / 4), a.rows, a.n, a.S,
-                                                              a.out_max, a.out_lse);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    e = launch_dependent(p1_park_softmax_kernel, dim3((unsigned)blocks), dim3(256), 0, a.stream, (const float *)raw,
+                         static_cast<float *>(a.out), (int64_t)(row_bytes / 4), a.rows, a.n, a.S, a.out_max,
+                         a.out_lse);
+    if (e != cudaSuccess) return e;
   } else {
     e = cudaFuncSetAttribute(p1_scores_kernel<kMaxN>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemA);
     if (e != cudaSuccess) return e;
     // Every CTA gets the same number of tiles (no partly empty last wave).
     const int64_t waves = (tiles + sm_count() - 1) / sm_count();
     const int64_t ga = (tiles + waves - 1) / waves;
-    p1_scores_kernel<kMaxN><<<(int)ga, kThreadsA, kSmemA, a.stream>>>(pa);
+    if (cudaError_t le = launch_dependent(p1_scores_kernel<kMaxN>, dim3((unsigned)(ga)), dim3(kThreadsA), kSmemA,
+                                          a.stream, pa); le != cudaSuccess)
+      return le;
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   // Kernel B
@@ -1107,8 +1145,7 @@ cudaError_t launch_phase1_tc(const Phase1Args &a) {
   if (occ < 1) occ = 1;
   const int64_t cap = (int64_t)occ * sm_count();
   const int64_t gb = a.rows < cap ? a.rows : cap;
-  kern<<<(int)gb, threads, smem, a.stream>>>(pb);
-  return cudaGetLastError();
+  return launch_dependent(kern, dim3((unsigned)gb), dim3(threads), smem, a.stream, pb);
 }
 
 bool phase1_many_supported(int n, int D, int dtype, int S, int64_t rows) {
@@ -1128,7 +1165,9 @@ cudaError_t launch_phase1_many(const Phase1ManyArgs &a) {
   {
     const int64_t total = (int64_t)kMaxS * a.D;
     const int blocks = (int)((total + 255) / 256 < 4 * sm_count() ? (total + 255) / 256 : 4 * sm_count());
-    p1_qsplit_kernel<<<blocks, 256, 0, a.stream>>>(a.queries, a.gains, a.S, a.D, parts);
+    if (cudaError_t le = launch_dependent(p1_qsplit_kernel, dim3((unsigned)(blocks)), dim3(256), 0, a.stream,
+                                          a.queries, a.gains, a.S, a.D, parts); le != cudaSuccess)
+      return le;
     cudaError_t e0 = cudaGetLastError();
     if (e0 != cudaSuccess) return e0;
   }
@@ -1181,13 +1220,17 @@ cudaError_t launch_phase1_many(const Phase1ManyArgs &a) {
     const int64_t slots = 2 * (int64_t)sm_count();   // resident CTAs
     const int64_t waves = (items + slots - 1) / slots;
     const int64_t ga = (items + waves - 1) / waves;
-    p1_scores_kernel<kManyMaps, kManyCh><<<(int)ga, kThreadsA, smem_a(kManyCh), a.stream>>>(pa);
+    if (cudaError_t le = launch_dependent((p1_scores_kernel<kManyMaps, kManyCh>), dim3((unsigned)(ga)),
+                                          dim3(kThreadsA), smem_a(kManyCh), a.stream, pa); le != cudaSuccess)
+      return le;
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   {
     const int64_t total = a.rows * a.S;
     const int64_t blocks = (total + 255) / 256 < 8 * sm_count() ? (total + 255) / 256 : 8 * sm_count();
-    p1_many_softmax_kernel<<<(int)blocks, 256, 0, a.stream>>>(a.scores, a.rows, a.n, a.S, a.out_max, a.out_lse);
+    if (cudaError_t le = launch_dependent(p1_many_softmax_kernel, dim3((unsigned)(blocks)), dim3(256), 0, a.stream,
+                                          a.scores, a.rows, a.n, a.S, a.out_max, a.out_lse); le != cudaSuccess)
+      return le;
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   if (a.S <= kTcK && a.D % (8 * kTcWarps * 2) == 0 && a.D <= 8 * kTcWarps * 16 &&
@@ -1204,7 +1247,9 @@ cudaError_t launch_phase1_many(const Phase1ManyArgs &a) {
     e = cudaFuncSetAttribute(p1_many_outputs_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem3);
     if (e != cudaSuccess) return e;
     const int64_t g3 = a.rows < sm_count() ? a.rows : sm_count();
-    p1_many_outputs_tc_kernel<<<(int)g3, kTcWarps * 32, smem3, a.stream>>>(pc);
+    if (cudaError_t le = launch_dependent(p1_many_outputs_tc_kernel, dim3((unsigned)(g3)), dim3(kTcWarps * 32),
+                                          smem3, a.stream, pc); le != cudaSuccess)
+      return le;
     return cudaGetLastError();
   }
   ParamsB2 pb;
@@ -1225,7 +1270,9 @@ cudaError_t launch_phase1_many(const Phase1ManyArgs &a) {
   if (occ < 1) occ = 1;
   const int64_t cap = (int64_t)occ * sm_count();
   const int64_t gb = a.rows < cap ? a.rows : cap;
-  p1_many_outputs_kernel<<<(int)gb, threads, smem, a.stream>>>(pb);
+  if (cudaError_t le = launch_dependent(p1_many_outputs_kernel, dim3((unsigned)(gb)), dim3(threads), smem,
+                                        a.stream, pb); le != cudaSuccess)
+    return le;
   return cudaGetLastError();
 }
 

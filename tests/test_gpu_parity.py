@@ -374,8 +374,9 @@ def test_synthetic_sublayer_nonlinearity_error_bound(gpu):
 
 
 def test_merge_update_fused_step(gpu):
-    # rows of 128..512 vectors take the cp.async ring kernel (4096 bf16, 2048 fp32, 1032 bf16 =
-    # 129 vectors, not a multiple of a warp); the others the register kernel
+    # Up to 4 rows per SM, rows of 65..1024 16-byte vectors take the few-rows kernel, two rows a
+    # CTA (4096 bf16, 2048 fp32, 7168 bf16, and 1032 bf16 = 129 vectors, not a multiple of a
+    # warp; odd row counts leave the last CTA one row); rows of at most 64 vectors the team kernel
     for dtype, D, rows in ((torch.bfloat16, 4096, 45), (torch.float32, 256, 70), (torch.bfloat16, 16, 33),
                            (torch.float32, 2048, 37), (torch.bfloat16, 1032, 300), (torch.bfloat16, 7168, 5)):
         for synth, with_pin in ((True, True), (True, False), (False, True)):
@@ -419,7 +420,7 @@ def test_rms_norm(gpu):
 
 def test_merge_update_with_prenorm(gpu):
     for dtype, D, rows in ((torch.bfloat16, 4096, 45), (torch.float32, 256, 70), (torch.bfloat16, 16, 33),
-                           (torch.bfloat16, 16384, 6), (torch.bfloat16, 7168, 11)):
+                           (torch.bfloat16, 16384, 6), (torch.bfloat16, 7168, 11), (torch.float32, 2048, 37)):
         for synth, with_pin in ((True, True), (True, False), (False, True)):
             g = wk.generator(D + rows + 3 * synth + with_pin + 11, gpu)
             (o, pin, sub), _ = wk.scaled_normal_sources(g, 3, (1, rows, D), 0.5, 3.0, dtype, gpu)

@@ -184,23 +184,15 @@ merge_update_kernel(const __grid_constant__ MergeUpdateParams P) {
   extern __shared__ float4 qu[];   // [EPV/4][nvec] q~, then u (SYNTH), then the norm weight (NORM)
   constexpr int Q4 = EPV / 4;
   constexpr int NW_AT = SYNTH ? 2 * Q4 : Q4;
-  // With two vectors a thread on whole-CTA rows (the few-rows launch, as in
-  // decode, one row a CTA) the staging follows the CTA's first row loads, so
-  // their latencies overlap instead of adding up; elsewhere it comes first,
-  // which holds fewer registers across it.
-  constexpr bool kLateStage = VPT == 2 && TEAM == 0 && TPR == 0;
-  auto stage_query = [&]() {
-    for (int idx = threadIdx.x; idx < nvec() * Q4; idx += blockDim.x) {
-      const int j = idx / Q4, e4 = (idx % Q4) * 4;
-      const float4 w4 = ld_f4(p.q + j * EPV + e4);
-      const float4 g4 = p.g ? ld_f4(p.g + j * EPV + e4) : make_float4(1.f, 1.f, 1.f, 1.f);
-      qu[(e4 / 4) * nvec() + j] = make_float4(w4.x * g4.x, w4.y * g4.y, w4.z * g4.z, w4.w * g4.w);
-      if (SYNTH) qu[(Q4 + e4 / 4) * nvec() + j] = ld_f4(P.u + j * EPV + e4);
-      if (NORM) qu[(NW_AT + e4 / 4) * nvec() + j] = ld_f4(P.nw + j * EPV + e4);
-    }
-    __syncthreads();
-  };
-  if (!kLateStage) stage_query();
+  for (int idx = threadIdx.x; idx < nvec() * Q4; idx += blockDim.x) {
+    const int j = idx / Q4, e4 = (idx % Q4) * 4;
+    const float4 w4 = ld_f4(p.q + j * EPV + e4);
+    const float4 g4 = p.g ? ld_f4(p.g + j * EPV + e4) : make_float4(1.f, 1.f, 1.f, 1.f);
+    qu[(e4 / 4) * nvec() + j] = make_float4(w4.x * g4.x, w4.y * g4.y, w4.z * g4.z, w4.w * g4.w);
+    if (SYNTH) qu[(Q4 + e4 / 4) * nvec() + j] = ld_f4(P.u + j * EPV + e4);
+    if (NORM) qu[(NW_AT + e4 / 4) * nvec() + j] = ld_f4(P.nw + j * EPV + e4);
+  }
+  __syncthreads();
   bool valid[VPT];
 #pragma unroll
   for (int k = 0; k < VPT; ++k) valid[k] = TPR ? true : lt + k * tpr < nvec();
@@ -366,13 +358,155 @@ merge_update_kernel(const __grid_constant__ MergeUpdateParams P) {
     if (base) prefetch_l2_bulk(static_cast<const char *>(base) + (size_t)row * row_bytes, (uint32_t)row_bytes);
   };
   prefetch_row(0);
-  // my_groups depends on the CTA alone, so the staging barrier is uniform.
   for (int64_t k = 0; k < my_groups; ++k) {
     uint4 ov[VPT], pv[VPT], sv[VPT];
     prefetch_row(k + 1);
     load_row(k, ov, pv, sv);
-    if (kLateStage && k == 0) stage_query();
     process(k, ov, pv, sv);
+  }
+}
+
+// Few rows (decode: about one row per SM or fewer).  A CTA takes two rows,
+// and each thread the same two 16-byte vectors of both, holding its vectors
+// of w~ = w (.) gamma, u and the norm weight in registers: they are read
+// once for two rows, with no shared-memory staging and no barrier before the
+// rows, and all loads are issued together.  The arithmetic is the fused step
+// above, element by element and reduction by reduction.
+template <typename T, bool SYNTH, bool NORM>
+__global__ void __launch_bounds__(512, 1)
+merge_update_few_kernel(const __grid_constant__ MergeUpdateParams P) {
+  grid_dependency_wait();
+  allow_dependents();
+  using E = Elt<T>;
+  constexpr int EPV = E::EPV;
+  constexpr int R = 2, V = 2;          // rows per CTA, vectors per thread
+  __shared__ float red[2 * 32 * 2 * R];
+  __shared__ float red_n[NORM ? 2 * 32 * R : 1];
+  const MergeParams &p = P.m;
+  const int lt = threadIdx.x, tpr = blockDim.x;
+  const size_t row_bytes = (size_t)p.D * sizeof(T);
+  bool valid[V], ok[R];
+  int64_t row[R];
+#pragma unroll
+  for (int k = 0; k < V; ++k) valid[k] = lt + k * tpr < p.nvec;
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    row[r] = (int64_t)blockIdx.x * R + r;
+    ok[r] = row[r] < p.rows;
+  }
+  auto off_of = [&](int r, int k) { return (size_t)row[r] * row_bytes + (size_t)(lt + k * tpr) * 16; };
+
+  uint4 ov[R][V], pv[R][V], sv[R][V];
+  float lse[R];
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    lse[r] = ok[r] ? p.lse[row[r]] : 0.f;
+#pragma unroll
+    for (int k = 0; k < V; ++k) {
+      ov[r][k] = pv[r][k] = sv[r][k] = make_uint4(0u, 0u, 0u, 0u);
+      if (!ok[r] || !valid[k]) continue;
+      ov[r][k] = ld_stream(static_cast<const char *>(p.o) + off_of(r, k));
+      // p_in and sub may be overwritten by this kernel: coherent loads
+      if (P.p_in) pv[r][k] = *reinterpret_cast<const uint4 *>(static_cast<const char *>(P.p_in) + off_of(r, k));
+      sv[r][k] = *reinterpret_cast<const uint4 *>(static_cast<const char *>(P.sub) + off_of(r, k));
+    }
+  }
+  float q[V][EPV], uu[V][EPV], nw[V][EPV];
+#pragma unroll
+  for (int k = 0; k < V; ++k)
+#pragma unroll
+    for (int e4 = 0; e4 < EPV; e4 += 4) {
+      float4 w4 = make_float4(0.f, 0.f, 0.f, 0.f), g4 = make_float4(1.f, 1.f, 1.f, 1.f), u4 = w4, n4 = w4;
+      const int j = lt + k * tpr;
+      if (valid[k]) {
+        w4 = ld_f4(p.q + j * EPV + e4);
+        if (p.g) g4 = ld_f4(p.g + j * EPV + e4);
+        if (SYNTH) u4 = ld_f4(P.u + j * EPV + e4);
+        if (NORM) n4 = ld_f4(P.nw + j * EPV + e4);
+      }
+      q[k][e4] = w4.x * g4.x; q[k][e4 + 1] = w4.y * g4.y; q[k][e4 + 2] = w4.z * g4.z; q[k][e4 + 3] = w4.w * g4.w;
+      uu[k][e4] = u4.x; uu[k][e4 + 1] = u4.y; uu[k][e4 + 2] = u4.z; uu[k][e4 + 3] = u4.w;
+      nw[k][e4] = n4.x; nw[k][e4 + 1] = n4.y; nw[k][e4 + 2] = n4.z; nw[k][e4 + 3] = n4.w;
+    }
+
+  // p_new = p_in + out, rounded as stored; s_p's dot and sum of squares.
+  uint4 pn[R][V];
+  float part[2 * R];
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    part[2 * r] = part[2 * r + 1] = 0.f;
+#pragma unroll
+    for (int k = 0; k < V; ++k) {
+      float xp[EPV], xs[EPV], y[EPV];
+      E::unpack(pv[r][k], xp);
+      E::unpack(sv[r][k], xs);
+#pragma unroll
+      for (int e = 0; e < EPV; ++e) y[e] = xp[e] + (SYNTH ? half_tanh(uu[k][e] * xs[e]) : xs[e]);
+      pn[r][k] = E::pack(y);
+      if (!valid[k]) continue;
+      float x[EPV];
+      E::unpack_again(pn[r][k], x);
+#pragma unroll
+      for (int e = 0; e < EPV; ++e) part[2 * r] = fmaf(q[k][e], x[e], part[2 * r]);
+#pragma unroll
+      for (int e = 0; e < EPV; ++e) part[2 * r + 1] = fmaf(x[e], x[e], part[2 * r + 1]);
+    }
+  }
+  cta_sum<2 * R>(part, red, 0);
+
+  float wa[R], wc[R], M[R], a[R], c[R], hs[R];
+#pragma unroll
+  for (int r = 0; r < R; ++r) {
+    wa[r] = wc[r] = M[r] = a[r] = c[r] = hs[r] = 0.f;
+    if (!ok[r]) continue;
+    const float sp = part[2 * r] * rsqrtf(fmaf(part[2 * r + 1], p.inv_D, p.eps));
+    M[r] = fmaxf(lse[r], sp);
+    a[r] = expf(lse[r] - M[r]);
+    c[r] = expf(sp - M[r]);
+    const float inv = 1.f / (a[r] + c[r]);
+    wa[r] = a[r] * inv;
+    wc[r] = c[r] * inv;
+  }
+#pragma unroll
+  for (int r = 0; r < R; ++r)
+#pragma unroll
+    for (int k = 0; k < V; ++k) {
+      if (!ok[r] || !valid[k]) continue;
+      st_vec(static_cast<char *>(P.p_out) + off_of(r, k), pn[r][k]);
+      float xo[EPV], xp[EPV], h[EPV];
+      E::unpack(ov[r][k], xo);
+      E::unpack_again(pn[r][k], xp);
+#pragma unroll
+      for (int e = 0; e < EPV; ++e) h[e] = fmaf(wa[r], xo[e], wc[r] * xp[e]);
+      if (p.h) st_vec(static_cast<char *>(p.h) + off_of(r, k), E::pack(h));
+      if (NORM) {
+#pragma unroll
+        for (int e = 0; e < EPV; ++e) hs[r] = fmaf(h[e], h[e], hs[r]);
+      }
+    }
+  if (NORM) {
+    // The next sublayer's pre-norm on the unrounded h: y = h / sqrt(mean h^2 + eps) (.) w_n.
+    cta_sum<R>(hs, red_n, 0);
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      if (!ok[r]) continue;
+      const float rn = rsqrtf(fmaf(hs[r], p.inv_D, P.neps));
+#pragma unroll
+      for (int k = 0; k < V; ++k) {
+        if (!valid[k]) continue;
+        float xo[EPV], xp[EPV], y[EPV];
+        E::unpack(ov[r][k], xo);
+        E::unpack_again(pn[r][k], xp);
+#pragma unroll
+        for (int e = 0; e < EPV; ++e) y[e] = fmaf(wa[r], xo[e], wc[r] * xp[e]) * rn * nw[k][e];
+        st_vec(static_cast<char *>(P.y) + off_of(r, k), E::pack(y));
+      }
+    }
+  }
+  if (lt == 0 && p.lse_out) {
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+      if (ok[r]) p.lse_out[row[r]] = M[r] + logf(a[r] + c[r]);
   }
 }
 
@@ -496,6 +630,7 @@ int epv_of(int dtype) { return dtype == ATTNRES_BF16 ? 8 : 4; }
 
 struct Cfg {
   int vpt, team, threads;
+  bool few = false;    // fused update+merge: two rows a CTA, query data in registers
 };
 
 bool choose(int D, int dtype, Cfg &c) {
@@ -576,7 +711,14 @@ cudaError_t run_mu(const MergeUpdateParams &P, const Cfg &c, cudaStream_t st) {
 }
 
 template <typename T, bool SYNTH, bool NORM>
+cudaError_t run_mu_few(const MergeUpdateParams &P, const Cfg &c, cudaStream_t st) {
+  const int64_t grid = (P.m.rows + 1) / 2;
+  return launch_dependent(merge_update_few_kernel<T, SYNTH, NORM>, dim3((unsigned)grid), dim3(c.threads), 0, st, P);
+}
+
+template <typename T, bool SYNTH, bool NORM>
 cudaError_t dispatch_mu(const MergeUpdateParams &P, const Cfg &c, cudaStream_t st) {
+  if (c.few) return run_mu_few<T, SYNTH, NORM>(P, c, st);
   // Rows that fill the CTA exactly run with its width built in, except the
   // plain step on 128 threads (D = 4096 bf16), where measured on a GB300 it
   // was slower (0.238 against 0.211 ms); with the pre-norm on the same rows
@@ -643,9 +785,10 @@ cudaError_t dispatch_norm(const RmsNormArgs &a, const Cfg &c) {
 cudaError_t launch_merge_update(const MergeUpdateArgs &a) {
   Cfg c;
   if (!choose(a.D, a.dtype, c)) return cudaErrorInvalidValue;
-  // Few rows (decode): two vectors per thread, twice the threads on each row.
+  // Few rows (decode): two vectors per thread, twice the threads on each
+  // row, two rows a CTA with the query data in registers.
   if (c.team == 0 && a.rows <= 4 * sm_count() && (a.D / epv_of(a.dtype) + 1) / 2 <= 512)
-    c = {2, 0, ((a.D / epv_of(a.dtype) + 1) / 2 + 31) / 32 * 32};
+    c = {2, 0, ((a.D / epv_of(a.dtype) + 1) / 2 + 31) / 32 * 32, true};
   MergeUpdateParams P;
   P.m.o = a.inter_out;
   P.m.lse = a.inter_lse;

@@ -131,8 +131,10 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_traffic(kernel: str, workload: str):
-    """DRAM bytes per launch from a committed ncu summary, if the kernel source is unchanged."""
+def kernel_traffic(kernel: str, workload: str, rows: int):
+    """DRAM bytes per launch from a committed ncu summary, if the kernel source is
+    unchanged.  A summary captured on fewer token rows than the workload's (to keep
+    the capture small) is scaled by rows: these kernels stream every row once."""
     path = os.path.join(ROOT, "profiles", f"traffic_{kernel}_{workload}.txt")
     src = {"phase1": "phase1_tc.cu", "merge": "merge.cu", "merge_update": "merge.cu", "update": "merge.cu",
            "aggregate": "aggregate.cu"}.get(kernel)
@@ -148,9 +150,11 @@ def kernel_traffic(kernel: str, workload: str):
     if info.get("source_sha256") != sha:
         return None
     try:
-        return float(info["traffic_bytes_per_launch"])
+        per_launch = float(info["traffic_bytes_per_launch"])
+        captured = int(info.get("rows_captured", rows))
     except (KeyError, ValueError):
         return None
+    return round(per_launch * rows / captured)
 
 
 # ---------------------------------------------------------------------------
@@ -182,8 +186,9 @@ def oracle_block_rows_per_s(wl, rows_target_s: float = 12.0, max_rows: int = 409
 # ---------------------------------------------------------------------------
 # GPU arm
 # ---------------------------------------------------------------------------
-def time_block(blk, K, dev, world, stream, fused):
-    """Run K block passes with per-kernel events; returns (elapsed max over ranks, events, clocks)."""
+def time_block(blk, K, dev, world, stream, fused, label="timed"):
+    """Run K block passes with per-kernel events; returns (elapsed max over ranks, events, clocks).
+    The passes sit in an NVTX range named `label`, which a profiler can select."""
     S = blk.S
     ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
     events = [{"phase1": (ev(), ev()), "merge": [(ev(), ev()) for _ in range(S - 1)],
@@ -194,10 +199,12 @@ def time_block(blk, K, dev, world, stream, fused):
     torch.cuda.synchronize(dev)
     clocks.start()
     time.sleep(0.3)
+    torch.cuda.nvtx.range_push(label)
     t_start.record(stream)
     for k in range(K):
         blk.run(events=events[k])
     t_end.record(stream)
+    torch.cuda.nvtx.range_pop()
     torch.cuda.synchronize(dev)
     clk = clocks.stop()
     barrier(world)
@@ -239,7 +246,7 @@ def run_two_phase(args, wl, dev, rank, world):
         k["frac_nominal"] = k["gbs"] / NOMINAL_HBM_GBS
     dom = max(kern, key=lambda n: kern[n]["total_ms"])
     d = kern[dom]
-    traffic = kernel_traffic(dom, wl.name)
+    traffic = kernel_traffic(dom, wl.name, rows)
     roofline = {"bound": "hbm", "kernel": dom, "achieved": round(d["gbs"], 1), "peak": peak,
                 "unit": "GB/s", "frac": round(d["frac"], 4), "traffic": traffic,
                 "algorithmic_bytes_per_launch": d["bytes"],
@@ -257,7 +264,7 @@ def run_two_phase(args, wl, dev, rank, world):
     for _ in range(args.warmup):
         blk_u.run()
     torch.cuda.synchronize(dev)
-    el_u, ev_u, _ = time_block(blk_u, K, dev, world, stream, fused=False)
+    el_u, ev_u, _ = time_block(blk_u, K, dev, world, stream, fused=False, label="timed_unfused")
     bu = accounting.two_phase_block_bytes(n_blocks, S, rows, D, elt, fused=False)
     mg_u = [a.elapsed_time(c) for e in ev_u for a, c in e["merge"]]
     up_u = [a.elapsed_time(c) for e in ev_u for a, c in e["update"]]
@@ -275,7 +282,7 @@ def run_two_phase(args, wl, dev, rank, world):
     for _ in range(args.warmup):
         blk_n.run()
     torch.cuda.synchronize(dev)
-    el_n, ev_n, _ = time_block(blk_n, K, dev, world, stream, fused=True)
+    el_n, ev_n, _ = time_block(blk_n, K, dev, world, stream, fused=True, label="timed_prenorm")
     mg_n = [a.elapsed_time(c) for e in ev_n for a, c in e["merge"]]
     prenorm = {"value": round(rows * K * world / (el_n * 1e-3), 1), "ms_per_step": round(el_n / K, 4),
                "merge_update_ms": round(statistics.mean(mg_n), 5),
@@ -468,9 +475,13 @@ def run_single(args, wl, dev, world):
     times = []
     for _ in range(args.steps):
         flush.zero_()  # L2 flush between timed launches
+        torch.cuda.synchronize(dev)
+        torch.cuda._sleep(HOST_AHEAD_CYCLES)
+        torch.cuda.nvtx.range_push("timed")
         a.record()
         api.depth_aggregate(inp["sources"], inp["query"], inp["gain"], inp["eps"], out=out)
         b.record()
+        torch.cuda.nvtx.range_pop()
         torch.cuda.synchronize(dev)
         times.append(a.elapsed_time(b))
     rows = inp["sources"][0].numel() // wl.D
@@ -493,6 +504,38 @@ def run_single(args, wl, dev, world):
             "backward": backward}
 
 
+def run_merge_update_only(args, wl, dev):
+    """One fused update+merge launch per step on its own (profiling): the two-phase
+    workload's width and dtype at --rows token rows (default 16384), holding only
+    what the launch touches (o_k, p_in, the sublayer row, p_out, h; 0.7 GB at
+    D = 4096), L2 flushed before each timed launch."""
+    from transformer_depth_wise_gb300 import api
+    rows = args.rows or 16384
+    g = wk.generator(wl.seed, dev)
+    (o, pin, sub), _ = wk.scaled_normal_sources(g, 3, (1, rows, wl.D), 0.5, 3.0, wl.dtype, dev)
+    W, G = wk.queries_and_gains(g, 1, wl.D, dev)
+    u = wk.sublayer_u(g, 1, wl.D, dev)[0].contiguous()
+    lse = torch.empty(rows, device=dev).normal_(0.0, 2.0, generator=g)
+    p_out, h = torch.empty_like(o), torch.empty_like(o)
+    call = lambda: api.block_merge_update(o, lse, pin, sub, u, W[0], G[0], 1e-8, partial_out=p_out,  # noqa
+                                          h_out=h)
+    for _ in range(args.warmup):
+        call()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    torch.cuda.synchronize(dev)
+    torch.cuda.nvtx.range_push("timed")
+    ms = _event_median_ms(call, args.steps, flush)
+    torch.cuda.nvtx.range_pop()
+    peak, src = measured_peak()
+    byts = accounting.merge_update_bytes(rows, wl.D, o.element_size(), first=False)
+    r = _rate(byts, ms, peak)
+    del o, pin, sub, p_out, h, flush
+    return {"metric": "fused update+merge launch", "kernel": "merge_update", "rows": rows, "D": wl.D,
+            "dtype": "bf16" if wl.dtype == torch.bfloat16 else "f32", "steps": args.steps,
+            "warmup": args.warmup, "peak_source": src, **r,
+            "timing": "one launch per sample, L2 flushed before each, median of %d" % args.steps}
+
+
 def run_full_stack(args, wl, dev, world):
     from transformer_depth_wise_gb300 import api
     inp = wk.full_stack_inputs(wl, device=dev, rows=args.rows or None)
@@ -502,10 +545,12 @@ def run_full_stack(args, wl, dev, world):
         api.full_stack_forward(inp["v0"], inp["queries"], inp["gains"], inp["u"], inp["eps"], srcs, y)
     torch.cuda.synchronize(dev)
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.nvtx.range_push("timed")
     a.record()
     for _ in range(args.steps):
         api.full_stack_forward(inp["v0"], inp["queries"], inp["gains"], inp["u"], inp["eps"], srcs, y)
     b.record()
+    torch.cuda.nvtx.range_pop()
     torch.cuda.synchronize(dev)
     ms = a.elapsed_time(b) / args.steps
     rows = inp["v0"].numel() // wl.D
@@ -519,10 +564,12 @@ def run_full_stack(args, wl, dev, world):
     for _ in range(args.warmup):
         api.full_stack_two_phase(inp["v0"], inp["queries"], inp["gains"], inp["u"], S, inp["eps"], srcs, y, ws)
     torch.cuda.synchronize(dev)
+    torch.cuda.nvtx.range_push("timed_two_phase")
     a.record()
     for _ in range(args.steps):
         api.full_stack_two_phase(inp["v0"], inp["queries"], inp["gains"], inp["u"], S, inp["eps"], srcs, y, ws)
     b.record()
+    torch.cuda.nvtx.range_pop()
     torch.cuda.synchronize(dev)
     ms2 = a.elapsed_time(b) / args.steps
     b2 = accounting.full_two_phase_bytes(wl.L, S, rows, wl.D, 2)
@@ -657,7 +704,7 @@ def run_configs(dev):
         blk.run()
     torch.cuda.synchronize()
     K = 3
-    el, events, _ = time_block(blk, K, dev, 1, torch.cuda.current_stream(dev), fused=True)
+    el, events, _ = time_block(blk, K, dev, 1, torch.cuda.current_stream(dev), fused=True, label="timed_long_prefill")
     n_blocks = len(tp["blocks"])
     b = accounting.two_phase_block_bytes(n_blocks, wl.S, wl.rows, wl.D, 2, fused=True)
     p1 = statistics.mean(e["phase1"][0].elapsed_time(e["phase1"][1]) for e in events)
@@ -690,6 +737,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-configs", action="store_true",
                     help="headline only: skip the per-workload measurements of the other configs")
+    ap.add_argument("--kernel", default="", choices=["", "merge_update"],
+                    help="time one kernel alone at --rows token rows (profiling; no headline line)")
     ap.add_argument("--schedule-block-size", type=int, default=14,
                     help="Full stack: block size S of the two-phase schedule timed beside the plain stack")
     args = ap.parse_args()
@@ -732,7 +781,9 @@ def main():
     from transformer_depth_wise_gb300 import _lib
     _lib.lib()
 
-    if wl.name in ("two_phase_bf16", "long_prefill_bf16", "decode_bf16"):
+    if args.kernel == "merge_update":
+        res = run_merge_update_only(args, wl, dev)
+    elif wl.name in ("two_phase_bf16", "long_prefill_bf16", "decode_bf16"):
         res = run_two_phase(args, wl, dev, rank, world)
     elif wl.name == "full_stack_bf16":
         res = run_full_stack(args, wl, dev, world)
@@ -740,7 +791,7 @@ def main():
         res = run_single(args, wl, dev, world)
 
     if rank == 0:
-        if not args.no_cpu_baseline and "two_phase" in wl.name and world == 1:
+        if not args.no_cpu_baseline and not args.kernel and not args.rows and "two_phase" in wl.name and world == 1:
             res["cpu_baseline"] = cpu_baseline_block(wl)
         print(json.dumps(res), flush=True)
     if world > 1:

@@ -51,7 +51,6 @@ template <typename T, int VPT, int TEAM, bool FUSED_F>
 __global__ void __launch_bounds__(TEAM ? 256 : 512)
 aggregate_kernel(const __grid_constant__ AggParams p) {
   grid_dependency_wait();
-  allow_dependents();
   using E = Elt<T>;
   constexpr int EPV = E::EPV;
   constexpr int NE = VPT * EPV;
@@ -248,7 +247,6 @@ template <typename T, bool FUSED_F, int G, int VPT, int TPR>
 __global__ void __launch_bounds__(TPR ? TPR : 256, TPR ? 512 / (TPR ? TPR : 512) : 2)
 aggregate_pipe_kernel(const __grid_constant__ AggParams p) {
   grid_dependency_wait();
-  allow_dependents();
   using E = Elt<T>;
   constexpr int EPV = E::EPV;
   static_assert(VPT >= 1 && VPT <= 4, "VPT: 1..4 vectors per thread");

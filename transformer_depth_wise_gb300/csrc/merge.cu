@@ -33,7 +33,6 @@ template <typename T, int VPT, int TEAM>
 __global__ void __launch_bounds__(TEAM ? 256 : 512)
 merge_kernel(const __grid_constant__ MergeParams p) {
   grid_dependency_wait();
-  allow_dependents();
   using E = Elt<T>;
   constexpr int EPV = E::EPV;
   constexpr int NE = VPT * EPV;
@@ -162,7 +161,6 @@ template <typename T, int VPT, int TEAM, bool SYNTH, bool NORM, int TPR>
 __global__ void __launch_bounds__(TEAM ? 256 : 512)
 merge_update_kernel(const __grid_constant__ MergeUpdateParams P) {
   grid_dependency_wait();
-  allow_dependents();
   using E = Elt<T>;
   constexpr int EPV = E::EPV;
   __shared__ float red[TEAM ? 1 : 2 * 32 * 2];
@@ -376,7 +374,6 @@ template <typename T, bool SYNTH, bool NORM>
 __global__ void __launch_bounds__(512, 1)
 merge_update_few_kernel(const __grid_constant__ MergeUpdateParams P) {
   grid_dependency_wait();
-  allow_dependents();
   using E = Elt<T>;
   constexpr int EPV = E::EPV;
   constexpr int R = 2, V = 2;          // rows per CTA, vectors per thread
@@ -520,7 +517,6 @@ __global__ void __launch_bounds__(TEAM ? 256 : 512)
 rms_norm_kernel(const void *x, const float *__restrict__ w, void *y, int64_t rows, int nvec,
                 float inv_D, float eps) {
   grid_dependency_wait();
-  allow_dependents();
   using E = Elt<T>;
   constexpr int EPV = E::EPV;
   __shared__ float red[TEAM ? 1 : 2 * 32];
@@ -585,7 +581,6 @@ partial_update_kernel(const void *__restrict__ h, const void *pin, const float *
   // pin may alias pout (in-place update): every vector is read, then written,
   // by the same thread, and pin is read through the coherent path.
   grid_dependency_wait();
-  allow_dependents();
   using E = Elt<T>;
   constexpr int EPV = E::EPV;
   constexpr int U = 4;

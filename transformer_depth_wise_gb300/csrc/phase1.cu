@@ -44,7 +44,6 @@ template <typename T, int VPT, int NS>
 __global__ void __launch_bounds__(512, 1)
 phase1_kernel(const __grid_constant__ P1Params p) {
   grid_dependency_wait();
-  allow_dependents();
   using E = Elt<T>;
   constexpr int EPV = E::EPV;
   constexpr int NM = kP1MaxN;

@@ -167,7 +167,6 @@ __global__ void __launch_bounds__(256) p1_qsplit_kernel(const float *__restrict_
                                                         const float *__restrict__ g, int S, int D,
                                                         __nv_bfloat16 *__restrict__ parts) {
   grid_dependency_wait();
-  allow_dependents();
   const int64_t total = (int64_t)kMaxS * D;
   for (int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; idx < total;
        idx += (int64_t)gridDim.x * blockDim.x) {
@@ -189,7 +188,6 @@ __global__ void __launch_bounds__(256) p1_qsplit_kernel(const float *__restrict_
 template <int NM, int CH = kMaxN>
 __global__ void __launch_bounds__(kThreadsA, CH == kMaxN ? 1 : 2) p1_scores_kernel(const __grid_constant__ ParamsAT<NM> p) {
   grid_dependency_wait();
-  allow_dependents();
   static_assert(CH >= 1 && CH <= CH, "summaries per work item");
   constexpr int ST = stages_a(CH);                 // stage ring
   constexpr uint32_t TC = tmem_cols_a(CH);         // TMEM columns of this CTA
@@ -486,7 +484,6 @@ __device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_gr
 template <int PARTS, int NS, int SQ>
 __global__ void __launch_bounds__(512, 1) p1_outputs_kernel(const __grid_constant__ ParamsB p) {
   grid_dependency_wait();
-  allow_dependents();
   extern __shared__ uint4 vbuf[];                     // [kBStages][n][nvp] 16-byte chunks
   __shared__ __align__(16) float alpha[kBStages][2 * kMaxN * kMaxS];   // [n][Sp][2]
   static_assert(NS <= kMaxN && SQ <= kMaxS, "built-in shape within the kernel's limits");
@@ -580,7 +577,6 @@ __global__ void __launch_bounds__(256)
 p1_park_softmax_kernel(const float *raw, float *alpha, int64_t row_floats, int64_t rows, int n, int S,
                        float *out_max, float *out_lse) {
   grid_dependency_wait();
-  allow_dependents();
   const int Sp = S + (S & 1);
   const int64_t total = rows * Sp;
   for (int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; g < total; g += (int64_t)gridDim.x * blockDim.x) {
@@ -622,7 +618,6 @@ __global__ void __launch_bounds__(kSplitThreads)
 p1_split_softmax_kernel(const float *raw, float *alpha, int64_t row_floats, int64_t rows, int n, int S, int kparts,
                         float inv_D, float eps, float *out_max, float *out_lse) {
   grid_dependency_wait();
-  allow_dependents();
   __shared__ float dots[kMaxN * kMaxS];
   __shared__ float rn[kMaxN];
   const int tid = threadIdx.x;
@@ -685,7 +680,6 @@ p1_split_softmax_kernel(const float *raw, float *alpha, int64_t row_floats, int6
 __global__ void __launch_bounds__(256)
 p1_many_softmax_kernel(float *scores, int64_t rows, int n, int S, float *out_max, float *out_lse) {
   grid_dependency_wait();
-  allow_dependents();
   const int64_t total = rows * S;
   for (int64_t g = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; g < total; g += (int64_t)gridDim.x * blockDim.x) {
     const int64_t row = g / S;
@@ -721,7 +715,6 @@ constexpr int kB2Ahead = 32;
 __global__ void __launch_bounds__(512)
 p1_many_outputs_kernel(const __grid_constant__ ParamsB2 p) {
   grid_dependency_wait();
-  allow_dependents();
   extern __shared__ uint64_t adup[];  // [n][Sp]
   const int tid = threadIdx.x;
   const int n = p.n, S = p.S, Sp = S + (S & 1);
@@ -838,7 +831,6 @@ __host__ __device__ constexpr size_t tc_smem(int n, int D) {
 __global__ void __launch_bounds__(kTcWarps * 32, 1)
 p1_many_outputs_tc_kernel(const __grid_constant__ ParamsB3 p) {
   grid_dependency_wait();
-  allow_dependents();
   extern __shared__ __align__(16) unsigned char sm3[];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int n = p.n, S = p.S, D = p.D;

@@ -106,6 +106,7 @@ struct ParamsAT {
   // its partial dot products and partial sums of squares, unnormalised, to
   // slot kp of the row's raw area: [kp][n S dots, then n sums of squares].
   int kparts;                         // 1: every item covers all of D
+  int chunk;                          // summaries per work item, 1..CH (the template's bound)
   long long wait_limit;               // SM clock cycles any wait of the work loop may take
 };
 // The fused path (up to ten summaries) and the raw-score path, which takes
@@ -228,10 +229,12 @@ __global__ void __launch_bounds__(kThreadsA, CH == kMaxN ? 1 : 2) p1_scores_kern
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  // Work items: (tile of 128 rows, chunk of up to CH summaries), tile-minor.
+  // Work items: (tile of 128 rows, chunk of up to p.chunk <= CH summaries),
+  // tile-minor.
   const int64_t tiles = (p.rows + kRows - 1) / kRows;
   const int kparts = p.kparts;
-  const int64_t items = tiles * ((n + CH - 1) / CH) * kparts;
+  const int ch = p.chunk;
+  const int64_t items = tiles * ((n + ch - 1) / ch) * kparts;
   const int64_t my_tiles = items > (int64_t)blockIdx.x ? (items - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
   const int KCP = p.D / kKc / kparts;                 // 64-feature chunks per item
   // item -> (tile, first summary i0 and count nc, feature chunks [kc0, kc0 + KCP))
@@ -240,8 +243,8 @@ __global__ void __launch_bounds__(kThreadsA, CH == kMaxN ? 1 : 2) p1_scores_kern
     tile = item % tiles;
     const int64_t rest = item / tiles;
     kc0 = (int)(rest % kparts) * KCP;
-    i0 = (int)(rest / kparts) * CH;
-    nc = n - i0 < CH ? n - i0 : CH;
+    i0 = (int)(rest / kparts) * ch;
+    nc = n - i0 < ch ? n - i0 : ch;
   };
 
   if (warp == 4) {
@@ -1038,6 +1041,7 @@ cudaError_t launch_phase1_tc(const Phase1Args &a) {
   pa.eps = a.eps;
   pa.inv_D = 1.f / (float)a.D;
   pa.kparts = 1;
+  pa.chunk = kMaxN;
   pa.wait_limit = wait_limit_cycles();
   cudaError_t e = cudaSuccess;
   const int64_t tiles = (a.rows + kRows - 1) / kRows;
@@ -1054,6 +1058,7 @@ cudaError_t launch_phase1_tc(const Phase1Args &a) {
     pa.raw_off = 0;
     pa.raw_stride = (int64_t)(row_bytes / 4);
     pa.kparts = kparts;
+    pa.chunk = kCh;
     e = cudaFuncSetAttribute(p1_scores_kernel<kMaxN, kCh>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem_a(kCh));
     if (e != cudaSuccess) return e;
@@ -1079,6 +1084,7 @@ cudaError_t launch_phase1_tc(const Phase1Args &a) {
   if (a.S >= 3 && (int64_t)(a.S - 2) * a.rows >= kNQ && (size_t)a.n * a.S * 4 <= row_bytes) {
     constexpr int kCh = 5;
     float *raw = reinterpret_cast<float *>(static_cast<char *>(a.out) + (size_t)a.rows * row_bytes);  // o[1]
+    pa.chunk = kCh;
     pa.raw = raw;
     pa.raw_n = a.n;
     pa.raw_off = 0;
@@ -1186,7 +1192,7 @@ cudaError_t launch_phase1_many(const Phase1ManyArgs &a) {
   pa.raw_stride = (int64_t)a.n * a.S;
   pa.kparts = 1;
   pa.wait_limit = wait_limit_cycles();
-  constexpr int kManyCh = 5;   // summaries per work item here: two CTAs per SM
+  constexpr int kManyCh = 5;   // at most five summaries per work item: two CTAs per SM
   cudaError_t e = cudaFuncSetAttribute(p1_scores_kernel<kManyMaps, kManyCh>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_a(kManyCh));
   if (e != cudaSuccess) return e;
@@ -1208,8 +1214,22 @@ cudaError_t launch_phase1_many(const Phase1ManyArgs &a) {
     }
     pa.n = nl;
     pa.raw_off = off;
-    const int64_t items = tiles * ((nl + kManyCh - 1) / kManyCh);
+    // Summaries per item: each CTA streams its tensor-map boxes at about the
+    // same rate however many it has in flight, so a launch takes about
+    // (waves of items) x (summaries per item); few summaries leave SMs idle
+    // with five per item, and a nearly empty last wave doubles the time.
+    // Pick the chunk of 1..5 with the least waves x (chunk + 1/4), the
+    // quarter standing for an item's fixed cost (ramp and epilogue).
     const int64_t slots = 2 * (int64_t)sm_count();   // resident CTAs
+    int best = kManyCh;
+    double best_cost = 1e30;
+    for (int c = 1; c <= kManyCh; ++c) {
+      const int64_t it = tiles * ((nl + c - 1) / c);
+      const double cost = (double)((it + slots - 1) / slots) * (c + 0.25);
+      if (cost < best_cost) { best_cost = cost; best = c; }
+    }
+    pa.chunk = best;
+    const int64_t items = tiles * ((nl + best - 1) / best);
     const int64_t waves = (items + slots - 1) / slots;
     const int64_t ga = (items + waves - 1) / waves;
     if (cudaError_t le = launch_dependent((p1_scores_kernel<kManyMaps, kManyCh>), dim3((unsigned)(ga)),

@@ -590,6 +590,37 @@ def test_decode_overlap_and_graph(gpu):
     assert torch.equal(p_new, ref) and not torch.equal(p_new, p_eager)
 
 
+def test_two_phase_stream_pipelined_passes(gpu):
+    """api.TwoPhaseStream: host inputs copied in on a copy stream, the block
+    pass on the current stream, the partial copied back on a third, two
+    device buffer sets in turn.  Four passes over different host inputs, all
+    submitted before any is awaited: each host result equals, bitwise, a
+    plain TwoPhaseBlock pass on the same inputs (a set reused too early, or a
+    partial read back before its pass ended, would show)."""
+    wl = wk.WORKLOADS["two_phase_bf16"]
+    rows, S, n = 640, 6, 9
+    passes = []
+    for j in range(4):
+        tp = wk.two_phase_inputs(wl, rows=rows + j, device="cpu", S=S, n=n)
+        tp["blocks"] = [b[:, :rows] for b in tp["blocks"]]          # same shape every pass
+        passes.append(tp)
+    host = [{"blocks": [b.contiguous().pin_memory() for b in tp["blocks"]],
+             "queries": tp["queries"].pin_memory(), "gains": tp["gains"].pin_memory(),
+             "u": tp["u"].pin_memory()} for tp in passes]
+    shape = tuple(host[0]["blocks"][0].shape)
+    pipe = api.TwoPhaseStream(n, shape, torch.bfloat16, S, gpu, wk.EPS)
+    outs = [torch.empty(shape, dtype=torch.bfloat16).pin_memory() for _ in host]
+    for h, out in zip(host, outs):
+        done = pipe.submit(h["blocks"], h["queries"], h["gains"], h["u"], out)
+    done.synchronize()
+    torch.cuda.synchronize()
+    for h, out in zip(host, outs):
+        want = api.TwoPhaseBlock([b.to(gpu) for b in h["blocks"]], h["queries"].to(gpu), h["gains"].to(gpu),
+                                 h["u"].to(gpu), wk.EPS).run().cpu()
+        assert torch.equal(out, want)
+    assert not torch.equal(outs[0], outs[1])
+
+
 # --------------------------------------------------------------------------
 # Full stack
 # --------------------------------------------------------------------------

@@ -442,6 +442,64 @@ class TwoPhaseBlock:
         return self.partial
 
 
+class TwoPhaseStream:
+    """Block passes over a stream of host inputs, pipelined across passes.
+
+    submit() copies one pass's summaries, queries, gains and u from (pinned)
+    host memory, runs the fused block pass (TwoPhaseBlock.run) and copies its
+    final partial back to a host tensor.  Two device buffer sets alternate:
+    the host->device copies of pass k+1 run on a copy stream while pass k's
+    kernels run on the current stream, and pass k's partial returns on a
+    third stream while pass k+1 runs.  Events order every reuse of a set (its
+    inputs are overwritten only after the pass that read them, its partial
+    only after it has reached the host), so each pass's result is exactly
+    TwoPhaseBlock.run()'s on the same inputs.
+    """
+
+    def __init__(self, n: int, shape, dtype, S: int, device, eps: float = 1e-8, with_gains: bool = True):
+        device = torch.device(device)
+        D = shape[-1]
+        self.sets = []
+        for _ in range(2):
+            blocks = [torch.empty(shape, dtype=dtype, device=device) for _ in range(n)]
+            q = torch.empty((S, D), dtype=torch.float32, device=device)
+            g = torch.empty((S, D), dtype=torch.float32, device=device) if with_gains else None
+            u = torch.empty((S, D), dtype=torch.float32, device=device)
+            self.sets.append({"blocks": blocks, "queries": q, "gains": g, "u": u,
+                              "blk": TwoPhaseBlock(blocks, q, g, u, eps),
+                              "copied": torch.cuda.Event(), "done": torch.cuda.Event(),
+                              "returned": torch.cuda.Event()})
+        self.device = device
+        self.copy_stream = torch.cuda.Stream(device=device)
+        self.d2h_stream = torch.cuda.Stream(device=device)
+        self.k = 0
+
+    def submit(self, host_blocks, host_queries, host_gains, host_u, out_host):
+        """Enqueue one pass; returns the event recorded once out_host holds its
+        final partial (out_host must not be reused before)."""
+        st = self.sets[self.k % 2]
+        self.k += 1
+        main = torch.cuda.current_stream(self.device)
+        self.copy_stream.wait_event(st["done"])            # the set's last pass has read its inputs
+        with torch.cuda.stream(self.copy_stream):
+            for dst, src in zip(st["blocks"], host_blocks):
+                dst.copy_(src, non_blocking=True)
+            st["queries"].copy_(host_queries, non_blocking=True)
+            if st["gains"] is not None:
+                st["gains"].copy_(host_gains, non_blocking=True)
+            st["u"].copy_(host_u, non_blocking=True)
+        st["copied"].record(self.copy_stream)
+        main.wait_event(st["copied"])
+        main.wait_event(st["returned"])                      # its last partial is back on the host
+        partial = st["blk"].run(stream=main.cuda_stream)
+        st["done"].record(main)
+        self.d2h_stream.wait_event(st["done"])
+        with torch.cuda.stream(self.d2h_stream):
+            out_host.copy_(partial, non_blocking=True)
+        st["returned"].record(self.d2h_stream)
+        return st["returned"]
+
+
 def block_two_phase(blocks, queries, gains, u, eps: float = 1e-8, fused: bool = True,
                     norm_weights=None, norm_eps: float = 1e-6):
     """Run one block of the two-phase scheme; returns (final partial, sublayer inputs [S, ...])."""

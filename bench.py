@@ -678,12 +678,20 @@ def run_configs(dev):
         plain(), two()
     ms_p = _event_median_ms(plain, 5, flush)
     ms_t = _event_median_ms(two, 5, flush)
+    # the same stacks as one CUDA graph each (api.FullStack)
+    graphs = {}
+    for name, S_g in (("plain", None), ("two_phase", S)):
+        fs = api.FullStack(inp["v0"], inp["queries"], inp["gains"], inp["u"], inp["eps"], S=S_g)
+        fs.capture()
+        graphs[name] = round(_event_median_ms(fs.replay, 5, flush), 4)
+        del fs
     rp = _rate(accounting.full_stack_bytes(wl.L, wl.rows, wl.D, 2), ms_p, peak)
     rt = _rate(accounting.full_two_phase_bytes(wl.L, S, wl.rows, wl.D, 2), ms_t, peak)
     rt.update({"schedule_block_size": S, "tokens_per_s": round(wl.rows / (ms_t * 1e-3), 1),
                "speedup_vs_plain": round(ms_p / ms_t, 3)})
     rp.update({"workload": wl.name, "tokens_per_s": round(wl.rows / (ms_p * 1e-3), 1), "launches": wl.L + 1,
-               "two_phase": rt, "timing": "one whole stack per sample, L2 flushed before each, median of 5"})
+               "two_phase": rt, "graph_ms": graphs,
+               "timing": "one whole stack per sample, L2 flushed before each, median of 5"})
     res[wl.name] = rp
     del inp, srcs, y, ws
 

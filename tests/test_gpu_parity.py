@@ -638,6 +638,26 @@ def test_full_stack_small(gpu):
         check(y.reshape(rows, D), oracle.round_to(oy, ODT[dtype]), tol, "y")
 
 
+def test_full_stack_as_one_cuda_graph(gpu):
+    """api.FullStack: the plain stack and the two-phase schedule captured as one
+    CUDA graph each replay bitwise the eager run, and a replay reads the live
+    v_0 (changed in place after the capture)."""
+    wl = wk.WORKLOADS["full_stack_bf16"]
+    inp = wk.full_stack_inputs(wl, rows=300, device=gpu, L=30, D=1024)
+    for S in (None, 6):
+        fs = api.FullStack(inp["v0"].clone(), inp["queries"], inp["gains"], inp["u"], inp["eps"], S=S)
+        want = fs.run().clone()
+        fs.capture()
+        got = fs.replay().clone()
+        torch.cuda.synchronize()
+        assert torch.equal(got, want), f"S={S}"
+        fs.v0.mul_(-1.0)
+        got2 = fs.replay().clone()
+        ref = api.FullStack(fs.v0.clone(), inp["queries"], inp["gains"], inp["u"], inp["eps"], S=S).run()
+        torch.cuda.synchronize()
+        assert torch.equal(got2, ref) and not torch.equal(got2, want), f"S={S} after v0 changed"
+
+
 def test_full_stack_config_full_size_sampled(gpu):
     wl = wk.WORKLOADS["full_stack_bf16"]
     inp = wk.full_stack_inputs(wl, device=gpu)

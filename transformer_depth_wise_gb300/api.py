@@ -225,6 +225,54 @@ def full_stack_two_phase(v0, queries, gains, u, S: int, eps: float = 1e-8, sourc
     return y, sources
 
 
+class FullStack:
+    """A whole Full AttnRes stack over preallocated buffers, as one call or as
+    one CUDA graph.  S = None runs the plain stack (attnres_full_stack_forward),
+    an integer S the two-phase schedule of block size S (with its workspace).
+    run() launches it eagerly; capture() records one run as a CUDA graph (after
+    one eager run, which settles the library's per-kernel launch settings) and
+    replay() launches the graph: the same kernels on the same buffers, so the
+    results are bitwise those of run()."""
+
+    def __init__(self, v0, queries, gains, u, eps: float = 1e-8, S=None):
+        _cuda(v0, "v0")
+        self.v0, self.queries, self.gains, self.u, self.eps, self.S = v0, queries, gains, u, float(eps), S
+        L = u.shape[0]
+        self.sources = [v0] + [torch.empty_like(v0) for _ in range(L)]
+        self.y = torch.empty_like(v0)
+        self.workspace = None
+        if S is not None:
+            B, T, D = _btd(v0)
+            need = int(_lib.lib().attnres_full_stack_two_phase_workspace_bytes(L, int(S), B, T, D, _code(v0)))
+            if need < 0:
+                _lib.check("attnres_full_stack_two_phase_workspace_bytes", need)
+            self.workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=v0.device)
+        self.graph = None
+
+    def run(self):
+        if self.S is None:
+            full_stack_forward(self.v0, self.queries, self.gains, self.u, self.eps, self.sources, self.y)
+        else:
+            full_stack_two_phase(self.v0, self.queries, self.gains, self.u, self.S, self.eps, self.sources, self.y,
+                                 self.workspace)
+        return self.y
+
+    def capture(self):
+        self.run()
+        torch.cuda.synchronize(self.v0.device)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            self.run()
+        self.graph = g
+        return g
+
+    def replay(self):
+        if self.graph is None:
+            raise RuntimeError("capture() first")
+        self.graph.replay()
+        return self.y
+
+
 def block_merge_update(inter_out, inter_lse, partial_in, sub_out, u, query, gain=None,
                        eps: float = 1e-8, partial_out=None, h_out=None, out_lse=None,
                        norm_weight=None, norm_eps: float = 1e-6, normed_out=None, write_h: bool = True):

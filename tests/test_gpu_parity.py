@@ -180,11 +180,12 @@ def test_aggregate_block_single_full_size_sampled(gpu):
 
 # Shapes that reach the aggregation's instantiations with the CTA width
 # built in and the many-rows shape (from 32 rows per SM on a 152-SM GPU,
-# 4864 rows): rows that exactly fill 64, 128 or 256 threads, and a ragged
-# width for contrast; rows compared on a sample (rows are independent).
+# 4864 rows): rows that exactly fill 64, 128, 224 or 256 threads, and a
+# ragged width for contrast; rows compared on a sample (rows are independent).
 @pytest.mark.parametrize("dtype,D,n,rows", [
     (torch.bfloat16, 4096, 5, 4900), (torch.bfloat16, 1024, 7, 5000), (torch.bfloat16, 8192, 3, 4870),
     (torch.float32, 2048, 4, 4900), (torch.bfloat16, 1024, 3, 2000), (torch.bfloat16, 2056, 6, 4900),
+    (torch.bfloat16, 7168, 10, 4900), (torch.float32, 3584, 3, 4871),
 ])
 def test_aggregate_exact_widths_sampled(gpu, dtype, D, n, rows):
     srcs, q, g = rand_sources(n, (1, rows, D), dtype, gpu, seed=D + 3 * n + rows)

@@ -525,7 +525,7 @@ bool choose_pipe(int n, int64_t rows, int D, int dtype, PipeCfg &c) {
   const bool exact = nvec == c.threads * c.vpt;
   c.tpr = 0;
   if (exact) {
-    const int built[] = {64, 128, 256};
+    const int built[] = {64, 128, 224, 256};   // 224: D = 7168 bf16 at four vectors a thread
     for (int b : built)
       if (b == c.threads) c.tpr = b;
   }
@@ -565,6 +565,7 @@ cudaError_t dispatch_pipe(const AggParams &p, const PipeCfg &c, cudaStream_t st)
   switch (c.tpr) {
     case 64: return run_pipe<T, F, 2, 4, 64>(p, c.threads, st);
     case 128: return run_pipe<T, F, 2, 4, 128>(p, c.threads, st);
+    case 224: return run_pipe<T, F, 2, 4, 224>(p, c.threads, st);
     case 256: return run_pipe<T, F, 2, 4, 256>(p, c.threads, st);
     default: return run_pipe<T, F, 2, 4, 0>(p, c.threads, st);
   }

@@ -792,7 +792,9 @@ p1_many_outputs_kernel(const __grid_constant__ ParamsB2 p) {
 // into the B fragments; alpha (fp32) is split into bf16 hi + lo, two MMAs per
 // tile, so it keeps about 16 significant bits.  The summary rows stream
 // through a two-slot cp.async ring, 16 rows per step (rows past n zero-filled);
-// each warp holds the accumulators of its 128 features across the steps.
+// each warp holds the accumulators of its 128 features across the steps.  A
+// work item is one of a token's `parts` pieces of WARPS x 128 features, so
+// two CTAs of 8 warps can share an SM at D = 2048.
 // -----------------------------------------------------------------------------
 constexpr int kTcK = 16;           // summaries per step (mma K)
 constexpr int kTcWarps = 16;       // 512 threads
@@ -803,6 +805,7 @@ struct ParamsB3 {
   void *out;            // [S, rows, D] bf16
   int64_t rows;
   int n, S, D;
+  int parts;            // a token's features in `parts` pieces, each a work item of its own
 };
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
@@ -831,33 +834,40 @@ __host__ __device__ constexpr size_t tc_smem(int n, int D) {
   return 2 * (size_t)kTcK * tc_row_v(D) + 2 * 2 * (size_t)kTcK * tc_row_a(n);
 }
 
-__global__ void __launch_bounds__(kTcWarps * 32, 1)
+template <int WARPS>
+__global__ void __launch_bounds__(WARPS * 32, 16 / WARPS)
 p1_many_outputs_tc_kernel(const __grid_constant__ ParamsB3 p) {
   grid_dependency_wait();
   extern __shared__ __align__(16) unsigned char sm3[];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int n = p.n, S = p.S, D = p.D;
+  const int n = p.n, S = p.S, D = p.D, parts = p.parts;
+  const int DF = D / parts;                                      // features per work item
   const int KS = (n + kTcK - 1) / kTcK, KP = KS * kTcK;
-  const size_t RV = tc_row_v(D), RA = tc_row_a(n);
+  const size_t RV = tc_row_v(DF), RA = tc_row_a(n);
   unsigned char *vring = sm3;                                    // [2][16][RV]
-  unsigned char *abuf = sm3 + 2 * kTcK * RV;                     // [2 tokens][hi, lo][16][RA]
+  unsigned char *abuf = sm3 + 2 * kTcK * RV;                     // [2 items][hi, lo][16][RA]
   const size_t row_bytes = (size_t)D * 2;
-  const int chunks = D / 8;                                      // 16-byte chunks per row
-  const int ntw = D / 8 / kTcWarps;                              // n-tiles per warp (even, <= 16)
-  const int64_t my_tokens = p.rows > (int64_t)blockIdx.x ? (p.rows - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
+  const int chunks = DF / 8;                                     // 16-byte chunks per item row
+  const int ntw = DF / 8 / WARPS;                                // n-tiles per warp (even, <= 16)
+  const int64_t items = p.rows * parts;
+  const int64_t my_tokens = items > (int64_t)blockIdx.x ? (items - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
   const int64_t total = my_tokens * KS;
 
-  auto token = [&](int64_t j) { return (int64_t)blockIdx.x + j * gridDim.x; };
+  // work item j of this CTA: (token, piece of the features), pieces of a
+  // token on different CTAs
+  auto token = [&](int64_t j) { return ((int64_t)blockIdx.x + j * gridDim.x) / parts; };
+  auto first_feature = [&](int64_t j) { return (int)(((int64_t)blockIdx.x + j * gridDim.x) % parts) * DF; };
   // When the CTA width is a multiple of the chunks per row, a thread's chunk
   // column is fixed and its rows step by a constant (no division per copy).
   const bool whole_rows = blockDim.x % chunks == 0;
   const int rstep = whole_rows ? blockDim.x / chunks : 0, r0 = tid / chunks, ch0 = tid % chunks;
   auto issue = [&](int64_t g) {                                  // step g: 16 summary rows -> slot g & 1
     const int64_t t = token(g / KS);
+    const size_t fo = (size_t)first_feature(g / KS) * 2;
     const int kk = (int)(g % KS);
     unsigned char *slot = vring + (size_t)(g & 1) * kTcK * RV;
     if (whole_rows) {
-      const size_t goff = (size_t)t * row_bytes + (size_t)ch0 * 16;
+      const size_t goff = (size_t)t * row_bytes + fo + (size_t)ch0 * 16;
       for (int r = r0; r < kTcK; r += rstep) {
         const int i = kk * kTcK + r;
         const char *gp = static_cast<const char *>(p.src[i < n ? i : 0]) + goff;
@@ -866,7 +876,7 @@ p1_many_outputs_tc_kernel(const __grid_constant__ ParamsB3 p) {
     } else {
       for (int c = tid; c < kTcK * chunks; c += blockDim.x) {
         const int r = c / chunks, ch = c % chunks, i = kk * kTcK + r;
-        const char *gp = static_cast<const char *>(p.src[i < n ? i : 0]) + (size_t)t * row_bytes + (size_t)ch * 16;
+        const char *gp = static_cast<const char *>(p.src[i < n ? i : 0]) + (size_t)t * row_bytes + fo + (size_t)ch * 16;
         cp_async16_zfill(slot + (size_t)r * RV + (size_t)ch * 16, gp, i < n ? 16u : 0u);
       }
     }
@@ -924,11 +934,11 @@ p1_many_outputs_tc_kernel(const __grid_constant__ ParamsB3 p) {
     }
     if (kk == KS - 1) {          // token done: rows q = lane/4 and lane/4 + 8, two features per tile
       const int64_t t = token(j);
-      const int q0 = lane >> 2, fc = (lane & 3) * 2;
+      const int q0 = lane >> 2, fc = (lane & 3) * 2, fo = first_feature(j);
 #pragma unroll
       for (int nt = 0; nt < 16; ++nt) {
         if (nt >= ntw) break;
-        const int f = (warp * ntw + nt) * 8 + fc;
+        const int f = fo + (warp * ntw + nt) * 8 + fc;
         if (q0 < S)
           __stcs(reinterpret_cast<uint32_t *>(static_cast<char *>(p.out) + ((size_t)q0 * p.rows + t) * row_bytes + (size_t)f * 2),
                  Elt<__nv_bfloat16>::pack_word(c[nt][0], c[nt][1]));
@@ -1245,6 +1255,38 @@ cudaError_t launch_phase1_many(const Phase1ManyArgs &a) {
       return le;
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
+  // Two CTAs share an SM, each taking a piece of 1024 features of a token
+  // with 8 warps: per-thread row copies stream at a limited rate per CTA, so
+  // two CTAs per SM keep more copies in flight (the Full two-phase schedule
+  // at D = 2048: 8.8 -> 8.57 ms; pieces of 512 on 4-warp CTAs, three per SM,
+  // measured 8.80 ms).  Otherwise one CTA of 16 warps takes the whole row.
+  for (int warps : {8}) {
+    const int DF = 8 * warps * 16;                // features per piece: 16 n-tiles per warp
+    if (a.S > kTcK || a.D % DF != 0 || a.D / DF < 2) continue;
+    const size_t smem3 = tc_smem(a.n, DF);
+    int occ = 0;
+    auto kern = p1_many_outputs_tc_kernel<8>;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem3);
+    if (e != cudaSuccess) return e;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, warps * 32, smem3);
+    if (e != cudaSuccess) return e;
+    if (occ < 2) continue;
+    ParamsB3 pc;
+    for (int i = 0; i < a.n; ++i) pc.src[i] = a.blocks[i];
+    pc.alpha = a.scores;
+    pc.out = a.out;
+    pc.rows = a.rows;
+    pc.n = a.n;
+    pc.S = a.S;
+    pc.D = a.D;
+    pc.parts = a.D / DF;
+    const int64_t items = a.rows * pc.parts, cap = (int64_t)occ * sm_count();
+    const int64_t g3 = items < cap ? items : cap;
+    if (cudaError_t le = launch_dependent(kern, dim3((unsigned)(g3)), dim3(warps * 32), smem3, a.stream, pc);
+        le != cudaSuccess)
+      return le;
+    return cudaGetLastError();
+  }
   if (a.S <= kTcK && a.D % (8 * kTcWarps * 2) == 0 && a.D <= 8 * kTcWarps * 16 &&
       tc_smem(a.n, a.D) <= 227 * 1024) {
     ParamsB3 pc;
@@ -1255,12 +1297,14 @@ cudaError_t launch_phase1_many(const Phase1ManyArgs &a) {
     pc.n = a.n;
     pc.S = a.S;
     pc.D = a.D;
+    pc.parts = 1;
     const size_t smem3 = tc_smem(a.n, a.D);
-    e = cudaFuncSetAttribute(p1_many_outputs_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem3);
+    e = cudaFuncSetAttribute(p1_many_outputs_tc_kernel<kTcWarps>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem3);
     if (e != cudaSuccess) return e;
     const int64_t g3 = a.rows < sm_count() ? a.rows : sm_count();
-    if (cudaError_t le = launch_dependent(p1_many_outputs_tc_kernel, dim3((unsigned)(g3)), dim3(kTcWarps * 32),
-                                          smem3, a.stream, pc); le != cudaSuccess)
+    if (cudaError_t le = launch_dependent(p1_many_outputs_tc_kernel<kTcWarps>, dim3((unsigned)(g3)),
+                                          dim3(kTcWarps * 32), smem3, a.stream, pc); le != cudaSuccess)
       return le;
     return cudaGetLastError();
   }

@@ -129,8 +129,13 @@ aggregate_backward_kernel(const __grid_constant__ BwdParams p) {
       PR::split(x, gp + k * NP);
     }
 
-    // Pass A: sum v^2, w~ . v and dh . v for every source.
+    // Pass A: sum v^2, w~ . v and dh . v for every source.  With a whole
+    // CTA on the row, a few threads first ask L2 for the next group's rows
+    // (one bulk prefetch per row), so its loads find them there after this
+    // group's reduction.
     for (int i0 = 0; i0 < p.n; i0 += GA) {
+      if (!TEAM && row_ok && threadIdx.x < GA && i0 + GA + (int)threadIdx.x < p.n)
+        prefetch_l2_bulk(static_cast<const char *>(p.src[i0 + GA + threadIdx.x]) + row_off, (uint32_t)row_bytes);
       uint4 v[GA][VPT];
 #pragma unroll
       for (int j = 0; j < GA; ++j)
@@ -214,6 +219,14 @@ aggregate_backward_kernel(const __grid_constant__ BwdParams p) {
     if (TEAM) __syncwarp(); else __syncthreads();
 
     // Pass B: dv_i = alpha_i dh + (ds_i r_i) w~ - (ds_i s_i r_i^2 / D) v_i.
+    // Meanwhile L2 is asked for the next row's dh and first group of sources.
+    if (!TEAM && threadIdx.x <= GA) {
+      const int64_t nrow = (rg + gridDim.x) * TPC;
+      if (nrow < p.rows) {
+        const void *base = threadIdx.x == GA ? p.dh : (threadIdx.x < p.n ? p.src[threadIdx.x] : nullptr);
+        if (base) prefetch_l2_bulk(static_cast<const char *>(base) + (size_t)nrow * row_bytes, (uint32_t)row_bytes);
+      }
+    }
     for (int i0 = 0; i0 < p.n; i0 += GB) {
       uint4 v[GB][VPT], din[GB][VPT];
 #pragma unroll

@@ -69,7 +69,6 @@ constexpr int kStages = 9;            // ring of (summary chunk 16 KB + query ch
 constexpr uint32_t kVBytes = kRows * kKc * 2;
 constexpr uint32_t kQBytes = kNQ * kKc * 2;
 constexpr uint32_t kStageBytes = kVBytes + kQBytes;   // both parts 1024-byte aligned
-constexpr int kTmemCols = 512;
 constexpr int kBStages = 3;           // kernel B: tokens in flight (cp.async stages)
 constexpr int kWarpsA = 6;            // 0-3: sums of squares + epilogue, 4: TMA, 5: MMA
 constexpr int kThreadsA = kWarpsA * 32;

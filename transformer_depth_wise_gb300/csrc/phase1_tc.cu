@@ -1001,6 +1001,27 @@ int split_parts(const Phase1Args &a) {
   return 1;
 }
 
+// Summaries per raw-mode work item, 1..max: each CTA streams its
+// tensor-map boxes at about the same rate however many it has in flight, so
+// a launch takes about (waves of items) x (summaries per item); few
+// summaries leave SMs idle with five per item, and a nearly empty last wave
+// doubles the time.  The chunk with the least waves x (chunk + 1/4), the
+// quarter standing for an item's fixed cost (ramp and epilogue).
+static int many_chunk(int64_t tiles, int n, int max_chunk) {
+  const int64_t slots = 2 * (int64_t)sm_count();   // resident CTAs
+  int best = max_chunk;
+  double best_cost = 1e30;
+  for (int c = 1; c <= max_chunk; ++c) {
+    const int64_t it = tiles * ((n + c - 1) / c);
+    const double cost = (double)((it + slots - 1) / slots) * (c + 0.25);
+    if (cost < best_cost) {
+      best_cost = cost;
+      best = c;
+    }
+  }
+  return best;
+}
+
 cudaError_t launch_phase1_tc(const Phase1Args &a) {
   using namespace tc;
   auto encode = encode_fn();
@@ -1093,7 +1114,7 @@ cudaError_t launch_phase1_tc(const Phase1Args &a) {
   if (a.S >= 3 && (int64_t)(a.S - 2) * a.rows >= kNQ && (size_t)a.n * a.S * 4 <= row_bytes) {
     constexpr int kCh = 5;
     float *raw = reinterpret_cast<float *>(static_cast<char *>(a.out) + (size_t)a.rows * row_bytes);  // o[1]
-    pa.chunk = kCh;
+    pa.chunk = many_chunk(tiles, a.n, kCh);
     pa.raw = raw;
     pa.raw_n = a.n;
     pa.raw_off = 0;
@@ -1101,7 +1122,7 @@ cudaError_t launch_phase1_tc(const Phase1Args &a) {
     e = cudaFuncSetAttribute(p1_scores_kernel<kMaxN, kCh>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)smem_a(kCh));
     if (e != cudaSuccess) return e;
-    const int64_t items = tiles * ((a.n + kCh - 1) / kCh);
+    const int64_t items = tiles * ((a.n + pa.chunk - 1) / pa.chunk);
     const int64_t slots = 2 * (int64_t)sm_count();
     const int64_t waves = (items + slots - 1) / slots;
     const int64_t ga = (items + waves - 1) / waves;
@@ -1223,22 +1244,9 @@ cudaError_t launch_phase1_many(const Phase1ManyArgs &a) {
     }
     pa.n = nl;
     pa.raw_off = off;
-    // Summaries per item: each CTA streams its tensor-map boxes at about the
-    // same rate however many it has in flight, so a launch takes about
-    // (waves of items) x (summaries per item); few summaries leave SMs idle
-    // with five per item, and a nearly empty last wave doubles the time.
-    // Pick the chunk of 1..5 with the least waves x (chunk + 1/4), the
-    // quarter standing for an item's fixed cost (ramp and epilogue).
     const int64_t slots = 2 * (int64_t)sm_count();   // resident CTAs
-    int best = kManyCh;
-    double best_cost = 1e30;
-    for (int c = 1; c <= kManyCh; ++c) {
-      const int64_t it = tiles * ((nl + c - 1) / c);
-      const double cost = (double)((it + slots - 1) / slots) * (c + 0.25);
-      if (cost < best_cost) { best_cost = cost; best = c; }
-    }
-    pa.chunk = best;
-    const int64_t items = tiles * ((nl + best - 1) / best);
+    pa.chunk = many_chunk(tiles, nl, kManyCh);
+    const int64_t items = tiles * ((nl + pa.chunk - 1) / pa.chunk);
     const int64_t waves = (items + slots - 1) / slots;
     const int64_t ga = (items + waves - 1) / waves;
     if (cudaError_t le = launch_dependent((p1_scores_kernel<kManyMaps, kManyCh>), dim3((unsigned)(ga)),

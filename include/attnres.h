@@ -28,6 +28,11 @@
  *     allocates no device memory, keeps no state between calls and never
  *     synchronises: work is queued on `stream` (a cudaStream_t; NULL is
  *     the legacy default stream) and the call returns.
+ *   - Stream order: the forward kernels are launched as programmatic
+ *     dependents of the kernel before them on the stream (their launch may
+ *     overlap its end), and each waits for that kernel to complete before
+ *     it touches any memory, so results follow plain stream order, also
+ *     under stream capture.
  *   - Errors: arguments are checked before anything is launched; a bad
  *     argument returns a negative attnres_status_t and launches nothing.
  *     A launch failure returns ATTNRES_ERR_CUDA.  Nothing aborts or prints.

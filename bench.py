@@ -745,8 +745,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-configs", action="store_true",
                     help="headline only: skip the per-workload measurements of the other configs")
-    ap.add_argument("--kernel", default="", choices=["", "merge_update"],
-                    help="time one kernel alone at --rows token rows (profiling; no headline line)")
+    ap.add_argument("--kernel", default="", choices=["", "merge_update", "aggregate"],
+                    help="time one kernel alone at --rows token rows (profiling; no headline line): the fused "
+                         "update+merge at the workload's width, or the workload's single aggregation")
     ap.add_argument("--schedule-block-size", type=int, default=14,
                     help="Full stack: block size S of the two-phase schedule timed beside the plain stack")
     args = ap.parse_args()
@@ -791,6 +792,8 @@ def main():
 
     if args.kernel == "merge_update":
         res = run_merge_update_only(args, wl, dev)
+    elif args.kernel == "aggregate":
+        res = run_single(args, wl, dev, world)
     elif wl.name in ("two_phase_bf16", "long_prefill_bf16", "decode_bf16"):
         res = run_two_phase(args, wl, dev, rank, world)
     elif wl.name == "full_stack_bf16":

@@ -301,6 +301,9 @@ def test_aggregate_backward_full_size_sampled(gpu):
     # shape, one partly filled tile, an odd S (pad query), ten summaries at S = 3
     (torch.bfloat16, 7168, 9, 24, 256), (torch.bfloat16, 4096, 9, 24, 100), (torch.bfloat16, 2048, 5, 7, 300),
     (torch.bfloat16, 1024, 10, 3, 64),
+    # the widest rows: nine summaries at D = 8192 fill kernel B's shared memory (two pieces of 4096); ten
+    # do not fit it, and those rows take the per-row kernel
+    (torch.bfloat16, 8192, 9, 24, 520), (torch.bfloat16, 8192, 10, 24, 512),
 ])
 def test_phase1_small(gpu, dtype, D, n, S, rows):
     g = wk.generator(D + n + S, gpu)

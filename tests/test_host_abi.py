@@ -179,6 +179,43 @@ def test_full_stack_argument_checks():
     assert f(arr, 4, 0, 2, 64, 1, FAKE, None, FAKE, 1e-8, FAKE, None) == OK
 
 
+def test_full_two_phase_argument_checks():
+    # L = 5 sublayers in blocks of S = 2: every block's phase 1 has at most ten
+    # sources, so the shape checks need no GPU
+    L = _lib.lib()
+    wsb = L.attnres_full_stack_two_phase_workspace_bytes
+    assert wsb(5, 2, 1, 4, 64, 1) > 0
+    assert wsb(0, 2, 1, 4, 64, 1) == SHAPE
+    assert wsb(5, 0, 1, 4, 64, 1) == SHAPE
+    assert wsb(5, 2, 1, 4, 64, 7) == DTYPE
+    assert wsb(5, 2, 1, 4, 36, 1) == ALIGN
+    need = wsb(5, 2, 1, 4, 64, 1)
+    arr = _lib.ptr_array([FAKE] * 6)
+    tp = L.attnres_full_stack_two_phase
+
+    def call(arr=arr, Lsub=5, S=2, B=1, ws=FAKE, wsbytes=need, eps=1e-8, y=FAKE, q=FAKE, u=FAKE):
+        return tp(arr, Lsub, S, B, 4, 64, 1, q, None, u, eps, y, ws, wsbytes, None)
+
+    assert call(S=0) == SHAPE
+    assert call(S=65) == SHAPE
+    assert call(Lsub=0) == SHAPE
+    big = _lib.ptr_array([FAKE] * 257)
+    assert call(arr=big, Lsub=256) == MANY
+    assert call(eps=-1.0) == VALUE
+    assert call(B=0, arr=None, ws=None, y=None, q=None, u=None) == OK    # empty: nothing checked or launched
+    assert call(arr=None) == NULL
+    assert call(ws=None) == NULL
+    assert call(q=None) == NULL
+    assert call(arr=_lib.ptr_array([FAKE] * 5 + [0])) == NULL
+    assert call(arr=_lib.ptr_array([FAKE] * 5 + [FAKE + 8])) == ALIGN
+    assert call(ws=FAKE + 16) == ALIGN                                   # the workspace is 256-byte aligned
+    assert call(wsbytes=need - 1) == CAP
+    # the backward with no token rows: nothing is read, launched or written
+    garr = _lib.ptr_array([FAKE + 4096] * 3)
+    assert L.attnres_depth_aggregate_backward(_lib.ptr_array([FAKE] * 3), 3, 0, 2, 64, 1, FAKE, None, 1e-8, FAKE,
+                                              garr, 0, None, None, None, 0, None) == OK
+
+
 @pytest.mark.parametrize("N", [1, 2, 5, 8, 23, 48, 93, 186])
 def test_schedule_matches_oracle_bit_exact(N):
     for S in sorted({1, 2, 3, 4, 6, 7, 24, N, N + 5}):

@@ -390,7 +390,8 @@ def test_merge_update_fused_step(gpu):
             u = wk.sublayer_u(g, 1, D, gpu)[0].contiguous() if synth else None
             lse = torch.empty(rows, device=gpu).normal_(0.0, 2.0, generator=g)
             p_in = pin if with_pin else None
-            p_out, h, _ = api.block_merge_update(o, lse, p_in, sub, u, W[0], G[0], 1e-8)
+            lse_out = torch.full((rows,), float("nan"), device=gpu)
+            p_out, h, _ = api.block_merge_update(o, lse, p_in, sub, u, W[0], G[0], 1e-8, out_lse=lse_out)
             subn = f64(sub).reshape(rows, D)
             out = oracle.synthetic_sublayer(f64(u), subn) if synth else subn
             want_p = oracle.round_to((f64(pin).reshape(rows, D) if with_pin else 0.0) + out, ODT[dtype])
@@ -399,6 +400,11 @@ def test_merge_update_fused_step(gpu):
             tol = TOL[dtype] * vmax([o, pin, sub])
             check(p_out.reshape(rows, D), want_p, tol, "fused p")
             check(h.reshape(rows, D), oracle.round_to(want_h, ODT[dtype]), tol, "fused h")
+            # the merged lse, from the partial as stored: the fast tanh may round a few elements of p to
+            # the neighbouring value (within p's tolerance above), which moves s_p with them
+            _, want_lse = oracle.block_phase2_merge(f64(o).reshape(rows, D), f64(lse), f64(p_out).reshape(rows, D),
+                                                    f64(W[0]), f64(G[0]), 1e-8)
+            check_stats(lse_out, want_lse, "fused merged lse")
             if with_pin:                                       # in place: p_out aliases p_in,
                 pi, hs = pin.clone(), sub.clone()              # h_out aliases sub_out
                 api.block_merge_update(o, lse, pi, hs, u, W[0], G[0], 1e-8, partial_out=pi, h_out=hs)
@@ -468,7 +474,8 @@ def test_merge_update_many_rows_sampled(gpu, D, rows):
         u = wk.sublayer_u(g, 1, D, gpu)[0].contiguous()
         lse = torch.empty(rows, device=gpu).normal_(0.0, 2.0, generator=g)
         kw = dict(norm_weight=Wn[0], norm_eps=1e-5) if norm else {}
-        res = api.block_merge_update(o, lse, pin, sub, u, W[0], G[0], 1e-8, **kw)
+        lse_out = torch.full((rows,), float("nan"), device=gpu)
+        res = api.block_merge_update(o, lse, pin, sub, u, W[0], G[0], 1e-8, out_lse=lse_out, **kw)
         p_out, h = res[0], res[1]
         idx = torch.as_tensor(sample, device=gpu)
         subn = f64(pick(sub, sample, D))
@@ -478,6 +485,9 @@ def test_merge_update_many_rows_sampled(gpu, D, rows):
         tol = TOL[dtype] * vmax([o, pin, sub])
         check(pick(p_out, sample, D), want_p, tol, f"p D={D} norm={norm}")
         check(pick(h, sample, D), oracle.round_to(want_h, ODT[dtype]), tol, f"h D={D} norm={norm}")
+        _, want_lse = oracle.block_phase2_merge(f64(pick(o, sample, D)), f64(lse[idx]), f64(pick(p_out, sample, D)),
+                                                f64(W[0]), f64(G[0]), 1e-8)   # from the partial as stored
+        check_stats(lse_out[idx], want_lse, f"merged lse D={D} norm={norm}")
         if norm:
             want_y = oracle.rms_norm(want_h, f64(Wn[0]), 1e-5)
             check(pick(res[2], sample, D), oracle.round_to(want_y, ODT[dtype]),

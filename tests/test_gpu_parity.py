@@ -153,6 +153,37 @@ def test_aggregate_many_sources(gpu):
     check(out, h, TOL[torch.bfloat16] * vmax(srcs), "n=187")
 
 
+def test_gain_absent_is_a_gain_of_one_bitwise(gpu):
+    """gain = NULL is a gain of one: the folded query w (.) 1 is w exactly, so every path gives bitwise the
+    result of an all-ones gain (the aggregation on its pipelined and team kernels, phase 1 on the tensor
+    cores and per row, the fused step on its few-row and CTA kernels, and the backward's gradients)."""
+    for D, n, rows, dtype in ((2048, 10, 600, torch.bfloat16), (256, 5, 33, torch.bfloat16),
+                              (512, 4, 70, torch.float32)):
+        srcs, q, _ = rand_sources(n, (1, rows, D), dtype, gpu, seed=D + n)
+        ones = torch.ones(D, device=gpu)
+        assert torch.equal(api.depth_aggregate(srcs, q, None, 1e-8), api.depth_aggregate(srcs, q, ones, 1e-8))
+    for rows in (600, 40):
+        blocks, _, _ = rand_sources(9, (1, rows, 4096), torch.bfloat16, gpu, seed=rows)
+        W, _ = wk.queries_and_gains(wk.generator(rows + 1, gpu), 24, 4096, gpu)
+        a = api.block_phase1(blocks, W, None, 1e-8)
+        b = api.block_phase1(blocks, W, torch.ones_like(W), 1e-8)
+        assert torch.equal(a[0], b[0]) and torch.equal(a[2], b[2]), f"phase 1, {rows} rows"
+    for rows in (45, 700):
+        g = wk.generator(rows + 2, gpu)
+        (o, pin, sub), _ = wk.scaled_normal_sources(g, 3, (1, rows, 4096), 0.5, 3.0, torch.bfloat16, gpu)
+        W, _ = wk.queries_and_gains(g, 1, 4096, gpu)
+        u = wk.sublayer_u(g, 1, 4096, gpu)[0].contiguous()
+        lse = torch.empty(rows, device=gpu).normal_(0.0, 2.0, generator=g)
+        a = api.block_merge_update(o, lse, pin, sub, u, W[0], None, 1e-8)
+        b = api.block_merge_update(o, lse, pin, sub, u, W[0], torch.ones(4096, device=gpu), 1e-8)
+        assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1]), f"fused step, {rows} rows"
+    srcs, q, _ = rand_sources(4, (1, 300, 2048), torch.bfloat16, gpu, seed=77)
+    dh = wk.upstream_grad(wk.generator(78, gpu), (1, 300, 2048), torch.bfloat16, gpu)
+    ga, qa, gga = api.depth_aggregate_backward(srcs, q, None, 1e-8, dh)
+    gb, qb, ggb = api.depth_aggregate_backward(srcs, q, torch.ones(2048, device=gpu), 1e-8, dh)
+    assert all(torch.equal(x, y) for x, y in zip(ga, gb)) and torch.equal(qa, qb) and torch.equal(gga, ggb)
+
+
 def pick(t, rows, D):
     """Rows (numpy indices) of a [.., D] CUDA tensor viewed as [rows, D]."""
     return t.reshape(-1, D)[torch.as_tensor(rows, device=t.device)]

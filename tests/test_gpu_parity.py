@@ -184,6 +184,41 @@ def test_gain_absent_is_a_gain_of_one_bitwise(gpu):
     assert all(torch.equal(x, y) for x, y in zip(ga, gb)) and torch.equal(qa, qb) and torch.equal(gga, ggb)
 
 
+def test_stream_order_with_dependent_launches(gpu):
+    """The library's kernels start as programmatic dependents of the kernel before them on the stream and
+    wait for it before touching memory: a query or a source rewritten by a torch kernel right before the call
+    is what the call reads.  Ten rewrite-then-call rounds queued back to back, on the pipelined aggregation and
+    on the fused step, against the same calls made after a full synchronisation."""
+    srcs, q, g = rand_sources(6, (1, 2000, 2048), torch.bfloat16, gpu, seed=31)
+    qs = [q * (1.0 + 0.5 * k) for k in range(10)]
+    outs, qbuf = [], torch.empty_like(q)
+    for k in range(10):
+        qbuf.copy_(qs[k])                                  # a torch kernel, then the library's on the same stream
+        srcs[0].mul_(-1.0)
+        outs.append(api.depth_aggregate(srcs, qbuf, g, 1e-8).clone())
+    torch.cuda.synchronize()                               # ten sign flips: srcs[0] is back to its start
+    for k in range(10):
+        srcs[0].mul_(-1.0)
+        torch.cuda.synchronize()
+        want = api.depth_aggregate(srcs, qs[k], g, 1e-8)
+        torch.cuda.synchronize()
+        assert torch.equal(outs[k], want), f"aggregation round {k}"
+    gen = wk.generator(32, gpu)
+    (o, pin, sub), _ = wk.scaled_normal_sources(gen, 3, (1, 3000, 4096), 0.5, 3.0, torch.bfloat16, gpu)
+    W, G = wk.queries_and_gains(gen, 1, 4096, gpu)
+    u = wk.sublayer_u(gen, 1, 4096, gpu)[0].contiguous()
+    lse = torch.empty(3000, device=gpu).normal_(0.0, 2.0, generator=gen)
+    res, wbuf = [], torch.empty_like(W[0])
+    for k in range(10):
+        wbuf.copy_(W[0] * (1.0 + 0.25 * k))
+        res.append(api.block_merge_update(o, lse, pin, sub, u, wbuf, G[0], 1e-8)[1].clone())
+    torch.cuda.synchronize()
+    for k in range(10):
+        want = api.block_merge_update(o, lse, pin, sub, u, (W[0] * (1.0 + 0.25 * k)).contiguous(), G[0], 1e-8)[1]
+        torch.cuda.synchronize()
+        assert torch.equal(res[k], want), f"fused step round {k}"
+
+
 def pick(t, rows, D):
     """Rows (numpy indices) of a [.., D] CUDA tensor viewed as [rows, D]."""
     return t.reshape(-1, D)[torch.as_tensor(rows, device=t.device)]

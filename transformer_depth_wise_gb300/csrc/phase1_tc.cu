@@ -796,6 +796,7 @@ p1_many_outputs_kernel(const __grid_constant__ ParamsB2 p) {
 // two CTAs of 8 warps can share an SM at D = 2048.
 // -----------------------------------------------------------------------------
 constexpr int kTcK = 16;           // summaries per step (mma K)
+static_assert(kTcK == 16, "alpha staging indexes queries with & 15 and summaries with >> 4");
 constexpr int kTcWarps = 16;       // 512 threads
 
 struct ParamsB3 {
@@ -853,18 +854,21 @@ p1_many_outputs_tc_kernel(const __grid_constant__ ParamsB3 p) {
   const int64_t total = my_tokens * KS;
 
   // work item j of this CTA: (token, piece of the features), pieces of a
-  // token on different CTAs
-  auto token = [&](int64_t j) { return ((int64_t)blockIdx.x + j * gridDim.x) / parts; };
-  auto first_feature = [&](int64_t j) { return (int)(((int64_t)blockIdx.x + j * gridDim.x) % parts) * DF; };
+  // token on different CTAs.  Taken once per item: the steps walk items with
+  // counters, no division per step.
+  auto item_at = [&](int64_t j, int64_t &t, int &fo) {
+    const int64_t it = (int64_t)blockIdx.x + j * gridDim.x;
+    t = it / parts;
+    fo = (int)(it - t * parts) * DF;
+  };
   // When the CTA width is a multiple of the chunks per row, a thread's chunk
   // column is fixed and its rows step by a constant (no division per copy).
   const bool whole_rows = blockDim.x % chunks == 0;
   const int rstep = whole_rows ? blockDim.x / chunks : 0, r0 = tid / chunks, ch0 = tid % chunks;
-  auto issue = [&](int64_t g) {                                  // step g: 16 summary rows -> slot g & 1
-    const int64_t t = token(g / KS);
-    const size_t fo = (size_t)first_feature(g / KS) * 2;
-    const int kk = (int)(g % KS);
-    unsigned char *slot = vring + (size_t)(g & 1) * kTcK * RV;
+  // step kk of the item (token t, first feature f0): 16 summary rows -> slot sl
+  auto issue = [&](int64_t t, int f0, int kk, int sl) {
+    const size_t fo = (size_t)f0 * 2;
+    unsigned char *slot = vring + (size_t)sl * kTcK * RV;
     if (whole_rows) {
       const size_t goff = (size_t)t * row_bytes + fo + (size_t)ch0 * 16;
       for (int r = r0; r < kTcK; r += rstep) {
@@ -881,12 +885,13 @@ p1_many_outputs_tc_kernel(const __grid_constant__ ParamsB3 p) {
     }
     cp_async_commit();
   };
-  auto stage_alpha = [&](int64_t j) {                            // alpha of token j -> bf16 hi / lo [q][i]
-    const int64_t t = token(j);
+  // alpha of item j (token t) -> bf16 hi / lo [q][i]; consecutive threads
+  // take consecutive queries of one summary (alpha is [n][S] per token)
+  auto stage_alpha = [&](int64_t j, int64_t t) {
     unsigned char *ab = abuf + (size_t)(j & 1) * 2 * kTcK * RA;
     const float *at = p.alpha + (size_t)t * n * S;
     for (int idx = tid; idx < kTcK * KP; idx += blockDim.x) {
-      const int q = idx / KP, i = idx % KP;
+      const int q = idx & (kTcK - 1), i = idx >> 4;
       const float a = (q < S && i < n) ? at[(size_t)i * S + q] : 0.f;
       const __nv_bfloat16 hi = __float2bfloat16_rn(a);
       const __nv_bfloat16 lo = __float2bfloat16_rn(a - __bfloat162float(hi));
@@ -896,17 +901,32 @@ p1_many_outputs_tc_kernel(const __grid_constant__ ParamsB3 p) {
   };
 
   float c[16][4];
+  // step g = j * KS + kk computes; step g + 1 = jn * KS + kn is issued
+  int64_t j = 0, t = 0, jn = 0, tn = 0;
+  int kk = 0, fo = 0, kn = 0, fon = 0;
   if (total > 0) {
-    stage_alpha(0);
-    issue(0);
+    item_at(0, t, fo);
+    tn = t;
+    fon = fo;
+    stage_alpha(0, t);
+    issue(t, fo, 0, 0);
   }
   for (int64_t g = 0; g < total; ++g) {
-    const int64_t j = g / KS;
-    const int kk = (int)(g % KS);
     cp_async_wait<0>();
     __syncthreads();             // step g's rows and token j's alpha are visible; slot (g + 1) & 1 is free
-    if (g + 1 < total) issue(g + 1);
-    if (kk == 0 && j + 1 < my_tokens) stage_alpha(j + 1);   // the other alpha buffer (last read by token j - 1)
+    if (g + 1 < total) {
+      if (++kn == KS) {
+        kn = 0;
+        item_at(++jn, tn, fon);
+      }
+      issue(tn, fon, kn, (int)((g + 1) & 1));
+    }
+    if (kk == 0 && j + 1 < my_tokens) {                      // the other alpha buffer (last read by token j - 1)
+      int64_t t1;
+      int f1;
+      item_at(j + 1, t1, f1);
+      stage_alpha(j + 1, t1);
+    }
     if (kk == 0) {
 #pragma unroll
       for (int nt = 0; nt < 16; ++nt) c[nt][0] = c[nt][1] = c[nt][2] = c[nt][3] = 0.f;
@@ -932,8 +952,7 @@ p1_many_outputs_tc_kernel(const __grid_constant__ ParamsB3 p) {
       mma_16816(c[2 * pr + 1], alo, b[2], b[3]);
     }
     if (kk == KS - 1) {          // token done: rows q = lane/4 and lane/4 + 8, two features per tile
-      const int64_t t = token(j);
-      const int q0 = lane >> 2, fc = (lane & 3) * 2, fo = first_feature(j);
+      const int q0 = lane >> 2, fc = (lane & 3) * 2;
 #pragma unroll
       for (int nt = 0; nt < 16; ++nt) {
         if (nt >= ntw) break;
@@ -945,6 +964,10 @@ p1_many_outputs_tc_kernel(const __grid_constant__ ParamsB3 p) {
           __stcs(reinterpret_cast<uint32_t *>(static_cast<char *>(p.out) + ((size_t)(q0 + 8) * p.rows + t) * row_bytes + (size_t)f * 2),
                  Elt<__nv_bfloat16>::pack_word(c[nt][2], c[nt][3]));
       }
+    }
+    if (++kk == KS) {
+      kk = 0;
+      if (++j < my_tokens) item_at(j, t, fo);
     }
   }
   cp_async_wait<0>();

@@ -39,8 +39,8 @@ def check(got, want, tol_abs, what=""):
     return err
 
 
-# Regression guard for the bf16 block chains, beside the benchmark spec's bound
-# (8e-3 * max|v| over the summaries, about 0.29 at their scale).  The GPU and
+# Regression guard for the bf16 block chains, beside the chain tolerance of
+# 8e-3 * max|v| over the summaries (about 0.29 at their scale).  The GPU and
 # the oracle round at the same points and differ only where fp32 and fp64
 # land on either side of a rounding boundary; such a flip in p_k carries on
 # through the later updates, so single elements can end a few ulps apart

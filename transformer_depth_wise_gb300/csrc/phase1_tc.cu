@@ -790,10 +790,11 @@ p1_many_outputs_kernel(const __grid_constant__ ParamsB2 p) {
 // summary rows are N-major (contiguous along d), which ldmatrix.trans turns
 // into the B fragments; alpha (fp32) is split into bf16 hi + lo, two MMAs per
 // tile, so it keeps about 16 significant bits.  The summary rows stream
-// through a two-slot cp.async ring, 16 rows per step (rows past n zero-filled);
-// each warp holds the accumulators of its 128 features across the steps.  A
-// work item is one of a token's `parts` pieces of WARPS x 128 features, so
-// two CTAs of 8 warps can share an SM at D = 2048.
+// through a cp.async ring of NS slots, 16 rows per step (rows past n
+// zero-filled), with NS - 1 steps in flight while one is multiplied; each
+// warp holds the accumulators of its 128 features across the steps.  A work
+// item is one of a token's `parts` pieces of WARPS x 128 features, so two
+// CTAs of 8 warps can share an SM at D = 2048.
 // -----------------------------------------------------------------------------
 constexpr int kTcK = 16;           // summaries per step (mma K)
 static_assert(kTcK == 16, "alpha staging indexes queries with & 15 and summaries with >> 4");
@@ -830,13 +831,17 @@ __device__ __forceinline__ void cp_async16_zfill(void *smem, const void *gmem, u
 
 __host__ __device__ constexpr size_t tc_row_v(int D) { return (size_t)D * 2 + 16; }   // padded: no bank conflicts
 __host__ __device__ constexpr size_t tc_row_a(int n) { return (size_t)((n + kTcK - 1) / kTcK * kTcK) * 2 + 16; }
-__host__ __device__ constexpr size_t tc_smem(int n, int D) {
-  return 2 * (size_t)kTcK * tc_row_v(D) + 2 * 2 * (size_t)kTcK * tc_row_a(n);
+// NS ring slots of 16 summary rows; alpha in two item buffers with two
+// slots, in one with three (staged between items behind a barrier).
+__host__ __device__ constexpr size_t tc_smem(int n, int D, int NS = 2) {
+  return (size_t)NS * kTcK * tc_row_v(D) + (NS == 2 ? 2 : 1) * 2 * (size_t)kTcK * tc_row_a(n);
 }
 
-template <int WARPS>
+template <int WARPS, int NS = 2>
 __global__ void __launch_bounds__(WARPS * 32, 16 / WARPS)
 p1_many_outputs_tc_kernel(const __grid_constant__ ParamsB3 p) {
+  static_assert(NS == 2 || NS == 3, "two or three ring slots");
+  constexpr int AB = NS == 2 ? 2 : 1;                            // alpha item buffers
   grid_dependency_wait();
   extern __shared__ __align__(16) unsigned char sm3[];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -844,8 +849,8 @@ p1_many_outputs_tc_kernel(const __grid_constant__ ParamsB3 p) {
   const int DF = D / parts;                                      // features per work item
   const int KS = (n + kTcK - 1) / kTcK, KP = KS * kTcK;
   const size_t RV = tc_row_v(DF), RA = tc_row_a(n);
-  unsigned char *vring = sm3;                                    // [2][16][RV]
-  unsigned char *abuf = sm3 + 2 * kTcK * RV;                     // [2 items][hi, lo][16][RA]
+  unsigned char *vring = sm3;                                    // [NS][16][RV]
+  unsigned char *abuf = sm3 + NS * kTcK * RV;                    // [AB items][hi, lo][16][RA]
   const size_t row_bytes = (size_t)D * 2;
   const int chunks = DF / 8;                                     // 16-byte chunks per item row
   const int ntw = DF / 8 / WARPS;                                // n-tiles per warp (even, <= 16)
@@ -888,7 +893,7 @@ p1_many_outputs_tc_kernel(const __grid_constant__ ParamsB3 p) {
   // alpha of item j (token t) -> bf16 hi / lo [q][i]; consecutive threads
   // take consecutive queries of one summary (alpha is [n][S] per token)
   auto stage_alpha = [&](int64_t j, int64_t t) {
-    unsigned char *ab = abuf + (size_t)(j & 1) * 2 * kTcK * RA;
+    unsigned char *ab = abuf + (size_t)(j % AB) * 2 * kTcK * RA;
     const float *at = p.alpha + (size_t)t * n * S;
     for (int idx = tid; idx < kTcK * KP; idx += blockDim.x) {
       const int q = idx & (kTcK - 1), i = idx >> 4;
@@ -908,20 +913,38 @@ p1_many_outputs_tc_kernel(const __grid_constant__ ParamsB3 p) {
     item_at(0, t, fo);
     tn = t;
     fon = fo;
-    stage_alpha(0, t);
+    if (NS == 2) stage_alpha(0, t);
     issue(t, fo, 0, 0);
+    for (int s = 1; s < NS - 1; ++s) {                       // steps 1 .. NS - 2, one commit group each
+      if (s < total) {
+        if (++kn == KS) {
+          kn = 0;
+          item_at(++jn, tn, fon);
+        }
+        issue(tn, fon, kn, s);
+      } else {
+        cp_async_commit();
+      }
+    }
   }
+  int slot_c = 0;                // slot of step g
   for (int64_t g = 0; g < total; ++g) {
-    cp_async_wait<0>();
-    __syncthreads();             // step g's rows and token j's alpha are visible; slot (g + 1) & 1 is free
-    if (g + 1 < total) {
+    cp_async_wait<NS - 2>();     // step g has landed (one commit group per step)
+    __syncthreads();             // step g's rows are visible; the slot of step g - 1 is free
+    if (NS == 3 && kk == 0) {    // a new item: its alpha into the single buffer (every warp is past the last item)
+      stage_alpha(j, t);
+      __syncthreads();
+    }
+    if (g + NS - 1 < total) {
       if (++kn == KS) {
         kn = 0;
         item_at(++jn, tn, fon);
       }
-      issue(tn, fon, kn, (int)((g + 1) & 1));
+      issue(tn, fon, kn, slot_c == 0 ? NS - 1 : slot_c - 1);
+    } else if (NS > 2) {
+      cp_async_commit();
     }
-    if (kk == 0 && j + 1 < my_tokens) {                      // the other alpha buffer (last read by token j - 1)
+    if (NS == 2 && kk == 0 && j + 1 < my_tokens) {           // the other alpha buffer (last read by token j - 1)
       int64_t t1;
       int f1;
       item_at(j + 1, t1, f1);
@@ -932,13 +955,13 @@ p1_many_outputs_tc_kernel(const __grid_constant__ ParamsB3 p) {
       for (int nt = 0; nt < 16; ++nt) c[nt][0] = c[nt][1] = c[nt][2] = c[nt][3] = 0.f;
     }
     // A fragments (hi, lo) of this step: rows q, columns kk*16 .. +15
-    const unsigned char *ab = abuf + (size_t)(j & 1) * 2 * kTcK * RA;
+    const unsigned char *ab = abuf + (size_t)(j % AB) * 2 * kTcK * RA;
     const int mrow = (lane & 7) + ((lane >> 3) & 1) * 8, mcol = kk * kTcK + (lane >> 4) * 8;
     uint32_t ahi[4], alo[4];
     ldsm_x4(smem_u32(ab + (size_t)mrow * RA + (size_t)mcol * 2), ahi);
     ldsm_x4(smem_u32(ab + (size_t)(kTcK + mrow) * RA + (size_t)mcol * 2), alo);
     // B fragments from the slot: rows k (summaries), 8 features per tile; two tiles per ldmatrix
-    const unsigned char *slot = vring + (size_t)(g & 1) * kTcK * RV;
+    const unsigned char *slot = vring + (size_t)slot_c * kTcK * RV;
     const int krow = (lane & 7) + ((lane >> 3) & 1) * 8, kcol = (lane >> 4) * 8;
 #pragma unroll
     for (int pr = 0; pr < 8; ++pr) {
@@ -969,6 +992,7 @@ p1_many_outputs_tc_kernel(const __grid_constant__ ParamsB3 p) {
       kk = 0;
       if (++j < my_tokens) item_at(j, t, fo);
     }
+    if (++slot_c == NS) slot_c = 0;
   }
   cp_async_wait<0>();
 }
@@ -1289,17 +1313,25 @@ cudaError_t launch_phase1_many(const Phase1ManyArgs &a) {
   // with 8 warps: per-thread row copies stream at a limited rate per CTA, so
   // two CTAs per SM keep more copies in flight (the Full two-phase schedule
   // at D = 2048: 8.8 -> 8.57 ms; pieces of 512 on 4-warp CTAs, three per SM,
-  // measured 8.80 ms).  Otherwise one CTA of 16 warps takes the whole row.
+  // measured 8.80 ms).  A ring of three slots, with alpha in one buffer,
+  // keeps two steps in flight through each step's MMAs and still fits two
+  // CTAs (8.58 -> 8.40 ms); two slots where it does not.  Otherwise one CTA
+  // of 16 warps takes the whole row.
   for (int warps : {8}) {
     const int DF = 8 * warps * 16;                // features per piece: 16 n-tiles per warp
     if (a.S > kTcK || a.D % DF != 0 || a.D / DF < 2) continue;
-    const size_t smem3 = tc_smem(a.n, DF);
-    int occ = 0;
-    auto kern = p1_many_outputs_tc_kernel<8>;
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem3);
-    if (e != cudaSuccess) return e;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, warps * 32, smem3);
-    if (e != cudaSuccess) return e;
+    int occ = 0, ns = 3;
+    size_t smem3 = 0;
+    auto kern = p1_many_outputs_tc_kernel<8, 3>;
+    for (; ns >= 2; --ns) {
+      kern = ns == 3 ? p1_many_outputs_tc_kernel<8, 3> : p1_many_outputs_tc_kernel<8, 2>;
+      smem3 = tc_smem(a.n, DF, ns);
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem3);
+      if (e != cudaSuccess) return e;
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, warps * 32, smem3);
+      if (e != cudaSuccess) return e;
+      if (occ >= 2) break;
+    }
     if (occ < 2) continue;
     ParamsB3 pc;
     for (int i = 0; i < a.n; ++i) pc.src[i] = a.blocks[i];

@@ -119,6 +119,19 @@ def test_aggregate_shapes(gpu, dtype, D, n, rows):
     check_stats(m, om, "m")
 
 
+# Few sources over short bf16 rows of 2048 (the pipelined kernel's group
+# chain at 1..13 sources, several rows per CTA, a ragged last round).
+@pytest.mark.parametrize("n,rows", [(1, 1000), (5, 457), (8, 1000), (9, 1000), (13, 2049)])
+def test_aggregate_short_rows(gpu, n, rows):
+    srcs, q, g = rand_sources(n, (1, rows, 2048), torch.bfloat16, gpu, seed=5 * n + rows)
+    out, m, lse = api.depth_aggregate(srcs, q, g, 1e-8, stats=True)
+    V = np.stack([f64(s) for s in srcs])
+    h, om, olse = oracle.depth_aggregate(V, f64(q), f64(g), 1e-8)
+    check(out, oracle.round_to(h, oracle.BF16), TOL[torch.bfloat16] * vmax(srcs), f"n={n} rows={rows}")
+    check_stats(lse, olse, "lse")
+    check_stats(m, om, "m")
+
+
 def test_aggregate_one_source_is_identity_bitwise(gpu):
     for dtype, D in ((torch.bfloat16, 2048), (torch.float32, 256), (torch.bfloat16, 40)):
         srcs, q, g = rand_sources(1, (2, 33, D), dtype, gpu, seed=5)
@@ -765,6 +778,23 @@ def test_full_stack_config_full_size_sampled(gpu):
                                         (2, 1024, 9, 600), (2, 512, 25, 520)])
 def test_full_two_phase_small(gpu, S, D, L, rows):
     wl = wk.WORKLOADS["full_stack_bf16"]
+    inp = wk.full_stack_inputs(wl, rows=rows, device=gpu, L=L, D=D)
+    y, srcs = api.full_stack_two_phase(inp["v0"], inp["queries"], inp["gains"], inp["u"], S, inp["eps"])
+    V, oy = oracle.full_stack_two_phase(f64(inp["v0"]).reshape(rows, D), f64(inp["queries"]), f64(inp["gains"]),
+                                        f64(inp["u"]), S, inp["eps"], oracle.BF16)
+    tol = TOL[torch.bfloat16] * float(inp["v0"].abs().max())
+    for l in range(1, L + 1):
+        check(srcs[l].reshape(rows, D), V[l], tol, f"S={S} v_{l}")
+    check(y.reshape(rows, D), oracle.round_to(oy, oracle.BF16), tol, f"S={S} y")
+
+
+# bf16 rows of 2048: the intra-block steps merge into the phase-1 state with
+# the two-pass kernel that holds each row in shared memory (up to seven rows
+# in flight with one intra source, one from seven), over several rows per CTA.
+@pytest.mark.parametrize("S,L,rows", [(7, 20, 1000), (14, 29, 600)])
+def test_full_two_phase_short_rows(gpu, S, L, rows):
+    wl = wk.WORKLOADS["full_stack_bf16"]
+    D = 2048
     inp = wk.full_stack_inputs(wl, rows=rows, device=gpu, L=L, D=D)
     y, srcs = api.full_stack_two_phase(inp["v0"], inp["queries"], inp["gains"], inp["u"], S, inp["eps"])
     V, oy = oracle.full_stack_two_phase(f64(inp["v0"]).reshape(rows, D), f64(inp["queries"]), f64(inp["gains"]),

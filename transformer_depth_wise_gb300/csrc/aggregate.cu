@@ -15,7 +15,14 @@
 // current one is folded in); aggregate_kernel takes short rows (lane teams of
 // a warp) and a prior state with no further source.
 //
-// Both, with u != nullptr, apply the synthetic sublayer v = 0.5 tanh(u (.) h)
+// aggregate_short_kernel takes bf16 rows of 2048 (256 vectors) merged into a
+// prior state, with few sources and few rows (the Full two-phase schedule's
+// intra-block steps):
+// the row's prior state and sources are held in shared memory and read
+// twice, once for the scores and once for the weighted sum, with one
+// reduction and one exact softmax per row instead of one per group.
+//
+// All, with u != nullptr, apply the synthetic sublayer v = 0.5 tanh(u (.) h)
 // to the fp32 h before the single rounding store: the Full stack uses it so
 // h_l never round-trips through memory.
 #include "common.cuh"
@@ -434,6 +441,201 @@ aggregate_pipe_kernel(const __grid_constant__ AggParams p) {
 }
 
 // ---------------------------------------------------------------------------
+// Few sources, few rows (bf16, rows of 256 16-byte vectors): a row of the
+// pipelined kernel costs one CTA-wide reduction, an exponential rescale and
+// a second unpacking of the group per group of sources, and with few rows a
+// CTA a chain of group steps each waiting on its copies.  Here a thread
+// copies its two vectors of the row's prior o and of each source into shared
+// memory (cp.async; each thread reads back only what it copied, so the
+// copies need no barrier), the scores of all sources are reduced at once,
+// the softmax is taken exactly (M = max of the prior's lse and the scores),
+// and the weighted sum reads the same vectors again.  The buffer holds 14
+// row units, so R = 14 / (1 + n) rows (at most seven) are in flight, and a
+// row's slot is refilled R rows later as soon as it has been read.  Same
+// arithmetic as the online form up to the order of the rescaling (eq. OS1 /
+// OS2 collapse to one step when every score is known).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void ring_copy16(void *smem, const void *gmem, uint32_t bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(smem)), "l"(gmem), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void ring_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void ring_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+// wait_group takes an immediate: the pending count 0..6 by cases
+__device__ __forceinline__ void ring_wait_upto(int pending) {
+  switch (pending) {
+    case 0: ring_wait<0>(); break;
+    case 1: ring_wait<1>(); break;
+    case 2: ring_wait<2>(); break;
+    case 3: ring_wait<3>(); break;
+    case 4: ring_wait<4>(); break;
+    case 5: ring_wait<5>(); break;
+    default: ring_wait<6>(); break;
+  }
+}
+
+constexpr int kShortUnits = 14;                 // prior + sources of a row held at once
+constexpr int kShortThreads = 128;              // two vectors a thread
+constexpr int kShortVectors = 2 * kShortThreads;
+constexpr size_t kShortSmem = (size_t)kShortUnits * kShortVectors * 16;
+
+template <bool FUSED_F, int K>
+__global__ void __launch_bounds__(kShortThreads, 3)
+aggregate_short_kernel(const __grid_constant__ AggParams p) {
+  grid_dependency_wait();
+  using T = __nv_bfloat16;
+  using E = Elt<T>;
+  using PR = Pairs<T>;
+  constexpr int NP = PR::NP, VPT = 2, TPR = kShortThreads, EPV = E::EPV;
+  // K: the most sources this instance takes (n <= K); two sums a source in one reduction
+  static_assert(K == 8 || K == 16, "K: 8 or 16 sources");
+  extern __shared__ uint4 units[];              // [kShortUnits][VPT][TPR]: 0 = prior o, 1 + i = source i
+  __shared__ float red[2 * 32 * (2 * K)];        // cta_sum_rs<2 K>: [parity][warp][value]
+  const int tid = threadIdx.x, n = p.n;
+  const bool prior = p.prior_o != nullptr;
+  const size_t row_bytes = (size_t)kShortVectors * 16;
+
+  uint64_t qp[VPT][NP];                         // this thread's w~ = w (.) gamma, as pairs
+#pragma unroll
+  for (int k = 0; k < VPT; ++k) {
+    const int j = tid + k * TPR;
+#pragma unroll
+    for (int c = 0; c < EPV / 4; ++c) {
+      const float4 w4 = ld_f4(p.q + j * EPV + c * 4);
+      const float4 g4 = p.g ? ld_f4(p.g + j * EPV + c * 4) : make_float4(1.f, 1.f, 1.f, 1.f);
+      qp[k][2 * c] = pair(w4.x * g4.x, w4.y * g4.y);
+      qp[k][2 * c + 1] = pair(w4.z * g4.z, w4.w * g4.w);
+    }
+  }
+  // A row takes U = 1 + n units (unit 0 the prior's); R rows fit the
+  // buffer and are in flight at once (R = 1 from seven sources).
+  const int U = 1 + n, R = kShortUnits / U < 7 ? kShortUnits / U : 7;
+  int ub = 0;                                   // first unit of the row being reduced
+  auto unit = [&](int u, int k) -> uint4 & { return units[((ub + u) * VPT + k) * TPR + tid]; };
+  auto issue = [&](int64_t row, int slot) {     // one commit group per row (empty past the end)
+    if (row < p.rows) {
+      const size_t off = (size_t)row * row_bytes + (size_t)tid * 16;
+      uint4 *base = units + (size_t)slot * U * VPT * TPR + tid;
+      if (prior) {
+#pragma unroll
+        for (int k = 0; k < VPT; ++k)
+          ring_copy16(base + k * TPR, static_cast<const char *>(p.prior_o) + off + (size_t)k * TPR * 16, 16u);
+      }
+      for (int i = 0; i < n; ++i) {
+        const char *src = static_cast<const char *>(p.src[i]) + off;
+#pragma unroll
+        for (int k = 0; k < VPT; ++k)
+          ring_copy16(base + ((1 + i) * VPT + k) * TPR, src + (size_t)k * TPR * 16, 16u);
+      }
+    }
+    ring_commit();
+  };
+
+  int parity = 0, slot = 0;
+  for (int r = 0; r < R; ++r) issue((int64_t)blockIdx.x + (int64_t)r * gridDim.x, r);
+  for (int64_t row = blockIdx.x; row < p.rows; row += gridDim.x) {
+    const float lse_p = prior ? p.prior_lse[row] : -INFINITY;
+    ring_wait_upto(R - 1);                      // this thread's vectors of the row have landed
+    ub = slot * U;
+    float part[2 * K];                          // w~.v_i and v_i.v_i
+#pragma unroll
+    for (int i = 0; i < K; ++i) {
+      uint64_t dot = 0ull, ss = 0ull;
+      if (i < n) {
+#pragma unroll
+        for (int k = 0; k < VPT; ++k) {
+          uint64_t x[NP];
+          PR::split(unit(1 + i, k), x);
+#pragma unroll
+          for (int j = 0; j < NP; ++j) {
+            fma_pair(dot, qp[k][j], x[j]);
+            fma_pair(ss, x[j], x[j]);
+          }
+        }
+      }
+      part[2 * i] = pair_sum(dot);
+      part[2 * i + 1] = pair_sum(ss);
+    }
+    cta_sum_rs<2 * K>(part, red, parity);
+    parity ^= 1;
+    float sc[K];
+    float M = lse_p;
+#pragma unroll
+    for (int i = 0; i < K; ++i) {
+      sc[i] = -INFINITY;
+      if (i < n) {
+        sc[i] = part[2 * i] * rsqrtf(fmaf(part[2 * i + 1], p.inv_D, p.eps));
+        M = fmaxf(M, sc[i]);
+      }
+    }
+    uint64_t acc[VPT][NP];
+    float den = 0.f;
+#pragma unroll
+    for (int k = 0; k < VPT; ++k)
+#pragma unroll
+      for (int j = 0; j < NP; ++j) acc[k][j] = 0ull;
+    if (prior) {                                // the prior state (lse, o, 1) as the first term
+      const float wpr = expf(lse_p - M);
+      den = wpr;
+      const uint64_t w2 = pair(wpr, wpr);
+#pragma unroll
+      for (int k = 0; k < VPT; ++k) {
+        uint64_t x[NP];
+        PR::split(unit(0, k), x);
+#pragma unroll
+        for (int j = 0; j < NP; ++j) fma_pair(acc[k][j], w2, x[j]);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < K; ++i) {
+      if (i < n) {
+        const float w = expf(sc[i] - M);
+        den += w;
+        const uint64_t w2 = pair(w, w);
+#pragma unroll
+        for (int k = 0; k < VPT; ++k) {
+          uint64_t x[NP];
+          PR::split(unit(1 + i, k), x);
+#pragma unroll
+          for (int j = 0; j < NP; ++j) fma_pair(acc[k][j], w2, x[j]);
+        }
+      }
+    }
+    // every vector of this row has been read into the sums above: the row R
+    // rounds later may overwrite them
+    issue(row + (int64_t)R * gridDim.x, slot);
+    if (++slot == R) slot = 0;
+    const float inv = 1.f / den;
+    const size_t row_off = (size_t)row * row_bytes;
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+      const int j = tid + k * TPR;
+      float h[EPV];
+#pragma unroll
+      for (int jj = 0; jj < NP; ++jj) unpair(acc[k][jj], h[2 * jj], h[2 * jj + 1]);
+#pragma unroll
+      for (int e4 = 0; e4 < EPV; e4 += 4) {
+        float4 u4 = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (FUSED_F) u4 = ld_f4(p.u + j * EPV + e4);
+        const float uu[4] = {u4.x, u4.y, u4.z, u4.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          h[e4 + e] *= inv;
+          if (FUSED_F) h[e4 + e] = half_tanh(uu[e] * h[e4 + e]);
+        }
+      }
+      st_vec(static_cast<char *>(p.out) + row_off + (size_t)j * 16, E::pack(h));
+    }
+    if (tid == 0) {
+      if (p.out_lse) p.out_lse[row] = M + logf(den);
+      if (p.out_max) p.out_max[row] = M;
+    }
+  }
+  ring_wait<0>();
+}
+
+// ---------------------------------------------------------------------------
 // Launch configuration
 // ---------------------------------------------------------------------------
 namespace {
@@ -552,6 +754,36 @@ cudaError_t run_pipe(const AggParams &p, int threads, cudaStream_t st) {
   return cudaGetLastError();
 }
 
+// The short-row kernel: bf16 rows of 2048 merged into a prior state (the
+// Full two-phase schedule's intra-block steps), 1..13 sources (unit 0 of the
+// shared-memory row is the prior's, sources take units 1..n), and fewer rows
+// than the many-rows shape of the pipelined kernel takes.  Measured on a
+// GB300 over the schedule at S = 14: 8.45 -> 8.36 ms.  Without a prior the
+// pipelined kernel stays faster (e.g. 8.2 against 9.8 us for one source over
+// 2048 rows, 27.7 against 31.3 us for 13; both pay about 5 us a launch of
+// ramp and tail), so plain calls keep it.
+bool short_fits(const AggregateArgs &a) {
+  return a.dtype == ATTNRES_BF16 && a.prior_o != nullptr && a.D == 8 * kShortVectors && a.n >= 1 &&
+         1 + a.n <= kShortUnits && a.rows < 32 * (int64_t)sm_count();
+}
+
+template <bool F, int K>
+cudaError_t run_short(const AggParams &p, cudaStream_t st) {
+  auto kern = aggregate_short_kernel<F, K>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kShortSmem);
+  if (e != cudaSuccess) return e;
+  int occ = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kShortThreads, kShortSmem);
+  if (e != cudaSuccess) return e;
+  if (occ < 1) occ = 1;
+  const int64_t cap = (int64_t)occ * sm_count();
+  const int grid = (int)(p.rows < cap ? p.rows : cap);
+  if (cudaError_t le = launch_dependent(kern, dim3((unsigned)grid), dim3(kShortThreads), kShortSmem, st, p);
+      le != cudaSuccess)
+    return le;
+  return cudaGetLastError();
+}
+
 template <typename T, bool F>
 cudaError_t dispatch_pipe(const AggParams &p, const PipeCfg &c, cudaStream_t st) {
   if (c.g == 4) {
@@ -598,6 +830,10 @@ cudaError_t launch_aggregate(const AggregateArgs &a) {
   p.prior_o = a.prior_o;
   p.prior_lse = a.prior_lse;
   const bool fused = a.u != nullptr;
+  if (short_fits(a)) {
+    if (a.n <= 8) return fused ? run_short<true, 8>(p, a.stream) : run_short<false, 8>(p, a.stream);
+    return fused ? run_short<true, 16>(p, a.stream) : run_short<false, 16>(p, a.stream);
+  }
   PipeCfg pc;
   if (choose_pipe(a.n, a.rows, a.D, a.dtype, pc)) {
     if (a.dtype == ATTNRES_BF16)

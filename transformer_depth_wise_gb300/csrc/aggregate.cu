@@ -538,20 +538,23 @@ aggregate_short_kernel(const __grid_constant__ AggParams p) {
     const float lse_p = prior ? p.prior_lse[row] : -INFINITY;
     ring_wait_upto(R - 1);                      // this thread's vectors of the row have landed
     ub = slot * U;
+    // The source loops are unrolled to K and left at n (uniform): no
+    // predicated-off work for the sources past n.
     float part[2 * K];                          // w~.v_i and v_i.v_i
 #pragma unroll
+    for (int i = 0; i < 2 * K; ++i) part[i] = 0.f;
+#pragma unroll
     for (int i = 0; i < K; ++i) {
+      if (i >= n) break;
       uint64_t dot = 0ull, ss = 0ull;
-      if (i < n) {
 #pragma unroll
-        for (int k = 0; k < VPT; ++k) {
-          uint64_t x[NP];
-          PR::split(unit(1 + i, k), x);
+      for (int k = 0; k < VPT; ++k) {
+        uint64_t x[NP];
+        PR::split(unit(1 + i, k), x);
 #pragma unroll
-          for (int j = 0; j < NP; ++j) {
-            fma_pair(dot, qp[k][j], x[j]);
-            fma_pair(ss, x[j], x[j]);
-          }
+        for (int j = 0; j < NP; ++j) {
+          fma_pair(dot, qp[k][j], x[j]);
+          fma_pair(ss, x[j], x[j]);
         }
       }
       part[2 * i] = pair_sum(dot);
@@ -562,12 +565,12 @@ aggregate_short_kernel(const __grid_constant__ AggParams p) {
     float sc[K];
     float M = lse_p;
 #pragma unroll
+    for (int i = 0; i < K; ++i) sc[i] = -INFINITY;
+#pragma unroll
     for (int i = 0; i < K; ++i) {
-      sc[i] = -INFINITY;
-      if (i < n) {
-        sc[i] = part[2 * i] * rsqrtf(fmaf(part[2 * i + 1], p.inv_D, p.eps));
-        M = fmaxf(M, sc[i]);
-      }
+      if (i >= n) break;
+      sc[i] = part[2 * i] * rsqrtf(fmaf(part[2 * i + 1], p.inv_D, p.eps));
+      M = fmaxf(M, sc[i]);
     }
     uint64_t acc[VPT][NP];
     float den = 0.f;
@@ -589,7 +592,8 @@ aggregate_short_kernel(const __grid_constant__ AggParams p) {
     }
 #pragma unroll
     for (int i = 0; i < K; ++i) {
-      if (i < n) {
+      if (i >= n) break;
+      {
         const float w = expf(sc[i] - M);
         den += w;
         const uint64_t w2 = pair(w, w);
@@ -758,10 +762,11 @@ cudaError_t run_pipe(const AggParams &p, int threads, cudaStream_t st) {
 // Full two-phase schedule's intra-block steps), 1..13 sources (unit 0 of the
 // shared-memory row is the prior's, sources take units 1..n), and fewer rows
 // than the many-rows shape of the pipelined kernel takes.  Measured on a
-// GB300 over the schedule at S = 14: 8.45 -> 8.36 ms.  Without a prior the
-// pipelined kernel stays faster (e.g. 8.2 against 9.8 us for one source over
-// 2048 rows, 27.7 against 31.3 us for 13; both pay about 5 us a launch of
-// ramp and tail), so plain calls keep it.
+// GB300 over the schedule at S = 14: 8.45 -> 7.98-8.07 ms.  Without a prior
+// neither kernel wins throughout (2048 rows: 8.3 us for one source either
+// way, 13.7 against 15.1 us for five, 20.2 against 17.4 us for eight, 28.7
+// against 27.8 us for 13; both pay about 5 us a launch of ramp and tail),
+// so plain calls keep the pipelined kernel.
 bool short_fits(const AggregateArgs &a) {
   return a.dtype == ATTNRES_BF16 && a.prior_o != nullptr && a.D == 8 * kShortVectors && a.n >= 1 &&
          1 + a.n <= kShortUnits && a.rows < 32 * (int64_t)sm_count();

@@ -147,7 +147,10 @@ aggregate_backward_kernel(const __grid_constant__ BwdParams p) {
         }
       float part[KR];
 #pragma unroll
+      for (int j = 0; j < KR; ++j) part[j] = 0.f;
+#pragma unroll
       for (int j = 0; j < GA; ++j) {
+        if (i0 + j >= p.n) break;   // the last group's sources past n (the same for every thread)
         uint64_t ss = 0ull, dq = 0ull, dg = 0ull;
 #pragma unroll
         for (int k = 0; k < VPT; ++k) {

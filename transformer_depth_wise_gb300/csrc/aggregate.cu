@@ -758,8 +758,9 @@ cudaError_t run_pipe(const AggParams &p, int threads, cudaStream_t st) {
   return cudaGetLastError();
 }
 
-// The short-row kernel: bf16 rows of 2048 merged into a prior state (the
-// Full two-phase schedule's intra-block steps), 1..13 sources (unit 0 of the
+// The short-row kernel: bf16 rows of 2048 merged into a prior state with the
+// sublayer fused (the Full two-phase schedule's intra-block steps, the only
+// caller that passes a prior), 1..13 sources (unit 0 of the
 // shared-memory row is the prior's, sources take units 1..n), and fewer rows
 // than the many-rows shape of the pipelined kernel takes.  Measured on a
 // GB300 over the schedule at S = 14: 8.45 -> 7.98-8.07 ms.  Without a prior
@@ -768,8 +769,8 @@ cudaError_t run_pipe(const AggParams &p, int threads, cudaStream_t st) {
 // against 27.8 us for 13; both pay about 5 us a launch of ramp and tail),
 // so plain calls keep the pipelined kernel.
 bool short_fits(const AggregateArgs &a) {
-  return a.dtype == ATTNRES_BF16 && a.prior_o != nullptr && a.D == 8 * kShortVectors && a.n >= 1 &&
-         1 + a.n <= kShortUnits && a.rows < 32 * (int64_t)sm_count();
+  return a.dtype == ATTNRES_BF16 && a.prior_o != nullptr && a.u != nullptr && a.D == 8 * kShortVectors &&
+         a.n >= 1 && 1 + a.n <= kShortUnits && a.rows < 32 * (int64_t)sm_count();
 }
 
 template <bool F, int K>
@@ -835,10 +836,7 @@ cudaError_t launch_aggregate(const AggregateArgs &a) {
   p.prior_o = a.prior_o;
   p.prior_lse = a.prior_lse;
   const bool fused = a.u != nullptr;
-  if (short_fits(a)) {
-    if (a.n <= 8) return fused ? run_short<true, 8>(p, a.stream) : run_short<false, 8>(p, a.stream);
-    return fused ? run_short<true, 16>(p, a.stream) : run_short<false, 16>(p, a.stream);
-  }
+  if (short_fits(a)) return a.n <= 8 ? run_short<true, 8>(p, a.stream) : run_short<true, 16>(p, a.stream);
   PipeCfg pc;
   if (choose_pipe(a.n, a.rows, a.D, a.dtype, pc)) {
     if (a.dtype == ATTNRES_BF16)

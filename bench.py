@@ -663,13 +663,13 @@ def run_configs(dev):
     res[wl.name] = r
     del inp, out
 
-    # Full 186-sublayer stack, plain and with the two-phase schedule (S = 14).
+    # Full 186-sublayer stack, plain and with the two-phase schedule (S = 16, the fastest block size on a GB300).
     wl = wk.WORKLOADS["full_stack_bf16"]
     inp = wk.full_stack_inputs(wl, device=dev)
     srcs = [inp["v0"]] + [torch.empty_like(inp["v0"]) for _ in range(wl.L)]
     y = torch.empty_like(inp["v0"])
     plain = lambda: api.full_stack_forward(inp["v0"], inp["queries"], inp["gains"], inp["u"], inp["eps"], srcs, y)  # noqa
-    S = 14
+    S = 16
     ws = torch.empty(int(api._lib.lib().attnres_full_stack_two_phase_workspace_bytes(wl.L, S, 1, wl.rows, wl.D, 1)),
                      dtype=torch.uint8, device=dev)
     two = lambda: api.full_stack_two_phase(inp["v0"], inp["queries"], inp["gains"], inp["u"], S, inp["eps"],  # noqa
@@ -748,7 +748,7 @@ def main():
     ap.add_argument("--kernel", default="", choices=["", "merge_update", "aggregate"],
                     help="time one kernel alone at --rows token rows (profiling; no headline line): the fused "
                          "update+merge at the workload's width, or the workload's single aggregation")
-    ap.add_argument("--schedule-block-size", type=int, default=14,
+    ap.add_argument("--schedule-block-size", type=int, default=16,
                     help="Full stack: block size S of the two-phase schedule timed beside the plain stack")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)

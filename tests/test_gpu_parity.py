@@ -159,6 +159,33 @@ def test_aggregate_empty_rows_is_a_noop(gpu):
     assert out.shape == (0, 5, 256)
 
 
+def test_empty_rows_every_entry_point(gpu):
+    """B*T = 0: every entry point returns at once (empty tensors may carry NULL data), and the backward's
+    parameter gradients come back as zeros."""
+    D, shape, bf = 256, (0, 5, 256), torch.bfloat16
+    srcs = [torch.empty(shape, dtype=bf, device=gpu) for _ in range(3)]
+    q = torch.randn(D, device=gpu)
+    g = torch.ones(D, device=gpu)
+    qs = torch.randn((4, D), device=gpu)
+    o, _, lse = api.block_phase1(srcs, qs, None, 1e-8)
+    assert o.shape == (4, 0, 5, D) and lse.shape == (4, 0, 5)
+    x = torch.empty(shape, dtype=bf, device=gpu)
+    lse1 = torch.empty((0, 5), dtype=torch.float32, device=gpu)
+    assert api.block_phase2_merge(x, lse1, x, q, g, 1e-8).shape == shape
+    p_out, h_out, _ = api.block_merge_update(x, lse1, x, x, q, q, g, 1e-8)
+    assert p_out.shape == shape and h_out.shape == shape
+    assert api.rms_norm(x, g).shape == shape
+    assert api.partial_update(x, x, q).shape == shape
+    qL, uL = torch.randn((7, D), device=gpu), torch.randn((6, D), device=gpu)
+    y, vs = api.full_stack_forward(x, qL, None, uL, 1e-8)
+    assert y.shape == shape and len(vs) == 7
+    y, vs = api.full_stack_two_phase(x, qL, None, uL, 3, 1e-8)
+    assert y.shape == shape and len(vs) == 7
+    gs, gq, gg = api.depth_aggregate_backward(srcs, q, g, 1e-8, x)
+    assert len(gs) == 3 and gs[0].shape == shape
+    assert torch.count_nonzero(gq) == 0 and torch.count_nonzero(gg) == 0
+
+
 def test_aggregate_many_sources(gpu):
     srcs, q, g = rand_sources(187, (1, 9, 256), torch.bfloat16, gpu, seed=187)
     out = api.depth_aggregate(srcs, q, g, 1e-8)
@@ -790,8 +817,9 @@ def test_full_two_phase_small(gpu, S, D, L, rows):
 
 # bf16 rows of 2048: the intra-block steps merge into the phase-1 state with
 # the two-pass kernel that holds each row in shared memory (up to seven rows
-# in flight with one intra source, one from seven), over several rows per CTA.
-@pytest.mark.parametrize("S,L,rows", [(7, 20, 1000), (14, 29, 600)])
+# in flight with one intra source, one from eight; 15 intra sources at S = 16),
+# over several rows per CTA.
+@pytest.mark.parametrize("S,L,rows", [(7, 20, 1000), (14, 29, 600), (16, 33, 500)])
 def test_full_two_phase_short_rows(gpu, S, L, rows):
     wl = wk.WORKLOADS["full_stack_bf16"]
     D = 2048
@@ -819,18 +847,18 @@ def test_full_two_phase_shape_limits(gpu):
         api.full_stack_two_phase(inp["v0"].float(), inp["queries"], inp["gains"], inp["u"], 3, inp["eps"])
 
 
-def test_full_two_phase_config_full_size_sampled(gpu):
+@pytest.mark.parametrize("S", [14, 16])
+def test_full_two_phase_config_full_size_sampled(gpu, S):
     wl = wk.WORKLOADS["full_stack_bf16"]                 # [1, 2048, 2048], L = 186
     inp = wk.full_stack_inputs(wl, device=gpu)
-    S = 14
     y, srcs = api.full_stack_two_phase(inp["v0"], inp["queries"], inp["gains"], inp["u"], S, inp["eps"])
     rows = sample_rows(wl.B, wl.T, 6, 8)
     V, oy = oracle.full_stack_two_phase(f64(pick(inp["v0"], rows, wl.D)), f64(inp["queries"]), f64(inp["gains"]),
                                         f64(inp["u"]), S, inp["eps"], oracle.BF16)
     tol = TOL[torch.bfloat16] * float(inp["v0"].abs().max())
-    for l in (1, 14, 15, 29, 100, 186):
-        check(pick(srcs[l], rows, wl.D), V[l], tol, f"v_{l}")
-    check(pick(y, rows, wl.D), oy, tol, "y")
+    for l in (1, S, S + 1, 2 * S + 1, 100, 186):
+        check(pick(srcs[l], rows, wl.D), V[l], tol, f"S={S} v_{l}")
+    check(pick(y, rows, wl.D), oy, tol, f"S={S} y")
 
 
 def test_no_kernel_wait_ran_out(gpu):

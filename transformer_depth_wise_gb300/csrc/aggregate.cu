@@ -449,8 +449,8 @@ aggregate_pipe_kernel(const __grid_constant__ AggParams p) {
 // memory (cp.async; each thread reads back only what it copied, so the
 // copies need no barrier), the scores of all sources are reduced at once,
 // the softmax is taken exactly (M = max of the prior's lse and the scores),
-// and the weighted sum reads the same vectors again.  The buffer holds 14
-// row units, so R = 14 / (1 + n) rows (at most seven) are in flight, and a
+// and the weighted sum reads the same vectors again.  The buffer holds 16
+// row units, so R = 16 / (1 + n) rows (at most seven) are in flight, and a
 // row's slot is refilled R rows later as soon as it has been read.  Same
 // arithmetic as the online form up to the order of the rescaling (eq. OS1 /
 // OS2 collapse to one step when every score is known).
@@ -475,7 +475,7 @@ __device__ __forceinline__ void ring_wait_upto(int pending) {
   }
 }
 
-constexpr int kShortUnits = 14;                 // prior + sources of a row held at once
+constexpr int kShortUnits = 16;                 // prior + sources of a row held at once (64 KB: three CTAs an SM)
 constexpr int kShortThreads = 128;              // two vectors a thread
 constexpr int kShortVectors = 2 * kShortThreads;
 constexpr size_t kShortSmem = (size_t)kShortUnits * kShortVectors * 16;
@@ -509,7 +509,7 @@ aggregate_short_kernel(const __grid_constant__ AggParams p) {
     }
   }
   // A row takes U = 1 + n units (unit 0 the prior's); R rows fit the
-  // buffer and are in flight at once (R = 1 from seven sources).
+  // buffer and are in flight at once (R = 1 from eight sources).
   const int U = 1 + n, R = kShortUnits / U < 7 ? kShortUnits / U : 7;
   int ub = 0;                                   // first unit of the row being reduced
   auto unit = [&](int u, int k) -> uint4 & { return units[((ub + u) * VPT + k) * TPR + tid]; };
@@ -760,7 +760,7 @@ cudaError_t run_pipe(const AggParams &p, int threads, cudaStream_t st) {
 
 // The short-row kernel: bf16 rows of 2048 merged into a prior state with the
 // sublayer fused (the Full two-phase schedule's intra-block steps, the only
-// caller that passes a prior), 1..13 sources (unit 0 of the
+// caller that passes a prior), 1..15 sources (unit 0 of the
 // shared-memory row is the prior's, sources take units 1..n), and fewer rows
 // than the many-rows shape of the pipelined kernel takes.  Measured on a
 // GB300 over the schedule at S = 14: 8.45 -> 7.98-8.07 ms.  Without a prior

@@ -478,10 +478,23 @@ __device__ __forceinline__ void ring_wait_upto(int pending) {
 constexpr int kShortUnits = 16;                 // prior + sources of a row held at once (64 KB: three CTAs an SM)
 constexpr int kShortThreads = 128;              // two vectors a thread
 constexpr int kShortVectors = 2 * kShortThreads;
-constexpr size_t kShortSmem = (size_t)kShortUnits * kShortVectors * 16;
+// Rows in flight for n sources: as many rows of 1 + n units as the buffer
+// holds, at most seven, and the launch sizes the buffer to R (1 + n) units.
+// Up to eight sources the buffer is held to 11 units (44 KB), so that five
+// CTAs share an SM (their register limit) instead of three with 16 units:
+// the Full two-phase schedule at S = 16 went 7.55 -> 7.48 ms on a GB300.
+__host__ __device__ constexpr int short_units(int n) { return n <= 8 ? 11 : kShortUnits; }
+__host__ __device__ constexpr int short_rows_in_flight(int n) {
+  return short_units(n) / (1 + n) < 7 ? short_units(n) / (1 + n) : 7;
+}
+__host__ __device__ constexpr size_t short_smem(int n) {
+  return (size_t)short_rows_in_flight(n) * (1 + n) * kShortVectors * 16;
+}
 
+// Five CTAs an SM by registers (96 and 89 a thread, no spills), as shared
+// memory allows: up to 10 row units.
 template <bool FUSED_F, int K>
-__global__ void __launch_bounds__(kShortThreads, 3)
+__global__ void __launch_bounds__(kShortThreads, 5)
 aggregate_short_kernel(const __grid_constant__ AggParams p) {
   grid_dependency_wait();
   using T = __nv_bfloat16;
@@ -491,7 +504,8 @@ aggregate_short_kernel(const __grid_constant__ AggParams p) {
   // K: the most sources this instance takes (n <= K); two sums a source in one reduction
   static_assert(K == 8 || K == 16, "K: 8 or 16 sources");
   extern __shared__ uint4 units[];              // [kShortUnits][VPT][TPR]: 0 = prior o, 1 + i = source i
-  __shared__ float red[2 * 32 * (2 * K)];        // cta_sum_rs<2 K>: [parity][warp][value]
+  constexpr int kWarps = kShortThreads / 32;
+  __shared__ float red[2 * kWarps * (2 * K)];    // cta_sum_rs<2 K, 4 warps>: [parity][warp][value]
   const int tid = threadIdx.x, n = p.n;
   const bool prior = p.prior_o != nullptr;
   const size_t row_bytes = (size_t)kShortVectors * 16;
@@ -510,7 +524,7 @@ aggregate_short_kernel(const __grid_constant__ AggParams p) {
   }
   // A row takes U = 1 + n units (unit 0 the prior's); R rows fit the
   // buffer and are in flight at once (R = 1 from eight sources).
-  const int U = 1 + n, R = kShortUnits / U < 7 ? kShortUnits / U : 7;
+  const int U = 1 + n, R = short_rows_in_flight(n);
   int ub = 0;                                   // first unit of the row being reduced
   auto unit = [&](int u, int k) -> uint4 & { return units[((ub + u) * VPT + k) * TPR + tid]; };
   auto issue = [&](int64_t row, int slot) {     // one commit group per row (empty past the end)
@@ -560,7 +574,7 @@ aggregate_short_kernel(const __grid_constant__ AggParams p) {
       part[2 * i] = pair_sum(dot);
       part[2 * i + 1] = pair_sum(ss);
     }
-    cta_sum_rs<2 * K>(part, red, parity);
+    cta_sum_rs<2 * K, kWarps>(part, red, parity);
     parity ^= 1;
     float sc[K];
     float M = lse_p;
@@ -776,15 +790,16 @@ bool short_fits(const AggregateArgs &a) {
 template <bool F, int K>
 cudaError_t run_short(const AggParams &p, cudaStream_t st) {
   auto kern = aggregate_short_kernel<F, K>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kShortSmem);
+  const size_t smem = short_smem(p.n);
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)short_smem(15));
   if (e != cudaSuccess) return e;
   int occ = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kShortThreads, kShortSmem);
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kShortThreads, smem);
   if (e != cudaSuccess) return e;
   if (occ < 1) occ = 1;
   const int64_t cap = (int64_t)occ * sm_count();
   const int grid = (int)(p.rows < cap ? p.rows : cap);
-  if (cudaError_t le = launch_dependent(kern, dim3((unsigned)grid), dim3(kShortThreads), kShortSmem, st, p);
+  if (cudaError_t le = launch_dependent(kern, dim3((unsigned)grid), dim3(kShortThreads), smem, st, p);
       le != cudaSuccess)
     return le;
   return cudaGetLastError();

@@ -292,8 +292,9 @@ template <> struct Pairs<__nv_bfloat16> {
 // 5 K), lanes < K publish to red[parity][warp][K], one barrier, each lane
 // adds the warps' totals of its value, and K shuffles hand every total to
 // every lane.  Alternating `parity` between calls saves a second barrier.
-template <int K>
-__device__ __forceinline__ void cta_sum_rs(float (&v)[K], float *red /*[2][32][K]*/, int parity) {
+// MAXW: the most warps a CTA of the caller has ([2][MAXW][K] scratch).
+template <int K, int MAXW = 32>
+__device__ __forceinline__ void cta_sum_rs(float (&v)[K], float *red /*[2][MAXW][K]*/, int parity) {
   static_assert(K >= 1 && K <= 32 && (K & (K - 1)) == 0, "K: power of two <= 32");
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
   float b[K];
@@ -314,7 +315,7 @@ __device__ __forceinline__ void cta_sum_rs(float (&v)[K], float *red /*[2][32][K
       b[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
     }
   }
-  float *slot = red + parity * 32 * K;
+  float *slot = red + parity * MAXW * K;
   if (lane < K) slot[warp * K + lane] = b[0];
   __syncthreads();
   float t = 0.f;

@@ -90,6 +90,8 @@ int attnres_depth_aggregate(const void *const *sources, int n, int64_t B, int64_
  * inter step; "attn_with_stats"): the S pseudo-queries of one block score
  * the same n completed block summaries in one pass.
  *   blocks   host array of n_blocks device pointers, each [B,T,D]
+ *   n_blocks 1 .. 16 (ATTNRES_ERR_TOO_MANY_SOURCES above; the Full
+ *            two-phase schedule runs phase 1 over more sources internally)
  *   queries  device fp32 [S,D]; gains device fp32 [S,D] or NULL
  *   S        1 .. ATTNRES_MAX_QUERIES
  *   out      device [S,B,T,D] of `dtype`: out[s] = normalised output o_s

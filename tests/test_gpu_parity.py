@@ -410,6 +410,8 @@ def test_aggregate_backward_full_size_sampled(gpu):
     # the widest rows: nine summaries at D = 8192 fill kernel B's shared memory (two pieces of 4096); ten
     # do not fit it, and those rows take the per-row kernel
     (torch.bfloat16, 8192, 9, 24, 520), (torch.bfloat16, 8192, 10, 24, 512),
+    # the most summaries a call takes, sixteen (more than ten take the per-row kernel), at S = 16
+    (torch.bfloat16, 2048, 16, 16, 160),
 ])
 def test_phase1_small(gpu, dtype, D, n, S, rows):
     g = wk.generator(D + n + S, gpu)
@@ -802,7 +804,10 @@ def test_full_stack_config_full_size_sampled(gpu):
                                         # S = 2 over 512+ rows: blocks of up to ten sources take the
                                         # tensor-core phase 1 with the softmax in the scores kernel,
                                         # wider ones the raw-score path
-                                        (2, 1024, 9, 600), (2, 512, 25, 520)])
+                                        (2, 1024, 9, 600), (2, 512, 25, 520),
+                                        # the last block over 241 sources at D = 2048: three copy slots no
+                                        # longer fit two CTAs per SM there, and the outputs take two
+                                        (16, 2048, 250, 48)])
 def test_full_two_phase_small(gpu, S, D, L, rows):
     wl = wk.WORKLOADS["full_stack_bf16"]
     inp = wk.full_stack_inputs(wl, rows=rows, device=gpu, L=L, D=D)

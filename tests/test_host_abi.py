@@ -82,6 +82,8 @@ def test_phase1_argument_checks():
     assert p1(S=0) == SHAPE
     assert p1(S=65) == SHAPE
     assert p1(n=0) == SHAPE
+    arr17 = _lib.ptr_array([FAKE] * 17)
+    assert L.attnres_block_phase1(arr17, 17, 1, 4, 4096, 1, FAKE, None, 24, 1e-8, FAKE, None, FAKE, None) == MANY
     assert p1(D=4100) == ALIGN
     assert p1(B=0) == OK
 

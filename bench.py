@@ -186,13 +186,20 @@ def oracle_block_rows_per_s(wl, rows_target_s: float = 12.0, max_rows: int = 409
 # ---------------------------------------------------------------------------
 # GPU arm
 # ---------------------------------------------------------------------------
+EVENT_EVERY = 5  # per-kernel events on one block pass in five
+
+
 def time_block(blk, K, dev, world, stream, fused, label="timed"):
-    """Run K block passes with per-kernel events; returns (elapsed max over ranks, events, clocks).
-    The passes sit in an NVTX range named `label`, which a profiler can select."""
+    """Run K block passes, every EVENT_EVERY-th with per-kernel events; returns (elapsed max over ranks,
+    events of the instrumented passes, clocks).  An event recorded between two dependent launches keeps the
+    second from starting early, so instrumenting every pass would add about 2 % to the step; the per-kernel
+    averages come from the instrumented passes inside the same timed region.  The passes sit in an NVTX
+    range named `label`, which a profiler can select."""
     S = blk.S
     ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
     events = [{"phase1": (ev(), ev()), "merge": [(ev(), ev()) for _ in range(S - 1)],
-               "update": [(ev(), ev()) for _ in range(1 if fused else S)]} for _ in range(K)]
+               "update": [(ev(), ev()) for _ in range(1 if fused else S)]}
+              for k in range(K) if k % EVENT_EVERY == 0]
     t_start, t_end = ev(), ev()
     clocks = ClockSampler(dev.index if dev.index is not None else 0)
     barrier(world)
@@ -202,13 +209,29 @@ def time_block(blk, K, dev, world, stream, fused, label="timed"):
     torch.cuda.nvtx.range_push(label)
     t_start.record(stream)
     for k in range(K):
-        blk.run(events=events[k])
+        blk.run(events=events[k // EVENT_EVERY] if k % EVENT_EVERY == 0 else None)
     t_end.record(stream)
     torch.cuda.nvtx.range_pop()
     torch.cuda.synchronize(dev)
     clk = clocks.stop()
     barrier(world)
     return max_over_ranks(t_start.elapsed_time(t_end), world, dev), events, clk
+
+
+def time_passes(run, K, dev, world, stream, label):
+    """K back-to-back block passes without per-kernel events (elapsed ms, max over ranks)."""
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    torch.cuda.nvtx.range_push(label)
+    t_start.record(stream)
+    for _ in range(K):
+        run()
+    t_end.record(stream)
+    torch.cuda.nvtx.range_pop()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    return max_over_ranks(t_start.elapsed_time(t_end), world, dev)
 
 
 def run_two_phase(args, wl, dev, rank, world):
@@ -290,6 +313,24 @@ def run_two_phase(args, wl, dev, rank, world):
                "step": "as the headline, each sublayer reading rms_norm(h) (.) w_n formed in the same pass"}
     del blk_n, nw
 
+    # The same block pass with the batch's sequences in two groups on two
+    # streams (TwoPhaseBlock(groups=2)): one group's phase-1 scores overlap
+    # the other's outputs kernel; the values are bitwise those of one pass.
+    groups = None
+    if wl.B % 2 == 0:
+        blk_g = api.TwoPhaseBlock(inp["blocks"], inp["queries"], inp["gains"], inp["u"], inp["eps"], fused=True,
+                                  groups=2)
+        for _ in range(args.warmup):
+            blk_g.run()
+        torch.cuda.synchronize(dev)
+        el_g = time_passes(blk_g.run, K, dev, world, stream, "timed_groups")
+        groups = {"groups": 2, "value": round(rows * K * world / (el_g * 1e-3), 1),
+                  "ms_per_step": round(el_g / K, 4),
+                  "frac_step": round(b["total"] / (el_g / K * 1e-3) / 1e9 / peak, 4),
+                  "launches_per_step": blk_g.launches_per_run,
+                  "step": "as the headline, the batch's sequences in two groups of B/2 on two streams"}
+        del blk_g
+
     # End to end through the public API: pinned host inputs -> device, block
     # pass, final partial (the new block summary) -> pinned host, every step.
     e2e = run_two_phase_e2e(args, wl, dev, inp, n_blocks, world)
@@ -318,6 +359,7 @@ def run_two_phase(args, wl, dev, rank, world):
                     for n, k in kern.items()},
         "unfused": unfused,
         "prenorm": prenorm,
+        "two_groups": groups,
         "decode": decode,
         "backward": backward,
         "configs": configs,

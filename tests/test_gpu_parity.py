@@ -638,6 +638,33 @@ def test_two_phase_block_chain_small(gpu, fused):
     check_chain(p.reshape(rows, D), OP, "chain p")
 
 
+def test_two_phase_block_groups_of_sequences(gpu):
+    """groups=2: the batch's sequences in two groups on two streams give bitwise the partial of one pass over
+    the whole batch, eagerly and as one CUDA graph, and match the oracle.  9728 rows a group take the same
+    kernels as one pass: below 76 tiles of 128 rows phase 1 splits its scores over feature slices, and below
+    four rows per SM the update+merge takes its few-rows kernel, each with a reduction order of its own."""
+    D, n, S, B, T = 512, 9, 6, 4, 4864
+    g = wk.generator(79, gpu)
+    blocks, _ = wk.scaled_normal_sources(g, n, (B, T, D), 0.5, 8.0, torch.bfloat16, gpu)
+    W, G = wk.queries_and_gains(g, S, D, gpu)
+    U = wk.sublayer_u(g, S, D, gpu)
+    one = api.TwoPhaseBlock(blocks, W, G, U, 1e-8)
+    p1 = one.run().clone()
+    two = api.TwoPhaseBlock(blocks, W, G, U, 1e-8, groups=2)
+    p2 = two.run().clone()
+    torch.cuda.synchronize()
+    assert torch.equal(p1, p2)
+    two.capture()
+    two.partial.zero_()
+    assert torch.equal(two.replay(), p1)
+    torch.cuda.synchronize()
+    _, OP = oracle.block_two_phase_chain([f64(b).reshape(B * T, D) for b in blocks], f64(W), f64(G), f64(U),
+                                         1e-8, oracle.BF16)
+    check(p2.reshape(B * T, D), OP, TOL[torch.bfloat16] * vmax(blocks), "groups=2 p")
+    with pytest.raises(ValueError):
+        api.TwoPhaseBlock(blocks, W, G, U, 1e-8, groups=3)
+
+
 @pytest.mark.parametrize("fused", [True, False])
 def test_two_phase_block_chain_full_size_sampled(gpu, fused):
     wl = wk.WORKLOADS["two_phase_bf16"]

@@ -339,25 +339,62 @@ class TwoPhaseBlock:
     first sublayer needs); the main stream joins the side stream before the
     first merge.  capture() records the whole pass as one CUDA graph and
     replay() launches it.
+
+    groups=G > 1 (G divides B): the batch's sequences are split into G groups,
+    each a block pass of its own over its rows, on G streams forked from the
+    current stream and joined back; the returned partial holds every group's
+    rows.  Rows never mix in any step of the pass, so the values are those of
+    one pass over the whole batch (bitwise where both take the same kernels:
+    a group of fewer than 76 x 128 rows splits its phase-1 scores over
+    feature slices, one of at most four rows per SM takes the few-rows
+    update+merge kernel, each with its own reduction order), and the groups'
+    kernels overlap
+    (one group's phase-1 scores beside another's outputs).  Per-kernel events
+    and overlap=True need groups=1.
+
+    partial ([B,T,D] of the sources' dtype, or None): where the final partial
+    is written (allocated when None).
     """
 
     def __init__(self, blocks, queries, gains, u, eps: float = 1e-8, keep_h: bool = False,
-                 fused: bool = True, norm_weights=None, norm_eps: float = 1e-6, overlap: bool = False):
+                 fused: bool = True, norm_weights=None, norm_eps: float = 1e-6, overlap: bool = False,
+                 groups: int = 1, partial=None):
         self.blocks = list(blocks)
         self.queries, self.gains, self.u, self.eps = queries, gains, u, float(eps)
         self.nw, self.norm_eps = norm_weights, float(norm_eps)
         self.overlap = overlap
         self.graph = None
+        self.groups = int(groups)
+        ref = self.blocks[0]
+        self.device = ref.device
+        if self.groups > 1:
+            if overlap:
+                raise ValueError("groups > 1 does not combine with overlap=True")
+            Bb = ref.shape[0]
+            if Bb % self.groups:
+                raise ValueError(f"groups={self.groups} must divide the batch B={Bb}")
+            self.partial = torch.empty_like(ref) if partial is None else partial
+            bg = Bb // self.groups
+            self.parts = [TwoPhaseBlock([b[g * bg:(g + 1) * bg] for b in self.blocks], queries, gains, u, eps,
+                                        keep_h=keep_h, fused=fused, norm_weights=norm_weights, norm_eps=norm_eps,
+                                        partial=self.partial[g * bg:(g + 1) * bg])
+                          for g in range(self.groups)]
+            self.streams = [torch.cuda.Stream(device=self.device) for _ in range(self.groups)]
+            self.ev_fork = torch.cuda.Event()
+            self.ev_parts = [torch.cuda.Event() for _ in range(self.groups)]
+            self.S = queries.shape[0]
+            self.B, self.T, self.D = _btd(ref)
+            self.launches_per_run = sum(p.launches_per_run for p in self.parts)
+            return
         if overlap:
             if not fused or norm_weights is not None:
                 raise ValueError("overlap=True runs the fused pass without a pre-norm")
             self.side = torch.cuda.Stream(device=blocks[0].device)
             self.ev_fork, self.ev_join = torch.cuda.Event(), torch.cuda.Event()
         S = queries.shape[0]
-        ref = self.blocks[0]
         self.o = torch.empty((S, *ref.shape), dtype=ref.dtype, device=ref.device)
         self.lse = torch.empty((S, *ref.shape[:-1]), dtype=torch.float32, device=ref.device)
-        self.partial = torch.empty_like(ref)
+        self.partial = torch.empty_like(ref) if partial is None else partial
         self.h = (torch.empty((S, *ref.shape), dtype=ref.dtype, device=ref.device) if keep_h
                   else torch.empty_like(ref))
         self.keep_h = keep_h
@@ -380,6 +417,8 @@ class TwoPhaseBlock:
         return (self.h[k] if self.keep_h else self.h).data_ptr()
 
     def run(self, stream=None, events=None):
+        if self.groups > 1:
+            return self._run_groups(stream, events)
         L = _lib.lib()
         st = stream if stream is not None else torch.cuda.current_stream(self.o.device).cuda_stream
         B, T, D, code, eps = self.B, self.T, self.D, self.code, self.eps
@@ -471,11 +510,29 @@ class TwoPhaseBlock:
                                              self._hptr(0), None, None, st))
         main.wait_event(self.ev_join)
 
+    def _run_groups(self, stream, events):
+        """Each group's pass on a stream of its own, forked from the current
+        stream and joined back before return."""
+        if events:
+            raise ValueError("per-kernel events need groups=1")
+        main = torch.cuda.current_stream(self.device)
+        if stream is not None and stream != main.cuda_stream:
+            raise ValueError("groups > 1 runs on the current stream")
+        self.ev_fork.record(main)
+        for s, p, e in zip(self.streams, self.parts, self.ev_parts):
+            s.wait_event(self.ev_fork)
+            with torch.cuda.stream(s):
+                p.run()
+            e.record(s)
+        for e in self.ev_parts:
+            main.wait_event(e)
+        return self.partial
+
     def capture(self):
         """Record one whole block pass as a CUDA graph (after one eager pass,
         which settles the library's per-kernel launch settings)."""
         self.run()
-        torch.cuda.synchronize(self.o.device)
+        torch.cuda.synchronize(self.device)
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
             self.run()

@@ -449,9 +449,10 @@ aggregate_pipe_kernel(const __grid_constant__ AggParams p) {
 // memory (cp.async; each thread reads back only what it copied, so the
 // copies need no barrier), the scores of all sources are reduced at once,
 // the softmax is taken exactly (M = max of the prior's lse and the scores),
-// and the weighted sum reads the same vectors again.  The buffer holds 16
-// row units, so R = 16 / (1 + n) rows (at most seven) are in flight, and a
-// row's slot is refilled R rows later as soon as it has been read.  Same
+// and the weighted sum reads the same vectors again.  The buffer holds up
+// to 16 row units (11 up to eight sources), so R = units / (1 + n) rows (at
+// most seven) are in flight, and a row's slot is refilled R rows later as
+// soon as it has been read.  Same
 // arithmetic as the online form up to the order of the rescaling (eq. OS1 /
 // OS2 collapse to one step when every score is known).
 // ---------------------------------------------------------------------------
@@ -503,7 +504,7 @@ aggregate_short_kernel(const __grid_constant__ AggParams p) {
   constexpr int NP = PR::NP, VPT = 2, TPR = kShortThreads, EPV = E::EPV;
   // K: the most sources this instance takes (n <= K); two sums a source in one reduction
   static_assert(K == 8 || K == 16, "K: 8 or 16 sources");
-  extern __shared__ uint4 units[];              // [kShortUnits][VPT][TPR]: 0 = prior o, 1 + i = source i
+  extern __shared__ uint4 units[];              // [R][1 + n][VPT][TPR]: unit 0 of a slot the prior's o, 1 + i source i
   constexpr int kWarps = kShortThreads / 32;
   __shared__ float red[2 * kWarps * (2 * K)];    // cta_sum_rs<2 K, 4 warps>: [parity][warp][value]
   const int tid = threadIdx.x, n = p.n;

@@ -638,6 +638,22 @@ def test_two_phase_block_chain_small(gpu, fused):
     check_chain(p.reshape(rows, D), OP, "chain p")
 
 
+@pytest.mark.parametrize("fused,prenorm", [(False, False), (True, True)])
+def test_two_phase_block_groups_other_forms(gpu, fused, prenorm):
+    """groups=2 for the unfused pass and for the fused pass with the sublayer pre-norm: bitwise the
+    partial of one pass over the whole batch (9728 rows a group, as below)."""
+    D, n, S, B, T = 512, 9, 6, 4, 4864
+    g = wk.generator(81, gpu)
+    blocks, _ = wk.scaled_normal_sources(g, n, (B, T, D), 0.5, 8.0, torch.bfloat16, gpu)
+    W, G = wk.queries_and_gains(g, S, D, gpu)
+    U = wk.sublayer_u(g, S, D, gpu)
+    NW = wk.queries_and_gains(g, S, D, gpu)[1] if prenorm else None
+    p1 = api.TwoPhaseBlock(blocks, W, G, U, 1e-8, fused=fused, norm_weights=NW).run().clone()
+    p2 = api.TwoPhaseBlock(blocks, W, G, U, 1e-8, fused=fused, norm_weights=NW, groups=2).run().clone()
+    torch.cuda.synchronize()
+    assert torch.equal(p1, p2)
+
+
 def test_two_phase_block_groups_of_sequences(gpu):
     """groups=2: the batch's sequences in two groups on two streams give bitwise the partial of one pass over
     the whole batch, eagerly and as one CUDA graph, and match the oracle.  9728 rows a group take the same

@@ -304,8 +304,10 @@ int attnres_full_stack_forward(void *const *sources, int L, int64_t B, int64_t T
  *              phase-1 outputs of one block and, for blocks past ten
  *              sources, their scores); contents on entry do not matter
  * Blocks with up to ten sources use the phase-1 kernels of
- * attnres_block_phase1; wider ones need bf16 and D a multiple of 64 up to
- * 2048 (else ATTNRES_ERR_SHAPE, checked before anything runs).
+ * attnres_block_phase1; wider ones need bf16, D a multiple of 64 up to
+ * 2048, and at least 48 phase-1 output rows (the block's sublayers x B x T
+ * >= 48: the split queries are kept in the last 48 of them); else
+ * ATTNRES_ERR_SHAPE, checked before anything runs.
  */
 int attnres_full_stack_two_phase(void *const *sources, int L, int S, int64_t B, int64_t T, int64_t D,
                                  int dtype, const float *queries, const float *gains, const float *u,

@@ -867,7 +867,9 @@ def test_full_two_phase_small(gpu, S, D, L, rows):
 # the two-pass kernel that holds each row in shared memory (up to seven rows
 # in flight with one intra source, one from eight; 15 intra sources at S = 16),
 # over several rows per CTA.
-@pytest.mark.parametrize("S,L,rows", [(7, 20, 1000), (14, 29, 600), (16, 33, 500)])
+@pytest.mark.parametrize("S,L,rows", [(7, 20, 1000), (14, 29, 600), (16, 33, 500),
+                                      # a grid of one and of five CTAs
+                                      (7, 12, 1), (16, 32, 5)])
 def test_full_two_phase_short_rows(gpu, S, L, rows):
     wl = wk.WORKLOADS["full_stack_bf16"]
     D = 2048

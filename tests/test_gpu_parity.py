@@ -679,6 +679,8 @@ def test_two_phase_block_groups_of_sequences(gpu):
     check(p2.reshape(B * T, D), OP, TOL[torch.bfloat16] * vmax(blocks), "groups=2 p")
     with pytest.raises(ValueError):
         api.TwoPhaseBlock(blocks, W, G, U, 1e-8, groups=3)
+    with pytest.raises(ValueError):                       # the partial must match the summaries
+        api.TwoPhaseBlock(blocks, W, G, U, 1e-8, partial=torch.empty(1, device=gpu))
 
 
 @pytest.mark.parametrize("fused", [True, False])

@@ -367,6 +367,9 @@ class TwoPhaseBlock:
         self.groups = int(groups)
         ref = self.blocks[0]
         self.device = ref.device
+        if partial is not None and (partial.shape != ref.shape or partial.dtype != ref.dtype
+                                    or partial.device != ref.device or not partial.is_contiguous()):
+            raise ValueError("partial must be a contiguous tensor of the summaries' shape, dtype and device")
         if self.groups > 1:
             if overlap:
                 raise ValueError("groups > 1 does not combine with overlap=True")

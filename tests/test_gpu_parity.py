@@ -132,6 +132,86 @@ def test_aggregate_short_rows(gpu, n, rows):
     check_stats(m, om, "m")
 
 
+def _random_shapes(seed, count, draw):
+    rng = np.random.default_rng(seed)
+    return [draw(rng) for _ in range(count)]
+
+
+def test_aggregate_random_shapes(gpu):
+    """Seeded random shapes (dtype, D, n, token rows) against the oracle: widths from 4 to 8192 elements,
+    1..40 sources, 1..3000 rows, kept to a few million elements each."""
+    def draw(rng):
+        dtype = torch.bfloat16 if rng.random() < 0.7 else torch.float32
+        step, top = (8, 8192) if dtype == torch.bfloat16 else (4, 4096)
+        D = int(rng.integers(1, top // step + 1)) * step
+        n = int(rng.integers(1, 41))
+        rows = int(rng.integers(1, 3001))
+        rows = max(1, min(rows, 4_000_000 // (n * D)))
+        return dtype, D, n, rows
+    for i, (dtype, D, n, rows) in enumerate(_random_shapes(2024, 40, draw)):
+        srcs, q, g = rand_sources(n, (1, rows, D), dtype, gpu, seed=900 + i)
+        out, m, lse = api.depth_aggregate(srcs, q, g, 1e-8, stats=True)
+        h, om, olse = oracle.depth_aggregate(np.stack([f64(s) for s in srcs]), f64(q), f64(g), 1e-8)
+        check(out, oracle.round_to(h, ODT[dtype]), TOL[dtype] * vmax(srcs), f"case {i}: {dtype} D={D} n={n} rows={rows}")
+        check_stats(lse, olse, f"case {i} lse")
+
+
+def test_phase1_random_shapes(gpu):
+    """Seeded random phase-1 shapes against the oracle: bf16 and fp32, 1..16 summaries, 1..24 queries,
+    widths up to 4096, 1..1200 rows (the tensor-core path from 512 bf16 rows, split mode from 64, the
+    per-row kernel below)."""
+    def draw(rng):
+        dtype = torch.bfloat16 if rng.random() < 0.75 else torch.float32
+        elt = 2 if dtype == torch.bfloat16 else 4
+        n = int(rng.integers(1, 17))
+        S = int(rng.integers(1, 25))
+        D = int(rng.integers(1, 65)) * 64
+        D = min(D, (200 * 1024) // (n * elt) // 64 * 64) or 64
+        rows = int(rng.integers(1, 1201))
+        rows = max(1, min(rows, 60_000_000 // (n * S * D)))
+        return dtype, D, n, S, rows
+    ran = 0
+    for i, (dtype, D, n, S, rows) in enumerate(_random_shapes(2025, 30, draw)):
+        g = wk.generator(700 + i, gpu)
+        blocks, _ = wk.scaled_normal_sources(g, n, (1, rows, D), 0.5, 8.0, dtype, gpu)
+        W, G = wk.queries_and_gains(g, S, D, gpu)
+        try:
+            o, m, lse = api.block_phase1(blocks, W, G, 1e-8, want_max=True)
+        except _lib.AttnResError as e:   # a shape no phase-1 kernel takes (refused before anything runs)
+            assert "SHAPE" in str(e), str(e)
+            continue
+        ran += 1
+        O, M, LSE = oracle.block_phase1([f64(b) for b in blocks], f64(W), f64(G), 1e-8)
+        tol = TOL[dtype] * vmax(blocks)
+        what = f"case {i}: {dtype} D={D} n={n} S={S} rows={rows}"
+        check(o.reshape(S, rows, D), oracle.round_to(O, ODT[dtype]), tol, what)
+        check_stats(lse.reshape(S, rows), LSE, what + " lse", STATS_TOL_SPLIT_Q)
+    assert ran >= 25, ran
+
+
+def test_full_two_phase_random_shapes(gpu):
+    """Seeded random Full two-phase schedules against the oracle: bf16, widths a multiple of 64 up to 2048,
+    2..30 sublayers in blocks of 1..24, 48..400 token rows."""
+    def draw(rng):
+        D = int(rng.integers(1, 33)) * 64
+        L = int(rng.integers(2, 31))
+        S = int(rng.integers(1, 25))
+        rows = int(rng.integers(48, 401))
+        rows = max(48, min(rows, 30_000_000 // (L * L * D)))
+        return D, L, S, rows
+    wl = wk.WORKLOADS["full_stack_bf16"]
+    for i, (D, L, S, rows) in enumerate(_random_shapes(2026, 10, draw)):
+        inp = wk.full_stack_inputs(wl, rows=rows, device=gpu, L=L, D=D)
+        y, srcs = api.full_stack_two_phase(inp["v0"], inp["queries"], inp["gains"], inp["u"], S, inp["eps"])
+        V, oy = oracle.full_stack_two_phase(f64(inp["v0"]).reshape(rows, D), f64(inp["queries"]),
+                                            f64(inp["gains"]), f64(inp["u"]), S, inp["eps"], oracle.BF16)
+        tol = TOL[torch.bfloat16] * float(inp["v0"].abs().max())
+        what = f"case {i}: D={D} L={L} S={S} rows={rows}"
+        for l in (1, L // 2, L):
+            check(srcs[l].reshape(rows, D), V[l], tol, f"{what} v_{l}")
+        check(y.reshape(rows, D), oracle.round_to(oy, oracle.BF16), tol, f"{what} y")
+
+
 def test_aggregate_one_source_is_identity_bitwise(gpu):
     for dtype, D in ((torch.bfloat16, 2048), (torch.float32, 256), (torch.bfloat16, 40)):
         srcs, q, g = rand_sources(1, (2, 33, D), dtype, gpu, seed=5)

@@ -417,6 +417,20 @@ def _bwd_case(gpu, dtype, D, n, rows, seed, accumulate=False):
     return srcs, W, G, dh, gs, gq, gg
 
 
+def test_aggregate_backward_random_shapes(gpu):
+    """Seeded random backward shapes against the oracle: bf16 and fp32, widths from 4 to 8192 elements,
+    1..24 sources, 1..2000 rows, overwriting or accumulating the source gradients."""
+    def draw(rng):
+        dtype = torch.bfloat16 if rng.random() < 0.7 else torch.float32
+        step, top = (8, 8192) if dtype == torch.bfloat16 else (4, 4096)
+        D = int(rng.integers(1, top // step + 1)) * step
+        n = int(rng.integers(1, 25))
+        rows = max(1, min(int(rng.integers(1, 2001)), 3_000_000 // (n * D)))
+        return dtype, D, n, rows, bool(rng.random() < 0.3)
+    for i, (dtype, D, n, rows, acc) in enumerate(_random_shapes(2028, 16, draw)):
+        _bwd_case(gpu, dtype, D, n, rows, seed=600 + i, accumulate=acc)
+
+
 @pytest.mark.parametrize("dtype,D,n,rows", [
     (torch.bfloat16, 16, 3, 33), (torch.float32, 64, 5, 20), (torch.bfloat16, 512, 7, 45),
     (torch.float32, 256, 2, 70), (torch.bfloat16, 2048, 10, 37), (torch.bfloat16, 8192, 4, 9),
@@ -597,6 +611,33 @@ def test_merge_update_fused_step(gpu):
                 pi, hs = pin.clone(), sub.clone()              # h_out aliases sub_out
                 api.block_merge_update(o, lse, pi, hs, u, W[0], G[0], 1e-8, partial_out=pi, h_out=hs)
                 assert torch.equal(pi, p_out) and torch.equal(hs, h)
+
+
+def test_merge_update_random_shapes(gpu):
+    """Seeded random fused update+merge steps against the oracle: bf16 and fp32, widths from 4 to 8192
+    elements, 1..3000 rows (the team, few-rows and general kernels), with and without the sublayer and the
+    incoming partial."""
+    def draw(rng):
+        dtype = torch.bfloat16 if rng.random() < 0.7 else torch.float32
+        step, top = (8, 8192) if dtype == torch.bfloat16 else (4, 4096)
+        D = int(rng.integers(1, top // step + 1)) * step
+        rows = max(1, min(int(rng.integers(1, 3001)), 6_000_000 // D))
+        return dtype, D, rows, bool(rng.random() < 0.7), bool(rng.random() < 0.8)
+    for i, (dtype, D, rows, synth, with_pin) in enumerate(_random_shapes(2027, 24, draw)):
+        g = wk.generator(500 + i, gpu)
+        (o, pin, sub), _ = wk.scaled_normal_sources(g, 3, (1, rows, D), 0.5, 3.0, dtype, gpu)
+        W, G = wk.queries_and_gains(g, 1, D, gpu)
+        u = wk.sublayer_u(g, 1, D, gpu)[0].contiguous() if synth else None
+        lse = torch.empty(rows, device=gpu).normal_(0.0, 2.0, generator=g)
+        p_out, h, _ = api.block_merge_update(o, lse, pin if with_pin else None, sub, u, W[0], G[0], 1e-8)
+        subn = f64(sub).reshape(rows, D)
+        out = oracle.synthetic_sublayer(f64(u), subn) if synth else subn
+        want_p = oracle.round_to((f64(pin).reshape(rows, D) if with_pin else 0.0) + out, ODT[dtype])
+        want_h, _ = oracle.block_phase2_merge(f64(o).reshape(rows, D), f64(lse), want_p, f64(W[0]), f64(G[0]), 1e-8)
+        tol = TOL[dtype] * vmax([o, pin, sub])
+        what = f"case {i}: {dtype} D={D} rows={rows} synth={synth} p_in={with_pin}"
+        check(p_out.reshape(rows, D), want_p, tol, what + " p")
+        check(h.reshape(rows, D), oracle.round_to(want_h, ODT[dtype]), tol, what + " h")
 
 
 # The next sublayer's pre-norm, standalone and fused into the update+merge.
